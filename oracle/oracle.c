@@ -1,0 +1,374 @@
+/*
+ * CPU oracle for the dense matrix multiply-accumulate D = A*B + C.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file; it exists so that the tests, the smoke check and the CPU
+ * baseline of the benchmark have an obviously correct result to compare the
+ * CUDA library against.  It shares no code, header or constant table with
+ * the CUDA library.
+ *
+ * What it computes (plain definition, no blocking, no fusion, no reordering):
+ *
+ *   D[i,j] = C[i,j] + sum_{k=0}^{K-1} A[i,k] * B[k,j]
+ *
+ * The sum over k is formed first and C is added once afterwards, as in the
+ * plain HIP kernel "MatMulAdd_kernel2" (forum.sourcefind.cn, "DCU K100 ..."
+ * article, section 5.2), where each thread forms the K-sum and then writes
+ * sum + C.  The sum over k ascends, as in the Triton "matmul_kernel" of the
+ * "Hopper Support in Triton" slides (slide 5: one fp32 accumulator that
+ * receives tl.dot of successive BLOCK_K slices).
+ *
+ * Floating point: fp16/bf16 operands are widened exactly to fp64 and the
+ * whole sum is formed in fp64 (every fp16/bf16 product is exact in fp64).
+ * Integer: int8 operands, int32 C, and the sum is formed in int64 (exact).
+ *
+ * Indexing follows the storage order of each operand.  Row-major X[r,c] is
+ * X[r*ld + c]; column-major X[r,c] is X[r + c*ld] (the article's kernel
+ * reads a column-major A as A[row + k*M] and a row-major B as B[k*N + col]).
+ *
+ * Output rounding to fp16/bf16 is a single round-to-nearest-even of the
+ * fp64 value, written out from the IEEE 754 definition.  The pages show the
+ * fp32 accumulator being narrowed to fp16 on store (slides 5-6, the
+ * arith.truncf before tt.store) but never state the rounding mode; the plain
+ * reading is the IEEE default, nearest with ties to even.
+ *
+ * Build: cc -O2 -fopenmp -shared -fPIC oracle.c -o liboracle.so -lm
+ */
+#include <stdint.h>
+#include <stddef.h>
+#include <stdlib.h>
+#include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Element type codes understood by this file. */
+#define OR_F16 1
+#define OR_BF16 2
+#define OR_F32 3
+#define OR_I8 4
+#define OR_I32 5
+
+/* Fault-planting hook for the oracle's own self-tests: a build with
+ * -DORACLE_MUTANT=n plants one plausible mistake so that the tests can show
+ * that their pins catch it.  The default build (n = 0) plants nothing.
+ *   1: a square A read transposed
+ *   2: C dropped            3: C subtracted
+ *   4: last k dropped       5: rounding ties away from zero
+ *   6: integer sum starts at k = 1
+ *   7: subnormal scale off by a factor of two in the widening
+ *   8: A's k index reversed (A[i, K-1-k] paired with B[k, j]) */
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+/* ---------------------------------------------------------------------------
+ * Binary16 and bfloat16 encodings.
+ *   binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits.
+ *   bfloat16: 1 sign, 8 exponent (bias 127), 7 fraction bits.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  int frac_bits; /* stored fraction bits */
+  int exp_bits;
+  int bias;
+} or_format;
+
+static const or_format FMT_F16 = {10, 5, 15};
+static const or_format FMT_BF16 = {7, 8, 127};
+
+/* Exact value of an encoding. */
+static double widen_bits(uint32_t bits, or_format f) {
+  const uint32_t frac_mask = (1u << f.frac_bits) - 1u;
+  const uint32_t exp_mask = (1u << f.exp_bits) - 1u;
+  const uint32_t frac = bits & frac_mask;
+  const uint32_t e = (bits >> f.frac_bits) & exp_mask;
+  const int neg = (int)((bits >> (f.frac_bits + f.exp_bits)) & 1u);
+  double v;
+  if (e == exp_mask) {
+    v = frac ? NAN : INFINITY;
+  } else if (e == 0) {
+    /* subnormal: frac * 2^(1 - bias - frac_bits) */
+#if ORACLE_MUTANT == 7
+    v = ldexp((double)frac, -f.bias - f.frac_bits);
+#else
+    v = ldexp((double)frac, 1 - f.bias - f.frac_bits);
+#endif
+  } else {
+    v = ldexp((double)((1u << f.frac_bits) | frac), (int)e - f.bias - f.frac_bits);
+  }
+  return neg ? -v : v;
+}
+
+/* Round x to the nearest value of format f, ties to the even significand.
+ * The exponent is unbounded above (a result beyond the largest finite value
+ * becomes infinity) and underflow is gradual (subnormals are produced).
+ * Returns the encoding. */
+static uint32_t round_bits(double x, or_format f) {
+  const int p = f.frac_bits + 1;          /* precision in bits */
+  const int emin = 1 - f.bias;            /* exponent of the smallest normal */
+  const int emax = f.bias;                /* exponent of the largest normal */
+  const uint32_t exp_all = (1u << f.exp_bits) - 1u;
+  const uint32_t sign = signbit(x) ? (1u << (f.frac_bits + f.exp_bits)) : 0u;
+  if (isnan(x)) return sign | (exp_all << f.frac_bits) | (1u << (f.frac_bits - 1));
+  const double a = fabs(x);
+  if (isinf(a)) return sign | (exp_all << f.frac_bits);
+  if (a == 0.0) return sign;
+
+  int E;
+  (void)frexp(a, &E);            /* a = m * 2^E with m in [0.5, 1) */
+  int e = E - 1;                 /* a in [2^e, 2^(e+1)) */
+  if (e < emin) e = emin;        /* below the normal range the spacing is fixed */
+  const int qexp = e - (p - 1);  /* log2 of the spacing of the format near a */
+  const double r = ldexp(a, -qexp); /* exact: scaling by a power of two */
+  double n = floor(r);
+  const double rem = r - n;      /* exact */
+#if ORACLE_MUTANT == 5
+  if (rem >= 0.5) n += 1.0;
+#else
+  if (rem > 0.5 || (rem == 0.5 && fmod(n, 2.0) != 0.0)) n += 1.0;
+#endif
+  const double v = ldexp(n, qexp); /* the rounded magnitude */
+
+  const double max_finite = ldexp((double)((1u << p) - 1u), emax - (p - 1));
+  if (v > max_finite) return sign | (exp_all << f.frac_bits);
+
+  if (v < ldexp(1.0, emin)) {
+    /* subnormal or zero: the fraction field is v / 2^(emin - (p-1)) */
+    return sign | (uint32_t)ldexp(v, -(emin - (p - 1)));
+  }
+  int E2;
+  (void)frexp(v, &E2);
+  const int e2 = E2 - 1;
+  const uint32_t sig = (uint32_t)ldexp(v, -(e2 - (p - 1))); /* in [2^(p-1), 2^p) */
+  const uint32_t ef = (uint32_t)(e2 + f.bias);
+  return sign | (ef << f.frac_bits) | (sig - (1u << (p - 1)));
+}
+
+/* Exported: exact widening of n encoded values of type t (OR_F16/OR_BF16). */
+int oracle_widen(const uint16_t* bits, int64_t n, int t, double* out) {
+  if (t != OR_F16 && t != OR_BF16) return -1;
+  const or_format f = (t == OR_F16) ? FMT_F16 : FMT_BF16;
+  for (int64_t i = 0; i < n; ++i) out[i] = widen_bits(bits[i], f);
+  return 0;
+}
+
+/* Exported: one round-to-nearest-even of each fp64 value to type t. */
+int oracle_round(const double* x, int64_t n, int t, uint16_t* out_bits) {
+  if (t != OR_F16 && t != OR_BF16) return -1;
+  const or_format f = (t == OR_F16) ? FMT_F16 : FMT_BF16;
+  for (int64_t i = 0; i < n; ++i) out_bits[i] = (uint16_t)round_bits(x[i], f);
+  return 0;
+}
+
+/* Exported: number of threads the parallel loops below use. */
+int oracle_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* Element (r, c) of an operand stored with leading dimension ld. */
+static int64_t at(int64_t r, int64_t c, int col_major, int64_t ld) {
+  return col_major ? r + c * ld : r * ld + c;
+}
+
+/* Element (i, k) of A, an M x K operand. */
+static int64_t at_a(int64_t i, int64_t k, int64_t M, int64_t K, int col_major, int64_t ld) {
+#if ORACLE_MUTANT == 1
+  if (M == K) return at(k, i, col_major, ld);
+#elif ORACLE_MUTANT == 8
+  return at(i, K - 1 - k, col_major, ld);
+#endif
+  (void)M;
+  (void)K;
+  return at(i, k, col_major, ld);
+}
+
+/* Floating-point element, widened to fp64. */
+static double load_f(const void* base, int t, int64_t idx) {
+  switch (t) {
+    case OR_F16: return widen_bits(((const uint16_t*)base)[idx], FMT_F16);
+    case OR_BF16: return widen_bits(((const uint16_t*)base)[idx], FMT_BF16);
+    case OR_F32: return (double)((const float*)base)[idx];
+    default: return NAN;
+  }
+}
+
+static double add_c(double sum, double c) {
+#if ORACLE_MUTANT == 2
+  (void)c;
+  return sum;
+#elif ORACLE_MUTANT == 3
+  return sum - c;
+#else
+  return sum + c;
+#endif
+}
+
+static int64_t k_end(int64_t K) {
+#if ORACLE_MUTANT == 4
+  return K > 0 ? K - 1 : 0;
+#else
+  return K;
+#endif
+}
+
+static int fp_types_ok(int ab_type, int c_type, const void* C) {
+  if (ab_type != OR_F16 && ab_type != OR_BF16) return 0;
+  if (C && c_type != OR_F16 && c_type != OR_BF16 && c_type != OR_F32) return 0;
+  return 1;
+}
+
+/* ---------------------------------------------------------------------------
+ * Floating-point oracle over whole rows.
+ *   rows == NULL: every row i in [0, M); otherwise the nrows rows listed.
+ *   D : nrows x N fp64, dense row-major (D[q*N + j] is row rows[q]).
+ *   S : optional, same shape: sum_k |A[i,k] * B[k,j]|, for the error bound.
+ *   C : may be NULL, meaning C = 0 (C is then never read).
+ * Loop order i, k, j over operands widened once; for every output the sum
+ * over k ascends.  Returns 0, -1 on bad arguments, -2 when out of memory.
+ * ------------------------------------------------------------------------- */
+int oracle_gemm_f64_rows(int64_t M, int64_t N, int64_t K, int ab_type, int c_type,
+                         int a_col, int b_col, int c_col,
+                         int64_t lda, int64_t ldb, int64_t ldc,
+                         const void* A, const void* B, const void* C,
+                         const int64_t* rows, int64_t nrows, double* D, double* S) {
+  if (M < 0 || N < 0 || K < 0 || !fp_types_ok(ab_type, c_type, C)) return -1;
+  const int64_t nr = rows ? nrows : M;
+  for (int64_t q = 0; q < nr; ++q)
+    if (rows && (rows[q] < 0 || rows[q] >= M)) return -1;
+  if (nr == 0 || N == 0) return 0;
+
+  double* Bw = (double*)malloc((size_t)(K > 0 ? K : 1) * (size_t)N * sizeof(double));
+  double* Aw = (double*)malloc((size_t)(K > 0 ? K : 1) * (size_t)nr * sizeof(double));
+  if (!Bw || !Aw) {
+    free(Bw);
+    free(Aw);
+    return -2;
+  }
+#pragma omp parallel for schedule(static)
+  for (int64_t k = 0; k < K; ++k)
+    for (int64_t j = 0; j < N; ++j) Bw[k * N + j] = load_f(B, ab_type, at(k, j, b_col, ldb));
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t q = 0; q < nr; ++q) {
+    const int64_t i = rows ? rows[q] : q;
+    double* a = Aw + q * K;
+    double* d = D + q * N;
+    double* s = S ? S + q * N : NULL;
+    for (int64_t k = 0; k < K; ++k) a[k] = load_f(A, ab_type, at_a(i, k, M, K, a_col, lda));
+    for (int64_t j = 0; j < N; ++j) d[j] = 0.0;
+    if (s)
+      for (int64_t j = 0; j < N; ++j) s[j] = 0.0;
+    const int64_t ke = k_end(K);
+    for (int64_t k = 0; k < ke; ++k) {
+      const double aik = a[k];
+      const double* brow = Bw + k * N;
+      for (int64_t j = 0; j < N; ++j) d[j] += aik * brow[j];
+      if (s)
+        for (int64_t j = 0; j < N; ++j) s[j] += fabs(aik * brow[j]);
+    }
+    if (C)
+      for (int64_t j = 0; j < N; ++j) d[j] = add_c(d[j], load_f(C, c_type, at(i, j, c_col, ldc)));
+  }
+  free(Bw);
+  free(Aw);
+  return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Floating-point oracle at single elements (pi[q], pj[q]), q < npts: the
+ * same definition, one length-K dot product per element with k ascending.
+ * D[q] and (optional) S[q] receive the value and sum_k |a*b|.
+ * ------------------------------------------------------------------------- */
+int oracle_gemm_f64_points(int64_t M, int64_t N, int64_t K, int ab_type, int c_type,
+                           int a_col, int b_col, int c_col,
+                           int64_t lda, int64_t ldb, int64_t ldc,
+                           const void* A, const void* B, const void* C,
+                           const int64_t* pi, const int64_t* pj, int64_t npts,
+                           double* D, double* S) {
+  if (M < 0 || N < 0 || K < 0 || !fp_types_ok(ab_type, c_type, C)) return -1;
+  for (int64_t q = 0; q < npts; ++q)
+    if (pi[q] < 0 || pi[q] >= M || pj[q] < 0 || pj[q] >= N) return -1;
+#pragma omp parallel for schedule(static)
+  for (int64_t q = 0; q < npts; ++q) {
+    const int64_t i = pi[q], j = pj[q];
+    double d = 0.0, s = 0.0;
+    const int64_t ke = k_end(K);
+    for (int64_t k = 0; k < ke; ++k) {
+      const double p = load_f(A, ab_type, at_a(i, k, M, K, a_col, lda)) *
+                       load_f(B, ab_type, at(k, j, b_col, ldb));
+      d += p;
+      s += fabs(p);
+    }
+    if (C) d = add_c(d, load_f(C, c_type, at(i, j, c_col, ldc)));
+    D[q] = d;
+    if (S) S[q] = s;
+  }
+  return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Integer oracle: int8 A and B, int32 C (or NULL), int64 sums (exact).
+ * Rows variant: D is nrows x N int64, dense row-major.
+ * ------------------------------------------------------------------------- */
+static int64_t int_k_begin(void) {
+#if ORACLE_MUTANT == 6
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+int oracle_gemm_i64_rows(int64_t M, int64_t N, int64_t K, int a_col, int b_col, int c_col,
+                         int64_t lda, int64_t ldb, int64_t ldc,
+                         const int8_t* A, const int8_t* B, const int32_t* C,
+                         const int64_t* rows, int64_t nrows, int64_t* D) {
+  if (M < 0 || N < 0 || K < 0) return -1;
+  const int64_t nr = rows ? nrows : M;
+  for (int64_t q = 0; q < nr; ++q)
+    if (rows && (rows[q] < 0 || rows[q] >= M)) return -1;
+  if (nr == 0 || N == 0) return 0;
+  int64_t* Bw = (int64_t*)malloc((size_t)(K > 0 ? K : 1) * (size_t)N * sizeof(int64_t));
+  if (!Bw) return -2;
+#pragma omp parallel for schedule(static)
+  for (int64_t k = 0; k < K; ++k)
+    for (int64_t j = 0; j < N; ++j) Bw[k * N + j] = B[at(k, j, b_col, ldb)];
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t q = 0; q < nr; ++q) {
+    const int64_t i = rows ? rows[q] : q;
+    int64_t* d = D + q * N;
+    for (int64_t j = 0; j < N; ++j) d[j] = 0;
+    for (int64_t k = int_k_begin(); k < K; ++k) {
+      const int64_t aik = A[at_a(i, k, M, K, a_col, lda)];
+      const int64_t* brow = Bw + k * N;
+      for (int64_t j = 0; j < N; ++j) d[j] += aik * brow[j];
+    }
+    if (C)
+      for (int64_t j = 0; j < N; ++j) d[j] += C[at(i, j, c_col, ldc)];
+  }
+  free(Bw);
+  return 0;
+}
+
+int oracle_gemm_i64_points(int64_t M, int64_t N, int64_t K, int a_col, int b_col, int c_col,
+                           int64_t lda, int64_t ldb, int64_t ldc,
+                           const int8_t* A, const int8_t* B, const int32_t* C,
+                           const int64_t* pi, const int64_t* pj, int64_t npts, int64_t* D) {
+  if (M < 0 || N < 0 || K < 0) return -1;
+  for (int64_t q = 0; q < npts; ++q)
+    if (pi[q] < 0 || pi[q] >= M || pj[q] < 0 || pj[q] >= N) return -1;
+#pragma omp parallel for schedule(static)
+  for (int64_t q = 0; q < npts; ++q) {
+    const int64_t i = pi[q], j = pj[q];
+    int64_t d = 0;
+    for (int64_t k = int_k_begin(); k < K; ++k)
+      d += (int64_t)A[at_a(i, k, M, K, a_col, lda)] * (int64_t)B[at(k, j, b_col, ldb)];
+    if (C) d += C[at(i, j, c_col, ldc)];
+    D[q] = d;
+  }
+  return 0;
+}
