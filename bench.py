@@ -1,0 +1,393 @@
+"""Benchmark: D = A*B + C through the C ABI on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step is one D = A*B + C of the workload (default: 4096^3 bf16, A
+row-major, B column-major, C and D bf16, the configuration the headline
+metric is quoted on).  Inputs are seeded synthetic data, resident in HBM
+before the timed region; the step rotates over enough input sets that the
+working set of consecutive steps exceeds L2.  Timing: W untimed warm-up
+steps, then K steps bracketed by a barrier and a device synchronisation,
+CUDA events on the launching stream; the line reports the maximum over
+ranks.  The GEMM is not sharded: N > 1 runs N independent replicas (one per
+GPU) and `value` sums their throughput ("weak" scaling).
+
+`e2e` is the same metric measured through the same call with the inputs in
+pinned host memory: every step copies A, B, C host->device, runs the GEMM
+and copies D back, all inside the timed region.
+
+`--impl reference` times the CPU oracle (test infrastructure, fp64 triple
+loop) on the host cores, on a bounded sample of rows of the same workload,
+and reports the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 10 ** 6
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="sq4096_bf16")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources; profile figures apply only to this build."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_tiled_gemm_02_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this build, or None."""
+    path = os.path.join(ROOT, "profiles", f"tc_gemm_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(w, inp, target_s: float) -> dict:
+    """The oracle as it stands, timed on a bounded sample of whole rows."""
+    import numpy as np
+    from workloads import I8
+    run, threads = oracle_rows_runner(w, inp)
+    n = min(w.M, 4)
+    t0 = time.perf_counter()
+    run(np.arange(n))
+    dt = max(time.perf_counter() - t0, 1e-6)
+    n2 = int(max(1, min(w.M, n * target_s / dt)))
+    t0 = time.perf_counter()
+    run(np.arange(n2))
+    dt = time.perf_counter() - t0
+    flops = 2.0 * n2 * w.N * w.K
+    return {"value": flops / dt / 1e12, "unit": "TOPS" if w.ab_type == I8 else "TFLOPS",
+            "cores": threads, "kind": "oracle",
+            "sample": f"{n2} of {w.M} output rows ({n2 * w.N} elements), fp64/int64 triple "
+                      f"loop, {dt:.1f} s"}
+
+
+def run_reference(args, w):
+    """The oracle as the reference arm: each step is a bounded sample of rows."""
+    import numpy as np
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from workloads import I8, make_inputs
+    inp = make_inputs(w)
+    total_steps = max(1, args.steps + args.warmup)
+    per_step_s = min(10.0, max(0.2, 120.0 / total_steps))
+    run, threads = oracle_rows_runner(w, inp)
+    n = min(w.M, 4)
+    t0 = time.perf_counter()
+    run(np.arange(n))
+    dt = max(time.perf_counter() - t0, 1e-6)
+    rows_per_step = int(max(1, min(w.M, n * per_step_s / dt)))
+    for i in range(args.warmup):
+        run((np.arange(rows_per_step) + i * rows_per_step) % w.M)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        run((np.arange(rows_per_step) + i * rows_per_step) % w.M)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows_per_step * w.N * w.K * args.steps
+    value = flops / dt / 1e12
+    unit = "TOPS" if w.ab_type == I8 else "TFLOPS"
+    sample = (f"{rows_per_step} of {w.M} output rows per step ({rows_per_step * w.N} elements), "
+              f"fp64/int64 triple loop, {args.steps} timed steps in {dt:.1f} s")
+    line = {"impl": "reference", "metric": metric_name(w), "value": value, "unit": unit,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64" if w.ab_type != I8 else "int64",
+            "data": "synthetic (seeded)", "config": config_of(w),
+            "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def oracle_rows_runner(w, inp):
+    import oracle
+    from workloads import I8, bits_u16
+    orc = oracle.get()
+    if w.ab_type == I8:
+        A, B = inp["A"].numpy(), inp["B"].numpy()
+        C = None if inp["C"] is None else inp["C"].numpy()
+        run = lambda rows: orc.gemm_i64_rows(w.M, w.N, w.K, A, B, C, a_col=w.layout_a,
+                                             b_col=w.layout_b, c_col=w.layout_c, rows=rows)
+    else:
+        A, B = bits_u16(inp["A"]), bits_u16(inp["B"])
+        C = None if inp["C"] is None else bits_u16(inp["C"])
+        run = lambda rows: orc.gemm_f64_rows(w.M, w.N, w.K, A, B, C, ab_type=w.ab_type,
+                                             c_type=w.c_type or 0, a_col=w.layout_a,
+                                             b_col=w.layout_b, c_col=w.layout_c, rows=rows,
+                                             want_s=False)
+    return run, orc.threads()
+
+
+def logical(storage, layout):
+    return storage if layout == 0 else storage.t()
+
+
+def metric_name(w) -> str:
+    from workloads import I8
+    return "GEMM TOPS (int8)" if w.ab_type == I8 else "GEMM TFLOPS (bf16/fp16)"
+
+
+def config_of(w) -> dict:
+    from workloads import TYPE_NAME
+    lay = lambda l: "row" if l == 0 else "col"
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+            "types": f"{TYPE_NAME[w.ab_type]}x{TYPE_NAME[w.ab_type]}+"
+                     f"{TYPE_NAME[w.c_type] if w.c_type else 'none'}->{TYPE_NAME[w.d_type]}",
+            "layouts": f"A {lay(w.layout_a)}, B {lay(w.layout_b)}, C {lay(w.layout_c)}, "
+                       f"D {lay(w.layout_d)}",
+            "parallelism": "replicas"}
+
+
+def main():
+    args = parse()
+    from workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    import torch.distributed as dist
+
+    import dense_tiled_gemm_02_gb300 as pkg
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkg.load()
+
+    from workloads import I8, TORCH_DTYPE, TYPE_NAME, make_inputs, storage_shape
+    inp = make_inputs(w)
+    set_bytes = sum(t.numel() * t.element_size() for t in inp.values() if t is not None)
+    set_bytes += w.M * w.N * TORCH_DTYPE[w.d_type].itemsize
+    nsets = max(2, -(-2 * L2_BYTES // set_bytes))  # working set of a step cycle > 2x L2
+    sets = []
+    for i in range(nsets):
+        A = logical(inp["A"].to(dev), w.layout_a)
+        B = logical(inp["B"].to(dev), w.layout_b)
+        C = None if inp["C"] is None else logical(inp["C"].to(dev), w.layout_c)
+        Ds = torch.empty(storage_shape(w.M, w.N, w.layout_d), dtype=TORCH_DTYPE[w.d_type], device=dev)
+        sets.append((A, B, C, logical(Ds, w.layout_d)))
+    g = pkg.Gemm.like(*sets[0])
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+
+    def step(i):
+        A, B, C, D = sets[i % nsets]
+        g.run_ptrs(A.data_ptr(), B.data_ptr(), None if C is None else C.data_ptr(),
+                   D.data_ptr(), sptr)
+
+    for i in range(args.warmup):
+        step(i)
+    st = g.status(stream)
+    if st != pkg.GEMM_OK:
+        raise RuntimeError(f"warm-up failed: {pkg.gemm_strerror(st)}")
+
+    # ---- device-timed region
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    st = g.status(stream)
+    if st != pkg.GEMM_OK:
+        raise RuntimeError(f"timed run failed: {pkg.gemm_strerror(st)}")
+    total_ms = start.elapsed_time(end)
+    per_launch = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    value = w.flops / (ms * 1e-3) / 1e12 * world
+
+    # ---- end to end through the same call, host buffers
+    e2e = e2e_measure(pkg, g, w, inp, dev, stream, max(3, args.steps // 5), world)
+
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    avg_launch_ms = statistics.mean(per_launch)
+    achieved = w.flops / (avg_launch_ms * 1e-3) / 1e12
+    traffic = profiled_traffic(w.name)
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": f"{src} bf16 burst (cuBLAS 8192^3)",
+                "kernel": "tc_gemm_kernel", "median_launch_ms": round(statistics.median(per_launch), 4)}
+
+    line = {"metric": metric_name(w), "value": round(value, 1),
+            "unit": "TOPS" if w.ab_type == I8 else "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": TYPE_NAME[w.ab_type],
+            "data": "synthetic (seeded, resident in HBM)",
+            "config": dict(config_of(w), l2="rotating %d input sets, %.0f MB > L2" %
+                           (nsets, nsets * set_bytes / 1e6), plan=g.plan()),
+            "roofline": roofline, "clocks": clk, "e2e": e2e,
+            "gpu_launches": launches_per_step(g) * args.steps}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
+    g.close()
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def launches_per_step(g) -> int:
+    plan = g.plan()
+    n = 1
+    if re.search(r"splits=(\d+)", plan) and int(re.search(r"splits=(\d+)", plan).group(1)) > 1:
+        n += 1
+    n += int(re.search(r"repack_a=(\d)", plan).group(1)) + int(re.search(r"repack_b=(\d)", plan).group(1))
+    return n
+
+
+def e2e_measure(pkg, g, w, inp, dev, stream, steps, world):
+    import torch
+    from workloads import TORCH_DTYPE, storage_shape
+    host = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
+    dA = torch.empty_like(host["A"], device=dev)
+    dB = torch.empty_like(host["B"], device=dev)
+    dC = None if host["C"] is None else torch.empty_like(host["C"], device=dev)
+    Ds = torch.empty(storage_shape(w.M, w.N, w.layout_d), dtype=TORCH_DTYPE[w.d_type], device=dev)
+    hD = torch.empty(Ds.shape, dtype=Ds.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = hD.numel() * hD.element_size()
+
+    def one():
+        dA.copy_(host["A"], non_blocking=True)
+        dB.copy_(host["B"], non_blocking=True)
+        if dC is not None:
+            dC.copy_(host["C"], non_blocking=True)
+        g.run(logical(dA, w.layout_a), logical(dB, w.layout_b),
+              None if dC is None else logical(dC, w.layout_c), logical(Ds, w.layout_d), stream)
+        hD.copy_(Ds, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(dev)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = s.elapsed_time(e) / steps
+    return {"value": round(w.flops / (ms * 1e-3) / 1e12 * world, 1),
+            "unit": "TOPS" if w.ab_type == 4 else "TFLOPS", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

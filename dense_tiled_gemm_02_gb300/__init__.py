@@ -1,0 +1,232 @@
+"""GB300 (sm_103a) tiled GEMM, D = A*B + C, behind a C ABI.
+
+This package is a thin ctypes binding over ``libgb300gemm.so`` (built from
+``csrc/`` by ``build.py``).  It only marshals arguments: every step of the
+computation runs in the library's CUDA kernels.  If the library is missing
+or cannot be loaded, importing the binding's entry points raises; there is
+no CPU fallback.
+
+Low-level names mirror ``include/gemm.h``: ``gemm_create``, ``gemm_run``,
+``gemm_get_status``, ``gemm_destroy``, ``gemm_strerror``,
+``gemm_plan_string``, ``gemm_workspace_bytes``, ``gemm_raster_tile``,
+``gemm_debug_set``.  ``Gemm`` wraps a handle for torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+GEMM_F16, GEMM_BF16, GEMM_F32, GEMM_I8, GEMM_I32 = 1, 2, 3, 4, 5
+GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = -1
+GEMM_ERR_UNSUPPORTED = -2
+GEMM_ERR_MISALIGNED = -3
+GEMM_ERR_CUDA = -4
+GEMM_ERR_DEVICE_TIMEOUT = -5
+GEMM_ERR_ALLOC_FAILED = -6
+GEMM_ERR_NO_DEVICE = -7
+GEMM_DEBUG_SKIP_FIRST_FILL = 1
+
+EXPORTED = ["gemm_create", "gemm_run", "gemm_get_status", "gemm_destroy", "gemm_strerror",
+            "gemm_plan_string", "gemm_workspace_bytes", "gemm_raster_tile", "gemm_debug_set"]
+
+
+class GemmDesc(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("ab_type", ctypes.c_int), ("c_type", ctypes.c_int), ("d_type", ctypes.c_int),
+                ("layout_a", ctypes.c_int), ("layout_b", ctypes.c_int),
+                ("layout_c", ctypes.c_int), ("layout_d", ctypes.c_int),
+                ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64),
+                ("ldd", ctypes.c_int64)]
+
+
+class GemmError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {gemm_strerror(code)} ({code})")
+        self.code = code
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_needed: bool = True) -> ctypes.CDLL:
+    """Load the CUDA library (building it first if asked); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_needed:
+        _build.build()
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError(f"CUDA library not built: {_build.LIB}")
+    lib = ctypes.CDLL(_build.LIB)
+    vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.gemm_create.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(GemmDesc)]
+    lib.gemm_create.restype = ci
+    lib.gemm_run.argtypes = [vp, vp, vp, vp, vp, vp]
+    lib.gemm_run.restype = ci
+    lib.gemm_get_status.argtypes = [vp, vp]
+    lib.gemm_get_status.restype = ci
+    lib.gemm_destroy.argtypes = [vp]
+    lib.gemm_destroy.restype = ci
+    lib.gemm_strerror.argtypes = [ci]
+    lib.gemm_strerror.restype = ctypes.c_char_p
+    lib.gemm_plan_string.argtypes = [vp, ctypes.c_char_p, ctypes.c_size_t]
+    lib.gemm_plan_string.restype = ci
+    lib.gemm_workspace_bytes.argtypes = [vp]
+    lib.gemm_workspace_bytes.restype = i64
+    lib.gemm_raster_tile.argtypes = [i64, i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    lib.gemm_raster_tile.restype = ci
+    lib.gemm_debug_set.argtypes = [vp, ci, ctypes.c_uint64]
+    lib.gemm_debug_set.restype = ci
+    _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------- the C ABI, by name
+def gemm_create(desc: GemmDesc) -> tuple[int, int | None]:
+    h = ctypes.c_void_p()
+    rc = load().gemm_create(ctypes.byref(h), ctypes.byref(desc))
+    return rc, (h.value if rc == GEMM_OK else None)
+
+
+def gemm_run(h: int, A: int, B: int, C: int | None, D: int, stream: int | None) -> int:
+    return load().gemm_run(h, A, B, C, D, stream)
+
+
+def gemm_get_status(h: int, stream: int | None) -> int:
+    return load().gemm_get_status(h, stream)
+
+
+def gemm_destroy(h: int | None) -> int:
+    return load().gemm_destroy(h)
+
+
+def gemm_strerror(code: int) -> str:
+    return load().gemm_strerror(code).decode()
+
+
+def gemm_plan_string(h: int) -> str:
+    buf = ctypes.create_string_buffer(1024)
+    load().gemm_plan_string(h, buf, len(buf))
+    return buf.value.decode()
+
+
+def gemm_workspace_bytes(h: int) -> int:
+    return load().gemm_workspace_bytes(h)
+
+
+def gemm_raster_tile(t: int, num_pid_m: int, num_pid_n: int, group_m: int):
+    pm, pn = ctypes.c_int64(), ctypes.c_int64()
+    rc = load().gemm_raster_tile(t, num_pid_m, num_pid_n, group_m, ctypes.byref(pm),
+                                 ctypes.byref(pn))
+    return rc, pm.value, pn.value
+
+
+def gemm_debug_set(h: int, flags: int, timeout_ns: int = 0) -> int:
+    return load().gemm_debug_set(h, flags, timeout_ns)
+
+
+# ---------------------------------------------------------------- torch convenience
+def _torch_type(dtype) -> int:
+    import torch
+    return {torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16, torch.float32: GEMM_F32,
+            torch.int8: GEMM_I8, torch.int32: GEMM_I32}[dtype]
+
+
+def layout_of(t) -> tuple[int, int]:
+    """(layout, ld) of a 2-D tensor that is row- or column-major strided."""
+    rows, cols = t.shape
+    s0, s1 = t.stride()
+    if s1 == 1 and (s0 >= max(cols, 1) or rows <= 1):
+        return GEMM_ROW_MAJOR, max(s0, cols, 1)
+    if s0 == 1 and (s1 >= max(rows, 1) or cols <= 1):
+        return GEMM_COL_MAJOR, max(s1, rows, 1)
+    raise ValueError(f"operand with strides {t.stride()} is neither row- nor column-major")
+
+
+class Gemm:
+    """A planned GEMM for fixed shapes, types and layouts."""
+
+    def __init__(self, desc: GemmDesc):
+        rc, h = gemm_create(desc)
+        if rc != GEMM_OK:
+            raise GemmError(rc, "gemm_create")
+        self.desc = desc
+        self.handle = h
+
+    @classmethod
+    def like(cls, A, B, C, D) -> "Gemm":
+        """Plan for the shapes, dtypes and strides of these tensors."""
+        M, K = A.shape
+        K2, N = B.shape
+        assert K == K2 and tuple(D.shape) == (M, N)
+        la, lda = layout_of(A)
+        lb, ldb = layout_of(B)
+        ld_, ldd = layout_of(D)
+        if C is not None:
+            assert tuple(C.shape) == (M, N)
+            lc, ldc = layout_of(C)
+            ct = _torch_type(C.dtype)
+        else:
+            lc, ldc, ct = GEMM_ROW_MAJOR, 0, 0
+        desc = GemmDesc(M, N, K, _torch_type(A.dtype), ct, _torch_type(D.dtype), la, lb, lc, ld_,
+                        lda, ldb, ldc, ldd)
+        return cls(desc)
+
+    def run(self, A, B, C, D, stream=None) -> None:
+        """Enqueue D = A*B + C on stream (torch.cuda.Stream or raw handle)."""
+        if stream is None:
+            import torch
+            stream = torch.cuda.current_stream()
+        s = getattr(stream, "cuda_stream", stream)
+        rc = gemm_run(self.handle, A.data_ptr(), B.data_ptr(),
+                      None if C is None else C.data_ptr(), D.data_ptr(), s)
+        if rc != GEMM_OK:
+            raise GemmError(rc, "gemm_run")
+
+    def run_ptrs(self, A: int, B: int, C: int | None, D: int, stream: int | None) -> None:
+        rc = gemm_run(self.handle, A, B, C, D, stream)
+        if rc != GEMM_OK:
+            raise GemmError(rc, "gemm_run")
+
+    def status(self, stream=None) -> int:
+        s = getattr(stream, "cuda_stream", stream)
+        return gemm_get_status(self.handle, s)
+
+    def plan(self) -> str:
+        return gemm_plan_string(self.handle)
+
+    def workspace_bytes(self) -> int:
+        return gemm_workspace_bytes(self.handle)
+
+    def close(self) -> None:
+        if self.handle is not None:
+            gemm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def matmul_add(A, B, C=None, out_dtype=None, D=None, stream=None):
+    """D = A @ B + C through the library (plans a fresh handle each call)."""
+    import torch
+    if D is None:
+        dt = out_dtype or (torch.int32 if A.dtype == torch.int8 else A.dtype)
+        D = torch.empty((A.shape[0], B.shape[1]), dtype=dt, device=A.device)
+    g = Gemm.like(A, B, C, D)
+    try:
+        g.run(A, B, C, D, stream)
+    finally:
+        g.close()
+    return D

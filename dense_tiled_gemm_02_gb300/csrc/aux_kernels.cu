@@ -1,0 +1,109 @@
+// aux_kernels.cu -- the bandwidth-bound helpers around the tensor-core kernel.
+//
+//  * splitk_reduce_kernel: sums the fp32 partial tiles of a split-K run in a
+//    fixed order (split 0, 1, ...), adds C in fp32 and stores D with one
+//    conversion.  With zero splits it computes D = C (the K = 0 case).
+//  * repack_kernel: copies an operand whose rows are not 16-byte aligned into
+//    a padded workspace that the TMA unit can read; for int8 operands it
+//    also widens every value to bf16 (exact: |v| <= 128 needs 8 bits).
+//
+// Both walk their arrays in storage order with consecutive threads on
+// consecutive addresses, in grid-stride loops sized to the SM count.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "common.h"
+
+namespace gb300 {
+
+__device__ __forceinline__ float ld_f(const void* base, int t, long long off) {
+  if (t == T_BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[off]);
+  if (t == T_F16) return __half2float(static_cast<const __half*>(base)[off]);
+  return static_cast<const float*>(base)[off];
+}
+
+__device__ __forceinline__ void st_f(void* base, int t, long long off, float v) {
+  if (t == T_BF16)
+    static_cast<__nv_bfloat16*>(base)[off] = __float2bfloat16_rn(v);
+  else if (t == T_F16)
+    static_cast<__half*>(base)[off] = __float2half_rn(v);
+  else
+    static_cast<float*>(base)[off] = v;
+}
+
+// row_order = 1: element index walks D row by row (D rows contiguous),
+// otherwise column by column.
+__global__ void splitk_reduce_kernel(const KParams p, int row_order) {
+  const long long total = static_cast<long long>(p.M) * p.N;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += stride) {
+    long long r, c;
+    if (row_order) {
+      r = idx / p.N;
+      c = idx - r * p.N;
+    } else {
+      c = idx / p.M;
+      r = idx - c * p.M;
+    }
+    if (p.d_type == T_I32) {
+      int v = 0;
+      if (p.C) v = static_cast<const int*>(p.C)[r * p.c_rs + c * p.c_cs];
+      static_cast<int*>(p.D)[r * p.d_rs + c * p.d_cs] = v;
+      continue;
+    }
+    float acc = 0.f;
+    for (int s = 0; s < p.splits; ++s) acc += p.ws[s * p.ws_split + r * p.ws_rs + c * p.ws_cs];
+    if (p.C) acc += ld_f(p.C, p.c_type, r * p.c_rs + c * p.c_cs);
+    st_f(p.D, p.d_type, r * p.d_rs + c * p.d_cs, acc);
+  }
+}
+
+// Copy rows x cols elements (storage order) from src (leading dimension
+// ld_src) to the 16-bit dst (leading dimension ld_dst).  src_type T_I8
+// widens to bf16; 16-bit types are copied bit for bit.
+__global__ void repack_kernel(const void* src, int src_type, long long ld_src, uint16_t* dst,
+                              long long ld_dst, long long rows, long long cols) {
+  const long long total = rows * cols;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += stride) {
+    const long long r = idx / cols;
+    const long long c = idx - r * cols;
+    uint16_t v;
+    if (src_type == T_I8) {
+      const __nv_bfloat16 b =
+          __float2bfloat16_rn(static_cast<float>(static_cast<const int8_t*>(src)[r * ld_src + c]));
+      v = *reinterpret_cast<const uint16_t*>(&b);
+    } else {
+      v = static_cast<const uint16_t*>(src)[r * ld_src + c];
+    }
+    dst[r * ld_dst + c] = v;
+  }
+}
+
+cudaError_t launch_reduce(const KParams& p, int row_order, int num_sms, cudaStream_t st) {
+  const long long total = static_cast<long long>(p.M) * p.N;
+  if (total == 0) return cudaSuccess;
+  long long blocks = (total + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(p, row_order);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint16_t* dst,
+                          long long ld_dst, long long rows, long long cols, int num_sms,
+                          cudaStream_t st) {
+  const long long total = rows * cols;
+  if (total == 0) return cudaSuccess;
+  long long blocks = (total + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  repack_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(src, src_type, ld_src, dst, ld_dst,
+                                                               rows, cols);
+  return cudaGetLastError();
+}
+
+}  // namespace gb300

@@ -1,0 +1,484 @@
+// gemm_host.cu -- the C ABI: validation, plan selection, workspace, tensor
+// maps and launches.  See include/gemm.h for the contract of each entry.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "common.h"
+#include "gemm.h"
+#include "plan_table.h"
+#include "tc_launch.h"
+
+using namespace gb300;
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per device-side wait
+
+int elem_size(int t) {
+  switch (t) {
+    case T_F16:
+    case T_BF16: return 2;
+    case T_F32:
+    case T_I32: return 4;
+    case T_I8: return 1;
+    default: return 0;
+  }
+}
+
+bool is_f16ish(int t) { return t == T_F16 || t == T_BF16; }
+
+// One operand as the kernel sees it: storage pointer (user's or workspace),
+// storage layout and leading dimension, logical rows x cols.
+struct Operand {
+  int layout;          // storage order of the internal operand
+  int64_t ld;          // leading dimension (elements)
+  int64_t rows, cols;  // logical extent (A': M' x K, B': K x N')
+  bool repack;         // copy into ws before the TMA can read it
+  int64_t ws_ld;       // leading dimension inside the workspace
+  size_t ws_off;       // byte offset of its workspace copy
+};
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+const TcVariant* find_variant(int bn, bool i8x) {
+  const TcVariant* tabs[3] = {kVariantsBN256, kVariantsBN128, kVariantsBN64};
+  const int counts[3] = {kNumVariantsBN256, kNumVariantsBN128, kNumVariantsBN64};
+  for (int t = 0; t < 3; ++t)
+    for (int i = 0; i < counts[t]; ++i)
+      if (tabs[t][i].bn == bn && tabs[t][i].i8x == i8x) return &tabs[t][i];
+  return nullptr;
+}
+
+}  // namespace
+
+struct gemm_plan {
+  gemm_desc_t desc;
+  int device = 0, num_sms = 0;
+  PlanChoice choice{};
+  const TcVariant* variant = nullptr;
+  bool i8x = false;
+  int mab_type = T_BF16;        // type the tensor cores read (bf16 for int8 input)
+  int64_t M = 0, N = 0, K = 0;  // internal problem
+  Operand a{}, b{};
+  int c_layout = 0, d_layout = 0;
+  int64_t ldc = 0, ldd = 0;
+  int grid = 0;
+  KParams kp{};                 // everything but pointers
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  size_t ws_partial_off = 0;
+  uint32_t* status = nullptr;
+  int debug_flags = 0;
+  uint64_t timeout_ns = kDefaultTimeoutNs;
+  // tensor-map cache
+  const void* last_a = nullptr;
+  const void* last_b = nullptr;
+  CUtensorMap tm_a{}, tm_b{};
+  std::string plan_str;
+};
+
+namespace {
+
+int64_t packed_ld(int layout, int64_t rows, int64_t cols) {
+  return layout == GEMM_ROW_MAJOR ? cols : rows;
+}
+
+bool valid_ld(int layout, int64_t ld, int64_t rows, int64_t cols) {
+  const int64_t need = packed_ld(layout, rows, cols);
+  return ld >= std::max<int64_t>(need, 1);
+}
+
+int validate(const gemm_desc_t& d) {
+  if (d.M < 0 || d.N < 0 || d.K < 0) return GEMM_ERR_INVALID_ARG;
+  if (d.M > INT32_MAX / 2 || d.N > INT32_MAX / 2 || d.K > INT32_MAX / 2) return GEMM_ERR_INVALID_ARG;
+  for (int l : {d.layout_a, d.layout_b, d.layout_c, d.layout_d})
+    if (l != GEMM_ROW_MAJOR && l != GEMM_COL_MAJOR) return GEMM_ERR_INVALID_ARG;
+  const int ab = d.ab_type, c = d.c_type, o = d.d_type;
+  if (is_f16ish(ab)) {
+    if (!(is_f16ish(o) || o == T_F32)) return GEMM_ERR_UNSUPPORTED;
+    if (!(is_f16ish(c) || c == T_F32 || c == 0)) return GEMM_ERR_UNSUPPORTED;
+  } else if (ab == T_I8) {
+    if (o != T_I32 || !(c == T_I32 || c == 0)) return GEMM_ERR_UNSUPPORTED;
+  } else {
+    return GEMM_ERR_UNSUPPORTED;
+  }
+  if (!valid_ld(d.layout_a, d.lda, d.M, d.K) || !valid_ld(d.layout_b, d.ldb, d.K, d.N) ||
+      !valid_ld(d.layout_c, d.ldc, d.M, d.N) || !valid_ld(d.layout_d, d.ldd, d.M, d.N))
+    return GEMM_ERR_INVALID_ARG;
+  return GEMM_OK;
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+void apply_force_plan(PlanChoice& c) {
+  const char* s = std::getenv("GEMM_FORCE_PLAN");
+  if (!s) return;
+  std::string str(s);
+  size_t pos = 0;
+  while (pos < str.size()) {
+    size_t end = str.find(',', pos);
+    if (end == std::string::npos) end = str.size();
+    const std::string kv = str.substr(pos, end - pos);
+    const size_t eq = kv.find('=');
+    if (eq != std::string::npos) {
+      const std::string k = kv.substr(0, eq);
+      const int v = std::atoi(kv.c_str() + eq + 1);
+      if (k == "bn") c.bn = v;
+      else if (k == "splits") c.splits = v;
+      else if (k == "group") c.group_m = v;
+      else if (k == "swap") c.swap = v;
+      else if (k == "grid") c.max_ctas = v;
+    }
+    pos = end + 1;
+  }
+}
+
+void make_plan_string(gemm_plan* h) {
+  char buf[512];
+  std::snprintf(buf, sizeof buf,
+                "M=%lld N=%lld K=%lld swap=%d bn=%d stages=%d group_m=%d splits=%d "
+                "kb_per_split=%d grid=%d i8x=%d a_mn=%d b_mn=%d repack_a=%d repack_b=%d "
+                "ws_bytes=%zu",
+                (long long)h->desc.M, (long long)h->desc.N, (long long)h->desc.K, h->choice.swap,
+                h->choice.bn, h->variant ? h->variant->stages : 0, h->kp.group_m, h->kp.splits,
+                h->kp.kb_per_split, h->grid, (int)h->i8x, h->kp.a_mn, h->kp.b_mn,
+                (int)h->a.repack, (int)h->b.repack, h->ws_bytes);
+  h->plan_str = buf;
+}
+
+// Build the tiled tensor map of an internal operand (16-bit elements).
+// K-major storage: dims {K, rows}, box {BK, box_rows}; MN-major storage:
+// dims {MN, K}, box {64, BK}; 128-byte swizzle; reads outside the tensor
+// return zeros.
+int encode_operand(CUtensorMap* tm, const void* base, int64_t ld, bool k_major, int64_t mn,
+                   int64_t K, int box_rows) {
+  EncodeFn enc = get_encode();
+  if (!enc) return GEMM_ERR_CUDA;
+  cuuint64_t dims[2], strides[1];
+  cuuint32_t box[2], estr[2] = {1, 1};
+  if (k_major) {
+    dims[0] = (cuuint64_t)K;
+    dims[1] = (cuuint64_t)mn;
+    box[0] = BK;
+    box[1] = (cuuint32_t)box_rows;
+  } else {
+    dims[0] = (cuuint64_t)mn;
+    dims[1] = (cuuint64_t)K;
+    box[0] = 64;
+    box[1] = BK;
+  }
+  strides[0] = (cuuint64_t)ld * 2;
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gemm_strerror(int s) {
+  switch (s) {
+    case GEMM_OK: return "success";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_ERR_UNSUPPORTED: return "unsupported type combination";
+    case GEMM_ERR_MISALIGNED: return "misaligned operand pointer";
+    case GEMM_ERR_CUDA: return "CUDA call or launch failed";
+    case GEMM_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait expired";
+    case GEMM_ERR_ALLOC_FAILED: return "allocation failed";
+    case GEMM_ERR_NO_DEVICE: return "no sm_103 device is current";
+    default: return "unknown status";
+  }
+}
+
+int gemm_raster_tile(int64_t t, int64_t num_pid_m, int64_t num_pid_n, int64_t group_m,
+                     int64_t* pid_m, int64_t* pid_n) {
+  if (num_pid_m <= 0 || num_pid_n <= 0 || group_m <= 0 || !pid_m || !pid_n) return GEMM_ERR_INVALID_ARG;
+  if (t < 0 || t >= num_pid_m * num_pid_n) return GEMM_ERR_INVALID_ARG;
+  raster_tile(t, num_pid_m, num_pid_n, group_m, *pid_m, *pid_n);
+  return GEMM_OK;
+}
+
+int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
+  if (!out || !desc) return GEMM_ERR_INVALID_ARG;
+  gemm_desc_t d = *desc;
+  if (d.lda == 0) d.lda = packed_ld(d.layout_a, d.M, d.K);
+  if (d.ldb == 0) d.ldb = packed_ld(d.layout_b, d.K, d.N);
+  if (d.ldc == 0) d.ldc = packed_ld(d.layout_c, d.M, d.N);
+  if (d.ldd == 0) d.ldd = packed_ld(d.layout_d, d.M, d.N);
+  int v = validate(d);
+  if (v != GEMM_OK) return v;
+
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_NO_DEVICE;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return GEMM_ERR_NO_DEVICE;
+  if (major != 10 || minor != 3) return GEMM_ERR_NO_DEVICE;
+
+  gemm_plan* h = new (std::nothrow) gemm_plan();
+  if (!h) return GEMM_ERR_ALLOC_FAILED;
+  h->desc = d;
+  h->device = dev;
+  h->num_sms = sms;
+  h->i8x = (d.ab_type == T_I8);
+  h->mab_type = h->i8x ? T_BF16 : d.ab_type;
+
+  h->choice = choose_plan(d.M, d.N, d.K, d.ab_type, d.layout_a, d.layout_b, sms);
+  apply_force_plan(h->choice);
+  if (h->i8x) {
+    h->choice.bn = 128;  // the exact-int8 variant keeps a 128-column int32 sum per thread
+    h->choice.splits = 1;
+  }
+  PlanChoice& c = h->choice;
+  const bool swap = c.swap != 0;
+  h->M = swap ? d.N : d.M;
+  h->N = swap ? d.M : d.N;
+  h->K = d.K;
+  auto flip = [](int l) { return l == GEMM_ROW_MAJOR ? GEMM_COL_MAJOR : GEMM_ROW_MAJOR; };
+  // Internal operands: A' is M' x K, B' is K x N'.  With the swap,
+  // A' = B^T and B' = A^T read the user's buffers in the other order.
+  h->a.layout = swap ? flip(d.layout_b) : d.layout_a;
+  h->a.ld = swap ? d.ldb : d.lda;
+  h->a.rows = h->M;
+  h->a.cols = h->K;
+  h->b.layout = swap ? flip(d.layout_a) : d.layout_b;
+  h->b.ld = swap ? d.lda : d.ldb;
+  h->b.rows = h->K;
+  h->b.cols = h->N;
+  h->c_layout = swap ? flip(d.layout_c) : d.layout_c;
+  h->d_layout = swap ? flip(d.layout_d) : d.layout_d;
+  h->ldc = d.ldc;
+  h->ldd = d.ldd;
+
+  h->variant = find_variant(c.bn, h->i8x);
+  if (!h->variant) {
+    delete h;
+    return GEMM_ERR_UNSUPPORTED;
+  }
+
+  // Tile grid and K split.
+  KParams& kp = h->kp;
+  kp.M = (int)h->M;
+  kp.N = (int)h->N;
+  kp.K = (int)h->K;
+  kp.tiles_m = (int)((h->M + BM - 1) / BM);
+  kp.tiles_n = (int)((h->N + c.bn - 1) / c.bn);
+  kp.group_m = std::max(1, std::min(c.group_m, kp.tiles_m));
+  kp.num_kb = (int)((h->K + BK - 1) / BK);
+  int splits = std::max(1, std::min(c.splits, std::max(1, kp.num_kb)));
+  kp.kb_per_split = kp.num_kb > 0 ? (kp.num_kb + splits - 1) / splits : 0;
+  if (kp.kb_per_split > 0) splits = (kp.num_kb + kp.kb_per_split - 1) / kp.kb_per_split;
+  kp.splits = splits;
+  c.splits = splits;
+  kp.kb_per_chunk = h->i8x ? 8 : std::max(1, kp.num_kb);  // int8: 512 K per exact fp32 pass
+  kp.a_mn = h->a.layout == GEMM_COL_MAJOR ? 1 : 0;  // A' contiguous along M'
+  kp.b_mn = h->b.layout == GEMM_ROW_MAJOR ? 1 : 0;  // B' contiguous along N'
+  kp.idesc = idesc_f16(h->mab_type == T_BF16 ? 1u : 0u, (uint32_t)kp.a_mn, (uint32_t)kp.b_mn,
+                       BM, (uint32_t)c.bn);
+  kp.c_type = d.c_type;
+  kp.d_type = d.d_type;
+  kp.c_rs = h->c_layout == GEMM_ROW_MAJOR ? h->ldc : 1;
+  kp.c_cs = h->c_layout == GEMM_ROW_MAJOR ? 1 : h->ldc;
+  kp.d_rs = h->d_layout == GEMM_ROW_MAJOR ? h->ldd : 1;
+  kp.d_cs = h->d_layout == GEMM_ROW_MAJOR ? 1 : h->ldd;
+  const int64_t units = (int64_t)kp.tiles_m * kp.tiles_n * kp.splits;
+  int max_ctas = sms;
+  if (c.max_ctas > 0) max_ctas = std::min(max_ctas, c.max_ctas);
+  h->grid = (int)std::max<int64_t>(1, std::min<int64_t>(units, max_ctas));
+
+  // Workspace: operand copies the TMA unit can read, then split-K partials.
+  size_t off = 0;
+  auto plan_copy = [&](Operand& o, bool k_major, int64_t in_es) {
+    const int64_t inner = o.layout == GEMM_ROW_MAJOR ? o.cols : o.rows;
+    const int64_t outer = o.layout == GEMM_ROW_MAJOR ? o.rows : o.cols;
+    (void)k_major;
+    o.repack = h->i8x || ((o.ld * in_es) % 16 != 0);
+    if (!o.repack) return;
+    o.ws_ld = round_up(std::max<int64_t>(inner, 1), 8);
+    o.ws_off = off;
+    off += (size_t)round_up(o.ws_ld * outer * 2, 256);
+  };
+  const int64_t in_es = elem_size(d.ab_type);
+  plan_copy(h->a, kp.a_mn == 0, in_es);
+  plan_copy(h->b, kp.b_mn == 1, in_es);
+  if (kp.splits > 1) {
+    h->ws_partial_off = off;
+    off += (size_t)round_up((int64_t)kp.splits * h->M * h->N * 4, 256);
+    const bool row = h->d_layout == GEMM_ROW_MAJOR;
+    kp.ws_rs = row ? h->N : 1;
+    kp.ws_cs = row ? 1 : h->M;
+    kp.ws_split = h->M * h->N;
+  }
+  h->ws_bytes = off;
+  if (off > 0 && cudaMalloc(&h->ws, off) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return GEMM_ERR_ALLOC_FAILED;
+  }
+  if (cudaMalloc(&h->status, 256) != cudaSuccess || cudaMemset(h->status, 0, 256) != cudaSuccess) {
+    cudaGetLastError();
+    if (h->ws) cudaFree(h->ws);
+    delete h;
+    return GEMM_ERR_ALLOC_FAILED;
+  }
+  if (h->variant->prepare() != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->status);
+    if (h->ws) cudaFree(h->ws);
+    delete h;
+    return GEMM_ERR_CUDA;
+  }
+  make_plan_string(h);
+  const char* lg = std::getenv("GEMM_LOG");
+  if (lg && lg[0] == '1') std::fprintf(stderr, "[gemm] plan: %s\n", h->plan_str.c_str());
+  *out = h;
+  return GEMM_OK;
+}
+
+int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
+             gemm_stream_t stream) {
+  if (!h || !D || (h->desc.K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
+  const gemm_desc_t& d = h->desc;
+  const int es_ab = elem_size(d.ab_type);
+  const int es_c = elem_size(d.c_type);
+  const int es_d = elem_size(d.d_type);
+  auto mis = [](const void* p, int a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; };
+  if ((A && mis(A, es_ab)) || (B && mis(B, es_ab)) || (C && mis(C, es_c)) || mis(D, es_d))
+    return GEMM_ERR_MISALIGNED;
+  if (C && d.c_type == 0) return GEMM_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) return GEMM_ERR_INVALID_ARG;
+  if (d.M == 0 || d.N == 0) return GEMM_OK;
+
+  KParams kp = h->kp;
+  kp.C = C;
+  kp.D = D;
+  kp.status = h->status;
+  kp.timeout_ns = h->timeout_ns;
+  kp.debug_flags = h->debug_flags;
+  h->debug_flags = 0;  // test hooks apply to one run
+  kp.c_vec = (C && kp.c_cs == 1 && (reinterpret_cast<uintptr_t>(C) % 16) == 0 &&
+              (kp.c_rs * es_c) % 16 == 0) ? 1 : 0;
+  kp.d_vec = (kp.d_cs == 1 && (reinterpret_cast<uintptr_t>(D) % 16) == 0 &&
+              (kp.d_rs * es_d) % 16 == 0) ? 1 : 0;
+  const bool row_order = h->d_layout == GEMM_ROW_MAJOR;
+
+  if (d.K == 0) {  // D = C
+    kp.splits = 0;
+    return launch_reduce(kp, row_order, h->num_sms, st) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  }
+
+  const bool swap = h->choice.swap != 0;
+  const void* pa = swap ? B : A;  // storage of A'
+  const void* pb = swap ? A : B;  // storage of B'
+  const void* ta = pa;
+  const void* tb = pb;
+  char* ws = static_cast<char*>(h->ws);
+  // Operands the TMA unit cannot read in place go through the workspace.
+  for (int which = 0; which < 2; ++which) {
+    Operand& o = which == 0 ? h->a : h->b;
+    const void* src = which == 0 ? pa : pb;
+    const bool need = o.repack || mis(src, 16);
+    if (!need) continue;
+    if (!o.repack) return GEMM_ERR_MISALIGNED;  // no workspace was planned for this operand
+    const int64_t inner = o.layout == GEMM_ROW_MAJOR ? o.cols : o.rows;
+    const int64_t outer = o.layout == GEMM_ROW_MAJOR ? o.rows : o.cols;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(ws + o.ws_off);
+    if (launch_repack(src, d.ab_type, o.ld, dst, o.ws_ld, outer, inner, h->num_sms, st) !=
+        cudaSuccess)
+      return GEMM_ERR_CUDA;
+    (which == 0 ? ta : tb) = dst;
+  }
+  const int64_t lda_eff = h->a.repack ? h->a.ws_ld : h->a.ld;
+  const int64_t ldb_eff = h->b.repack ? h->b.ws_ld : h->b.ld;
+
+  if (ta != h->last_a) {
+    if (encode_operand(&h->tm_a, ta, lda_eff, kp.a_mn == 0, h->M, h->K, BM) != GEMM_OK) {
+      h->last_a = nullptr;
+      return GEMM_ERR_CUDA;
+    }
+    h->last_a = ta;
+  }
+  if (tb != h->last_b) {
+    if (encode_operand(&h->tm_b, tb, ldb_eff, kp.b_mn == 0, h->N, h->K, h->choice.bn) != GEMM_OK) {
+      h->last_b = nullptr;
+      return GEMM_ERR_CUDA;
+    }
+    h->last_b = tb;
+  }
+  if (kp.splits > 1) kp.ws = reinterpret_cast<float*>(ws + h->ws_partial_off);
+  if (h->variant->launch(h->tm_a, h->tm_b, kp, h->grid, st) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (kp.splits > 1 && launch_reduce(kp, row_order, h->num_sms, st) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  return GEMM_OK;
+}
+
+int gemm_get_status(gemm_handle_t h, gemm_stream_t stream) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (cudaMemcpy(&word, h->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  if (word != 0 && cudaMemset(h->status, 0, sizeof word) != cudaSuccess) return GEMM_ERR_CUDA;
+  return (word & STATUS_TIMEOUT) ? GEMM_ERR_DEVICE_TIMEOUT : GEMM_OK;
+}
+
+int gemm_destroy(gemm_handle_t h) {
+  if (!h) return GEMM_OK;
+  int rc = GEMM_OK;
+  if (cudaDeviceSynchronize() != cudaSuccess) rc = GEMM_ERR_CUDA;
+  if (h->ws) cudaFree(h->ws);
+  if (h->status) cudaFree(h->status);
+  delete h;
+  return rc;
+}
+
+int gemm_plan_string(gemm_handle_t h, char* buf, size_t n) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  if (buf && n > 0) {
+    std::strncpy(buf, h->plan_str.c_str(), n - 1);
+    buf[n - 1] = '\0';
+  }
+  return (int)h->plan_str.size();
+}
+
+int64_t gemm_workspace_bytes(gemm_handle_t h) { return h ? (int64_t)h->ws_bytes : -1; }
+
+int gemm_debug_set(gemm_handle_t h, int flags, uint64_t timeout_ns) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  h->debug_flags = flags;
+  h->timeout_ns = timeout_ns ? timeout_ns : kDefaultTimeoutNs;
+  return GEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// plan_table.h -- per-shape choice of tile width, raster group, split-K and
+// operand swap.
+//
+// The selection key is the whole problem (M, N, K, operand type, layouts):
+// a key that leaves out a dimension silently serves a tile tuned for another
+// shape ("Tuning Triton" skill page, section 3, where a decode shape reusing
+// the square-shape tile ran several times slower).  Rows of kTable come from
+// the measured sweep of the tuning script (bench.py --sweep); shapes without
+// a row fall back to the rules in choose_plan(), which follow the regime
+// split of that page's section 4 (skinny shapes get their own candidates).
+#pragma once
+
+#include <cstdint>
+
+namespace gb300 {
+
+struct PlanChoice {
+  int bn;        // output tile width (64, 128 or 256); tile height is BM = 128
+  int group_m;   // GROUP_M of the grouped raster
+  int splits;    // split-K factor (1 = none)
+  int swap;      // 1: compute D^T = B^T A^T (long dimension on the tensor-core M side)
+  int max_ctas;  // 0 = one CTA per SM
+};
+
+struct PlanRow {
+  int64_t M, N, K;
+  int ab_type, layout_a, layout_b;  // -1 = any
+  PlanChoice choice;
+};
+
+// Measured rows (exact shape match).
+static const PlanRow kTable[] = {
+    {0, 0, 0, -1, -1, -1, {0, 0, 0, 0, 0}},  // sentinel
+};
+
+inline int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline PlanChoice choose_plan(int64_t M, int64_t N, int64_t K, int ab_type, int layout_a,
+                              int layout_b, int num_sms) {
+  for (const PlanRow& r : kTable) {
+    if (r.M == M && r.N == N && r.K == K && (r.ab_type < 0 || r.ab_type == ab_type) &&
+        (r.layout_a < 0 || r.layout_a == layout_a) && (r.layout_b < 0 || r.layout_b == layout_b))
+      return r.choice;
+  }
+  PlanChoice c{256, 8, 1, 0, 0};
+  // Skinny M: put the long N dimension on the 128-row tensor-core side.
+  if (M < 128 && N >= 2 * M) c.swap = 1;
+  const int64_t Mi = c.swap ? N : M;
+  const int64_t Ni = c.swap ? M : N;
+  // Tile width: the widest tile that still gives every SM a tile, else the
+  // one with the most tiles in flight.
+  const int64_t tm = cdiv64(Mi, 128);
+  if (Ni <= 64) c.bn = 64;
+  else if (Ni <= 128) c.bn = 128;
+  else if (tm * cdiv64(Ni, 256) >= num_sms) c.bn = 256;
+  else if (tm * cdiv64(Ni, 128) >= num_sms / 2) c.bn = 128;
+  else c.bn = 64;
+  const int64_t tiles = tm * cdiv64(Ni, c.bn);
+  // Split K when the tiles alone leave most SMs idle and K is long.
+  const int64_t kb = cdiv64(K, 64);
+  if (tiles * 2 <= num_sms && kb >= 16) {
+    int64_t s = num_sms / tiles;
+    if (s > kb / 8) s = kb / 8;
+    if (s > 8) s = 8;
+    if (s < 1) s = 1;
+    c.splits = (int)s;
+  }
+  return c;
+}
+
+}  // namespace gb300

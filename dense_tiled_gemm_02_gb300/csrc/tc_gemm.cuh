@@ -1,0 +1,462 @@
+// tc_gemm.cuh -- the warp-specialised, persistent tcgen05 GEMM kernel.
+//
+// One CTA of 192 threads per SM walks output tiles in the grouped order
+// (FlagGems "Hygon optimization": grouped scheduling for L2 reuse of B):
+//
+//   warp 0  (one lane) TMA producer: for every BK-slice of K, waits for a
+//           free stage of the shared-memory ring, then loads the BM x BK
+//           slice of A and the BK x BN slice of B into it.  Loads beyond M,
+//           N or K read zeros (the masked K tail of the "Hopper Support in
+//           Triton" slides 14-15, done here by the TMA unit).
+//   warp 1  (one lane) MMA issuer: waits for a full stage, issues BK/16
+//           tcgen05.mma (fp16/bf16 in, fp32 accumulator in tensor memory),
+//           and commits the stage back to the producer.  This is the
+//           "accumulator += dot(a, b)" K-loop of slide 5, software-pipelined
+//           against the loads (the FlagGems page's num_stages).
+//   warps 2-5 epilogue: wait for a finished accumulator, read it from tensor
+//           memory, add C in fp32, convert once and store with M/N masks
+//           (D = sum + C, forum.sourcefind.cn "DCU K100" article, 5.2).
+//
+// Two accumulator buffers in tensor memory let the epilogue of one tile run
+// under the main loop of the next.  Every wait is bounded (ptx.cuh).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.h"
+#include "ptx.cuh"
+
+namespace gb300 {
+
+template <int BN>
+struct TileCfg {
+  static constexpr uint32_t A_BYTES = BM * BK * 2;       // 16 KiB
+  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;          // two fp32 accumulators
+  static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
+};
+
+template <int BN, int STAGES>
+constexpr uint32_t smem_bytes() {
+  // ring + barriers/flags + slack to align the ring to 1024 bytes
+  return STAGES * TileCfg<BN>::STAGE_TX + 256 + 1024;
+}
+
+struct Unit {
+  int m0, n0, kb0, kb1, split;
+};
+
+__device__ __forceinline__ Unit decode_unit(const KParams& p, int u, int bn) {
+  Unit w;
+  const int t = u / p.splits;
+  w.split = u - t * p.splits;
+  int64_t pm, pn;
+  raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
+  w.m0 = static_cast<int>(pm) * BM;
+  w.n0 = static_cast<int>(pn) * bn;
+  w.kb0 = w.split * p.kb_per_split;
+  w.kb1 = min(p.num_kb, w.kb0 + p.kb_per_split);
+  return w;
+}
+
+// ------------------------------------------------------------------ epilogue helpers
+__device__ __forceinline__ float load_elem_f(const void* base, int t, long long off) {
+  if (t == T_BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[off]);
+  if (t == T_F16) return __half2float(static_cast<const __half*>(base)[off]);
+  return static_cast<const float*>(base)[off];
+}
+
+__device__ __forceinline__ void store_elem_f(void* base, int t, long long off, float v) {
+  if (t == T_BF16)
+    static_cast<__nv_bfloat16*>(base)[off] = __float2bfloat16_rn(v);
+  else if (t == T_F16)
+    static_cast<__half*>(base)[off] = __float2half_rn(v);
+  else
+    static_cast<float*>(base)[off] = v;
+}
+
+__device__ __forceinline__ uint32_t pack2(int t, float lo, float hi) {
+  if (t == T_BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void unpack2(int t, uint32_t w, float& lo, float& hi) {
+  if (t == T_BF16) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w);
+    lo = __low2float(h);
+    hi = __high2float(h);
+  } else {
+    __half2 h = *reinterpret_cast<__half2*>(&w);
+    lo = __low2float(h);
+    hi = __high2float(h);
+  }
+}
+
+// Add C to 32 consecutive outputs of row r starting at column c0.
+__device__ __forceinline__ void add_c_f(const KParams& p, int r, int c0, float (&f)[32]) {
+  if (p.C == nullptr || r >= p.M) return;
+  if (p.c_vec && c0 + 32 <= p.N) {
+    if (p.c_type == T_F32) {
+      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.C) +
+                                                          r * p.c_rs + c0);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const float4 x = src[v];
+        f[4 * v] += x.x;
+        f[4 * v + 1] += x.y;
+        f[4 * v + 2] += x.z;
+        f[4 * v + 3] += x.w;
+      }
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          static_cast<const uint16_t*>(p.C) + r * p.c_rs + c0);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const uint4 x = src[v];
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float lo, hi;
+          unpack2(p.c_type, w[e], lo, hi);
+          f[8 * v + 2 * e] += lo;
+          f[8 * v + 2 * e + 1] += hi;
+        }
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int c = c0 + j;
+    if (c < p.N) f[j] += load_elem_f(p.C, p.c_type, r * p.c_rs + c * p.c_cs);
+  }
+}
+
+// Convert and store 32 consecutive outputs of row r starting at column c0.
+__device__ __forceinline__ void store_d_f(const KParams& p, int r, int c0, const float (&f)[32]) {
+  if (r >= p.M) return;
+  if (p.d_vec && c0 + 32 <= p.N) {
+    if (p.d_type == T_F32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.D) + r * p.d_rs + c0);
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        dst[v] = make_float4(f[4 * v], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]);
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.D) + r * p.d_rs + c0);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        uint4 x;
+        x.x = pack2(p.d_type, f[8 * v + 0], f[8 * v + 1]);
+        x.y = pack2(p.d_type, f[8 * v + 2], f[8 * v + 3]);
+        x.z = pack2(p.d_type, f[8 * v + 4], f[8 * v + 5]);
+        x.w = pack2(p.d_type, f[8 * v + 6], f[8 * v + 7]);
+        dst[v] = x;
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int c = c0 + j;
+    if (c < p.N) store_elem_f(p.D, p.d_type, r * p.d_rs + c * p.d_cs, f[j]);
+  }
+}
+
+// Raw fp32 partial sums of one split into the workspace.
+__device__ __forceinline__ void store_partial(const KParams& p, int r, int c0, int split,
+                                              const float (&f)[32]) {
+  if (r >= p.M) return;
+  float* base = p.ws + split * p.ws_split;
+  if (p.ws_cs == 1 && c0 + 32 <= p.N) {
+    float4* dst = reinterpret_cast<float4*>(base + r * p.ws_rs + c0);
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+      dst[v] = make_float4(f[4 * v], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]);
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int c = c0 + j;
+    if (c < p.N) base[r * p.ws_rs + c * p.ws_cs] = f[j];
+  }
+}
+
+// Exact-int8 mode: add int32 C and store int32 D.
+__device__ __forceinline__ void store_d_i32(const KParams& p, int r, int c0, int (&s)[32]) {
+  if (r >= p.M) return;
+  const int32_t* C = static_cast<const int32_t*>(p.C);
+  int32_t* D = static_cast<int32_t*>(p.D);
+  if (p.d_vec && c0 + 32 <= p.N && (C == nullptr || p.c_vec)) {
+    if (C) {
+      const int4* src = reinterpret_cast<const int4*>(C + r * p.c_rs + c0);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const int4 x = src[v];
+        s[4 * v] += x.x;
+        s[4 * v + 1] += x.y;
+        s[4 * v + 2] += x.z;
+        s[4 * v + 3] += x.w;
+      }
+    }
+    int4* dst = reinterpret_cast<int4*>(D + r * p.d_rs + c0);
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+      dst[v] = make_int4(s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int c = c0 + j;
+    if (c < p.N) {
+      int v = s[j];
+      if (C) v += C[r * p.c_rs + c * p.c_cs];
+      D[r * p.d_rs + c * p.d_cs] = v;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+// I8X: exact-int8 mode.  Operands are int8 values held exactly in bf16; the
+// fp32 accumulator is drained to int32 every kb_per_chunk k-blocks, while its
+// magnitude is still below 2^24 and every partial sum is an exact integer.
+template <int BN, int STAGES, bool I8X>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const KParams p) {
+  using Cfg = TileCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * Cfg::B_BYTES);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](uint32_t s) { return bar0 + 8u * s; };
+  auto empty = [&](uint32_t s) { return bar0 + 8u * (STAGES + s); };
+  auto acc_full = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto acc_empty = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 128);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int num_units = p.tiles_m * p.tiles_n * p.splits;
+  const uint64_t tmo = p.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      int64_t skipped = -1;
+      bool stop = false;
+      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
+        const Unit w = decode_unit(p, u, BN);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!bounded_wait(empty(s), ph ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
+            stop = true;
+            break;
+          }
+          if ((p.debug_flags & DBG_SKIP_FIRST_FILL) && it == 0) {
+            skipped = 0;  // test hook: leave stage 0 empty so its consumer times out
+            ++it;
+            continue;
+          }
+          mbar_arrive_expect_tx(full(s), Cfg::STAGE_TX);
+          const uint32_t a_dst = smem_u32(sA + s * Cfg::A_BYTES);
+          const uint32_t b_dst = smem_u32(sB + s * Cfg::B_BYTES);
+          const int k0 = kb * BK;
+          if (!p.a_mn) {
+            tma_load_2d(a_dst, &tmA, k0, w.m0, full(s));
+          } else {
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j)
+              tma_load_2d(a_dst + j * 8192u, &tmA, w.m0 + 64 * j, k0, full(s));
+          }
+          if (!p.b_mn) {
+            tma_load_2d(b_dst, &tmB, k0, w.n0, full(s));
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(b_dst + j * 8192u, &tmB, w.n0 + 64 * j, k0, full(s));
+          }
+          ++it;
+        }
+      }
+      // Let every copy still in flight land before the CTA can exit.
+      for (uint32_t j = it > STAGES ? it - STAGES : 0; j < it; ++j) {
+        if (static_cast<int64_t>(j) == skipped) continue;
+        drain_wait(full(j % STAGES), (j / STAGES) & 1u, 200000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, acc_it = 0, buf = 0;
+      bool stop = false;
+      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
+        const Unit w = decode_unit(p, u, BN);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          const int kc = (kb - w.kb0) % p.kb_per_chunk;
+          if (kc == 0) {
+            buf = acc_it & 1u;
+            if (!bounded_wait(acc_empty(buf), ((acc_it >> 1) & 1u) ^ 1u, abort_flag, p.status,
+                              STATUS_TIMEOUT, tmo)) {
+              stop = true;
+              break;
+            }
+            tc_fence_after();
+          }
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!bounded_wait(full(s), ph, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + s * Cfg::A_BYTES);
+          const uint32_t b_addr = smem_u32(sB + s * Cfg::B_BYTES);
+          const uint32_t d_tmem = tmem_base + buf * BN;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // K-major: the 16-element K step moves 32 bytes inside the
+            // swizzled 128-byte rows; MN-major: it moves 16 rows of 128 B.
+            const uint64_t ad = p.a_mn ? smem_desc_sw128(a_addr + kk * 2048u, 8192u, 1024u)
+                                       : smem_desc_sw128(a_addr + kk * 32u, 16u, 1024u);
+            const uint64_t bd = p.b_mn ? smem_desc_sw128(b_addr + kk * 2048u, 8192u, 1024u)
+                                       : smem_desc_sw128(b_addr + kk * 32u, 16u, 1024u);
+            mma_f16_ss(d_tmem, ad, bd, p.idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(empty(s));
+          ++it;
+          if (kc == p.kb_per_chunk - 1 || kb == w.kb1 - 1) {
+            mma_commit(acc_full(buf));
+            ++acc_it;
+          }
+        }
+      }
+      // Every MMA issued so far must finish before tensor memory is freed.
+      mma_commit(done_bar);
+      drain_wait(done_bar, 0, 200000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // the tensor-memory lane quarter this warp may read
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t acc_it = 0;
+    bool stop = false;
+    for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
+      const Unit w = decode_unit(p, u, BN);
+      const int r = w.m0 + q * 32 + lane;
+      if constexpr (!I8X) {
+        const uint32_t buf = acc_it & 1u;
+        if (!bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status,
+                          STATUS_TIMEOUT, tmo)) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_base + lane_base + buf * BN + c * 32, v);
+          tmem_ld_wait();
+          if (c == BN / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(acc_empty(buf));
+          }
+          float f[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+          const int c0 = w.n0 + c * 32;
+          if (p.splits > 1) {
+            store_partial(p, r, c0, w.split, f);
+          } else {
+            add_c_f(p, r, c0, f);
+            store_d_f(p, r, c0, f);
+          }
+        }
+        ++acc_it;
+      } else {
+        int isum[BN];
+#pragma unroll
+        for (int j = 0; j < BN; ++j) isum[j] = 0;
+        const int nchunks = (w.kb1 - w.kb0 + p.kb_per_chunk - 1) / p.kb_per_chunk;
+        for (int ch = 0; ch < nchunks; ++ch) {
+          const uint32_t buf = acc_it & 1u;
+          if (!bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status,
+                            STATUS_TIMEOUT, tmo)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem_base + lane_base + buf * BN + c * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) isum[c * 32 + j] += __float2int_rn(__uint_as_float(v[j]));
+          }
+          tc_fence_before();
+          mbar_arrive(acc_empty(buf));
+          ++acc_it;
+        }
+        if (stop) break;
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          int s[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s[j] = isum[c * 32 + j];
+          store_d_i32(p, r, w.n0 + c * 32, s);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+}  // namespace gb300

@@ -1,0 +1,47 @@
+// tc_launch.cu -- instantiations and launchers of the tcgen05 GEMM kernel.
+// Compiled once per tile width (TC_BN) so that the instantiations build in
+// parallel.
+#include <cuda_runtime.h>
+
+#include "tc_gemm.cuh"
+#include "tc_launch.h"
+
+#ifndef TC_BN
+#error "TC_BN must be defined"
+#endif
+
+namespace gb300 {
+
+namespace {
+template <int BN, int STAGES, bool I8X>
+cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b, const KParams& p, int grid,
+                        cudaStream_t st) {
+  constexpr uint32_t smem = smem_bytes<BN, STAGES>();
+  tc_gemm_kernel<BN, STAGES, I8X><<<grid, NUM_THREADS, smem, st>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+template <int BN, int STAGES, bool I8X>
+cudaError_t prepare_impl() {
+  constexpr uint32_t smem = smem_bytes<BN, STAGES>();
+  return cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES, I8X>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+}  // namespace
+
+#define GB_VARIANT(BN_, ST_, I8_)                                                         \
+  TcVariant{BN_, ST_, I8_, smem_bytes<BN_, ST_>(), &launch_impl<BN_, ST_, I8_>,          \
+            &prepare_impl<BN_, ST_, I8_>}
+
+#if TC_BN == 256
+const TcVariant kVariantsBN256[] = {GB_VARIANT(256, 4, false)};
+const int kNumVariantsBN256 = 1;
+#elif TC_BN == 128
+const TcVariant kVariantsBN128[] = {GB_VARIANT(128, 6, false), GB_VARIANT(128, 6, true)};
+const int kNumVariantsBN128 = 2;
+#elif TC_BN == 64
+const TcVariant kVariantsBN64[] = {GB_VARIANT(64, 8, false)};
+const int kNumVariantsBN64 = 1;
+#endif
+
+}  // namespace gb300

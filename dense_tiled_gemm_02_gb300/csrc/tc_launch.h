@@ -1,0 +1,33 @@
+// tc_launch.h -- host-side view of the compiled tcgen05 kernel variants.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.h"
+
+namespace gb300 {
+
+struct TcVariant {
+  int bn;
+  int stages;
+  bool i8x;
+  uint32_t smem;
+  cudaError_t (*launch)(const CUtensorMap&, const CUtensorMap&, const KParams&, int grid,
+                        cudaStream_t);
+  cudaError_t (*prepare)();  // sets the dynamic shared-memory limit on the current device
+};
+
+extern const TcVariant kVariantsBN256[];
+extern const int kNumVariantsBN256;
+extern const TcVariant kVariantsBN128[];
+extern const int kNumVariantsBN128;
+extern const TcVariant kVariantsBN64[];
+extern const int kNumVariantsBN64;
+
+cudaError_t launch_reduce(const KParams& p, int row_order, int num_sms, cudaStream_t st);
+cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint16_t* dst,
+                          long long ld_dst, long long rows, long long cols, int num_sms,
+                          cudaStream_t st);
+
+}  // namespace gb300

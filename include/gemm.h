@@ -1,0 +1,159 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) tiled GEMM library.
+ *
+ * One operation:  D = A * B + C
+ *   A is M x K, B is K x N, C and D are M x N; any operand may be stored
+ *   row-major or column-major with its own leading dimension.
+ *
+ * The operation is the matrix multiply-accumulate of the plain HIP kernel
+ * "MatMulAdd_kernel2" (forum.sourcefind.cn, "DCU K100 ..." article, section
+ * 5.2: each output is the K-sum of products plus C, with a column-major A and
+ * a row-major B), computed the way the Triton "matmul_kernel" of the "Hopper
+ * Support in Triton" slides does it (slide 5: BLOCK_M x BLOCK_N output tiles,
+ * a loop over BLOCK_K slices into an fp32 accumulator, one conversion on
+ * store), with the masked K tail of slides 14-15 (loads beyond K read zero)
+ * and the GROUP_M tile order of the FlagGems "Hygon optimization" page
+ * ("Grouped scheduling: improve L2 data reuse").
+ *
+ * Supported type combinations (ab_type, c_type, d_type):
+ *   (F16|BF16, F16|BF16|F32 or C absent, F16|BF16|F32): fp32 accumulation,
+ *       C widened to fp32 and added to the fp32 sum, one round-to-nearest-
+ *       even conversion to d_type.
+ *   (I8, I32 or C absent, I32): exact integer result (int32).
+ *
+ * Device pointers, caller-owned.  Every call is asynchronous on the given
+ * stream.  All sizes are element counts.
+ */
+#ifndef GB300_GEMM_H
+#define GB300_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GEMM_API __attribute__((visibility("default")))
+#else
+#define GEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. */
+typedef enum {
+  GEMM_F16 = 1,
+  GEMM_BF16 = 2,
+  GEMM_F32 = 3,
+  GEMM_I8 = 4,
+  GEMM_I32 = 5
+} gemm_dtype_t;
+
+/* Storage order: row-major X[r,c] = X[r*ld + c]; column-major X[r + c*ld]. */
+typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_layout_t;
+
+/* Status codes (0 = success, negative = failure). */
+enum {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_ARG = -1,    /* a size, leading dimension or pointer is invalid */
+  GEMM_ERR_UNSUPPORTED = -2,    /* type combination not supported */
+  GEMM_ERR_MISALIGNED = -3,     /* an operand pointer is not aligned to its element size */
+  GEMM_ERR_CUDA = -4,           /* a CUDA runtime/driver call or a launch failed */
+  GEMM_ERR_DEVICE_TIMEOUT = -5, /* a bounded device-side wait expired (see gemm_get_status) */
+  GEMM_ERR_ALLOC_FAILED = -6,   /* device or host allocation failed */
+  GEMM_ERR_NO_DEVICE = -7       /* no sm_103 device is current */
+};
+
+/* Problem description.  ld* = 0 means packed (K or M for A, N or K for B,
+ * N or M for C/D, by layout).  A leading dimension smaller than the packed
+ * one is rejected.  c_type = 0 declares that C is always absent. */
+typedef struct {
+  int64_t M, N, K;
+  gemm_dtype_t ab_type, c_type, d_type;
+  gemm_layout_t layout_a, layout_b, layout_c, layout_d;
+  int64_t lda, ldb, ldc, ldd;
+} gemm_desc_t;
+
+typedef struct gemm_plan* gemm_handle_t;
+
+/* cudaStream_t without the CUDA headers: pass the stream handle (NULL = the
+ * legacy default stream). */
+typedef void* gemm_stream_t;
+
+/*
+ * gemm_create: validate desc, choose a plan (tile, stage count, raster
+ * group, split-K, operand swap, repack) from the measured selection table
+ * keyed on (M, N, K, types, layouts), and allocate on the current device the
+ * workspace and the device status word that the plan needs.
+ *   out:  receives the handle (untouched on failure).
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED,
+ * GEMM_ERR_NO_DEVICE, GEMM_ERR_ALLOC_FAILED or GEMM_ERR_CUDA.
+ * Environment: GEMM_LOG=1 prints the chosen plan to stderr;
+ * GEMM_FORCE_PLAN="bn=128,splits=2,group=8,swap=1" overrides fields of the
+ * plan (for tuning sweeps).
+ */
+GEMM_API int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc);
+
+/*
+ * gemm_run: enqueue D = A*B + C on stream.  Never allocates and never
+ * synchronises.  A, B, D must be non-NULL device pointers aligned to their
+ * element size (more alignment enables faster paths); C may be NULL, which
+ * means C = 0 and C is not read.  D may alias C only when both have the same
+ * type, layout and leading dimension; D must not overlap A or B.
+ * One handle must not be used by two streams at the same time (its
+ * workspace and status word are shared by its calls).
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_MISALIGNED or
+ * GEMM_ERR_CUDA (launch failure).  Device-side failures are reported by
+ * gemm_get_status.
+ */
+GEMM_API int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
+             gemm_stream_t stream);
+
+/*
+ * gemm_get_status: synchronise stream, then return and clear the device
+ * status word of h: GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT when a kernel of an
+ * earlier gemm_run gave up a bounded wait (its D is then undefined).
+ * Returns GEMM_ERR_CUDA if the synchronisation itself fails.
+ */
+GEMM_API int gemm_get_status(gemm_handle_t h, gemm_stream_t stream);
+
+/* gemm_destroy: free the handle's workspace and status word (after
+ * synchronising the device work that may still use them).  NULL is a no-op. */
+GEMM_API int gemm_destroy(gemm_handle_t h);
+
+/* gemm_strerror: static description of a status code. */
+GEMM_API const char* gemm_strerror(int status);
+
+/* gemm_plan_string: write a one-line description of the plan of h into buf
+ * (at most n bytes including the terminator).  Returns the full length. */
+GEMM_API int gemm_plan_string(gemm_handle_t h, char* buf, size_t n);
+
+/* gemm_workspace_bytes: device workspace held by h (bytes), or -1. */
+GEMM_API int64_t gemm_workspace_bytes(gemm_handle_t h);
+
+/*
+ * gemm_raster_tile: the grouped tile order, exported for host-side tests.
+ * Maps the 1-D tile index t to (pid_m, pid_n) so that GROUP_M consecutive
+ * tile rows share a column of B while they are in L2 (FlagGems "Hygon
+ * optimization", "Grouped scheduling"); the final group is clamped to the
+ * tile rows that remain.  Returns 0, or GEMM_ERR_INVALID_ARG when t is
+ * outside [0, num_pid_m * num_pid_n) or a count is not positive.
+ */
+GEMM_API int gemm_raster_tile(int64_t t, int64_t num_pid_m, int64_t num_pid_n, int64_t group_m,
+                     int64_t* pid_m, int64_t* pid_n);
+
+/*
+ * Test hooks (not for production use).
+ * gemm_debug_set: flags bit 0 makes the load warp of the next gemm_run skip
+ * its first stage fill, so that the consumer's bounded wait expires and the
+ * kernel exits with GEMM_ERR_DEVICE_TIMEOUT; timeout_ns (0 = default, two
+ * seconds) bounds every device-side wait of later runs.
+ */
+#define GEMM_DEBUG_SKIP_FIRST_FILL 1
+GEMM_API int gemm_debug_set(gemm_handle_t h, int flags, uint64_t timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_GEMM_H */

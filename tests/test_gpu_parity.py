@@ -1,0 +1,210 @@
+"""GPU parity: the CUDA library through its C ABI against the CPU oracle.
+
+Floating point uses the acceptance rule of oracle/compare.py (one output ulp
+of the correctly rounded fp64 value, plus the fp32 accumulation bound where
+the sum cancels); fp32 output uses the fp32 bound alone; int8 is bit-exact.
+Closed forms (identity / permutation operands) are checked bit for bit,
+which exposes any transposed or mis-swizzled operand tile.
+"""
+from __future__ import annotations
+
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import dense_tiled_gemm_02_gb300 as pkg
+from gpu_helpers import check_points, check_rows, logical, run_gpu
+from workloads import (BF16, COL, F16, F32, I8, I32, ROW, WORKLOADS, Workload, draw,
+                       make_inputs, sample_points, sample_rows, storage_shape)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    pkg.load()
+
+
+def _assert_ok(rep, what):
+    assert rep["ok"], f"{what}: {rep['n_fail']} of {rep['n']} outside tolerance; first {rep['first_failures']}"
+
+
+# ------------------------------------------------------------------ closed forms, bit-exact
+@pytest.mark.parametrize("bn", [64, 128, 256])
+@pytest.mark.parametrize("a_col,b_col", list(itertools.product((ROW, COL), repeat=2)))
+@pytest.mark.parametrize("swap", [0, 1])
+def test_permutation_is_exact(bn, a_col, b_col, swap):
+    """A = P (a permutation): D = P B exactly, for every operand layout."""
+    M = K = 320
+    N = 384
+    g = torch.Generator().manual_seed(bn * 7 + a_col * 3 + b_col + 11 * swap)
+    perm = torch.randperm(M, generator=g)
+    P = torch.zeros(M, K, dtype=torch.bfloat16)
+    P[torch.arange(M), perm] = 1
+    B = torch.randn(K, N, generator=g).to(torch.bfloat16)
+    w = Workload("perm", 0, M, N, K, BF16, None, BF16, "normal", a_col, b_col, ROW, ROW)
+    inp = {"A": P if a_col == ROW else P.t().contiguous(),
+           "B": B if b_col == ROW else B.t().contiguous(), "C": None}
+    D, plan = run_gpu(w, inp, plan=f"bn={bn},swap={swap}")
+    assert torch.equal(D.view(torch.int16), B[perm].view(torch.int16)), plan
+
+
+@pytest.mark.parametrize("bn", [64, 128, 256])
+def test_identity_plus_c(bn):
+    """A = I: D = rnd(B + C); checked against the oracle (one rounding)."""
+    M = K = 256
+    N = 320
+    g = torch.Generator().manual_seed(5 + bn)
+    I = torch.eye(M, K).to(torch.float16)
+    B = torch.randn(K, N, generator=g).to(torch.float16)
+    C = torch.randn(M, N, generator=g).to(torch.float16)
+    w = Workload("ident", 0, M, N, K, F16, F16, F16, "normal")
+    inp = {"A": I, "B": B, "C": C}
+    D, plan = run_gpu(w, inp, plan=f"bn={bn}")
+    _assert_ok(check_rows(w, inp, D), plan)
+
+
+# ------------------------------------------------------------------ the small configs, every element
+@pytest.mark.parametrize("name", ["sq256_f16_f32", "sq1024_f16", "rag1000_bf16"])
+@pytest.mark.parametrize("plan", [None, "bn=64", "bn=128", "bn=256", "bn=128,splits=3",
+                                  "bn=64,group=1", "bn=128,swap=1"])
+def test_small_config(name, plan):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    D, p = run_gpu(w, inp, plan=plan)
+    _assert_ok(check_rows(w, inp, D), f"{name} [{p}]")
+
+
+SHAPES = [
+    # (M, N, K, layout_a, layout_b, layout_c, layout_d, ab, c, d)
+    (1, 1, 1, ROW, ROW, ROW, ROW, BF16, BF16, BF16),
+    (1, 1, 17, ROW, COL, ROW, ROW, F16, F16, F32),
+    (129, 257, 65, ROW, ROW, ROW, ROW, BF16, BF16, BF16),
+    (129, 257, 65, COL, COL, COL, COL, F16, F32, F16),
+    (7, 300, 1000, ROW, ROW, ROW, ROW, BF16, BF16, BF16),
+    (513, 77, 129, COL, ROW, ROW, COL, BF16, None, F32),
+    (300, 520, 200, ROW, COL, ROW, ROW, BF16, BF16, BF16),
+    (64, 2048, 4096, ROW, ROW, ROW, ROW, BF16, BF16, BF16),
+    (1000, 96, 3000, ROW, COL, COL, ROW, F16, F16, F16),
+    (255, 255, 255, ROW, ROW, ROW, ROW, BF16, BF16, BF16),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"{s[0]}x{s[1]}x{s[2]}-{s[3]}{s[4]}{s[5]}{s[6]}"
+                                               for s in SHAPES])
+def test_ragged_shapes(shape):
+    M, N, K, la, lb, lc, ld, ab, ct, dt = shape
+    w = Workload("shape", 7, M, N, K, ab, ct, dt, "normal", la, lb, lc, ld)
+    inp = make_inputs(w, seed_offset=M + N + K)
+    D, p = run_gpu(w, inp)
+    _assert_ok(check_rows(w, inp, D), f"{shape} [{p}]")
+
+
+def test_k_zero_gives_c():
+    w = Workload("k0", 8, 130, 70, 0, BF16, F16, F32, "normal")
+    inp = make_inputs(w)
+    D, _ = run_gpu(w, inp)
+    assert torch.equal(D, inp["C"].float())
+
+
+def test_guard_bands_untouched():
+    """D written into a larger buffer (ldd > N, extra rows): canaries survive."""
+    M, N, K = 200, 300, 130
+    w = Workload("guard", 9, M, N, K, BF16, BF16, BF16, "normal")
+    inp = make_inputs(w)
+    big = torch.full((M + 9, N + 40), 12345.0, dtype=torch.bfloat16, device="cuda")
+    view = big[3:3 + M, 8:8 + N]
+    import dense_tiled_gemm_02_gb300 as g_
+    A, B, C = inp["A"].cuda(), inp["B"].cuda(), inp["C"].cuda()
+    g = g_.Gemm.like(A, B, C, view)
+    g.run(A, B, C, view)
+    assert g.status() == 0
+    g.close()
+    host = big.cpu()
+    mask = torch.ones_like(host, dtype=torch.bool)
+    mask[3:3 + M, 8:8 + N] = False
+    assert torch.all(host[mask] == 12345.0)
+    _assert_ok(check_rows(w, inp, host[3:3 + M, 8:8 + N].contiguous()), "guard")
+
+
+def test_side_stream_and_reuse():
+    """One handle, two runs on a side stream with different buffers."""
+    w = WORKLOADS["rag1000_bf16"]
+    s = torch.cuda.Stream()
+    for off in (0, 1):
+        inp = make_inputs(w, seed_offset=off)
+        with torch.cuda.stream(s):
+            D, _ = run_gpu(w, inp, stream=s)
+        _assert_ok(check_rows(w, inp, D), f"stream run {off}")
+
+
+# ------------------------------------------------------------------ full-size configs
+@pytest.mark.parametrize("name", ["sq4096_bf16", "skinny64x8192x8192_bf16",
+                                  "skinny8192x128x4096_bf16", "rag4095x4097x4099_bf16"])
+def test_full_config_every_element(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    D, p = run_gpu(w, inp)
+    rep = check_rows(w, inp, D)
+    _assert_ok(rep, f"{name} [{p}]")
+    print(f"{name}: {rep['n']} elements ok, {rep['n_needed_slack']} needed the fp32 slack [{p}]")
+
+
+@pytest.mark.parametrize("name", ["sq8192_bf16", "sq8192_i8"])
+def test_8192_sampled(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    D, p = run_gpu(w, inp)
+    pi, pj = sample_points(w.M, w.N)
+    _assert_ok(check_points(w, inp, D, pi.numpy(), pj.numpy()), f"{name} points [{p}]")
+    rows = sample_rows(w.M).numpy()
+    _assert_ok(check_rows(w, inp, D, rows=rows), f"{name} rows [{p}]")
+
+
+# ------------------------------------------------------------------ exact int8
+@pytest.mark.parametrize("shape", [(300, 200, 1500, ROW, ROW), (129, 257, 2049, COL, COL),
+                                   (64, 384, 600, ROW, COL)])
+def test_int8_exact_small(shape):
+    M, N, K, la, lb = shape
+    w = Workload("i8", 51, M, N, K, I8, I32, I32, "int", la, lb)
+    inp = make_inputs(w)
+    D, p = run_gpu(w, inp)
+    _assert_ok(check_rows(w, inp, D), f"int8 {shape} [{p}]")
+
+
+@pytest.mark.parametrize("fill", [-128, 127])
+def test_int8_extremes(fill):
+    """All entries at one extreme, K = 8192: |sum| = 2^27 (or 127^2 * 8192)."""
+    M, N, K = 256, 256, 8192
+    A = torch.full((M, K), fill, dtype=torch.int8)
+    B = torch.full((K, N), -128 if fill == -128 else 127, dtype=torch.int8)
+    C = torch.randint(-(2 ** 20), 2 ** 20 + 1, (M, N), generator=torch.Generator().manual_seed(3),
+                      dtype=torch.int32)
+    w = Workload("i8x", 52, M, N, K, I8, I32, I32, "int")
+    inp = {"A": A, "B": B, "C": C}
+    D, p = run_gpu(w, inp)
+    want = (A[0, 0].long() * B[0, 0].long() * K) + C.long()
+    assert torch.equal(D.long(), want), p
+
+
+# ------------------------------------------------------------------ failure detection
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A stage that is never filled: the consumer's wait expires after the
+    short limit, every role exits, the status word says so, and the next
+    GEMM on the same context is correct."""
+    w = WORKLOADS["rag1000_bf16"]
+    inp = make_inputs(w)
+    A, B, C = (inp[k].cuda() for k in "ABC")
+    D = torch.empty(w.M, w.N, dtype=torch.bfloat16, device="cuda")
+    g = pkg.Gemm.like(A, B, C, D)
+    assert pkg.gemm_debug_set(g.handle, pkg.GEMM_DEBUG_SKIP_FIRST_FILL, 50_000_000) == 0
+    g.run(A, B, C, D)
+    assert g.status() == pkg.GEMM_ERR_DEVICE_TIMEOUT
+    assert pkg.gemm_debug_set(g.handle, 0, 0) == 0
+    g.run(A, B, C, D)
+    assert g.status() == pkg.GEMM_OK
+    g.close()
+    _assert_ok(check_rows(w, inp, D.cpu()), "after timeout")
