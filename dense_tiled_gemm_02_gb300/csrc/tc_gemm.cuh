@@ -174,7 +174,8 @@ __device__ __forceinline__ void store_partial(const KParams& p, int r, int c0, i
                                               const float (&f)[32]) {
   if (r >= p.M) return;
   float* base = p.ws + split * p.ws_split;
-  if (p.ws_cs == 1 && c0 + 32 <= p.N) {
+  // float4 stores need every workspace row to start on a 16-byte boundary
+  if (p.ws_cs == 1 && (p.ws_rs & 3) == 0 && c0 + 32 <= p.N) {
     float4* dst = reinterpret_cast<float4*>(base + r * p.ws_rs + c0);
 #pragma unroll
     for (int v = 0; v < 8; ++v)

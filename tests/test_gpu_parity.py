@@ -90,6 +90,9 @@ SHAPES = [
     (64, 2048, 4096, ROW, ROW, ROW, ROW, BF16, BF16, BF16),
     (1000, 96, 3000, ROW, COL, COL, ROW, F16, F16, F16),
     (255, 255, 255, ROW, ROW, ROW, ROW, BF16, BF16, BF16),
+    # split-K with workspace rows that are not 16-byte multiples
+    (1000, 90, 4096, ROW, ROW, ROW, ROW, BF16, BF16, BF16),
+    (999, 130, 2000, ROW, COL, ROW, ROW, F16, F32, F32),
 ]
 
 
