@@ -5,7 +5,7 @@
 // a key that leaves out a dimension silently serves a tile tuned for another
 // shape ("Tuning Triton" skill page, section 3, where a decode shape reusing
 // the square-shape tile ran several times slower).  Rows of kTable come from
-// the measured sweep of the tuning script (bench.py --sweep); shapes without
+// the measured sweep of the tuning script (dense_tiled_gemm_02_gb300/tune.py); shapes without
 // a row fall back to the rules in choose_plan(), which follow the regime
 // split of that page's section 4 (skinny shapes get their own candidates).
 #pragma once
