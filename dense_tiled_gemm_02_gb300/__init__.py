@@ -31,7 +31,9 @@ GEMM_ERR_NO_DEVICE = -7
 GEMM_DEBUG_SKIP_FIRST_FILL = 1
 
 EXPORTED = ["gemm_create", "gemm_run", "gemm_get_status", "gemm_destroy", "gemm_strerror",
-            "gemm_plan_string", "gemm_workspace_bytes", "gemm_raster_tile", "gemm_debug_set"]
+            "gemm_plan_string", "gemm_workspace_bytes", "gemm_raster_tile", "gemm_debug_set",
+            "gemm_run_splitk_noalloc"]
+GEMM_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class GemmDesc(ctypes.Structure):
@@ -85,6 +87,8 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
     lib.gemm_raster_tile.restype = ci
     lib.gemm_debug_set.argtypes = [vp, ci, ctypes.c_uint64]
     lib.gemm_debug_set.restype = ci
+    lib.gemm_run_splitk_noalloc.argtypes = [ctypes.POINTER(GemmDesc), ci, vp, vp, vp, vp, vp]
+    lib.gemm_run_splitk_noalloc.restype = ci
     _lib = lib
     return lib
 
@@ -131,6 +135,13 @@ def gemm_raster_tile(t: int, num_pid_m: int, num_pid_n: int, group_m: int):
 
 def gemm_debug_set(h: int, flags: int, timeout_ns: int = 0) -> int:
     return load().gemm_debug_set(h, flags, timeout_ns)
+
+
+def gemm_run_splitk_noalloc(desc: GemmDesc, splits: int, A: int, B: int, C: int | None, D: int,
+                            stream: int | None) -> int:
+    """Split-K GEMM for callers that cannot allocate device memory (scratch is a
+    static device array; see include/gemm.h)."""
+    return load().gemm_run_splitk_noalloc(ctypes.byref(desc), splits, A, B, C, D, stream)
 
 
 # ---------------------------------------------------------------- torch convenience

@@ -29,6 +29,7 @@ FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", 
 UNITS = [
     ("gemm_host.cu", [], "gemm_host.o"),
     ("aux_kernels.cu", [], "aux_kernels.o"),
+    ("noalloc.cu", [], "noalloc.o"),
     ("tc_launch.cu", ["-DTC_BN=256"], "tc_bn256.o"),
     ("tc_launch.cu", ["-DTC_BN=128"], "tc_bn128.o"),
     ("tc_launch.cu", ["-DTC_BN=64"], "tc_bn64.o"),

@@ -143,6 +143,39 @@ GEMM_API int gemm_raster_tile(int64_t t, int64_t num_pid_m, int64_t num_pid_n, i
                      int64_t* pid_m, int64_t* pid_n);
 
 /*
+ * gemm_run_splitk_noalloc: D = A*B + C (fp16/bf16 A and B) with K split
+ * `splits` ways (1..16), for callers that cannot allocate device memory when
+ * they need the product: code running under a framework whose caching
+ * allocator owns all device memory (a side cudaMalloc escapes its accounting
+ * and can fail once the pool holds the device), and latency-critical paths
+ * that cannot afford cudaMalloc or the device-wide synchronisation of
+ * cudaFree.  The pages have no counterpart to this entry point; it exists
+ * only for such callers.
+ *
+ * It allocates nothing: the fp32 partial sums and the device status word
+ * live in one static device array of GEMM_NOALLOC_SCRATCH_BYTES that every
+ * GPU loading this library holds until the process exits.  The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.
+ * Every call shares the array (its status word is cleared by each call and
+ * every partial sum is rewritten before it is read): calls whose kernels
+ * overlap on the GPU race, so serialise them (one stream, or events).
+ *
+ * desc: as for gemm_create (layouts and leading dimensions); A and B must be
+ * 16-byte aligned with 16-byte-multiple row strides (read in place by TMA).
+ * Returns GEMM_OK; GEMM_ERR_INVALID_ARG for bad sizes, splits outside
+ * [1, 16], or when splits * M * N * 4 bytes of partial sums exceed
+ * GEMM_NOALLOC_SCRATCH_BYTES - 256; GEMM_ERR_UNSUPPORTED for other types;
+ * GEMM_ERR_MISALIGNED; GEMM_ERR_NO_DEVICE; GEMM_ERR_CUDA.  A bounded
+ * device-side wait that expires leaves D undefined; this entry point keeps
+ * no handle through which to report it.
+ */
+#define GEMM_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+GEMM_API int gemm_run_splitk_noalloc(const gemm_desc_t* desc, int splits, const void* A,
+                                     const void* B, const void* C, void* D,
+                                     gemm_stream_t stream);
+
+/*
  * Test hooks (not for production use).
  * gemm_debug_set: flags bit 0 makes the load warp of the next gemm_run skip
  * its first stage fill, so that the consumer's bounded wait expires and the
