@@ -144,11 +144,7 @@ def cpu_baseline(w, inp, target_s: float) -> dict:
     import numpy as np
     from workloads import I8
     run, threads = oracle_rows_runner(w, inp)
-    n = min(w.M, 4)
-    t0 = time.perf_counter()
-    run(np.arange(n))
-    dt = max(time.perf_counter() - t0, 1e-6)
-    n2 = int(max(1, min(w.M, n * target_s / dt)))
+    n2 = calibrate_rows(run, w.M, target_s)
     t0 = time.perf_counter()
     run(np.arange(n2))
     dt = time.perf_counter() - t0
@@ -170,11 +166,7 @@ def run_reference(args, w):
     total_steps = max(1, args.steps + args.warmup)
     per_step_s = min(10.0, max(0.2, 120.0 / total_steps))
     run, threads = oracle_rows_runner(w, inp)
-    n = min(w.M, 4)
-    t0 = time.perf_counter()
-    run(np.arange(n))
-    dt = max(time.perf_counter() - t0, 1e-6)
-    rows_per_step = int(max(1, min(w.M, n * per_step_s / dt)))
+    rows_per_step = calibrate_rows(run, w.M, per_step_s)
     for i in range(args.warmup):
         run((np.arange(rows_per_step) + i * rows_per_step) % w.M)
     t0 = time.perf_counter()
@@ -197,6 +189,25 @@ def run_reference(args, w):
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
+
+
+def calibrate_rows(run, M: int, target_s: float) -> int:
+    """Rows per oracle call so that one call takes about target_s seconds.
+
+    A call has a fixed cost (widening B) and a per-row cost; two timed calls
+    separate them."""
+    import numpy as np
+    n1, n2 = min(M, 4), min(M, 36)
+    t0 = time.perf_counter()
+    run(np.arange(n1))
+    t1 = time.perf_counter()
+    run(np.arange(n2))
+    t2 = time.perf_counter()
+    if n2 == n1:
+        return n1
+    per_row = max((t2 - t1) - (t1 - t0), 1e-9) / (n2 - n1)
+    fixed = max((t1 - t0) - n1 * per_row, 0.0)
+    return int(max(1, min(M, (target_s - fixed) / per_row)))
 
 
 def oracle_rows_runner(w, inp):
@@ -323,7 +334,8 @@ def main():
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": f"{src} bf16 burst (cuBLAS 8192^3)",
-                "kernel": "tc_gemm_kernel", "median_launch_ms": round(statistics.median(per_launch), 4)}
+                "kernel": kernel_name(g.plan()),
+                "median_launch_ms": round(statistics.median(per_launch), 4)}
 
     line = {"metric": metric_name(w), "value": round(value, 1),
             "unit": "TOPS" if w.ab_type == I8 else "TFLOPS", "n_gpus": world,
@@ -343,6 +355,13 @@ def main():
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def kernel_name(plan: str) -> str:
+    f = dict(kv.split("=") for kv in plan.split() if "=" in kv)
+    if f.get("pair") == "1":
+        return f"tc_gemm_pair_kernel<{f['bn']}, {f['stages']}>"
+    return f"tc_gemm_kernel<{f['bn']}, {f['stages']}, {f.get('i8x', '0')}>"
 
 
 def launches_per_step(g) -> int:

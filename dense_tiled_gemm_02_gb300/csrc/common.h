@@ -55,7 +55,7 @@ struct KParams {
 // (bits 4-5 = 1), A/B element type (bits 7-9, 10-12: 0 fp16, 1 bf16),
 // operand majors (bit 15 A, bit 16 B: 0 K-major, 1 MN-major), N/8 in bits
 // 17-22 and M/16 in bits 24-28.
-constexpr uint32_t idesc_f16(uint32_t bf16, uint32_t a_mn, uint32_t b_mn,
+GB_HD constexpr uint32_t idesc_f16(uint32_t bf16, uint32_t a_mn, uint32_t b_mn,
                                                  uint32_t m, uint32_t n) {
   return (1u << 4) | (bf16 << 7) | (bf16 << 10) | (a_mn << 15) | (b_mn << 16) |
          ((n >> 3) << 17) | ((m >> 4) << 24);

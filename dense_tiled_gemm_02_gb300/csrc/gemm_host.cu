@@ -74,6 +74,12 @@ const TcVariant* find_variant(int bn, bool i8x) {
   return nullptr;
 }
 
+const PairVariant* find_pair(int bn) {
+  for (int i = 0; i < kNumPairVariants; ++i)
+    if (kPairVariants[i].bn == bn) return &kPairVariants[i];
+  return nullptr;
+}
+
 }  // namespace
 
 struct gemm_plan {
@@ -81,6 +87,7 @@ struct gemm_plan {
   int device = 0, num_sms = 0;
   PlanChoice choice{};
   const TcVariant* variant = nullptr;
+  const PairVariant* pair = nullptr;  // set when the CTA-pair kernel runs the plan
   bool i8x = false;
   int mab_type = T_BF16;        // type the tensor cores read (bf16 for int8 input)
   int64_t M = 0, N = 0, K = 0;  // internal problem
@@ -153,6 +160,7 @@ void apply_force_plan(PlanChoice& c) {
       else if (k == "group") c.group_m = v;
       else if (k == "swap") c.swap = v;
       else if (k == "grid") c.max_ctas = v;
+      else if (k == "pair") c.pair = v;
     }
     pos = end + 1;
   }
@@ -161,11 +169,13 @@ void apply_force_plan(PlanChoice& c) {
 void make_plan_string(gemm_plan* h) {
   char buf[512];
   std::snprintf(buf, sizeof buf,
-                "M=%lld N=%lld K=%lld swap=%d bn=%d stages=%d group_m=%d splits=%d "
+                "M=%lld N=%lld K=%lld swap=%d pair=%d bn=%d stages=%d group_m=%d splits=%d "
                 "kb_per_split=%d grid=%d i8x=%d a_mn=%d b_mn=%d repack_a=%d repack_b=%d "
                 "ws_bytes=%zu",
                 (long long)h->desc.M, (long long)h->desc.N, (long long)h->desc.K, h->choice.swap,
-                h->choice.bn, h->variant ? h->variant->stages : 0, h->kp.group_m, h->kp.splits,
+                h->pair ? 1 : 0, h->choice.bn,
+                h->pair ? h->pair->stages : (h->variant ? h->variant->stages : 0), h->kp.group_m,
+                h->kp.splits,
                 h->kp.kb_per_split, h->grid, (int)h->i8x, h->kp.a_mn, h->kp.b_mn,
                 (int)h->a.repack, (int)h->b.repack, h->ws_bytes);
   h->plan_str = buf;
@@ -248,8 +258,8 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   h->desc = d;
   h->device = dev;
   h->num_sms = sms;
-  h->i8x = (d.ab_type == T_I8);
-  h->mab_type = h->i8x ? T_BF16 : d.ab_type;
+  h->i8x = (static_cast<int>(d.ab_type) == T_I8);
+  h->mab_type = h->i8x ? static_cast<int>(T_BF16) : static_cast<int>(d.ab_type);
 
   h->choice = choose_plan(d.M, d.N, d.K, d.ab_type, d.layout_a, d.layout_b, sms);
   apply_force_plan(h->choice);
@@ -278,18 +288,30 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   h->ldc = d.ldc;
   h->ldd = d.ldd;
 
-  h->variant = find_variant(c.bn, h->i8x);
-  if (!h->variant) {
-    delete h;
-    return GEMM_ERR_UNSUPPORTED;
+  // The pair kernel stages bn/2 columns of B per CTA; an N-major B needs
+  // whole 64-column swizzle atoms there.
+  const bool b_n_major = h->b.layout == GEMM_ROW_MAJOR;
+  if (c.pair && (h->i8x || (b_n_major && (c.bn / 2) % 64 != 0))) c.pair = 0;
+  if (c.pair) {
+    h->pair = find_pair(c.bn);
+    if (!h->pair) c.pair = 0;
   }
+  if (!c.pair) {
+    if (c.bn == 224) c.bn = 256;
+    h->variant = find_variant(c.bn, h->i8x);
+    if (!h->variant) {
+      delete h;
+      return GEMM_ERR_UNSUPPORTED;
+    }
+  }
+  const int tile_m = c.pair ? 2 * BM : BM;
 
   // Tile grid and K split.
   KParams& kp = h->kp;
   kp.M = (int)h->M;
   kp.N = (int)h->N;
   kp.K = (int)h->K;
-  kp.tiles_m = (int)((h->M + BM - 1) / BM);
+  kp.tiles_m = (int)((h->M + tile_m - 1) / tile_m);
   kp.tiles_n = (int)((h->N + c.bn - 1) / c.bn);
   kp.group_m = std::max(1, std::min(c.group_m, kp.tiles_m));
   kp.num_kb = (int)((h->K + BK - 1) / BK);
@@ -302,7 +324,7 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   kp.a_mn = h->a.layout == GEMM_COL_MAJOR ? 1 : 0;  // A' contiguous along M'
   kp.b_mn = h->b.layout == GEMM_ROW_MAJOR ? 1 : 0;  // B' contiguous along N'
   kp.idesc = idesc_f16(h->mab_type == T_BF16 ? 1u : 0u, (uint32_t)kp.a_mn, (uint32_t)kp.b_mn,
-                       BM, (uint32_t)c.bn);
+                       (uint32_t)tile_m, (uint32_t)c.bn);
   kp.c_type = d.c_type;
   kp.d_type = d.d_type;
   kp.c_rs = h->c_layout == GEMM_ROW_MAJOR ? h->ldc : 1;
@@ -312,7 +334,7 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   const int64_t units = (int64_t)kp.tiles_m * kp.tiles_n * kp.splits;
   int max_ctas = sms;
   if (c.max_ctas > 0) max_ctas = std::min(max_ctas, c.max_ctas);
-  h->grid = (int)std::max<int64_t>(1, std::min<int64_t>(units, max_ctas));
+  if (!c.pair) h->grid = (int)std::max<int64_t>(1, std::min<int64_t>(units, max_ctas));
 
   // Workspace: operand copies the TMA unit can read, then split-K partials.
   size_t off = 0;
@@ -349,7 +371,15 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     delete h;
     return GEMM_ERR_ALLOC_FAILED;
   }
-  if (h->variant->prepare() != cudaSuccess) {
+  const cudaError_t prep = h->pair ? h->pair->prepare() : h->variant->prepare();
+  int clusters = 0;
+  if (prep == cudaSuccess && h->pair) {
+    // one persistent 2-CTA cluster per resident slot, at most one per tile
+    clusters = h->pair->max_clusters();
+    if (c.max_ctas > 0) clusters = std::min(clusters, c.max_ctas / 2);
+    h->grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(units, clusters));
+  }
+  if (prep != cudaSuccess || (h->pair && clusters <= 0)) {
     cudaGetLastError();
     cudaFree(h->status);
     if (h->ws) cudaFree(h->ws);
@@ -429,14 +459,17 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
     h->last_a = ta;
   }
   if (tb != h->last_b) {
-    if (encode_operand(&h->tm_b, tb, ldb_eff, kp.b_mn == 0, h->N, h->K, h->choice.bn) != GEMM_OK) {
+    const int b_box = h->pair ? h->choice.bn / 2 : h->choice.bn;  // B rows staged per CTA
+    if (encode_operand(&h->tm_b, tb, ldb_eff, kp.b_mn == 0, h->N, h->K, b_box) != GEMM_OK) {
       h->last_b = nullptr;
       return GEMM_ERR_CUDA;
     }
     h->last_b = tb;
   }
   if (kp.splits > 1) kp.ws = reinterpret_cast<float*>(ws + h->ws_partial_off);
-  if (h->variant->launch(h->tm_a, h->tm_b, kp, h->grid, st) != cudaSuccess) return GEMM_ERR_CUDA;
+  const cudaError_t le = h->pair ? h->pair->launch(h->tm_a, h->tm_b, kp, h->grid, st)
+                                 : h->variant->launch(h->tm_a, h->tm_b, kp, h->grid, st);
+  if (le != cudaSuccess) return GEMM_ERR_CUDA;
   if (kp.splits > 1 && launch_reduce(kp, row_order, h->num_sms, st) != cudaSuccess)
     return GEMM_ERR_CUDA;
   return GEMM_OK;

@@ -125,8 +125,9 @@ extern "C" GEMM_API int gemm_run_splitk_noalloc(const gemm_desc_t* desc, int spl
   for (int l : {d.layout_a, d.layout_b, d.layout_c, d.layout_d})
     if (l != GEMM_ROW_MAJOR && l != GEMM_COL_MAJOR) return GEMM_ERR_INVALID_ARG;
   if (!half_type(d.ab_type)) return GEMM_ERR_UNSUPPORTED;
-  if (!(half_type(d.d_type) || d.d_type == T_F32)) return GEMM_ERR_UNSUPPORTED;
-  if (C && !(half_type(d.c_type) || d.c_type == T_F32)) return GEMM_ERR_UNSUPPORTED;
+  if (!(half_type(d.d_type) || static_cast<int>(d.d_type) == T_F32)) return GEMM_ERR_UNSUPPORTED;
+  if (C && !(half_type(d.c_type) || static_cast<int>(d.c_type) == T_F32))
+    return GEMM_ERR_UNSUPPORTED;
   if (d.lda == 0) d.lda = packed(d.layout_a, d.M, d.K);
   if (d.ldb == 0) d.ldb = packed(d.layout_b, d.K, d.N);
   if (d.ldc == 0) d.ldc = packed(d.layout_c, d.M, d.N);
@@ -155,8 +156,8 @@ extern "C" GEMM_API int gemm_run_splitk_noalloc(const gemm_desc_t* desc, int spl
   kp.kb_per_chunk = kp.num_kb;
   kp.a_mn = d.layout_a == GEMM_COL_MAJOR ? 1 : 0;
   kp.b_mn = d.layout_b == GEMM_ROW_MAJOR ? 1 : 0;
-  kp.idesc = idesc_f16(d.ab_type == T_BF16 ? 1u : 0u, (uint32_t)kp.a_mn, (uint32_t)kp.b_mn, BM,
-                       (uint32_t)bn);
+  const uint32_t bf16 = static_cast<int>(d.ab_type) == T_BF16 ? 1u : 0u;
+  kp.idesc = idesc_f16(bf16, (uint32_t)kp.a_mn, (uint32_t)kp.b_mn, BM, (uint32_t)bn);
   const bool row_d = d.layout_d == GEMM_ROW_MAJOR;
   // Reject problems whose partial sums do not fit in the scratch array.
   const uint64_t need = (uint64_t)kp.splits * (uint64_t)d.M * (uint64_t)d.N * 4u;

@@ -20,6 +20,7 @@ struct PlanChoice {
   int splits;    // split-K factor (1 = none)
   int swap;      // 1: compute D^T = B^T A^T (long dimension on the tensor-core M side)
   int max_ctas;  // 0 = one CTA per SM
+  int pair;      // 1: CTA-pair kernel (cta_group::2), tile 256 x bn
 };
 
 struct PlanRow {
@@ -30,7 +31,7 @@ struct PlanRow {
 
 // Measured rows (exact shape match).
 static const PlanRow kTable[] = {
-    {0, 0, 0, -1, -1, -1, {0, 0, 0, 0, 0}},  // sentinel
+    {0, 0, 0, -1, -1, -1, {0, 0, 0, 0, 0, 0}},  // sentinel
 };
 
 inline int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -42,7 +43,7 @@ inline PlanChoice choose_plan(int64_t M, int64_t N, int64_t K, int ab_type, int 
         (r.layout_a < 0 || r.layout_a == layout_a) && (r.layout_b < 0 || r.layout_b == layout_b))
       return r.choice;
   }
-  PlanChoice c{256, 8, 1, 0, 0};
+  PlanChoice c{256, 8, 1, 0, 0, 0};
   // Skinny M: put the long N dimension on the 128-row tensor-core side.
   if (M < 128 && N >= 2 * M) c.swap = 1;
   const int64_t Mi = c.swap ? N : M;
@@ -55,6 +56,13 @@ inline PlanChoice choose_plan(int64_t M, int64_t N, int64_t K, int ab_type, int 
   else if (tm * cdiv64(Ni, 256) >= num_sms) c.bn = 256;
   else if (tm * cdiv64(Ni, 128) >= num_sms / 2) c.bn = 128;
   else c.bn = 64;
+  // Large problems: the CTA-pair 256 x 256 tile when its tiles fill at
+  // least one wave of 2-CTA clusters (measured faster than 128 x 256 per SM).
+  if (Ni > 128 && cdiv64(Mi, 256) * cdiv64(Ni, 256) >= num_sms / 2) {
+    c.pair = 1;
+    c.bn = 256;
+    return c;
+  }
   const int64_t tiles = tm * cdiv64(Ni, c.bn);
   // Split K when the tiles alone leave most SMs idle and K is long.
   const int64_t kb = cdiv64(K, 64);

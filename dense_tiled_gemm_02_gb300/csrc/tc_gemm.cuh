@@ -284,13 +284,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t it = 0, s = 0, ph = 0;  // it: slices issued; (s, ph): ring slot and phase
       int64_t skipped = -1;
       bool stop = false;
       for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
         const Unit w = decode_unit(p, u, BN);
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!bounded_wait(empty(s), ph ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
             stop = true;
             break;
@@ -298,6 +297,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if ((p.debug_flags & DBG_SKIP_FIRST_FILL) && it == 0) {
             skipped = 0;  // test hook: leave stage 0 empty so its consumer times out
             ++it;
+            if (++s == STAGES) {
+              s = 0;
+              ph ^= 1u;
+            }
             continue;
           }
           mbar_arrive_expect_tx(full(s), Cfg::STAGE_TX);
@@ -319,6 +322,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tma_load_2d(b_dst + j * 8192u, &tmB, w.n0 + 64 * j, k0, full(s));
           }
           ++it;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
       }
       // Let every copy still in flight land before the CTA can exit.
@@ -330,13 +337,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // The issue loop is kept short: a single thread feeds the tensor core and
+    // its queue holds only a few MMAs, so every instruction spent here per
+    // K slice must fit in the slack of the MMAs already queued.
     if (lane == 0) {
-      uint32_t it = 0, acc_it = 0, buf = 0;
+      const uint32_t a_lo0 = sdesc_lo(smem_u32(sA), p.a_mn ? 8192u : 16u);
+      const uint32_t b_lo0 = sdesc_lo(smem_u32(sB), p.b_mn ? 8192u : 16u);
+      const uint32_t dhi = sdesc_hi_sw128(1024u);
+      // one 16-wide K step: 32 bytes along a K-major row, 16 rows of an MN-major tile
+      const uint32_t a_kstep = p.a_mn ? (2048u >> 4) : (32u >> 4);
+      const uint32_t b_kstep = p.b_mn ? (2048u >> 4) : (32u >> 4);
+      uint32_t s = 0, ph = 0, acc_it = 0;
       bool stop = false;
       for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
         const Unit w = decode_unit(p, u, BN);
+        int kc = 0;  // K slices into the current accumulation pass
+        uint32_t buf = 0, d_tmem = 0;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          const int kc = (kb - w.kb0) % p.kb_per_chunk;
           if (kc == 0) {
             buf = acc_it & 1u;
             if (!bounded_wait(acc_empty(buf), ((acc_it >> 1) & 1u) ^ 1u, abort_flag, p.status,
@@ -345,31 +362,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               break;
             }
             tc_fence_after();
+            d_tmem = tmem_base + buf * BN;
           }
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!bounded_wait(full(s), ph, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
             stop = true;
             break;
           }
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + s * Cfg::A_BYTES);
-          const uint32_t b_addr = smem_u32(sB + s * Cfg::B_BYTES);
-          const uint32_t d_tmem = tmem_base + buf * BN;
+          const uint32_t a_lo = a_lo0 + s * (Cfg::A_BYTES >> 4);
+          const uint32_t b_lo = b_lo0 + s * (Cfg::B_BYTES >> 4);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            // K-major: the 16-element K step moves 32 bytes inside the
-            // swizzled 128-byte rows; MN-major: it moves 16 rows of 128 B.
-            const uint64_t ad = p.a_mn ? smem_desc_sw128(a_addr + kk * 2048u, 8192u, 1024u)
-                                       : smem_desc_sw128(a_addr + kk * 32u, 16u, 1024u);
-            const uint64_t bd = p.b_mn ? smem_desc_sw128(b_addr + kk * 2048u, 8192u, 1024u)
-                                       : smem_desc_sw128(b_addr + kk * 32u, 16u, 1024u);
-            mma_f16_ss(d_tmem, ad, bd, p.idesc, (kc > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_f16_ss(d_tmem, sdesc(dhi, a_lo + kk * a_kstep), sdesc(dhi, b_lo + kk * b_kstep),
+                       p.idesc, (kc | kk) != 0 ? 1u : 0u);
           mma_commit(empty(s));
-          ++it;
-          if (kc == p.kb_per_chunk - 1 || kb == w.kb1 - 1) {
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+          if (++kc == p.kb_per_chunk || kb + 1 == w.kb1) {
             mma_commit(acc_full(buf));
             ++acc_it;
+            kc = 0;
           }
         }
       }

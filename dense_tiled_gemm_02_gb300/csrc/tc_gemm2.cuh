@@ -1,0 +1,279 @@
+// tc_gemm2.cuh -- the CTA-pair (tcgen05 cta_group::2) variant of the GEMM.
+//
+// A cluster of two CTAs on neighbouring SMs owns a 256 x BN output tile.
+// Each CTA stages its own 128 rows of A and half of the tile's BN columns of
+// B per K-slice; the even CTA issues one 256 x BN x 16 pair MMA per 16-wide
+// K step, which reads A from both CTAs' shared memory and the two B halves
+// from both, and writes each CTA's 128 accumulator rows into that CTA's
+// tensor memory.  Per SM this halves the B bytes that must be staged and
+// read by the tensor core for the same work as the single-CTA 128 x BN
+// tile, which is what keeps the tensor pipe fed.
+//
+// Roles per CTA (192 threads) are those of tc_gemm.cuh:
+//   warp 0  TMA producer (both CTAs): waits for its own free stage, loads its
+//           A rows and B half; completion bytes of both CTAs are counted on
+//           the even CTA's "full" barrier, which the even producer arms with
+//           the pair's byte count.
+//   warp 1  MMA issuer (even CTA only; both CTAs own the tensor memory).
+//           Each stage is released to both producers, and each finished
+//           accumulator announced to both epilogues, by one commit that
+//           arrives on the same barrier of both CTAs.
+//   warps 2-5 epilogue (both CTAs): drain their 128 rows, then tell the even
+//           CTA's MMA warp that the accumulator buffer is free.
+// All waits are bounded (ptx.cuh); the kernel ends with a cluster barrier so
+// neither CTA leaves while its partner may still signal it.
+#pragma once
+
+#include "tc_gemm.cuh"
+
+namespace gb300 {
+
+template <int BN>
+struct PairCfg {
+  static constexpr int BNH = BN / 2;                    // B columns staged per CTA
+  static constexpr uint32_t A_BYTES = BM * BK * 2;      // this CTA's 128 rows: 16 KiB
+  static constexpr uint32_t B_BYTES = BNH * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t PAIR_TX = 2 * STAGE_BYTES;  // bytes both CTAs land per stage
+  static constexpr uint32_t TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
+  static_assert(BN == 128 || BN == 224 || BN == 256, "pair tile width");
+  static_assert(B_BYTES % 1024 == 0, "stage alignment");
+};
+
+template <int BN, int STAGES>
+constexpr uint32_t pair_smem_bytes() {
+  return STAGES * PairCfg<BN>::STAGE_BYTES + 256 + 1024;
+}
+
+__device__ __forceinline__ Unit decode_pair_unit(const KParams& p, int u, int bn) {
+  Unit w;
+  const int t = u / p.splits;
+  w.split = u - t * p.splits;
+  int64_t pm, pn;
+  raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
+  w.m0 = static_cast<int>(pm) * (2 * BM);
+  w.n0 = static_cast<int>(pn) * bn;
+  w.kb0 = w.split * p.kb_per_split;
+  w.kb1 = min(p.num_kb, w.kb0 + p.kb_per_split);
+  return w;
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const KParams p) {
+  using Cfg = PairCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * Cfg::B_BYTES);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](uint32_t s) { return bar0 + 8u * s; };
+  auto empty = [&](uint32_t s) { return bar0 + 8u * (STAGES + s); };
+  auto acc_full = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto acc_empty = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 8);  // one arrival per epilogue warp of both CTAs
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_holder), Cfg::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers exist before either signals the other
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int num_units = p.tiles_m * p.tiles_n * p.splits;
+  const int cid = blockIdx.x >> 1;
+  const int ncl = gridDim.x >> 1;
+  const uint64_t tmo = p.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      uint32_t it = 0, s = 0, ph = 0;  // it: slices issued; (s, ph): ring slot and phase
+      int64_t skipped = -1;
+      bool stop = false;
+      for (int u = cid; u < num_units && !stop; u += ncl) {
+        const Unit w = decode_pair_unit(p, u, BN);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!bounded_wait(empty(s), ph ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
+            stop = true;
+            break;
+          }
+          if (leader && (p.debug_flags & DBG_SKIP_FIRST_FILL) && it == 0) {
+            skipped = 0;  // test hook: never arm stage 0, so the MMA wait on it expires
+            ++it;
+            if (++s == STAGES) {
+              s = 0;
+              ph ^= 1u;
+            }
+            continue;
+          }
+          const uint32_t fb = map_shared_rank(full(s), 0);
+          if (leader) mbar_arrive_expect_tx(full(s), Cfg::PAIR_TX);
+          const uint32_t a_dst = smem_u32(sA + s * Cfg::A_BYTES);
+          const uint32_t b_dst = smem_u32(sB + s * Cfg::B_BYTES);
+          const int k0 = kb * BK;
+          const int am = w.m0 + BM * static_cast<int>(rank);
+          const int bn0 = w.n0 + Cfg::BNH * static_cast<int>(rank);
+          if (!p.a_mn) {
+            tma_load_2d_pair(a_dst, &tmA, k0, am, fb);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j)
+              tma_load_2d_pair(a_dst + j * 8192u, &tmA, am + 64 * j, k0, fb);
+          }
+          if (!p.b_mn) {
+            tma_load_2d_pair(b_dst, &tmB, k0, bn0, fb);
+          } else {
+#pragma unroll
+            for (int j = 0; j < Cfg::BNH / 64; ++j)
+              tma_load_2d_pair(b_dst + j * 8192u, &tmB, bn0 + 64 * j, k0, fb);
+          }
+          ++it;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (leader) {
+        // Both CTAs' copies of the last stages are counted here: let them land.
+        for (uint32_t j = it > STAGES ? it - STAGES : 0; j < it; ++j) {
+          if (static_cast<int64_t>(j) == skipped) continue;
+          drain_wait(full(j % STAGES), (j / STAGES) & 1u, 200000000ull);
+        }
+      } else if (stop) {
+        // The odd CTA cannot watch the even CTA's barrier: give copies it
+        // issued before giving up time to land.
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 1000000ull) __nanosleep(1000);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && leader) {
+      const uint32_t a_lo0 = sdesc_lo(smem_u32(sA), p.a_mn ? 8192u : 16u);
+      const uint32_t b_lo0 = sdesc_lo(smem_u32(sB), p.b_mn ? 8192u : 16u);
+      const uint32_t dhi = sdesc_hi_sw128(1024u);
+      const uint32_t a_kstep = p.a_mn ? (2048u >> 4) : (32u >> 4);
+      const uint32_t b_kstep = p.b_mn ? (2048u >> 4) : (32u >> 4);
+      uint32_t s = 0, ph = 0, acc_it = 0;
+      bool stop = false;
+      for (int u = cid; u < num_units && !stop; u += ncl) {
+        const Unit w = decode_pair_unit(p, u, BN);
+        int kc = 0;
+        uint32_t buf = 0, d_tmem = 0;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (kc == 0) {
+            buf = acc_it & 1u;
+            if (!bounded_wait(acc_empty(buf), ((acc_it >> 1) & 1u) ^ 1u, abort_flag, p.status,
+                              STATUS_TIMEOUT, tmo)) {
+              stop = true;
+              break;
+            }
+            tc_fence_after();
+            d_tmem = tmem_base + buf * BN;
+          }
+          if (!bounded_wait(full(s), ph, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
+            stop = true;
+            break;
+          }
+          const uint32_t a_lo = a_lo0 + s * (Cfg::A_BYTES >> 4);
+          const uint32_t b_lo = b_lo0 + s * (Cfg::B_BYTES >> 4);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_f16_ss_pair(d_tmem, sdesc(dhi, a_lo + kk * a_kstep),
+                            sdesc(dhi, b_lo + kk * b_kstep), p.idesc, (kc | kk) != 0 ? 1u : 0u);
+          mma_commit_pair_both(empty(s));
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+          if (++kc == p.kb_per_chunk || kb + 1 == w.kb1) {
+            mma_commit_pair_both(acc_full(buf));
+            ++acc_it;
+            kc = 0;
+          }
+        }
+      }
+      mma_commit_pair_both(done_bar);
+      drain_wait(done_bar, 0, 200000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t acc_it = 0;
+    for (int u = cid; u < num_units; u += ncl) {
+      const Unit w = decode_pair_unit(p, u, BN);
+      const int r = w.m0 + BM * static_cast<int>(rank) + q * 32 + lane;
+      const uint32_t buf = acc_it & 1u;
+      if (!bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status, STATUS_TIMEOUT,
+                        tmo))
+        break;
+      tc_fence_after();
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + lane_base + buf * BN + c * 32, v);
+        tmem_ld_wait();
+        if (c == BN / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(map_shared_rank(acc_empty(buf), 0));
+        }
+        float f[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+        const int c0 = w.n0 + c * 32;
+        if (p.splits > 1) {
+          store_partial(p, r, c0, w.split, f);
+        } else {
+          add_c_f(p, r, c0, f);
+          store_d_f(p, r, c0, f);
+        }
+      }
+      ++acc_it;
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+}  // namespace gb300

@@ -25,6 +25,22 @@ extern const int kNumVariantsBN128;
 extern const TcVariant kVariantsBN64[];
 extern const int kNumVariantsBN64;
 
+// CTA-pair variants (clusters of 2, tile 256 x bn).  max_clusters() is the
+// number of 2-CTA clusters that can be resident at once on the current
+// device (0 on failure); call prepare() first.
+struct PairVariant {
+  int bn;
+  int stages;
+  uint32_t smem;
+  cudaError_t (*launch)(const CUtensorMap&, const CUtensorMap&, const KParams&, int grid,
+                        cudaStream_t);
+  cudaError_t (*prepare)();
+  int (*max_clusters)();
+};
+
+extern const PairVariant kPairVariants[];
+extern const int kNumPairVariants;
+
 cudaError_t launch_reduce(const KParams& p, int row_order, int num_sms, cudaStream_t st);
 cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint16_t* dst,
                           long long ld_dst, long long rows, long long cols, int num_sms,

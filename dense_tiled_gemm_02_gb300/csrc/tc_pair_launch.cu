@@ -1,0 +1,62 @@
+// tc_pair_launch.cu -- instantiations and cluster launches of the CTA-pair
+// (cta_group::2) GEMM kernel.
+#include <cuda_runtime.h>
+
+#include "tc_gemm2.cuh"
+#include "tc_launch.h"
+
+namespace gb300 {
+
+namespace {
+template <int BN, int STAGES>
+cudaLaunchConfig_t pair_config(int grid, cudaStream_t st, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = pair_smem_bytes<BN, STAGES>();
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const KParams& p, int grid,
+                        cudaStream_t st) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pair_config<BN, STAGES>(grid, st, attr);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES>, a, b, p);
+}
+
+template <int BN, int STAGES>
+cudaError_t prepare_pair() {
+  return cudaFuncSetAttribute(tc_gemm_pair_kernel<BN, STAGES>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              pair_smem_bytes<BN, STAGES>());
+}
+
+template <int BN, int STAGES>
+int max_clusters_pair() {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pair_config<BN, STAGES>(2, nullptr, attr);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<BN, STAGES>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+}  // namespace
+
+#define GB_PAIR(BN_, ST_)                                                          \
+  PairVariant{BN_, ST_, pair_smem_bytes<BN_, ST_>(), &launch_pair<BN_, ST_>,       \
+              &prepare_pair<BN_, ST_>, &max_clusters_pair<BN_, ST_>}
+
+const PairVariant kPairVariants[] = {GB_PAIR(256, 6), GB_PAIR(224, 7), GB_PAIR(128, 8)};
+const int kNumPairVariants = 3;
+
+}  // namespace gb300

@@ -33,11 +33,15 @@ def _assert_ok(rep, what):
 
 
 # ------------------------------------------------------------------ closed forms, bit-exact
-@pytest.mark.parametrize("bn", [64, 128, 256])
+PERM_PLANS = [(bn, 0) for bn in (64, 128, 256)] + [(bn, 1) for bn in (128, 224, 256)]
+
+
+@pytest.mark.parametrize("bn,pair", PERM_PLANS, ids=[f"bn{b}-pair{p}" for b, p in PERM_PLANS])
 @pytest.mark.parametrize("a_col,b_col", list(itertools.product((ROW, COL), repeat=2)))
 @pytest.mark.parametrize("swap", [0, 1])
-def test_permutation_is_exact(bn, a_col, b_col, swap):
-    """A = P (a permutation): D = P B exactly, for every operand layout."""
+def test_permutation_is_exact(bn, pair, a_col, b_col, swap):
+    """A = P (a permutation): D = P B exactly, for every operand layout and
+    both the single-CTA and the CTA-pair kernels."""
     M = K = 320
     N = 384
     g = torch.Generator().manual_seed(bn * 7 + a_col * 3 + b_col + 11 * swap)
@@ -48,7 +52,7 @@ def test_permutation_is_exact(bn, a_col, b_col, swap):
     w = Workload("perm", 0, M, N, K, BF16, None, BF16, "normal", a_col, b_col, ROW, ROW)
     inp = {"A": P if a_col == ROW else P.t().contiguous(),
            "B": B if b_col == ROW else B.t().contiguous(), "C": None}
-    D, plan = run_gpu(w, inp, plan=f"bn={bn},swap={swap}")
+    D, plan = run_gpu(w, inp, plan=f"bn={bn},swap={swap},pair={pair}")
     assert torch.equal(D.view(torch.int16), B[perm].view(torch.int16)), plan
 
 
@@ -70,7 +74,9 @@ def test_identity_plus_c(bn):
 # ------------------------------------------------------------------ the small configs, every element
 @pytest.mark.parametrize("name", ["sq256_f16_f32", "sq1024_f16", "rag1000_bf16"])
 @pytest.mark.parametrize("plan", [None, "bn=64", "bn=128", "bn=256", "bn=128,splits=3",
-                                  "bn=64,group=1", "bn=128,swap=1"])
+                                  "bn=64,group=1", "bn=128,swap=1", "pair=1,bn=256",
+                                  "pair=1,bn=128", "pair=1,bn=224", "pair=1,bn=256,splits=2",
+                                  "pair=1,bn=128,swap=1"])
 def test_small_config(name, plan):
     w = WORKLOADS[name]
     inp = make_inputs(w)
@@ -96,13 +102,14 @@ SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("plan", [None, "pair=1"])
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"{s[0]}x{s[1]}x{s[2]}-{s[3]}{s[4]}{s[5]}{s[6]}"
                                                for s in SHAPES])
-def test_ragged_shapes(shape):
+def test_ragged_shapes(shape, plan):
     M, N, K, la, lb, lc, ld, ab, ct, dt = shape
     w = Workload("shape", 7, M, N, K, ab, ct, dt, "normal", la, lb, lc, ld)
     inp = make_inputs(w, seed_offset=M + N + K)
-    D, p = run_gpu(w, inp)
+    D, p = run_gpu(w, inp, plan=plan)
     _assert_ok(check_rows(w, inp, D), f"{shape} [{p}]")
 
 
@@ -145,12 +152,17 @@ def test_side_stream_and_reuse():
 
 
 # ------------------------------------------------------------------ full-size configs
-@pytest.mark.parametrize("name", ["sq4096_bf16", "skinny64x8192x8192_bf16",
-                                  "skinny8192x128x4096_bf16", "rag4095x4097x4099_bf16"])
-def test_full_config_every_element(name):
+FULL = [("sq4096_bf16", None), ("sq4096_bf16", "pair=1,bn=256"), ("sq4096_bf16", "pair=1,bn=224"),
+        ("sq4096_bf16", "pair=0,bn=256"), ("skinny64x8192x8192_bf16", None),
+        ("skinny8192x128x4096_bf16", None), ("rag4095x4097x4099_bf16", None),
+        ("rag4095x4097x4099_bf16", "pair=1,bn=256")]
+
+
+@pytest.mark.parametrize("name,plan", FULL, ids=[f"{n}-{p}" for n, p in FULL])
+def test_full_config_every_element(name, plan):
     w = WORKLOADS[name]
     inp = make_inputs(w)
-    D, p = run_gpu(w, inp)
+    D, p = run_gpu(w, inp, plan=plan)
     rep = check_rows(w, inp, D)
     _assert_ok(rep, f"{name} [{p}]")
     print(f"{name}: {rep['n']} elements ok, {rep['n_needed_slack']} needed the fp32 slack [{p}]")
@@ -194,15 +206,19 @@ def test_int8_extremes(fill):
 
 
 # ------------------------------------------------------------------ failure detection
-def test_bounded_wait_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("plan", ["pair=0", "pair=1,bn=128"])
+def test_bounded_wait_reports_timeout_and_context_survives(plan):
     """A stage that is never filled: the consumer's wait expires after the
     short limit, every role exits, the status word says so, and the next
     GEMM on the same context is correct."""
+    from gpu_helpers import forced_plan
     w = WORKLOADS["rag1000_bf16"]
     inp = make_inputs(w)
     A, B, C = (inp[k].cuda() for k in "ABC")
     D = torch.empty(w.M, w.N, dtype=torch.bfloat16, device="cuda")
-    g = pkg.Gemm.like(A, B, C, D)
+    with forced_plan(plan):
+        g = pkg.Gemm.like(A, B, C, D)
+    assert ("pair=1" in g.plan()) == plan.startswith("pair=1"), g.plan()
     assert pkg.gemm_debug_set(g.handle, pkg.GEMM_DEBUG_SKIP_FIRST_FILL, 50_000_000) == 0
     g.run(A, B, C, D)
     assert g.status() == pkg.GEMM_ERR_DEVICE_TIMEOUT
