@@ -62,24 +62,41 @@ __global__ void splitk_reduce_kernel(const KParams p, int row_order) {
 
 // Copy rows x cols elements (storage order) from src (leading dimension
 // ld_src) to the 16-bit dst (leading dimension ld_dst).  src_type T_I8
-// widens to bf16; 16-bit types are copied bit for bit.
+// widens to bf16 (exact); 16-bit types are copied bit for bit.  Block x
+// covers 256 consecutive columns of one row band; rows are strided over
+// block y, so neighbouring threads touch neighbouring addresses and no
+// thread divides.
 __global__ void repack_kernel(const void* src, int src_type, long long ld_src, uint16_t* dst,
                               long long ld_dst, long long rows, long long cols) {
-  const long long total = rows * cols;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += stride) {
-    const long long r = idx / cols;
-    const long long c = idx - r * cols;
+  const long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
     uint16_t v;
     if (src_type == T_I8) {
-      const __nv_bfloat16 b =
-          __float2bfloat16_rn(static_cast<float>(static_cast<const int8_t*>(src)[r * ld_src + c]));
+      const __nv_bfloat16 b = __float2bfloat16_rn(
+          static_cast<float>(static_cast<const int8_t*>(src)[r * ld_src + c]));
       v = *reinterpret_cast<const uint16_t*>(&b);
     } else {
       v = static_cast<const uint16_t*>(src)[r * ld_src + c];
     }
     dst[r * ld_dst + c] = v;
+  }
+}
+
+// int8 -> bf16 widening, 4 elements per thread (rows whose starts and
+// lengths are multiples of 4 elements).
+__global__ void widen_i8_x4_kernel(const char4* src, long long ld_src4, uint2* dst,
+                                   long long ld_dst4, long long rows, long long cols4) {
+  const long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c >= cols4) return;
+  for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
+    const char4 x = src[r * ld_src4 + c];
+    __nv_bfloat162 lo = __floats2bfloat162_rn(static_cast<float>(x.x), static_cast<float>(x.y));
+    __nv_bfloat162 hi = __floats2bfloat162_rn(static_cast<float>(x.z), static_cast<float>(x.w));
+    uint2 o;
+    o.x = *reinterpret_cast<const uint32_t*>(&lo);
+    o.y = *reinterpret_cast<const uint32_t*>(&hi);
+    dst[r * ld_dst4 + c] = o;
   }
 }
 
@@ -96,13 +113,21 @@ cudaError_t launch_reduce(const KParams& p, int row_order, int num_sms, cudaStre
 cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint16_t* dst,
                           long long ld_dst, long long rows, long long cols, int num_sms,
                           cudaStream_t st) {
-  const long long total = rows * cols;
-  if (total == 0) return cudaSuccess;
-  long long blocks = (total + 255) / 256;
-  const long long cap = static_cast<long long>(num_sms) * 8;
-  if (blocks > cap) blocks = cap;
-  repack_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(src, src_type, ld_src, dst, ld_dst,
-                                                               rows, cols);
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  const bool x4 = src_type == T_I8 && cols % 4 == 0 && ld_src % 4 == 0 && ld_dst % 4 == 0 &&
+                  reinterpret_cast<uintptr_t>(src) % 4 == 0;
+  const long long ccols = x4 ? cols / 4 : cols;
+  const unsigned gx = static_cast<unsigned>((ccols + 255) / 256);
+  long long gy = (static_cast<long long>(num_sms) * 16 + gx - 1) / gx;
+  if (gy > rows) gy = rows;
+  if (gy > 65535) gy = 65535;
+  const dim3 grid(gx, static_cast<unsigned>(gy));
+  if (x4)
+    widen_i8_x4_kernel<<<grid, 256, 0, st>>>(static_cast<const char4*>(src), ld_src / 4,
+                                             reinterpret_cast<uint2*>(dst), ld_dst / 4, rows,
+                                             ccols);
+  else
+    repack_kernel<<<grid, 256, 0, st>>>(src, src_type, ld_src, dst, ld_dst, rows, cols);
   return cudaGetLastError();
 }
 

@@ -74,9 +74,9 @@ const TcVariant* find_variant(int bn, bool i8x) {
   return nullptr;
 }
 
-const PairVariant* find_pair(int bn) {
+const PairVariant* find_pair(int bn, int ksub) {
   for (int i = 0; i < kNumPairVariants; ++i)
-    if (kPairVariants[i].bn == bn) return &kPairVariants[i];
+    if (kPairVariants[i].bn == bn && kPairVariants[i].ksub == ksub) return &kPairVariants[i];
   return nullptr;
 }
 
@@ -161,6 +161,7 @@ void apply_force_plan(PlanChoice& c) {
       else if (k == "swap") c.swap = v;
       else if (k == "grid") c.max_ctas = v;
       else if (k == "pair") c.pair = v;
+      else if (k == "ksub") c.ksub = v;
     }
     pos = end + 1;
   }
@@ -169,11 +170,11 @@ void apply_force_plan(PlanChoice& c) {
 void make_plan_string(gemm_plan* h) {
   char buf[512];
   std::snprintf(buf, sizeof buf,
-                "M=%lld N=%lld K=%lld swap=%d pair=%d bn=%d stages=%d group_m=%d splits=%d "
-                "kb_per_split=%d grid=%d i8x=%d a_mn=%d b_mn=%d repack_a=%d repack_b=%d "
+                "M=%lld N=%lld K=%lld swap=%d pair=%d bn=%d ksub=%d stages=%d group_m=%d "
+                "splits=%d kb_per_split=%d grid=%d i8x=%d a_mn=%d b_mn=%d repack_a=%d repack_b=%d "
                 "ws_bytes=%zu",
                 (long long)h->desc.M, (long long)h->desc.N, (long long)h->desc.K, h->choice.swap,
-                h->pair ? 1 : 0, h->choice.bn,
+                h->pair ? 1 : 0, h->choice.bn, h->choice.ksub,
                 h->pair ? h->pair->stages : (h->variant ? h->variant->stages : 0), h->kp.group_m,
                 h->kp.splits,
                 h->kp.kb_per_split, h->grid, (int)h->i8x, h->kp.a_mn, h->kp.b_mn,
@@ -293,9 +294,11 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   const bool b_n_major = h->b.layout == GEMM_ROW_MAJOR;
   if (c.pair && (h->i8x || (b_n_major && (c.bn / 2) % 64 != 0))) c.pair = 0;
   if (c.pair) {
-    h->pair = find_pair(c.bn);
+    h->pair = find_pair(c.bn, c.ksub);
+    if (!h->pair) h->pair = find_pair(c.bn, 1);
     if (!h->pair) c.pair = 0;
   }
+  c.ksub = h->pair ? h->pair->ksub : 1;
   if (!c.pair) {
     if (c.bn == 224) c.bn = 256;
     h->variant = find_variant(c.bn, h->i8x);
@@ -317,6 +320,8 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   kp.num_kb = (int)((h->K + BK - 1) / BK);
   int splits = std::max(1, std::min(c.splits, std::max(1, kp.num_kb)));
   kp.kb_per_split = kp.num_kb > 0 ? (kp.num_kb + splits - 1) / splits : 0;
+  // a ring stage covers ksub K slices: splits start on stage boundaries
+  kp.kb_per_split = (int)round_up(kp.kb_per_split, c.ksub);
   if (kp.kb_per_split > 0) splits = (kp.num_kb + kp.kb_per_split - 1) / kp.kb_per_split;
   kp.splits = splits;
   c.splits = splits;

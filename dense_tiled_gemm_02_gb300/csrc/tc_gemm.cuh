@@ -345,45 +345,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t b_lo0 = sdesc_lo(smem_u32(sB), p.b_mn ? 8192u : 16u);
       const uint32_t dhi = sdesc_hi_sw128(1024u);
       // one 16-wide K step: 32 bytes along a K-major row, 16 rows of an MN-major tile
-      const uint32_t a_kstep = p.a_mn ? (2048u >> 4) : (32u >> 4);
-      const uint32_t b_kstep = p.b_mn ? (2048u >> 4) : (32u >> 4);
+      uint32_t a_off[BK / 16], b_off[BK / 16];
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk) {
+        a_off[kk] = kk * (p.a_mn ? (2048u >> 4) : (32u >> 4));
+        b_off[kk] = kk * (p.b_mn ? (2048u >> 4) : (32u >> 4));
+      }
       uint32_t s = 0, ph = 0, acc_it = 0;
       bool stop = false;
       for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
         const Unit w = decode_unit(p, u, BN);
-        int kc = 0;  // K slices into the current accumulation pass
-        uint32_t buf = 0, d_tmem = 0;
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (kc == 0) {
-            buf = acc_it & 1u;
-            if (!bounded_wait(acc_empty(buf), ((acc_it >> 1) & 1u) ^ 1u, abort_flag, p.status,
-                              STATUS_TIMEOUT, tmo)) {
-              stop = true;
-              break;
-            }
-            tc_fence_after();
-            d_tmem = tmem_base + buf * BN;
-          }
-          if (!bounded_wait(full(s), ph, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
+        // One accumulation pass per chunk of kb_per_chunk K slices (the whole
+        // K range except in exact-int8 mode).
+        for (int c0 = w.kb0; c0 < w.kb1 && !stop; c0 += p.kb_per_chunk) {
+          const int c1 = min(w.kb1, c0 + p.kb_per_chunk);
+          const uint32_t buf = acc_it & 1u;
+          if (!bounded_wait(acc_empty(buf), ((acc_it >> 1) & 1u) ^ 1u, abort_flag, p.status,
+                            STATUS_TIMEOUT, tmo)) {
             stop = true;
             break;
           }
-          const uint32_t a_lo = a_lo0 + s * (Cfg::A_BYTES >> 4);
-          const uint32_t b_lo = b_lo0 + s * (Cfg::B_BYTES >> 4);
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * BN;
+          uint32_t accumulate = 0;
+          for (int kb = c0; kb < c1; ++kb) {
+            if (!bounded_wait(full(s), ph, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
+              stop = true;
+              break;
+            }
+            const uint32_t a_lo = a_lo0 + s * (Cfg::A_BYTES >> 4);
+            const uint32_t b_lo = b_lo0 + s * (Cfg::B_BYTES >> 4);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            mma_f16_ss(d_tmem, sdesc(dhi, a_lo + kk * a_kstep), sdesc(dhi, b_lo + kk * b_kstep),
-                       p.idesc, (kc | kk) != 0 ? 1u : 0u);
-          mma_commit(empty(s));
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1u;
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_f16_ss(d_tmem, sdesc(dhi, a_lo + a_off[kk]), sdesc(dhi, b_lo + b_off[kk]),
+                         p.idesc, accumulate | kk);
+            accumulate = 1;
+            mma_commit(empty(s));
+            if (++s == STAGES) {
+              s = 0;
+              ph ^= 1u;
+            }
           }
-          if (++kc == p.kb_per_chunk || kb + 1 == w.kb1) {
-            mma_commit(acc_full(buf));
-            ++acc_it;
-            kc = 0;
-          }
+          if (stop) break;
+          mma_commit(acc_full(buf));
+          ++acc_it;
         }
       }
       // Every MMA issued so far must finish before tensor memory is freed.

@@ -5,9 +5,13 @@
 // B per K-slice; the even CTA issues one 256 x BN x 16 pair MMA per 16-wide
 // K step, which reads A from both CTAs' shared memory and the two B halves
 // from both, and writes each CTA's 128 accumulator rows into that CTA's
-// tensor memory.  Per SM this halves the B bytes that must be staged and
-// read by the tensor core for the same work as the single-CTA 128 x BN
-// tile, which is what keeps the tensor pipe fed.
+// tensor memory.  Per SM this halves the B bytes that must be staged for the
+// same work as the single-CTA 128 x BN tile.
+//
+// A ring stage holds KSUB 64-wide K slices (one 128-byte swizzle atom each),
+// so one barrier wait and one commit cover 4*KSUB MMAs: the single issuing
+// thread has little time between MMAs (the tensor core queues only a few),
+// and every instruction it spends per stage is taken from that slack.
 //
 // Roles per CTA (192 threads) are those of tc_gemm.cuh:
 //   warp 0  TMA producer (both CTAs): waits for its own free stage, loads its
@@ -28,21 +32,23 @@
 
 namespace gb300 {
 
-template <int BN>
+template <int BN, int KSUB>
 struct PairCfg {
-  static constexpr int BNH = BN / 2;                    // B columns staged per CTA
-  static constexpr uint32_t A_BYTES = BM * BK * 2;      // this CTA's 128 rows: 16 KiB
-  static constexpr uint32_t B_BYTES = BNH * BK * 2;
+  static constexpr int BNH = BN / 2;                        // B columns staged per CTA
+  static constexpr uint32_t A_ATOM = BM * BK * 2;           // 128 rows x 64 K: 16 KiB
+  static constexpr uint32_t B_ATOM = BNH * BK * 2;
+  static constexpr uint32_t A_BYTES = KSUB * A_ATOM;        // per stage
+  static constexpr uint32_t B_BYTES = KSUB * B_ATOM;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr uint32_t PAIR_TX = 2 * STAGE_BYTES;  // bytes both CTAs land per stage
+  static constexpr uint32_t PAIR_TX = 2 * STAGE_BYTES;      // bytes both CTAs land per stage
   static constexpr uint32_t TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
   static_assert(BN == 128 || BN == 224 || BN == 256, "pair tile width");
-  static_assert(B_BYTES % 1024 == 0, "stage alignment");
+  static_assert(B_ATOM % 1024 == 0, "stage alignment");
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int KSUB>
 constexpr uint32_t pair_smem_bytes() {
-  return STAGES * PairCfg<BN>::STAGE_BYTES + 256 + 1024;
+  return STAGES * PairCfg<BN, KSUB>::STAGE_BYTES + 256 + 1024;
 }
 
 __device__ __forceinline__ Unit decode_pair_unit(const KParams& p, int u, int bn) {
@@ -58,11 +64,12 @@ __device__ __forceinline__ Unit decode_pair_unit(const KParams& p, int u, int bn
   return w;
 }
 
-template <int BN, int STAGES>
+// kb0/kb1 count 64-wide K slices; a stage covers KSUB of them.
+template <int BN, int STAGES, int KSUB>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const KParams p) {
-  using Cfg = PairCfg<BN>;
+  using Cfg = PairCfg<BN, KSUB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -119,45 +126,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
-      uint32_t it = 0, s = 0, ph = 0;  // it: slices issued; (s, ph): ring slot and phase
+      uint32_t it = 0, s = 0, ph = 0;  // it: stages issued; (s, ph): ring slot and phase
       int64_t skipped = -1;
       bool stop = false;
       for (int u = cid; u < num_units && !stop; u += ncl) {
         const Unit w = decode_pair_unit(p, u, BN);
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        const int am = w.m0 + BM * static_cast<int>(rank);
+        const int bn0 = w.n0 + Cfg::BNH * static_cast<int>(rank);
+        for (int kb = w.kb0; kb < w.kb1; kb += KSUB) {
           if (!bounded_wait(empty(s), ph ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
             stop = true;
             break;
           }
           if (leader && (p.debug_flags & DBG_SKIP_FIRST_FILL) && it == 0) {
             skipped = 0;  // test hook: never arm stage 0, so the MMA wait on it expires
-            ++it;
-            if (++s == STAGES) {
-              s = 0;
-              ph ^= 1u;
+          } else {
+            const uint32_t fb = map_shared_rank(full(s), 0);
+            if (leader) mbar_arrive_expect_tx(full(s), Cfg::PAIR_TX);
+#pragma unroll
+            for (int j = 0; j < KSUB; ++j) {
+              // a K slice past the end still lands (as zeros) and is counted
+              const int k0 = (kb + j) * BK;
+              const uint32_t a_dst = smem_u32(sA + s * Cfg::A_BYTES + j * Cfg::A_ATOM);
+              const uint32_t b_dst = smem_u32(sB + s * Cfg::B_BYTES + j * Cfg::B_ATOM);
+              if (!p.a_mn) {
+                tma_load_2d_pair(a_dst, &tmA, k0, am, fb);
+              } else {
+#pragma unroll
+                for (int i = 0; i < BM / 64; ++i)
+                  tma_load_2d_pair(a_dst + i * 8192u, &tmA, am + 64 * i, k0, fb);
+              }
+              if (!p.b_mn) {
+                tma_load_2d_pair(b_dst, &tmB, k0, bn0, fb);
+              } else {
+#pragma unroll
+                for (int i = 0; i < Cfg::BNH / 64; ++i)
+                  tma_load_2d_pair(b_dst + i * 8192u, &tmB, bn0 + 64 * i, k0, fb);
+              }
             }
-            continue;
-          }
-          const uint32_t fb = map_shared_rank(full(s), 0);
-          if (leader) mbar_arrive_expect_tx(full(s), Cfg::PAIR_TX);
-          const uint32_t a_dst = smem_u32(sA + s * Cfg::A_BYTES);
-          const uint32_t b_dst = smem_u32(sB + s * Cfg::B_BYTES);
-          const int k0 = kb * BK;
-          const int am = w.m0 + BM * static_cast<int>(rank);
-          const int bn0 = w.n0 + Cfg::BNH * static_cast<int>(rank);
-          if (!p.a_mn) {
-            tma_load_2d_pair(a_dst, &tmA, k0, am, fb);
-          } else {
-#pragma unroll
-            for (int j = 0; j < BM / 64; ++j)
-              tma_load_2d_pair(a_dst + j * 8192u, &tmA, am + 64 * j, k0, fb);
-          }
-          if (!p.b_mn) {
-            tma_load_2d_pair(b_dst, &tmB, k0, bn0, fb);
-          } else {
-#pragma unroll
-            for (int j = 0; j < Cfg::BNH / 64; ++j)
-              tma_load_2d_pair(b_dst + j * 8192u, &tmB, bn0 + 64 * j, k0, fb);
           }
           ++it;
           if (++s == STAGES) {
@@ -186,25 +192,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t a_lo0 = sdesc_lo(smem_u32(sA), p.a_mn ? 8192u : 16u);
       const uint32_t b_lo0 = sdesc_lo(smem_u32(sB), p.b_mn ? 8192u : 16u);
       const uint32_t dhi = sdesc_hi_sw128(1024u);
-      const uint32_t a_kstep = p.a_mn ? (2048u >> 4) : (32u >> 4);
-      const uint32_t b_kstep = p.b_mn ? (2048u >> 4) : (32u >> 4);
+      // Offsets (16-byte units) of the 4*KSUB K steps of a stage: 32 bytes
+      // along a K-major row or 16 rows of an MN-major tile per step, one
+      // swizzle atom per 64-wide slice.
+      uint32_t a_off[4 * KSUB], b_off[4 * KSUB];
+#pragma unroll
+      for (int kk = 0; kk < 4 * KSUB; ++kk) {
+        a_off[kk] = (kk / 4) * (Cfg::A_ATOM >> 4) + (kk % 4) * (p.a_mn ? 128u : 2u);
+        b_off[kk] = (kk / 4) * (Cfg::B_ATOM >> 4) + (kk % 4) * (p.b_mn ? 128u : 2u);
+      }
       uint32_t s = 0, ph = 0, acc_it = 0;
       bool stop = false;
       for (int u = cid; u < num_units && !stop; u += ncl) {
         const Unit w = decode_pair_unit(p, u, BN);
-        int kc = 0;
-        uint32_t buf = 0, d_tmem = 0;
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (kc == 0) {
-            buf = acc_it & 1u;
-            if (!bounded_wait(acc_empty(buf), ((acc_it >> 1) & 1u) ^ 1u, abort_flag, p.status,
-                              STATUS_TIMEOUT, tmo)) {
-              stop = true;
-              break;
-            }
-            tc_fence_after();
-            d_tmem = tmem_base + buf * BN;
-          }
+        const uint32_t buf = acc_it & 1u;
+        if (!bounded_wait(acc_empty(buf), ((acc_it >> 1) & 1u) ^ 1u, abort_flag, p.status,
+                          STATUS_TIMEOUT, tmo))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        uint32_t accumulate = 0;
+        for (int kb = w.kb0; kb < w.kb1; kb += KSUB) {
           if (!bounded_wait(full(s), ph, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
             stop = true;
             break;
@@ -212,20 +220,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t a_lo = a_lo0 + s * (Cfg::A_BYTES >> 4);
           const uint32_t b_lo = b_lo0 + s * (Cfg::B_BYTES >> 4);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            mma_f16_ss_pair(d_tmem, sdesc(dhi, a_lo + kk * a_kstep),
-                            sdesc(dhi, b_lo + kk * b_kstep), p.idesc, (kc | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < 4 * KSUB; ++kk)
+            mma_f16_ss_pair(d_tmem, sdesc(dhi, a_lo + a_off[kk]), sdesc(dhi, b_lo + b_off[kk]),
+                            p.idesc, accumulate | kk);
+          accumulate = 1;
           mma_commit_pair_both(empty(s));
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
-          if (++kc == p.kb_per_chunk || kb + 1 == w.kb1) {
-            mma_commit_pair_both(acc_full(buf));
-            ++acc_it;
-            kc = 0;
-          }
         }
+        if (stop) break;
+        mma_commit_pair_both(acc_full(buf));
+        ++acc_it;
       }
       mma_commit_pair_both(done_bar);
       drain_wait(done_bar, 0, 200000000ull);

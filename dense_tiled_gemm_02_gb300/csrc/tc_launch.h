@@ -31,6 +31,7 @@ extern const int kNumVariantsBN64;
 struct PairVariant {
   int bn;
   int stages;
+  int ksub;  // 64-wide K slices per ring stage
   uint32_t smem;
   cudaError_t (*launch)(const CUtensorMap&, const CUtensorMap&, const KParams&, int grid,
                         cudaStream_t);

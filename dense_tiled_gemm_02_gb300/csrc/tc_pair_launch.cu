@@ -8,12 +8,12 @@
 namespace gb300 {
 
 namespace {
-template <int BN, int STAGES>
+template <int BN, int STAGES, int KSUB>
 cudaLaunchConfig_t pair_config(int grid, cudaStream_t st, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = pair_smem_bytes<BN, STAGES>();
+  cfg.dynamicSmemBytes = pair_smem_bytes<BN, STAGES, KSUB>();
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -24,27 +24,28 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t st, cudaLaunchAttribute* a
   return cfg;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int KSUB>
 cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const KParams& p, int grid,
                         cudaStream_t st) {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pair_config<BN, STAGES>(grid, st, attr);
-  return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES>, a, b, p);
+  cudaLaunchConfig_t cfg = pair_config<BN, STAGES, KSUB>(grid, st, attr);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, KSUB>, a, b, p);
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int KSUB>
 cudaError_t prepare_pair() {
-  return cudaFuncSetAttribute(tc_gemm_pair_kernel<BN, STAGES>,
+  return cudaFuncSetAttribute(tc_gemm_pair_kernel<BN, STAGES, KSUB>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              pair_smem_bytes<BN, STAGES>());
+                              pair_smem_bytes<BN, STAGES, KSUB>());
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int KSUB>
 int max_clusters_pair() {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pair_config<BN, STAGES>(2, nullptr, attr);
+  cudaLaunchConfig_t cfg = pair_config<BN, STAGES, KSUB>(2, nullptr, attr);
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<BN, STAGES>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<BN, STAGES, KSUB>, &cfg) !=
+      cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -52,11 +53,12 @@ int max_clusters_pair() {
 }
 }  // namespace
 
-#define GB_PAIR(BN_, ST_)                                                          \
-  PairVariant{BN_, ST_, pair_smem_bytes<BN_, ST_>(), &launch_pair<BN_, ST_>,       \
-              &prepare_pair<BN_, ST_>, &max_clusters_pair<BN_, ST_>}
+#define GB_PAIR(BN_, ST_, KS_)                                                            \
+  PairVariant{BN_, ST_, KS_, pair_smem_bytes<BN_, ST_, KS_>(), &launch_pair<BN_, ST_, KS_>, \
+              &prepare_pair<BN_, ST_, KS_>, &max_clusters_pair<BN_, ST_, KS_>}
 
-const PairVariant kPairVariants[] = {GB_PAIR(256, 6), GB_PAIR(224, 7), GB_PAIR(128, 8)};
-const int kNumPairVariants = 3;
+const PairVariant kPairVariants[] = {GB_PAIR(256, 6, 1), GB_PAIR(256, 3, 2), GB_PAIR(224, 7, 1),
+                                     GB_PAIR(128, 8, 1), GB_PAIR(128, 4, 2)};
+const int kNumPairVariants = 5;
 
 }  // namespace gb300

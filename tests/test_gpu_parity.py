@@ -33,13 +33,15 @@ def _assert_ok(rep, what):
 
 
 # ------------------------------------------------------------------ closed forms, bit-exact
-PERM_PLANS = [(bn, 0) for bn in (64, 128, 256)] + [(bn, 1) for bn in (128, 224, 256)]
+PERM_PLANS = ([(bn, 0, 1) for bn in (64, 128, 256)] + [(bn, 1, 1) for bn in (128, 224, 256)]
+              + [(bn, 1, 2) for bn in (128, 256)])
 
 
-@pytest.mark.parametrize("bn,pair", PERM_PLANS, ids=[f"bn{b}-pair{p}" for b, p in PERM_PLANS])
+@pytest.mark.parametrize("bn,pair,ksub", PERM_PLANS,
+                         ids=[f"bn{b}-pair{p}-ksub{k}" for b, p, k in PERM_PLANS])
 @pytest.mark.parametrize("a_col,b_col", list(itertools.product((ROW, COL), repeat=2)))
 @pytest.mark.parametrize("swap", [0, 1])
-def test_permutation_is_exact(bn, pair, a_col, b_col, swap):
+def test_permutation_is_exact(bn, pair, ksub, a_col, b_col, swap):
     """A = P (a permutation): D = P B exactly, for every operand layout and
     both the single-CTA and the CTA-pair kernels."""
     M = K = 320
@@ -52,7 +54,7 @@ def test_permutation_is_exact(bn, pair, a_col, b_col, swap):
     w = Workload("perm", 0, M, N, K, BF16, None, BF16, "normal", a_col, b_col, ROW, ROW)
     inp = {"A": P if a_col == ROW else P.t().contiguous(),
            "B": B if b_col == ROW else B.t().contiguous(), "C": None}
-    D, plan = run_gpu(w, inp, plan=f"bn={bn},swap={swap},pair={pair}")
+    D, plan = run_gpu(w, inp, plan=f"bn={bn},swap={swap},pair={pair},ksub={ksub}")
     assert torch.equal(D.view(torch.int16), B[perm].view(torch.int16)), plan
 
 
@@ -76,7 +78,8 @@ def test_identity_plus_c(bn):
 @pytest.mark.parametrize("plan", [None, "bn=64", "bn=128", "bn=256", "bn=128,splits=3",
                                   "bn=64,group=1", "bn=128,swap=1", "pair=1,bn=256",
                                   "pair=1,bn=128", "pair=1,bn=224", "pair=1,bn=256,splits=2",
-                                  "pair=1,bn=128,swap=1"])
+                                  "pair=1,bn=128,swap=1", "pair=1,bn=256,ksub=2",
+                                  "pair=1,bn=256,ksub=2,splits=3", "pair=1,bn=128,ksub=2"])
 def test_small_config(name, plan):
     w = WORKLOADS[name]
     inp = make_inputs(w)
@@ -102,7 +105,7 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("plan", [None, "pair=1"])
+@pytest.mark.parametrize("plan", [None, "pair=1", "pair=1,ksub=2"])
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"{s[0]}x{s[1]}x{s[2]}-{s[3]}{s[4]}{s[5]}{s[6]}"
                                                for s in SHAPES])
 def test_ragged_shapes(shape, plan):
@@ -155,7 +158,8 @@ def test_side_stream_and_reuse():
 FULL = [("sq4096_bf16", None), ("sq4096_bf16", "pair=1,bn=256"), ("sq4096_bf16", "pair=1,bn=224"),
         ("sq4096_bf16", "pair=0,bn=256"), ("skinny64x8192x8192_bf16", None),
         ("skinny8192x128x4096_bf16", None), ("rag4095x4097x4099_bf16", None),
-        ("rag4095x4097x4099_bf16", "pair=1,bn=256")]
+        ("rag4095x4097x4099_bf16", "pair=1,bn=256"), ("sq4096_bf16", "pair=1,bn=256,ksub=2"),
+        ("rag4095x4097x4099_bf16", "pair=1,bn=256,ksub=2")]
 
 
 @pytest.mark.parametrize("name,plan", FULL, ids=[f"{n}-{p}" for n, p in FULL])
