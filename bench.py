@@ -360,7 +360,7 @@ def main():
 def kernel_name(plan: str) -> str:
     f = dict(kv.split("=") for kv in plan.split() if "=" in kv)
     if f.get("pair") == "1":
-        return f"tc_gemm_pair_kernel<{f['bn']}, {f['stages']}>"
+        return f"tc_gemm_pair_kernel<{f['bn']}, {f['stages']}, {f.get('ksub', '1')}>"
     return f"tc_gemm_kernel<{f['bn']}, {f['stages']}, {f.get('i8x', '0')}>"
 
 

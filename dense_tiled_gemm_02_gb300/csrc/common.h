@@ -49,6 +49,15 @@ struct KParams {
   uint32_t* status;              // device status word
   unsigned long long timeout_ns; // bound of every device-side wait
   int debug_flags;
+  // Last-wave split (pair kernel): tiles from tail_start on (in raster
+  // order) are each computed as two K halves by two clusters; the second
+  // half leaves its fp32 partial in tail_ws and raises tail_flags to
+  // epoch, the first half adds it and finishes the tile.
+  int tail_start;                // first split tile (= number of whole tiles)
+  int tail_parts;                // 1 = no split, 2 = split in two K halves
+  float* tail_ws;                // [split tile][CTA half][128 rows][BN] fp32
+  uint32_t* tail_flags;          // [split tile][CTA half]
+  uint32_t epoch;                // value the flags take during this run
 };
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator

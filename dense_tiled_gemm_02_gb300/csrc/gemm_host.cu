@@ -99,13 +99,18 @@ struct gemm_plan {
   void* ws = nullptr;
   size_t ws_bytes = 0;
   size_t ws_partial_off = 0;
+  size_t ws_tail_off = 0, ws_flags_off = 0;  // last-wave partials and their flags
+  uint32_t epoch = 0;                         // flag value of the latest run
   uint32_t* status = nullptr;
   int debug_flags = 0;
   uint64_t timeout_ns = kDefaultTimeoutNs;
-  // tensor-map cache
-  const void* last_a = nullptr;
-  const void* last_b = nullptr;
-  CUtensorMap tm_a{}, tm_b{};
+  // Tensor maps of recently seen operand addresses (a few entries per
+  // operand, replaced round-robin): encoding one costs microseconds of host
+  // time, which short GEMMs cannot hide.
+  static constexpr int kMapCache = 8;
+  const void* map_ptr[2][kMapCache] = {};
+  CUtensorMap map[2][kMapCache] = {};
+  int map_next[2] = {0, 0};
   std::string plan_str;
 };
 
@@ -162,6 +167,7 @@ void apply_force_plan(PlanChoice& c) {
       else if (k == "grid") c.max_ctas = v;
       else if (k == "pair") c.pair = v;
       else if (k == "ksub") c.ksub = v;
+      else if (k == "tail") c.tail = v;
     }
     pos = end + 1;
   }
@@ -171,13 +177,15 @@ void make_plan_string(gemm_plan* h) {
   char buf[512];
   std::snprintf(buf, sizeof buf,
                 "M=%lld N=%lld K=%lld swap=%d pair=%d bn=%d ksub=%d stages=%d group_m=%d "
-                "splits=%d kb_per_split=%d grid=%d i8x=%d a_mn=%d b_mn=%d repack_a=%d repack_b=%d "
-                "ws_bytes=%zu",
+                "splits=%d kb_per_split=%d tail=%d grid=%d i8x=%d a_mn=%d b_mn=%d repack_a=%d "
+                "repack_b=%d ws_bytes=%zu",
                 (long long)h->desc.M, (long long)h->desc.N, (long long)h->desc.K, h->choice.swap,
                 h->pair ? 1 : 0, h->choice.bn, h->choice.ksub,
                 h->pair ? h->pair->stages : (h->variant ? h->variant->stages : 0), h->kp.group_m,
                 h->kp.splits,
-                h->kp.kb_per_split, h->grid, (int)h->i8x, h->kp.a_mn, h->kp.b_mn,
+                h->kp.kb_per_split,
+                h->kp.tail_parts > 1 ? h->kp.tiles_m * h->kp.tiles_n - h->kp.tail_start : 0,
+                h->grid, (int)h->i8x, h->kp.a_mn, h->kp.b_mn,
                 (int)h->a.repack, (int)h->b.repack, h->ws_bytes);
   h->plan_str = buf;
 }
@@ -300,7 +308,6 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   }
   c.ksub = h->pair ? h->pair->ksub : 1;
   if (!c.pair) {
-    if (c.bn == 224) c.bn = 256;
     h->variant = find_variant(c.bn, h->i8x);
     if (!h->variant) {
       delete h;
@@ -341,12 +348,43 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   if (c.max_ctas > 0) max_ctas = std::min(max_ctas, c.max_ctas);
   if (!c.pair) h->grid = (int)std::max<int64_t>(1, std::min<int64_t>(units, max_ctas));
 
-  // Workspace: operand copies the TMA unit can read, then split-K partials.
+  // Kernel attributes and, for the pair kernel, how many 2-CTA clusters
+  // can be resident at once (the persistent grid).
+  const cudaError_t prep = h->pair ? h->pair->prepare() : h->variant->prepare();
+  int clusters = 0;
+  if (prep == cudaSuccess && h->pair) {
+    clusters = h->pair->max_clusters();
+    if (c.max_ctas > 0) clusters = std::min(clusters, c.max_ctas / 2);
+  }
+  if (prep != cudaSuccess || (h->pair && clusters <= 0)) {
+    cudaGetLastError();
+    delete h;
+    return GEMM_ERR_CUDA;
+  }
+  // Last-wave split: when the tiles leave a partial final wave that fits
+  // twice over into the clusters, its tiles are computed as two K halves.
+  const int64_t tiles = (int64_t)kp.tiles_m * kp.tiles_n;
+  kp.tail_parts = 1;
+  kp.tail_start = (int)tiles;
+  int64_t tail_tiles = 0;
+  if (h->pair && c.tail && kp.splits == 1 && tiles >= clusters && kp.num_kb >= 4 * c.ksub) {
+    const int64_t rem = tiles % clusters;
+    if (rem > 0 && 2 * rem <= clusters) {
+      tail_tiles = rem;
+      kp.tail_parts = 2;
+      kp.tail_start = (int)(tiles - rem);
+    }
+  }
+  const int64_t units_all =
+      kp.tail_parts > 1 ? kp.tail_start + tail_tiles * kp.tail_parts : units;
+  if (h->pair) h->grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(units_all, clusters));
+
+  // Workspace: operand copies the TMA unit can read, split-K partials, and
+  // the last-wave partials with their flags.
   size_t off = 0;
-  auto plan_copy = [&](Operand& o, bool k_major, int64_t in_es) {
+  auto plan_copy = [&](Operand& o, int64_t in_es) {
     const int64_t inner = o.layout == GEMM_ROW_MAJOR ? o.cols : o.rows;
     const int64_t outer = o.layout == GEMM_ROW_MAJOR ? o.rows : o.cols;
-    (void)k_major;
     o.repack = h->i8x || ((o.ld * in_es) % 16 != 0);
     if (!o.repack) return;
     o.ws_ld = round_up(std::max<int64_t>(inner, 1), 8);
@@ -354,8 +392,8 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     off += (size_t)round_up(o.ws_ld * outer * 2, 256);
   };
   const int64_t in_es = elem_size(d.ab_type);
-  plan_copy(h->a, kp.a_mn == 0, in_es);
-  plan_copy(h->b, kp.b_mn == 1, in_es);
+  plan_copy(h->a, in_es);
+  plan_copy(h->b, in_es);
   if (kp.splits > 1) {
     h->ws_partial_off = off;
     off += (size_t)round_up((int64_t)kp.splits * h->M * h->N * 4, 256);
@@ -364,32 +402,31 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     kp.ws_cs = row ? 1 : h->M;
     kp.ws_split = h->M * h->N;
   }
+  if (tail_tiles > 0) {
+    h->ws_tail_off = off;
+    off += (size_t)round_up(tail_tiles * 2 * BM * c.bn * 4, 256);
+    h->ws_flags_off = off;
+    off += (size_t)round_up(tail_tiles * 2 * 4, 256);
+  }
   h->ws_bytes = off;
   if (off > 0 && cudaMalloc(&h->ws, off) != cudaSuccess) {
     cudaGetLastError();
     delete h;
     return GEMM_ERR_ALLOC_FAILED;
   }
+  if (tail_tiles > 0 &&
+      cudaMemset(static_cast<char*>(h->ws) + h->ws_flags_off, 0, tail_tiles * 2 * 4) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->ws);
+    delete h;
+    return GEMM_ERR_CUDA;
+  }
   if (cudaMalloc(&h->status, 256) != cudaSuccess || cudaMemset(h->status, 0, 256) != cudaSuccess) {
     cudaGetLastError();
     if (h->ws) cudaFree(h->ws);
     delete h;
     return GEMM_ERR_ALLOC_FAILED;
-  }
-  const cudaError_t prep = h->pair ? h->pair->prepare() : h->variant->prepare();
-  int clusters = 0;
-  if (prep == cudaSuccess && h->pair) {
-    // one persistent 2-CTA cluster per resident slot, at most one per tile
-    clusters = h->pair->max_clusters();
-    if (c.max_ctas > 0) clusters = std::min(clusters, c.max_ctas / 2);
-    h->grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(units, clusters));
-  }
-  if (prep != cudaSuccess || (h->pair && clusters <= 0)) {
-    cudaGetLastError();
-    cudaFree(h->status);
-    if (h->ws) cudaFree(h->ws);
-    delete h;
-    return GEMM_ERR_CUDA;
   }
   make_plan_string(h);
   const char* lg = std::getenv("GEMM_LOG");
@@ -456,24 +493,33 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
   const int64_t lda_eff = h->a.repack ? h->a.ws_ld : h->a.ld;
   const int64_t ldb_eff = h->b.repack ? h->b.ws_ld : h->b.ld;
 
-  if (ta != h->last_a) {
-    if (encode_operand(&h->tm_a, ta, lda_eff, kp.a_mn == 0, h->M, h->K, BM) != GEMM_OK) {
-      h->last_a = nullptr;
-      return GEMM_ERR_CUDA;
-    }
-    h->last_a = ta;
-  }
-  if (tb != h->last_b) {
-    const int b_box = h->pair ? h->choice.bn / 2 : h->choice.bn;  // B rows staged per CTA
-    if (encode_operand(&h->tm_b, tb, ldb_eff, kp.b_mn == 0, h->N, h->K, b_box) != GEMM_OK) {
-      h->last_b = nullptr;
-      return GEMM_ERR_CUDA;
-    }
-    h->last_b = tb;
+  const int b_box = h->pair ? h->choice.bn / 2 : h->choice.bn;  // B rows staged per CTA
+  const CUtensorMap* tm[2] = {nullptr, nullptr};
+  for (int which = 0; which < 2; ++which) {
+    const void* base = which == 0 ? ta : tb;
+    for (int i = 0; i < gemm_plan::kMapCache; ++i)
+      if (h->map_ptr[which][i] == base) tm[which] = &h->map[which][i];
+    if (tm[which]) continue;
+    const int slot = h->map_next[which];
+    h->map_next[which] = (slot + 1) % gemm_plan::kMapCache;
+    h->map_ptr[which][slot] = nullptr;
+    const int rc = which == 0
+                       ? encode_operand(&h->map[0][slot], ta, lda_eff, kp.a_mn == 0, h->M, h->K, BM)
+                       : encode_operand(&h->map[1][slot], tb, ldb_eff, kp.b_mn == 0, h->N, h->K,
+                                        b_box);
+    if (rc != GEMM_OK) return GEMM_ERR_CUDA;
+    h->map_ptr[which][slot] = base;
+    tm[which] = &h->map[which][slot];
   }
   if (kp.splits > 1) kp.ws = reinterpret_cast<float*>(ws + h->ws_partial_off);
-  const cudaError_t le = h->pair ? h->pair->launch(h->tm_a, h->tm_b, kp, h->grid, st)
-                                 : h->variant->launch(h->tm_a, h->tm_b, kp, h->grid, st);
+  if (kp.tail_parts > 1) {
+    kp.tail_ws = reinterpret_cast<float*>(ws + h->ws_tail_off);
+    kp.tail_flags = reinterpret_cast<uint32_t*>(ws + h->ws_flags_off);
+    if (++h->epoch == 0) h->epoch = 1;  // flags start at 0: never reuse it
+    kp.epoch = h->epoch;
+  }
+  const cudaError_t le = h->pair ? h->pair->launch(*tm[0], *tm[1], kp, h->grid, st)
+                                 : h->variant->launch(*tm[0], *tm[1], kp, h->grid, st);
   if (le != cudaSuccess) return GEMM_ERR_CUDA;
   if (kp.splits > 1 && launch_reduce(kp, row_order, h->num_sms, st) != cudaSuccess)
     return GEMM_ERR_CUDA;

@@ -22,6 +22,7 @@ struct PlanChoice {
   int max_ctas;  // 0 = one CTA per SM
   int pair;      // 1: CTA-pair kernel (cta_group::2), tile 256 x bn
   int ksub;      // pair kernel: 64-wide K slices per ring stage (1 or 2)
+  int tail;      // pair kernel: split the tiles of a partial last wave in two K halves
 };
 
 struct PlanRow {
@@ -32,7 +33,7 @@ struct PlanRow {
 
 // Measured rows (exact shape match).
 static const PlanRow kTable[] = {
-    {0, 0, 0, -1, -1, -1, {0, 0, 0, 0, 0, 0, 0}},  // sentinel
+    {0, 0, 0, -1, -1, -1, {0, 0, 0, 0, 0, 0, 0, 0}},  // sentinel
 };
 
 inline int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -44,7 +45,7 @@ inline PlanChoice choose_plan(int64_t M, int64_t N, int64_t K, int ab_type, int 
         (r.layout_a < 0 || r.layout_a == layout_a) && (r.layout_b < 0 || r.layout_b == layout_b))
       return r.choice;
   }
-  PlanChoice c{256, 8, 1, 0, 0, 0, 1};
+  PlanChoice c{256, 8, 1, 0, 0, 0, 1, 1};
   // Skinny M: put the long N dimension on the 128-row tensor-core side.
   if (M < 128 && N >= 2 * M) c.swap = 1;
   const int64_t Mi = c.swap ? N : M;

@@ -83,6 +83,43 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
   return true;
 }
 
+// ---------------------------------------------------------------- flags in global memory
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Barrier among `nthreads` threads (a multiple of 32) on hardware barrier id.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Wait until *flag == value, with the same bound and abort rules as
+// bounded_wait.
+__device__ __forceinline__ bool bounded_flag_wait(const uint32_t* flag, uint32_t value,
+                                                  volatile int* abort, uint32_t* status,
+                                                  uint32_t code, uint64_t timeout_ns) {
+  if (ld_acquire_gpu(flag) == value) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(flag) == value) return true;
+    if ((n & 31u) == 0u) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > timeout_ns) {
+        *abort = 1;
+        atomicOr(status, code);
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

@@ -47,6 +47,9 @@ constexpr uint32_t smem_bytes() {
 
 struct Unit {
   int m0, n0, kb0, kb1, split;
+  int tail;  // 1: a K half of a last-wave tile (pair kernel)
+  int part;  // which half: 0 finishes the tile, 1 leaves its partial sums
+  int ti;    // index of the split tile
 };
 
 __device__ __forceinline__ Unit decode_unit(const KParams& p, int u, int bn) {
@@ -59,6 +62,9 @@ __device__ __forceinline__ Unit decode_unit(const KParams& p, int u, int bn) {
   w.n0 = static_cast<int>(pn) * bn;
   w.kb0 = w.split * p.kb_per_split;
   w.kb1 = min(p.num_kb, w.kb0 + p.kb_per_split);
+  w.tail = 0;
+  w.part = 0;
+  w.ti = 0;
   return w;
 }
 
@@ -136,6 +142,42 @@ __device__ __forceinline__ void add_c_f(const KParams& p, int r, int c0, float (
   for (int j = 0; j < 32; ++j) {
     const int c = c0 + j;
     if (c < p.N) f[j] += load_elem_f(p.C, p.c_type, r * p.c_rs + c * p.c_cs);
+  }
+}
+
+// C of one thread's whole tile row (16-bit C, rows contiguous and 16-byte
+// aligned, tile inside N), loaded before the accumulator is ready so that
+// its latency hides under the main loop; ok = false selects the per-chunk
+// path above.
+template <int BN>
+struct CRow {
+  uint4 v[BN / 8];
+  bool ok;
+};
+
+template <int BN>
+__device__ __forceinline__ void prefetch_c_row(const KParams& p, int r, int n0, CRow<BN>& c) {
+  c.ok = p.C != nullptr && p.splits == 1 && p.c_vec && p.c_type != T_F32 && r < p.M &&
+         n0 + BN <= p.N;
+  if (!c.ok) return;
+  const uint4* src =
+      reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.C) + r * p.c_rs + n0);
+#pragma unroll
+  for (int i = 0; i < BN / 8; ++i) c.v[i] = __ldg(src + i);
+}
+
+// f += the 32 prefetched C values starting at uint4 index q (8 values each).
+__device__ __forceinline__ void add_c_prefetched(int c_type, const uint4* q, float (&f)[32]) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint32_t w[4] = {q[v].x, q[v].y, q[v].z, q[v].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float lo, hi;
+      unpack2(c_type, w[e], lo, hi);
+      f[8 * v + 2 * e] += lo;
+      f[8 * v + 2 * e + 1] += hi;
+    }
   }
 }
 
@@ -406,6 +448,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Unit w = decode_unit(p, u, BN);
       const int r = w.m0 + q * 32 + lane;
       if constexpr (!I8X) {
+        CRow<BN> crow;
+        prefetch_c_row<BN>(p, r, w.n0, crow);
         const uint32_t buf = acc_it & 1u;
         if (!bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status,
                           STATUS_TIMEOUT, tmo)) {
@@ -413,6 +457,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         tc_fence_after();
+#pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem_base + lane_base + buf * BN + c * 32, v);
@@ -428,7 +473,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (p.splits > 1) {
             store_partial(p, r, c0, w.split, f);
           } else {
-            add_c_f(p, r, c0, f);
+            if (crow.ok)
+              add_c_prefetched(p.c_type, crow.v + 4 * c, f);
+            else
+              add_c_f(p, r, c0, f);
             store_d_f(p, r, c0, f);
           }
         }

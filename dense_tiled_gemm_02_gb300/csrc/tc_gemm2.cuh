@@ -42,7 +42,7 @@ struct PairCfg {
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t PAIR_TX = 2 * STAGE_BYTES;      // bytes both CTAs land per stage
   static constexpr uint32_t TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
-  static_assert(BN == 128 || BN == 224 || BN == 256, "pair tile width");
+  static_assert(BN == 128 || BN == 256, "pair tile width");
   static_assert(B_ATOM % 1024 == 0, "stage alignment");
 };
 
@@ -51,16 +51,42 @@ constexpr uint32_t pair_smem_bytes() {
   return STAGES * PairCfg<BN, KSUB>::STAGE_BYTES + 256 + 1024;
 }
 
+// Units: whole 256 x BN tiles (or split-K pieces), then, when the last
+// wave is split, two K halves per remaining tile.
+__device__ __forceinline__ int pair_num_units(const KParams& p) {
+  const int tiles = p.tiles_m * p.tiles_n;
+  return p.tail_parts > 1 ? p.tail_start + (tiles - p.tail_start) * p.tail_parts
+                          : tiles * p.splits;
+}
+
+template <int KSUB>
 __device__ __forceinline__ Unit decode_pair_unit(const KParams& p, int u, int bn) {
   Unit w;
-  const int t = u / p.splits;
-  w.split = u - t * p.splits;
+  int t;
+  if (p.tail_parts > 1 && u >= p.tail_start) {
+    const int v = u - p.tail_start;
+    w.ti = v / p.tail_parts;
+    w.part = v - w.ti * p.tail_parts;
+    w.tail = 1;
+    w.split = 0;
+    t = p.tail_start + w.ti;
+    const int per = (p.num_kb + p.tail_parts - 1) / p.tail_parts;
+    const int half = (per + KSUB - 1) / KSUB * KSUB;  // halves start on stage boundaries
+    w.kb0 = w.part * half;
+    w.kb1 = min(p.num_kb, w.kb0 + half);
+  } else {
+    t = u / p.splits;
+    w.split = u - t * p.splits;
+    w.tail = 0;
+    w.part = 0;
+    w.ti = 0;
+    w.kb0 = w.split * p.kb_per_split;
+    w.kb1 = min(p.num_kb, w.kb0 + p.kb_per_split);
+  }
   int64_t pm, pn;
   raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
   w.m0 = static_cast<int>(pm) * (2 * BM);
   w.n0 = static_cast<int>(pn) * bn;
-  w.kb0 = w.split * p.kb_per_split;
-  w.kb1 = min(p.num_kb, w.kb0 + p.kb_per_split);
   return w;
 }
 
@@ -118,7 +144,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  const int num_units = p.tiles_m * p.tiles_n * p.splits;
+  const int num_units = pair_num_units(p);
   const int cid = blockIdx.x >> 1;
   const int ncl = gridDim.x >> 1;
   const uint64_t tmo = p.timeout_ns;
@@ -130,7 +156,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int64_t skipped = -1;
       bool stop = false;
       for (int u = cid; u < num_units && !stop; u += ncl) {
-        const Unit w = decode_pair_unit(p, u, BN);
+        const Unit w = decode_pair_unit<KSUB>(p, u, BN);
         const int am = w.m0 + BM * static_cast<int>(rank);
         const int bn0 = w.n0 + Cfg::BNH * static_cast<int>(rank);
         for (int kb = w.kb0; kb < w.kb1; kb += KSUB) {
@@ -204,7 +230,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t s = 0, ph = 0, acc_it = 0;
       bool stop = false;
       for (int u = cid; u < num_units && !stop; u += ncl) {
-        const Unit w = decode_pair_unit(p, u, BN);
+        const Unit w = decode_pair_unit<KSUB>(p, u, BN);
         const uint32_t buf = acc_it & 1u;
         if (!bounded_wait(acc_empty(buf), ((acc_it >> 1) & 1u) ^ 1u, abort_flag, p.status,
                           STATUS_TIMEOUT, tmo))
@@ -244,13 +270,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     uint32_t acc_it = 0;
     for (int u = cid; u < num_units; u += ncl) {
-      const Unit w = decode_pair_unit(p, u, BN);
+      const Unit w = decode_pair_unit<KSUB>(p, u, BN);
       const int r = w.m0 + BM * static_cast<int>(rank) + q * 32 + lane;
+      const bool leaves_partial = w.tail && w.part == 1;
+      CRow<BN> crow;
+      if (!leaves_partial)
+        prefetch_c_row<BN>(p, r, w.n0, crow);
+      else
+        crow.ok = false;
       const uint32_t buf = acc_it & 1u;
       if (!bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status, STATUS_TIMEOUT,
                         tmo))
         break;
       tc_fence_after();
+      // The split tile's fp32 partial sums (one CTA half), stored so that the
+      // 128 threads' float4s of each 4-column group are adjacent: a warp then
+      // moves 512 contiguous bytes per access instead of 32 scattered pieces.
+      float4* pbase = w.tail ? reinterpret_cast<float4*>(
+                                   p.tail_ws + static_cast<size_t>(w.ti * 2 + rank) * BM * BN) +
+                                   (q * 32 + lane)
+                             : nullptr;
+      uint32_t* flag = w.tail ? p.tail_flags + w.ti * 2 + rank : nullptr;
+      if (w.tail && w.part == 0 &&
+          !bounded_flag_wait(flag, p.epoch, abort_flag, p.status, STATUS_TIMEOUT, tmo))
+        break;
+#pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem_base + lane_base + buf * BN + c * 32, v);
@@ -264,11 +308,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
         const int c0 = w.n0 + c * 32;
+        if (leaves_partial) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            pbase[(c * 8 + j) * BM] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2],
+                                                  f[4 * j + 3]);
+          continue;
+        }
+        if (w.tail) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 x = pbase[(c * 8 + j) * BM];
+            f[4 * j] += x.x;
+            f[4 * j + 1] += x.y;
+            f[4 * j + 2] += x.z;
+            f[4 * j + 3] += x.w;
+          }
+        }
         if (p.splits > 1) {
           store_partial(p, r, c0, w.split, f);
         } else {
-          add_c_f(p, r, c0, f);
+          if (crow.ok)
+            add_c_prefetched(p.c_type, crow.v + 4 * c, f);
+          else
+            add_c_f(p, r, c0, f);
           store_d_f(p, r, c0, f);
+        }
+      }
+      if (leaves_partial) {
+        // Publish: every epilogue thread of this CTA has written its row.
+        __threadfence();
+        named_barrier_sync(1, 128);
+        if (warp == 2 && lane == 0) {
+          __threadfence();
+          st_release_gpu(flag, p.epoch);
         }
       }
       ++acc_it;

@@ -57,8 +57,8 @@ int max_clusters_pair() {
   PairVariant{BN_, ST_, KS_, pair_smem_bytes<BN_, ST_, KS_>(), &launch_pair<BN_, ST_, KS_>, \
               &prepare_pair<BN_, ST_, KS_>, &max_clusters_pair<BN_, ST_, KS_>}
 
-const PairVariant kPairVariants[] = {GB_PAIR(256, 6, 1), GB_PAIR(256, 3, 2), GB_PAIR(224, 7, 1),
-                                     GB_PAIR(128, 8, 1), GB_PAIR(128, 4, 2)};
-const int kNumPairVariants = 5;
+const PairVariant kPairVariants[] = {GB_PAIR(256, 6, 1), GB_PAIR(256, 3, 2), GB_PAIR(128, 8, 1),
+                                     GB_PAIR(128, 4, 2)};
+const int kNumPairVariants = 4;
 
 }  // namespace gb300
