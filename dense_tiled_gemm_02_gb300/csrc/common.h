@@ -43,6 +43,7 @@ struct KParams {
   int d_type;
   long long d_rs, d_cs;
   int d_vec;                     // D rows contiguous and 16-byte aligned
+  int d_tma;                     // 16-bit D stored through shared memory by TMA (pair kernel)
   int c_vec;                     // C rows contiguous and 16-byte aligned
   float* ws;                     // split-K partial sums (fp32), or null
   long long ws_rs, ws_cs, ws_split;

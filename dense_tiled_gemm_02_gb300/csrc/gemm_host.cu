@@ -108,9 +108,9 @@ struct gemm_plan {
   // operand, replaced round-robin): encoding one costs microseconds of host
   // time, which short GEMMs cannot hide.
   static constexpr int kMapCache = 8;
-  const void* map_ptr[2][kMapCache] = {};
-  CUtensorMap map[2][kMapCache] = {};
-  int map_next[2] = {0, 0};
+  const void* map_ptr[3][kMapCache] = {};  // A', B', D
+  CUtensorMap map[3][kMapCache] = {};
+  int map_next[3] = {0, 0, 0};
   std::string plan_str;
 };
 
@@ -214,6 +214,22 @@ int encode_operand(CUtensorMap* tm, const void* base, int64_t ld, bool k_major, 
   strides[0] = (cuuint64_t)ld * 2;
   CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// Tensor map of a row-contiguous 16-bit D (internal coordinates): dims
+// {N, M}, box {64, 128} with 128-byte swizzle, for stores from the staging
+// buffers of the pair kernel.
+int encode_store_d(CUtensorMap* tm, void* base, int64_t ld, int64_t M, int64_t N) {
+  EncodeFn enc = get_encode();
+  if (!enc) return GEMM_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)BM};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -518,7 +534,27 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
     if (++h->epoch == 0) h->epoch = 1;  // flags start at 0: never reuse it
     kp.epoch = h->epoch;
   }
-  const cudaError_t le = h->pair ? h->pair->launch(*tm[0], *tm[1], kp, h->grid, st)
+  // The pair kernel stores a 16-bit, row-contiguous D with TMA from swizzled
+  // shared memory (rows 16-byte aligned, as TMA requires).
+  const CUtensorMap* tmd = tm[0];  // placeholder argument when D is stored directly
+  kp.d_tma = (h->pair && kp.splits == 1 && kp.d_vec && (d.d_type == GEMM_BF16 ||
+                                                         d.d_type == GEMM_F16)) ? 1 : 0;
+  if (kp.d_tma) {
+    const CUtensorMap* hit = nullptr;
+    for (int i = 0; i < gemm_plan::kMapCache; ++i)
+      if (h->map_ptr[2][i] == D) hit = &h->map[2][i];
+    if (!hit) {
+      const int slot = h->map_next[2];
+      h->map_next[2] = (slot + 1) % gemm_plan::kMapCache;
+      h->map_ptr[2][slot] = nullptr;
+      if (encode_store_d(&h->map[2][slot], D, kp.d_rs, h->M, h->N) != GEMM_OK)
+        return GEMM_ERR_CUDA;
+      h->map_ptr[2][slot] = D;
+      hit = &h->map[2][slot];
+    }
+    tmd = hit;
+  }
+  const cudaError_t le = h->pair ? h->pair->launch(*tm[0], *tm[1], *tmd, kp, h->grid, st)
                                  : h->variant->launch(*tm[0], *tm[1], kp, h->grid, st);
   if (le != cudaSuccess) return GEMM_ERR_CUDA;
   if (kp.splits > 1 && launch_reduce(kp, row_order, h->num_sms, st) != cudaSuccess)

@@ -46,9 +46,13 @@ struct PairCfg {
   static_assert(B_ATOM % 1024 == 0, "stage alignment");
 };
 
+// Staging for the TMA store of D: two buffers of 128 rows x 64 16-bit
+// columns (one 128-byte swizzle row each).
+constexpr uint32_t D_STAGE_BYTES = BM * 64 * 2;
+
 template <int BN, int STAGES, int KSUB>
 constexpr uint32_t pair_smem_bytes() {
-  return STAGES * PairCfg<BN, KSUB>::STAGE_BYTES + 256 + 1024;
+  return STAGES * PairCfg<BN, KSUB>::STAGE_BYTES + 2 * D_STAGE_BYTES + 256 + 1024;
 }
 
 // Units: whole 256 x BN tiles (or split-K pieces), then, when the last
@@ -94,16 +98,19 @@ __device__ __forceinline__ Unit decode_pair_unit(const KParams& p, int u, int bn
 template <int BN, int STAGES, int KSUB>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const KParams p) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmD, const KParams p) {
   using Cfg = PairCfg<BN, KSUB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * Cfg::B_BYTES);
+  uint8_t* sD = sB + STAGES * Cfg::B_BYTES;  // 2 x D_STAGE_BYTES, 1024-aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sD + 2 * D_STAGE_BYTES);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* ep_go = abort_flag + 1;  // the epilogue leader's verdict for its warps
 
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](uint32_t s) { return bar0 + 8u * s; };
@@ -134,6 +141,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (p.d_tma) tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_holder), Cfg::TMEM_COLS);
@@ -266,12 +274,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
+    // One thread (the epilogue leader) waits for each accumulator and tells
+    // the other 127 through a named barrier, so that all of them always take
+    // the same path through the barriers below.
     const int q = warp & 3;
+    const int row_local = q * 32 + lane;  // this thread's row of the CTA's 128
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    uint32_t acc_it = 0;
+    const bool ep_leader = threadIdx.x == 64;
+    uint32_t acc_it = 0, staged = 0;
     for (int u = cid; u < num_units; u += ncl) {
       const Unit w = decode_pair_unit<KSUB>(p, u, BN);
-      const int r = w.m0 + BM * static_cast<int>(rank) + q * 32 + lane;
+      const int r = w.m0 + BM * static_cast<int>(rank) + row_local;
       const bool leaves_partial = w.tail && w.part == 1;
       CRow<BN> crow;
       if (!leaves_partial)
@@ -279,73 +292,117 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       else
         crow.ok = false;
       const uint32_t buf = acc_it & 1u;
-      if (!bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status, STATUS_TIMEOUT,
-                        tmo))
-        break;
+      uint32_t* flag = w.tail ? p.tail_flags + w.ti * 2 + rank : nullptr;
+      if (ep_leader) {
+        bool ok = bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status,
+                               STATUS_TIMEOUT, tmo);
+        if (ok && w.tail && w.part == 0)
+          ok = bounded_flag_wait(flag, p.epoch, abort_flag, p.status, STATUS_TIMEOUT, tmo);
+        *ep_go = ok ? 1 : 0;
+      }
+      named_barrier_sync(1, 128);
+      const bool go = *ep_go != 0;
+      named_barrier_sync(1, 128);
+      if (!go) break;
       tc_fence_after();
       // The split tile's fp32 partial sums (one CTA half), stored so that the
       // 128 threads' float4s of each 4-column group are adjacent: a warp then
       // moves 512 contiguous bytes per access instead of 32 scattered pieces.
       float4* pbase = w.tail ? reinterpret_cast<float4*>(
                                    p.tail_ws + static_cast<size_t>(w.ti * 2 + rank) * BM * BN) +
-                                   (q * 32 + lane)
+                                   row_local
                              : nullptr;
-      uint32_t* flag = w.tail ? p.tail_flags + w.ti * 2 + rank : nullptr;
-      if (w.tail && w.part == 0 &&
-          !bounded_flag_wait(flag, p.epoch, abort_flag, p.status, STATUS_TIMEOUT, tmo))
-        break;
+      const bool staged_store = p.d_tma && !leaves_partial && p.splits == 1;
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + lane_base + buf * BN + c * 32, v);
-        tmem_ld_wait();
-        if (c == BN / 32 - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(map_shared_rank(acc_empty(buf), 0));
+      for (int c2 = 0; c2 < BN / 64; ++c2) {
+        uint8_t* stage = sD + (staged & 1u) * D_STAGE_BYTES;
+        if (staged_store && staged >= 2) {
+          // the store issued from this buffer two chunks ago must have read it
+          if (ep_leader) bulk_wait_read_le1();
+          named_barrier_sync(1, 128);
         }
-        float f[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
-        const int c0 = w.n0 + c * 32;
-        if (leaves_partial) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            pbase[(c * 8 + j) * BM] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2],
-                                                  f[4 * j + 3]);
-          continue;
-        }
-        if (w.tail) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 x = pbase[(c * 8 + j) * BM];
-            f[4 * j] += x.x;
-            f[4 * j + 1] += x.y;
-            f[4 * j + 2] += x.z;
-            f[4 * j + 3] += x.w;
+        for (int h = 0; h < 2; ++h) {
+          const int c = 2 * c2 + h;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_base + lane_base + buf * BN + c * 32, v);
+          tmem_ld_wait();
+          if (c == BN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_shared_rank(acc_empty(buf), 0));
           }
-        }
-        if (p.splits > 1) {
-          store_partial(p, r, c0, w.split, f);
-        } else {
+          float f[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+          const int c0 = w.n0 + c * 32;
+          if (leaves_partial) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              pbase[(c * 8 + j) * BM] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2],
+                                                    f[4 * j + 3]);
+            continue;
+          }
+          if (w.tail) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 x = pbase[(c * 8 + j) * BM];
+              f[4 * j] += x.x;
+              f[4 * j + 1] += x.y;
+              f[4 * j + 2] += x.z;
+              f[4 * j + 3] += x.w;
+            }
+          }
+          if (p.splits > 1) {
+            store_partial(p, r, c0, w.split, f);
+            continue;
+          }
           if (crow.ok)
             add_c_prefetched(p.c_type, crow.v + 4 * c, f);
           else
             add_c_f(p, r, c0, f);
-          store_d_f(p, r, c0, f);
+          if (!staged_store) {
+            store_d_f(p, r, c0, f);
+            continue;
+          }
+          // 16 bytes = 8 outputs per swizzle unit; the unit's position in
+          // the 128-byte row is XORed with row % 8 (the TMA's 128B swizzle),
+          // which also spreads a warp's stores over all banks.
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 x;
+            x.x = pack2(p.d_type, f[8 * k + 0], f[8 * k + 1]);
+            x.y = pack2(p.d_type, f[8 * k + 2], f[8 * k + 3]);
+            x.z = pack2(p.d_type, f[8 * k + 4], f[8 * k + 5]);
+            x.w = pack2(p.d_type, f[8 * k + 6], f[8 * k + 7]);
+            const int unit = (h * 4 + k) ^ (row_local & 7);
+            *reinterpret_cast<uint4*>(stage + row_local * 128 + unit * 16) = x;
+          }
+        }
+        if (staged_store) {
+          fence_proxy_async_smem();
+          named_barrier_sync(1, 128);
+          const int x0 = w.n0 + 64 * c2, y0 = w.m0 + BM * static_cast<int>(rank);
+          if (ep_leader && x0 < p.N && y0 < p.M) {  // boxes entirely outside D are skipped
+            tma_store_2d(&tmD, smem_u32(stage), x0, y0);
+          }
+          if (ep_leader) bulk_commit();
+          ++staged;
         }
       }
       if (leaves_partial) {
         // Publish: every epilogue thread of this CTA has written its row.
         __threadfence();
         named_barrier_sync(1, 128);
-        if (warp == 2 && lane == 0) {
+        if (ep_leader) {
           __threadfence();
           st_release_gpu(flag, p.epoch);
         }
       }
       ++acc_it;
     }
+    // Shared memory must outlive the stores that read it.
+    if (ep_leader) bulk_wait_all();
   }
 
   tc_fence_before();

@@ -33,8 +33,9 @@ struct PairVariant {
   int stages;
   int ksub;  // 64-wide K slices per ring stage
   uint32_t smem;
-  cudaError_t (*launch)(const CUtensorMap&, const CUtensorMap&, const KParams&, int grid,
-                        cudaStream_t);
+  // tensor maps of A, B and (when KParams::d_tma) D
+  cudaError_t (*launch)(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                        const KParams&, int grid, cudaStream_t);
   cudaError_t (*prepare)();
   int (*max_clusters)();
 };

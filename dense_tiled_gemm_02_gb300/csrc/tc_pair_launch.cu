@@ -25,11 +25,11 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t st, cudaLaunchAttribute* a
 }
 
 template <int BN, int STAGES, int KSUB>
-cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const KParams& p, int grid,
-                        cudaStream_t st) {
+cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
+                        const KParams& p, int grid, cudaStream_t st) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pair_config<BN, STAGES, KSUB>(grid, st, attr);
-  return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, KSUB>, a, b, p);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, KSUB>, a, b, d, p);
 }
 
 template <int BN, int STAGES, int KSUB>
