@@ -83,6 +83,17 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
   return true;
 }
 
+// 16-byte global load issued exactly here: an asm volatile keeps its place
+// among the other volatile asm (the barrier waits), so a prefetch is not
+// moved down to its first use.
+__device__ __forceinline__ uint4 ld_global_v4_pinned(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 // ---------------------------------------------------------------- flags in global memory
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;
@@ -152,6 +163,10 @@ __device__ __forceinline__ void bulk_commit() {
 // Wait until at most one committed store group still reads shared memory.
 __device__ __forceinline__ void bulk_wait_read_le1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// Wait until no committed store group still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 // Wait until every committed store group has completed.
 __device__ __forceinline__ void bulk_wait_all() {

@@ -105,6 +105,37 @@ __device__ __forceinline__ void unpack2(int t, uint32_t w, float& lo, float& hi)
   }
 }
 
+// Compile-time-typed conversions for loops specialised on the element
+// types (T_BF16 or T_F16): bf16 widens by placing its bits in the upper half
+// of an fp32 word.
+template <int V>
+struct IntTag {
+  static constexpr int value = V;
+};
+
+template <int T>
+__device__ __forceinline__ void unpack2_t(uint32_t w, float& lo, float& hi) {
+  if constexpr (T == T_BF16) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xFFFF0000u);
+  } else {
+    const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w));
+    lo = v.x;
+    hi = v.y;
+  }
+}
+
+template <int T>
+__device__ __forceinline__ uint32_t pack2_t(float lo, float hi) {
+  if constexpr (T == T_BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
 // Add C to 32 consecutive outputs of row r starting at column c0.
 __device__ __forceinline__ void add_c_f(const KParams& p, int r, int c0, float (&f)[32]) {
   if (p.C == nullptr || r >= p.M) return;
@@ -163,7 +194,7 @@ __device__ __forceinline__ void prefetch_c_row(const KParams& p, int r, int n0, 
   const uint4* src =
       reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.C) + r * p.c_rs + n0);
 #pragma unroll
-  for (int i = 0; i < BN / 8; ++i) c.v[i] = __ldg(src + i);
+  for (int i = 0; i < BN / 8; ++i) c.v[i] = ld_global_v4_pinned(src + i);
 }
 
 // f += the 32 prefetched C values starting at uint4 index q (8 values each).

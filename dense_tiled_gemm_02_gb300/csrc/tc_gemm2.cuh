@@ -276,7 +276,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     // One thread (the epilogue leader) waits for each accumulator and tells
     // the other 127 through a named barrier, so that all of them always take
-    // the same path through the barriers below.
+    // the same path through the barriers below.  The per-tile loop over
+    // 32-column slices is kept rolled: unrolled, its code no longer fits the
+    // instruction cache next to the producer and MMA loops, and every slice
+    // then waits on instruction fetch.
     const int q = warp & 3;
     const int row_local = q * 32 + lane;  // this thread's row of the CTA's 128
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
@@ -286,11 +289,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Unit w = decode_pair_unit<KSUB>(p, u, BN);
       const int r = w.m0 + BM * static_cast<int>(rank) + row_local;
       const bool leaves_partial = w.tail && w.part == 1;
-      CRow<BN> crow;
-      if (!leaves_partial)
-        prefetch_c_row<BN>(p, r, w.n0, crow);
-      else
-        crow.ok = false;
+      const bool staged_store = p.d_tma && !leaves_partial && p.splits == 1;
+      // C of a slice comes as four 16-byte loads of this thread's row, issued
+      // one slice ahead (the first one before the accumulator wait).
+      const bool c_rows = !leaves_partial && p.C != nullptr && p.c_vec && p.c_type != T_F32 &&
+                          r < p.M && w.n0 + BN <= p.N;
+      const uint16_t* crow =
+          c_rows ? static_cast<const uint16_t*>(p.C) + r * p.c_rs + w.n0 : nullptr;
+      uint4 cnext[4];
+      if (c_rows) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) cnext[k] = ld_global_v4_pinned(crow + 8 * k);
+      }
       const uint32_t buf = acc_it & 1u;
       uint32_t* flag = w.tail ? p.tail_flags + w.ti * 2 + rank : nullptr;
       if (ep_leader) {
@@ -312,82 +322,130 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                    p.tail_ws + static_cast<size_t>(w.ti * 2 + rank) * BM * BN) +
                                    row_local
                              : nullptr;
-      const bool staged_store = p.d_tma && !leaves_partial && p.splits == 1;
-#pragma unroll
-      for (int c2 = 0; c2 < BN / 64; ++c2) {
+      // One 32-column slice; CT/DT are the C and D element types when known
+      // at compile time (0: no C), -1 for the generic run-time path.
+      auto slice = [&](const int c, auto ct_tag, auto dt_tag) {
+        constexpr int CT = decltype(ct_tag)::value;
+        constexpr int DT = decltype(dt_tag)::value;
+        const int h = c & 1;  // which half of a 64-column staging chunk
         uint8_t* stage = sD + (staged & 1u) * D_STAGE_BYTES;
-        if (staged_store && staged >= 2) {
+        if (staged_store && h == 0 && staged >= 2) {
           // the store issued from this buffer two chunks ago must have read it
           if (ep_leader) bulk_wait_read_le1();
           named_barrier_sync(1, 128);
         }
+        uint4 ccur[4];
+        if (CT != 0 && c_rows) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int c = 2 * c2 + h;
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem_base + lane_base + buf * BN + c * 32, v);
-          tmem_ld_wait();
-          if (c == BN / 32 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(map_shared_rank(acc_empty(buf), 0));
+          for (int k = 0; k < 4; ++k) ccur[k] = cnext[k];
+          if (c + 1 < BN / 32) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              cnext[k] = ld_global_v4_pinned(crow + 32 * (c + 1) + 8 * k);
           }
-          float f[32];
+        }
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + lane_base + buf * BN + c * 32, v);
+        tmem_ld_wait();
+        if (c == BN / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(map_shared_rank(acc_empty(buf), 0));
+        }
+        float f[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
-          const int c0 = w.n0 + c * 32;
-          if (leaves_partial) {
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+        const int c0 = w.n0 + c * 32;
+        if (leaves_partial) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              pbase[(c * 8 + j) * BM] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2],
-                                                    f[4 * j + 3]);
-            continue;
+          for (int j = 0; j < 8; ++j)
+            pbase[(c * 8 + j) * BM] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2],
+                                                  f[4 * j + 3]);
+          return;
+        }
+        if (w.tail) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 x = pbase[(c * 8 + j) * BM];
+            f[4 * j] += x.x;
+            f[4 * j + 1] += x.y;
+            f[4 * j + 2] += x.z;
+            f[4 * j + 3] += x.w;
           }
-          if (w.tail) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float4 x = pbase[(c * 8 + j) * BM];
-              f[4 * j] += x.x;
-              f[4 * j + 1] += x.y;
-              f[4 * j + 2] += x.z;
-              f[4 * j + 3] += x.w;
-            }
-          }
+        }
+        if (CT < 0) {
           if (p.splits > 1) {
             store_partial(p, r, c0, w.split, f);
-            continue;
+            return;
           }
-          if (crow.ok)
-            add_c_prefetched(p.c_type, crow.v + 4 * c, f);
+          if (c_rows)
+            add_c_prefetched(p.c_type, ccur, f);
           else
             add_c_f(p, r, c0, f);
           if (!staged_store) {
             store_d_f(p, r, c0, f);
-            continue;
+            return;
           }
-          // 16 bytes = 8 outputs per swizzle unit; the unit's position in
-          // the 128-byte row is XORed with row % 8 (the TMA's 128B swizzle),
-          // which also spreads a warp's stores over all banks.
+        } else if (CT != 0) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            uint4 x;
+            const uint32_t cw[4] = {ccur[k].x, ccur[k].y, ccur[k].z, ccur[k].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float lo, hi;
+              unpack2_t<CT>(cw[e], lo, hi);
+              f[8 * k + 2 * e] += lo;
+              f[8 * k + 2 * e + 1] += hi;
+            }
+          }
+        }
+        // 16 bytes = 8 outputs per swizzle unit; the unit's position in the
+        // 128-byte row is XORed with row % 8 (the TMA's 128B swizzle), which
+        // also spreads a warp's stores over all banks.
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint4 x;
+          if constexpr (DT < 0) {
             x.x = pack2(p.d_type, f[8 * k + 0], f[8 * k + 1]);
             x.y = pack2(p.d_type, f[8 * k + 2], f[8 * k + 3]);
             x.z = pack2(p.d_type, f[8 * k + 4], f[8 * k + 5]);
             x.w = pack2(p.d_type, f[8 * k + 6], f[8 * k + 7]);
-            const int unit = (h * 4 + k) ^ (row_local & 7);
-            *reinterpret_cast<uint4*>(stage + row_local * 128 + unit * 16) = x;
+          } else {
+            x.x = pack2_t<DT>(f[8 * k + 0], f[8 * k + 1]);
+            x.y = pack2_t<DT>(f[8 * k + 2], f[8 * k + 3]);
+            x.z = pack2_t<DT>(f[8 * k + 4], f[8 * k + 5]);
+            x.w = pack2_t<DT>(f[8 * k + 6], f[8 * k + 7]);
           }
+          const int unit = (h * 4 + k) ^ (row_local & 7);
+          *reinterpret_cast<uint4*>(stage + row_local * 128 + unit * 16) = x;
         }
-        if (staged_store) {
+        if (h == 1) {
           fence_proxy_async_smem();
           named_barrier_sync(1, 128);
-          const int x0 = w.n0 + 64 * c2, y0 = w.m0 + BM * static_cast<int>(rank);
-          if (ep_leader && x0 < p.N && y0 < p.M) {  // boxes entirely outside D are skipped
+          const int x0 = w.n0 + 32 * (c - 1), y0 = w.m0 + BM * static_cast<int>(rank);
+          if (ep_leader && x0 < p.N && y0 < p.M)  // boxes entirely outside D are skipped
             tma_store_2d(&tmD, smem_u32(stage), x0, y0);
-          }
           if (ep_leader) bulk_commit();
           ++staged;
+        }
+      };
+      // Typed paths: staged 16-bit D with C of the same type read by rows,
+      // or no C; everything else takes the generic path.  The choice must be
+      // the same for all 128 threads (the slices hold warp-wide barriers), so
+      // it only depends on the CTA's row band lying inside M.
+      const bool band_inside = w.m0 + BM * static_cast<int>(rank) + BM <= p.M;
+      const bool c_typed = p.C != nullptr && p.c_vec && p.c_type == p.d_type &&
+                           w.n0 + BN <= p.N && band_inside;
+      const bool typed = staged_store && p.splits == 1 && (p.C == nullptr || c_typed);
+      const int kind = !typed ? 0 : (p.C ? 1 : 2) + (p.d_type == T_F16 ? 2 : 0);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        switch (kind) {
+          case 1: slice(c, IntTag<T_BF16>{}, IntTag<T_BF16>{}); break;
+          case 2: slice(c, IntTag<0>{}, IntTag<T_BF16>{}); break;
+          case 3: slice(c, IntTag<T_F16>{}, IntTag<T_F16>{}); break;
+          case 4: slice(c, IntTag<0>{}, IntTag<T_F16>{}); break;
+          default: slice(c, IntTag<-1>{}, IntTag<-1>{}); break;
         }
       }
       if (leaves_partial) {
