@@ -219,14 +219,14 @@ int encode_operand(CUtensorMap* tm, const void* base, int64_t ld, bool k_major, 
 }
 
 // Tensor map of a row-contiguous 16-bit D (internal coordinates): dims
-// {N, M}, box {64, 128} with 128-byte swizzle, for stores from the staging
-// buffers of the pair kernel.
+// {N, M}, box {64, 32} with 128-byte swizzle, for the per-warp stores from
+// the staging buffers of the pair kernel.
 int encode_store_d(CUtensorMap* tm, void* base, int64_t ld, int64_t M, int64_t N) {
   EncodeFn enc = get_encode();
   if (!enc) return GEMM_ERR_CUDA;
   cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
   cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)BM};
+  cuuint32_t box[2] = {64, 32};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -296,10 +296,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                           r < p.M && w.n0 + BN <= p.N;
       const uint16_t* crow =
           c_rows ? static_cast<const uint16_t*>(p.C) + r * p.c_rs + w.n0 : nullptr;
-      uint4 cnext[4];
+      // Two slices of C in flight: slice c lives in cb[c & 1] and is
+      // reloaded with slice c + 2 once used (a loop unrolled by two keeps the
+      // buffers in fixed registers).
+      uint4 cb0[4], cb1[4];
       if (c_rows) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) cnext[k] = ld_global_v4_pinned(crow + 8 * k);
+        for (int k = 0; k < 4; ++k) cb0[k] = ld_global_v4_pinned(crow + 8 * k);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) cb1[k] = ld_global_v4_pinned(crow + 32 + 8 * k);
       }
       const uint32_t buf = acc_it & 1u;
       uint32_t* flag = w.tail ? p.tail_flags + w.ti * 2 + rank : nullptr;
@@ -324,25 +329,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                              : nullptr;
       // One 32-column slice; CT/DT are the C and D element types when known
       // at compile time (0: no C), -1 for the generic run-time path.
-      auto slice = [&](const int c, auto ct_tag, auto dt_tag) {
+      // Once slice c's C has been added, its buffer takes slice c + 2.
+      auto reload_c = [&](const int c, uint4 (&cbuf)[4]) {
+        if (c + 2 < BN / 32) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) cbuf[k] = ld_global_v4_pinned(crow + 32 * (c + 2) + 8 * k);
+        }
+      };
+      auto slice = [&](const int c, uint4 (&cbuf)[4], auto ct_tag, auto dt_tag) {
         constexpr int CT = decltype(ct_tag)::value;
         constexpr int DT = decltype(dt_tag)::value;
         const int h = c & 1;  // which half of a 64-column staging chunk
+        // Each warp stages its own 32 rows and stores them itself, so the
+        // chunk loop needs no barrier across warps.
         uint8_t* stage = sD + (staged & 1u) * D_STAGE_BYTES;
         if (staged_store && h == 0 && staged >= 2) {
-          // the store issued from this buffer two chunks ago must have read it
-          if (ep_leader) bulk_wait_read_le1();
-          named_barrier_sync(1, 128);
-        }
-        uint4 ccur[4];
-        if (CT != 0 && c_rows) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) ccur[k] = cnext[k];
-          if (c + 1 < BN / 32) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              cnext[k] = ld_global_v4_pinned(crow + 32 * (c + 1) + 8 * k);
-          }
+          // the store this warp issued from this buffer two chunks ago must have read it
+          if (lane == 0) bulk_wait_read_le1();
+          __syncwarp();
         }
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem_base + lane_base + buf * BN + c * 32, v);
@@ -378,10 +382,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             store_partial(p, r, c0, w.split, f);
             return;
           }
-          if (c_rows)
-            add_c_prefetched(p.c_type, ccur, f);
-          else
+          if (c_rows) {
+            add_c_prefetched(p.c_type, cbuf, f);
+            reload_c(c, cbuf);
+          } else {
             add_c_f(p, r, c0, f);
+          }
           if (!staged_store) {
             store_d_f(p, r, c0, f);
             return;
@@ -389,7 +395,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         } else if (CT != 0) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint32_t cw[4] = {ccur[k].x, ccur[k].y, ccur[k].z, ccur[k].w};
+            const uint32_t cw[4] = {cbuf[k].x, cbuf[k].y, cbuf[k].z, cbuf[k].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               float lo, hi;
@@ -398,6 +404,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               f[8 * k + 2 * e + 1] += hi;
             }
           }
+          reload_c(c, cbuf);
         }
         // 16 bytes = 8 outputs per swizzle unit; the unit's position in the
         // 128-byte row is XORed with row % 8 (the TMA's 128B swizzle), which
@@ -421,11 +428,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (h == 1) {
           fence_proxy_async_smem();
-          named_barrier_sync(1, 128);
-          const int x0 = w.n0 + 32 * (c - 1), y0 = w.m0 + BM * static_cast<int>(rank);
-          if (ep_leader && x0 < p.N && y0 < p.M)  // boxes entirely outside D are skipped
-            tma_store_2d(&tmD, smem_u32(stage), x0, y0);
-          if (ep_leader) bulk_commit();
+          __syncwarp();
+          const int x0 = w.n0 + 32 * (c - 1), y0 = w.m0 + BM * static_cast<int>(rank) + 32 * q;
+          if (lane == 0 && x0 < p.N && y0 < p.M)  // boxes entirely outside D are skipped
+            tma_store_2d(&tmD, smem_u32(stage + q * 32 * 128), x0, y0);
+          if (lane == 0) bulk_commit();
           ++staged;
         }
       };
@@ -439,13 +446,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool typed = staged_store && p.splits == 1 && (p.C == nullptr || c_typed);
       const int kind = !typed ? 0 : (p.C ? 1 : 2) + (p.d_type == T_F16 ? 2 : 0);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < BN / 32; c += 2) {
         switch (kind) {
-          case 1: slice(c, IntTag<T_BF16>{}, IntTag<T_BF16>{}); break;
-          case 2: slice(c, IntTag<0>{}, IntTag<T_BF16>{}); break;
-          case 3: slice(c, IntTag<T_F16>{}, IntTag<T_F16>{}); break;
-          case 4: slice(c, IntTag<0>{}, IntTag<T_F16>{}); break;
-          default: slice(c, IntTag<-1>{}, IntTag<-1>{}); break;
+          case 1:
+            slice(c, cb0, IntTag<T_BF16>{}, IntTag<T_BF16>{});
+            slice(c + 1, cb1, IntTag<T_BF16>{}, IntTag<T_BF16>{});
+            break;
+          case 2:
+            slice(c, cb0, IntTag<0>{}, IntTag<T_BF16>{});
+            slice(c + 1, cb1, IntTag<0>{}, IntTag<T_BF16>{});
+            break;
+          case 3:
+            slice(c, cb0, IntTag<T_F16>{}, IntTag<T_F16>{});
+            slice(c + 1, cb1, IntTag<T_F16>{}, IntTag<T_F16>{});
+            break;
+          case 4:
+            slice(c, cb0, IntTag<0>{}, IntTag<T_F16>{});
+            slice(c + 1, cb1, IntTag<0>{}, IntTag<T_F16>{});
+            break;
+          default:
+            slice(c, cb0, IntTag<-1>{}, IntTag<-1>{});
+            slice(c + 1, cb1, IntTag<-1>{}, IntTag<-1>{});
+            break;
         }
       }
       if (leaves_partial) {
@@ -460,7 +482,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ++acc_it;
     }
     // Shared memory must outlive the stores that read it.
-    if (ep_leader) bulk_wait_all();
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
