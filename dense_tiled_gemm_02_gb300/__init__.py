@@ -9,7 +9,7 @@ no CPU fallback.
 Low-level names mirror ``include/gemm.h``: ``gemm_create``, ``gemm_run``,
 ``gemm_get_status``, ``gemm_destroy``, ``gemm_strerror``,
 ``gemm_plan_string``, ``gemm_workspace_bytes``, ``gemm_raster_tile``,
-``gemm_debug_set``.  ``Gemm`` wraps a handle for torch tensors.
+``gemm_debug_set``, ``gemm_timing_enable``, ``gemm_timing_read``.  ``Gemm`` wraps a handle for torch tensors.
 """
 from __future__ import annotations
 
@@ -32,7 +32,7 @@ GEMM_DEBUG_SKIP_FIRST_FILL = 1
 
 EXPORTED = ["gemm_create", "gemm_run", "gemm_get_status", "gemm_destroy", "gemm_strerror",
             "gemm_plan_string", "gemm_workspace_bytes", "gemm_raster_tile", "gemm_debug_set",
-            "gemm_run_splitk_noalloc"]
+            "gemm_run_splitk_noalloc", "gemm_timing_enable", "gemm_timing_read"]
 GEMM_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
@@ -89,6 +89,10 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
     lib.gemm_debug_set.restype = ci
     lib.gemm_run_splitk_noalloc.argtypes = [ctypes.POINTER(GemmDesc), ci, vp, vp, vp, vp, vp]
     lib.gemm_run_splitk_noalloc.restype = ci
+    lib.gemm_timing_enable.argtypes = [vp, ci]
+    lib.gemm_timing_enable.restype = ci
+    lib.gemm_timing_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ci]
+    lib.gemm_timing_read.restype = ci
     _lib = lib
     return lib
 
@@ -135,6 +139,16 @@ def gemm_raster_tile(t: int, num_pid_m: int, num_pid_n: int, group_m: int):
 
 def gemm_debug_set(h: int, flags: int, timeout_ns: int = 0) -> int:
     return load().gemm_debug_set(h, flags, timeout_ns)
+
+
+def gemm_timing_enable(h: int, n: int) -> int:
+    return load().gemm_timing_enable(h, n)
+
+
+def gemm_timing_read(h: int, n: int) -> tuple[int, list[float]]:
+    buf = (ctypes.c_float * max(n, 1))()
+    rc = load().gemm_timing_read(h, buf, n)
+    return rc, [buf[i] for i in range(max(rc, 0))]
 
 
 def gemm_run_splitk_noalloc(desc: GemmDesc, splits: int, A: int, B: int, C: int | None, D: int,
@@ -213,6 +227,19 @@ class Gemm:
 
     def plan(self) -> str:
         return gemm_plan_string(self.handle)
+
+    def timing_enable(self, n: int) -> None:
+        """Time the tensor-core kernel of the next n runs with CUDA events."""
+        rc = gemm_timing_enable(self.handle, n)
+        if rc != GEMM_OK:
+            raise GemmError(rc, "gemm_timing_enable")
+
+    def timing_read(self, n: int) -> list[float]:
+        """Kernel durations (ms) of the runs recorded since timing_enable."""
+        rc, ms = gemm_timing_read(self.handle, n)
+        if rc < 0:
+            raise GemmError(rc, "gemm_timing_read")
+        return ms
 
     def workspace_bytes(self) -> int:
         return gemm_workspace_bytes(self.handle)

@@ -66,37 +66,62 @@ __global__ void splitk_reduce_kernel(const KParams p, int row_order) {
 // covers 256 consecutive columns of one row band; rows are strided over
 // block y, so neighbouring threads touch neighbouring addresses and no
 // thread divides.
-__global__ void repack_kernel(const void* src, int src_type, long long ld_src, uint16_t* dst,
-                              long long ld_dst, long long rows, long long cols) {
+__global__ void repack_kernel(const void* __restrict__ src, int src_type, long long ld_src,
+                              uint16_t* __restrict__ dst, long long ld_dst, long long rows,
+                              long long cols) {
   const long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c >= cols) return;
-  for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
-    uint16_t v;
-    if (src_type == T_I8) {
-      const __nv_bfloat16 b = __float2bfloat16_rn(
-          static_cast<float>(static_cast<const int8_t*>(src)[r * ld_src + c]));
-      v = *reinterpret_cast<const uint16_t*>(&b);
-    } else {
-      v = static_cast<const uint16_t*>(src)[r * ld_src + c];
+  // Four rows per step: their loads are independent, so four are in flight.
+  constexpr int R = 4;
+  const long long step = static_cast<long long>(gridDim.y) * R;
+  for (long long r0 = static_cast<long long>(blockIdx.y) * R; r0 < rows; r0 += step) {
+    uint16_t v[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const long long r = r0 + i;
+      if (r >= rows) break;
+      if (src_type == T_I8) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(
+            static_cast<float>(static_cast<const int8_t*>(src)[r * ld_src + c]));
+        v[i] = *reinterpret_cast<const uint16_t*>(&b);
+      } else {
+        v[i] = static_cast<const uint16_t*>(src)[r * ld_src + c];
+      }
     }
-    dst[r * ld_dst + c] = v;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      if (r0 + i >= rows) break;
+      dst[(r0 + i) * ld_dst + c] = v[i];
+    }
   }
 }
 
 // int8 -> bf16 widening, 4 elements per thread (rows whose starts and
-// lengths are multiples of 4 elements).
-__global__ void widen_i8_x4_kernel(const char4* src, long long ld_src4, uint2* dst,
-                                   long long ld_dst4, long long rows, long long cols4) {
+// lengths are multiples of 4 elements), four rows per step.
+__global__ void widen_i8_x4_kernel(const char4* __restrict__ src, long long ld_src4,
+                                   uint2* __restrict__ dst, long long ld_dst4, long long rows,
+                                   long long cols4) {
   const long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c >= cols4) return;
-  for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
-    const char4 x = src[r * ld_src4 + c];
-    __nv_bfloat162 lo = __floats2bfloat162_rn(static_cast<float>(x.x), static_cast<float>(x.y));
-    __nv_bfloat162 hi = __floats2bfloat162_rn(static_cast<float>(x.z), static_cast<float>(x.w));
-    uint2 o;
-    o.x = *reinterpret_cast<const uint32_t*>(&lo);
-    o.y = *reinterpret_cast<const uint32_t*>(&hi);
-    dst[r * ld_dst4 + c] = o;
+  constexpr int R = 4;
+  const long long step = static_cast<long long>(gridDim.y) * R;
+  for (long long r0 = static_cast<long long>(blockIdx.y) * R; r0 < rows; r0 += step) {
+    char4 x[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      if (r0 + i < rows) x[i] = src[(r0 + i) * ld_src4 + c];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      if (r0 + i >= rows) break;
+      const __nv_bfloat162 lo =
+          __floats2bfloat162_rn(static_cast<float>(x[i].x), static_cast<float>(x[i].y));
+      const __nv_bfloat162 hi =
+          __floats2bfloat162_rn(static_cast<float>(x[i].z), static_cast<float>(x[i].w));
+      uint2 o;
+      o.x = *reinterpret_cast<const uint32_t*>(&lo);
+      o.y = *reinterpret_cast<const uint32_t*>(&hi);
+      dst[(r0 + i) * ld_dst4 + c] = o;
+    }
   }
 }
 
@@ -119,7 +144,8 @@ cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint1
   const long long ccols = x4 ? cols / 4 : cols;
   const unsigned gx = static_cast<unsigned>((ccols + 255) / 256);
   long long gy = (static_cast<long long>(num_sms) * 16 + gx - 1) / gx;
-  if (gy > rows) gy = rows;
+  const long long row_steps = (rows + 3) / 4;  // both kernels take four rows a step
+  if (gy > row_steps) gy = row_steps;
   if (gy > 65535) gy = 65535;
   const dim3 grid(gx, static_cast<unsigned>(gy));
   if (x4)

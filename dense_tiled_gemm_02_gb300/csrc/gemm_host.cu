@@ -10,6 +10,7 @@
 #include <mutex>
 #include <new>
 #include <string>
+#include <vector>
 
 #include "common.h"
 #include "gemm.h"
@@ -74,9 +75,10 @@ const TcVariant* find_variant(int bn, bool i8x) {
   return nullptr;
 }
 
-const PairVariant* find_pair(int bn, int ksub) {
+const PairVariant* find_pair(int bn, int ksub, bool i8x) {
   for (int i = 0; i < kNumPairVariants; ++i)
-    if (kPairVariants[i].bn == bn && kPairVariants[i].ksub == ksub) return &kPairVariants[i];
+    if (kPairVariants[i].bn == bn && kPairVariants[i].ksub == ksub && kPairVariants[i].i8x == i8x)
+      return &kPairVariants[i];
   return nullptr;
 }
 
@@ -112,6 +114,10 @@ struct gemm_plan {
   CUtensorMap map[3][kMapCache] = {};
   int map_next[3] = {0, 0, 0};
   std::string plan_str;
+  // Kernel timing: event pairs recorded around the tensor-core launch of the
+  // next timing_n runs (created by gemm_timing_enable, never by gemm_run).
+  std::vector<cudaEvent_t> timing_ev;
+  int timing_n = 0, timing_used = 0;
 };
 
 namespace {
@@ -289,8 +295,11 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   h->choice = choose_plan(d.M, d.N, d.K, d.ab_type, d.layout_a, d.layout_b, sms);
   apply_force_plan(h->choice);
   if (h->i8x) {
-    h->choice.bn = 128;  // the exact-int8 variant keeps a 128-column int32 sum per thread
+    // The exact-int8 kernels keep 128 columns of int32 sums (tensor memory in
+    // the pair kernel, registers in the single-CTA one) and no K split.
+    h->choice.bn = 128;
     h->choice.splits = 1;
+    h->choice.tail = 0;
   }
   PlanChoice& c = h->choice;
   const bool swap = c.swap != 0;
@@ -316,10 +325,10 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   // The pair kernel stages bn/2 columns of B per CTA; an N-major B needs
   // whole 64-column swizzle atoms there.
   const bool b_n_major = h->b.layout == GEMM_ROW_MAJOR;
-  if (c.pair && (h->i8x || (b_n_major && (c.bn / 2) % 64 != 0))) c.pair = 0;
+  if (c.pair && b_n_major && (c.bn / 2) % 64 != 0) c.pair = 0;
   if (c.pair) {
-    h->pair = find_pair(c.bn, c.ksub);
-    if (!h->pair) h->pair = find_pair(c.bn, 1);
+    h->pair = find_pair(c.bn, c.ksub, h->i8x);
+    if (!h->pair) h->pair = find_pair(c.bn, 1, h->i8x);
     if (!h->pair) c.pair = 0;
   }
   c.ksub = h->pair ? h->pair->ksub : 1;
@@ -554,9 +563,17 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
     }
     tmd = hit;
   }
+  const bool timed = h->timing_used < h->timing_n;
+  if (timed && cudaEventRecord(h->timing_ev[2 * h->timing_used], st) != cudaSuccess)
+    return GEMM_ERR_CUDA;
   const cudaError_t le = h->pair ? h->pair->launch(*tm[0], *tm[1], *tmd, kp, h->grid, st)
                                  : h->variant->launch(*tm[0], *tm[1], kp, h->grid, st);
   if (le != cudaSuccess) return GEMM_ERR_CUDA;
+  if (timed) {
+    if (cudaEventRecord(h->timing_ev[2 * h->timing_used + 1], st) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    ++h->timing_used;
+  }
   if (kp.splits > 1 && launch_reduce(kp, row_order, h->num_sms, st) != cudaSuccess)
     return GEMM_ERR_CUDA;
   return GEMM_OK;
@@ -579,6 +596,7 @@ int gemm_destroy(gemm_handle_t h) {
   if (cudaDeviceSynchronize() != cudaSuccess) rc = GEMM_ERR_CUDA;
   if (h->ws) cudaFree(h->ws);
   if (h->status) cudaFree(h->status);
+  for (cudaEvent_t e : h->timing_ev) cudaEventDestroy(e);
   delete h;
   return rc;
 }
@@ -599,6 +617,37 @@ int gemm_debug_set(gemm_handle_t h, int flags, uint64_t timeout_ns) {
   h->debug_flags = flags;
   h->timeout_ns = timeout_ns ? timeout_ns : kDefaultTimeoutNs;
   return GEMM_OK;
+}
+
+int gemm_timing_enable(gemm_handle_t h, int n) {
+  if (!h || n < 0) return GEMM_ERR_INVALID_ARG;
+  for (cudaEvent_t e : h->timing_ev) cudaEventDestroy(e);
+  h->timing_ev.clear();
+  h->timing_n = h->timing_used = 0;
+  if (n == 0) return GEMM_OK;
+  if (cudaSetDevice(h->device) != cudaSuccess) return GEMM_ERR_CUDA;
+  h->timing_ev.resize(2 * static_cast<size_t>(n));
+  for (auto& e : h->timing_ev) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      e = nullptr;
+      gemm_timing_enable(h, 0);
+      return GEMM_ERR_CUDA;
+    }
+  }
+  h->timing_n = n;
+  return GEMM_OK;
+}
+
+int gemm_timing_read(gemm_handle_t h, float* ms, int n) {
+  if (!h || (n > 0 && !ms)) return GEMM_ERR_INVALID_ARG;
+  const int k = std::min(n, h->timing_used);
+  for (int i = 0; i < k; ++i) {
+    if (cudaEventSynchronize(h->timing_ev[2 * i + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms[i], h->timing_ev[2 * i], h->timing_ev[2 * i + 1]) !=
+            cudaSuccess)
+      return GEMM_ERR_CUDA;
+  }
+  return k;
 }
 
 }  // extern "C"

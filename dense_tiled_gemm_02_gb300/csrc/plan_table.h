@@ -12,6 +12,8 @@
 
 #include <cstdint>
 
+#include "common.h"
+
 namespace gb300 {
 
 struct PlanChoice {
@@ -60,7 +62,9 @@ inline PlanChoice choose_plan(int64_t M, int64_t N, int64_t K, int ab_type, int 
   else c.bn = 64;
   // Large problems: the CTA-pair 256 x 256 tile when its tiles fill at
   // least one wave of 2-CTA clusters (measured faster than 128 x 256 per SM).
-  if (Ni > 128 && cdiv64(Mi, 256) * cdiv64(Ni, 256) >= num_sms / 2) {
+  // Exact int8 stays on the single-CTA 128 x 128 kernel: at 8192^3 it
+  // measured 851 TOPS against 759 for the pair kernel's 256 x 128 tile.
+  if (ab_type != T_I8 && Ni > 128 && cdiv64(Mi, 256) * cdiv64(Ni, 256) >= num_sms / 2) {
     c.pair = 1;
     c.bn = 256;
     return c;

@@ -479,8 +479,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Unit w = decode_unit(p, u, BN);
       const int r = w.m0 + q * 32 + lane;
       if constexpr (!I8X) {
-        CRow<BN> crow;
-        prefetch_c_row<BN>(p, r, w.n0, crow);
+        // C of a slice as four 16-byte loads of this thread's row, two
+        // slices in flight (slice c in cb[c & 1]); the loop over slices is
+        // kept rolled so that its code stays in the instruction cache.
+        const bool c_rows = p.splits == 1 && p.C != nullptr && p.c_vec && p.c_type != T_F32 &&
+                            r < p.M && w.n0 + BN <= p.N;
+        const uint16_t* crow =
+            c_rows ? static_cast<const uint16_t*>(p.C) + r * p.c_rs + w.n0 : nullptr;
+        uint4 cb0[4], cb1[4];
+        if (c_rows) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) cb0[k] = ld_global_v4_pinned(crow + 8 * k);
+          if (BN >= 64) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) cb1[k] = ld_global_v4_pinned(crow + 32 + 8 * k);
+          }
+        }
         const uint32_t buf = acc_it & 1u;
         if (!bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status,
                           STATUS_TIMEOUT, tmo)) {
@@ -488,8 +502,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
+        // Typed fast path: 16-bit D rows contiguous and 16-byte aligned, the
+        // tile inside N, C absent or of D's type read by rows.  Every slice
+        // starts with a warp-wide tcgen05.ld, so the path must be the same
+        // for all threads: it may depend on the tile, never on the thread's
+        // row (a C tile takes the typed path only when all 128 rows are
+        // inside M, where c_rows holds for every thread).
+        const bool band_inside = w.m0 + BM <= p.M;
+        const bool typed = p.splits == 1 && p.d_vec && w.n0 + BN <= p.N &&
+                           (p.d_type == T_BF16 || p.d_type == T_F16) &&
+                           (p.C == nullptr ||
+                            (band_inside && p.c_vec && p.c_type == p.d_type));
+        const int kind = !typed ? 0 : (p.C ? 1 : 2) + (p.d_type == T_F16 ? 2 : 0);
+        auto slice = [&](const int c, uint4 (&cbuf)[4], auto ct_tag, auto dt_tag) {
+          constexpr int CT = decltype(ct_tag)::value;
+          constexpr int DT = decltype(dt_tag)::value;
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem_base + lane_base + buf * BN + c * 32, v);
           tmem_ld_wait();
@@ -503,12 +530,71 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int c0 = w.n0 + c * 32;
           if (p.splits > 1) {
             store_partial(p, r, c0, w.split, f);
-          } else {
-            if (crow.ok)
-              add_c_prefetched(p.c_type, crow.v + 4 * c, f);
-            else
-              add_c_f(p, r, c0, f);
+            return;
+          }
+          if (CT != 0 && c_rows) {
+            if constexpr (CT < 0) {
+              add_c_prefetched(p.c_type, cbuf, f);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint32_t cw[4] = {cbuf[k].x, cbuf[k].y, cbuf[k].z, cbuf[k].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  float lo, hi;
+                  unpack2_t<CT>(cw[e], lo, hi);
+                  f[8 * k + 2 * e] += lo;
+                  f[8 * k + 2 * e + 1] += hi;
+                }
+              }
+            }
+            if (c + 2 < BN / 32) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                cbuf[k] = ld_global_v4_pinned(crow + 32 * (c + 2) + 8 * k);
+            }
+          } else if (CT < 0) {
+            add_c_f(p, r, c0, f);
+          }
+          if constexpr (DT < 0) {
             store_d_f(p, r, c0, f);
+          } else {
+            if (r >= p.M) return;
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.D) + r * p.d_rs + c0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint4 x;
+              x.x = pack2_t<DT>(f[8 * k + 0], f[8 * k + 1]);
+              x.y = pack2_t<DT>(f[8 * k + 2], f[8 * k + 3]);
+              x.z = pack2_t<DT>(f[8 * k + 4], f[8 * k + 5]);
+              x.w = pack2_t<DT>(f[8 * k + 6], f[8 * k + 7]);
+              dst[k] = x;
+            }
+          }
+        };
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; c += 2) {
+          switch (kind) {
+            case 1:
+              slice(c, cb0, IntTag<T_BF16>{}, IntTag<T_BF16>{});
+              slice(c + 1, cb1, IntTag<T_BF16>{}, IntTag<T_BF16>{});
+              break;
+            case 2:
+              slice(c, cb0, IntTag<0>{}, IntTag<T_BF16>{});
+              slice(c + 1, cb1, IntTag<0>{}, IntTag<T_BF16>{});
+              break;
+            case 3:
+              slice(c, cb0, IntTag<T_F16>{}, IntTag<T_F16>{});
+              slice(c + 1, cb1, IntTag<T_F16>{}, IntTag<T_F16>{});
+              break;
+            case 4:
+              slice(c, cb0, IntTag<0>{}, IntTag<T_F16>{});
+              slice(c + 1, cb1, IntTag<0>{}, IntTag<T_F16>{});
+              break;
+            default:
+              slice(c, cb0, IntTag<-1>{}, IntTag<-1>{});
+              slice(c + 1, cb1, IntTag<-1>{}, IntTag<-1>{});
+              break;
           }
         }
         ++acc_it;

@@ -32,7 +32,7 @@
 
 namespace gb300 {
 
-template <int BN, int KSUB>
+template <int BN, int KSUB, bool I8X = false>
 struct PairCfg {
   static constexpr int BNH = BN / 2;                        // B columns staged per CTA
   static constexpr uint32_t A_ATOM = BM * BK * 2;           // 128 rows x 64 K: 16 KiB
@@ -41,8 +41,11 @@ struct PairCfg {
   static constexpr uint32_t B_BYTES = KSUB * B_ATOM;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t PAIR_TX = 2 * STAGE_BYTES;      // bytes both CTAs land per stage
-  static constexpr uint32_t TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
+  // Two fp32 accumulators of BN columns; the exact-int8 variant adds BN
+  // columns of int32 running sums.
+  static constexpr uint32_t TMEM_COLS = (!I8X && 2 * BN <= 256) ? 256 : 512;
   static_assert(BN == 128 || BN == 256, "pair tile width");
+  static_assert(!I8X || 3 * BN <= 512, "int8 sums must fit in tensor memory");
   static_assert(B_ATOM % 1024 == 0, "stage alignment");
 };
 
@@ -95,12 +98,20 @@ __device__ __forceinline__ Unit decode_pair_unit(const KParams& p, int u, int bn
 }
 
 // kb0/kb1 count 64-wide K slices; a stage covers KSUB of them.
-template <int BN, int STAGES, int KSUB>
+//
+// I8X: exact int8 GEMM on the bf16 tensor pipe (operands widened to bf16
+// beforehand, which is exact for |v| <= 128).  Each run of kb_per_chunk K
+// slices (512 K) is accumulated afresh in fp32, where every partial sum is an
+// integer of magnitude at most 512 * 2^14 = 2^23 and therefore exact; the
+// epilogue converts each finished chunk to int32 and adds it to a running sum
+// kept in tensor memory, while the MMA fills the other accumulator with the
+// next chunk.  The last chunk's sum gets C added and is stored as int32.
+template <int BN, int STAGES, int KSUB, bool I8X>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmD, const KParams p) {
-  using Cfg = PairCfg<BN, KSUB>;
+  using Cfg = PairCfg<BN, KSUB, I8X>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -239,34 +250,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool stop = false;
       for (int u = cid; u < num_units && !stop; u += ncl) {
         const Unit w = decode_pair_unit<KSUB>(p, u, BN);
-        const uint32_t buf = acc_it & 1u;
-        if (!bounded_wait(acc_empty(buf), ((acc_it >> 1) & 1u) ^ 1u, abort_flag, p.status,
-                          STATUS_TIMEOUT, tmo))
-          break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * BN;
-        uint32_t accumulate = 0;
-        for (int kb = w.kb0; kb < w.kb1; kb += KSUB) {
-          if (!bounded_wait(full(s), ph, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
+        // One accumulator per unit; the int8 variant takes a fresh one for
+        // every chunk of kb_per_chunk K slices.
+        int kc = w.kb0;
+        do {
+          const int ke = I8X ? min(w.kb1, kc + p.kb_per_chunk) : w.kb1;
+          const uint32_t buf = acc_it & 1u;
+          if (!bounded_wait(acc_empty(buf), ((acc_it >> 1) & 1u) ^ 1u, abort_flag, p.status,
+                            STATUS_TIMEOUT, tmo)) {
             stop = true;
             break;
           }
-          const uint32_t a_lo = a_lo0 + s * (Cfg::A_BYTES >> 4);
-          const uint32_t b_lo = b_lo0 + s * (Cfg::B_BYTES >> 4);
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * BN;
+          uint32_t accumulate = 0;
+          for (int kb = kc; kb < ke; kb += KSUB) {
+            if (!bounded_wait(full(s), ph, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
+              stop = true;
+              break;
+            }
+            const uint32_t a_lo = a_lo0 + s * (Cfg::A_BYTES >> 4);
+            const uint32_t b_lo = b_lo0 + s * (Cfg::B_BYTES >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 4 * KSUB; ++kk)
-            mma_f16_ss_pair(d_tmem, sdesc(dhi, a_lo + a_off[kk]), sdesc(dhi, b_lo + b_off[kk]),
-                            p.idesc, accumulate | kk);
-          accumulate = 1;
-          mma_commit_pair_both(empty(s));
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1u;
+            for (int kk = 0; kk < 4 * KSUB; ++kk)
+              mma_f16_ss_pair(d_tmem, sdesc(dhi, a_lo + a_off[kk]),
+                              sdesc(dhi, b_lo + b_off[kk]), p.idesc, accumulate | kk);
+            accumulate = 1;
+            mma_commit_pair_both(empty(s));
+            if (++s == STAGES) {
+              s = 0;
+              ph ^= 1u;
+            }
           }
-        }
-        if (stop) break;
-        mma_commit_pair_both(acc_full(buf));
-        ++acc_it;
+          if (stop) break;
+          mma_commit_pair_both(acc_full(buf));
+          ++acc_it;
+          kc = ke;
+        } while (I8X && kc < w.kb1);
       }
       mma_commit_pair_both(done_bar);
       drain_wait(done_bar, 0, 200000000ull);
@@ -285,6 +305,58 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const bool ep_leader = threadIdx.x == 64;
     uint32_t acc_it = 0, staged = 0;
+    if constexpr (I8X) {
+      // Exact int8: per chunk, convert the fp32 accumulator (integers below
+      // 2^24, so cvt.rni is exact) and add it to the int32 sums kept in
+      // tensor memory columns [2*BN, 3*BN); the last chunk adds C and stores.
+      const uint32_t isum = tmem_base + lane_base + 2 * BN;
+      bool ok = true;
+      for (int u = cid; u < num_units && ok; u += ncl) {
+        const Unit w = decode_pair_unit<KSUB>(p, u, BN);
+        const int r = w.m0 + BM * static_cast<int>(rank) + row_local;
+        const int nch = (w.kb1 - w.kb0 + p.kb_per_chunk - 1) / p.kb_per_chunk;
+        for (int ch = 0; ch < nch; ++ch) {
+          const uint32_t buf = acc_it & 1u;
+          if (ep_leader)
+            *ep_go = bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status,
+                                  STATUS_TIMEOUT, tmo) ? 1 : 0;
+          named_barrier_sync(1, 128);
+          ok = *ep_go != 0;
+          named_barrier_sync(1, 128);
+          if (!ok) break;
+          tc_fence_after();
+          const bool first = ch == 0, last = ch == nch - 1;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32], sm[32];
+            tmem_ld_32x32b_x32(tmem_base + lane_base + buf * BN + c * 32, v);
+            if (!first) tmem_ld_32x32b_x32(isum + c * 32, sm);
+            tmem_ld_wait();
+            if (c == BN / 32 - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster(map_shared_rank(acc_empty(buf), 0));
+            }
+            int t[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int x = __float2int_rn(__uint_as_float(v[j]));
+              t[j] = first ? x : static_cast<int>(sm[j]) + x;
+            }
+            if (!last) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) sm[j] = static_cast<uint32_t>(t[j]);
+              tmem_st_32x32b_x32(isum + c * 32, sm);
+            } else {
+              store_d_i32(p, r, w.n0 + c * 32, t);
+            }
+          }
+          // the next chunk reads these sums back
+          if (!last) tmem_st_wait();
+          ++acc_it;
+        }
+      }
+    } else {
     for (int u = cid; u < num_units; u += ncl) {
       const Unit w = decode_pair_unit<KSUB>(p, u, BN);
       const int r = w.m0 + BM * static_cast<int>(rank) + row_local;
@@ -483,6 +555,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     // Shared memory must outlive the stores that read it.
     if (lane == 0) bulk_wait_all();
+    }
   }
 
   tc_fence_before();

@@ -32,6 +32,7 @@ struct PairVariant {
   int bn;
   int stages;
   int ksub;  // 64-wide K slices per ring stage
+  bool i8x;  // exact int8 (bf16-widened operands, chunked int32 sums)
   uint32_t smem;
   // tensor maps of A, B and (when KParams::d_tma) D
   cudaError_t (*launch)(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,

@@ -24,27 +24,27 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t st, cudaLaunchAttribute* a
   return cfg;
 }
 
-template <int BN, int STAGES, int KSUB>
+template <int BN, int STAGES, int KSUB, bool I8X>
 cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
                         const KParams& p, int grid, cudaStream_t st) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pair_config<BN, STAGES, KSUB>(grid, st, attr);
-  return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, KSUB>, a, b, d, p);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, KSUB, I8X>, a, b, d, p);
 }
 
-template <int BN, int STAGES, int KSUB>
+template <int BN, int STAGES, int KSUB, bool I8X>
 cudaError_t prepare_pair() {
-  return cudaFuncSetAttribute(tc_gemm_pair_kernel<BN, STAGES, KSUB>,
+  return cudaFuncSetAttribute(tc_gemm_pair_kernel<BN, STAGES, KSUB, I8X>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               pair_smem_bytes<BN, STAGES, KSUB>());
 }
 
-template <int BN, int STAGES, int KSUB>
+template <int BN, int STAGES, int KSUB, bool I8X>
 int max_clusters_pair() {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pair_config<BN, STAGES, KSUB>(2, nullptr, attr);
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<BN, STAGES, KSUB>, &cfg) !=
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<BN, STAGES, KSUB, I8X>, &cfg) !=
       cudaSuccess) {
     cudaGetLastError();
     return 0;
@@ -53,12 +53,14 @@ int max_clusters_pair() {
 }
 }  // namespace
 
-#define GB_PAIR(BN_, ST_, KS_)                                                            \
-  PairVariant{BN_, ST_, KS_, pair_smem_bytes<BN_, ST_, KS_>(), &launch_pair<BN_, ST_, KS_>, \
-              &prepare_pair<BN_, ST_, KS_>, &max_clusters_pair<BN_, ST_, KS_>}
+#define GB_PAIR(BN_, ST_, KS_, I8_)                                                 \
+  PairVariant{BN_, ST_, KS_, I8_, pair_smem_bytes<BN_, ST_, KS_>(),                 \
+              &launch_pair<BN_, ST_, KS_, I8_>, &prepare_pair<BN_, ST_, KS_, I8_>, \
+              &max_clusters_pair<BN_, ST_, KS_, I8_>}
 
-const PairVariant kPairVariants[] = {GB_PAIR(256, 6, 1), GB_PAIR(256, 3, 2), GB_PAIR(128, 8, 1),
-                                     GB_PAIR(128, 4, 2)};
-const int kNumPairVariants = 4;
+const PairVariant kPairVariants[] = {GB_PAIR(256, 6, 1, false), GB_PAIR(256, 3, 2, false),
+                                     GB_PAIR(128, 8, 1, false), GB_PAIR(128, 4, 2, false),
+                                     GB_PAIR(128, 8, 1, true),  GB_PAIR(128, 4, 2, true)};
+const int kNumPairVariants = 6;
 
 }  // namespace gb300

@@ -176,6 +176,23 @@ GEMM_API int gemm_run_splitk_noalloc(const gemm_desc_t* desc, int splits, const 
                                      gemm_stream_t stream);
 
 /*
+ * Kernel timing (a measurement hook; the operation is unchanged).
+ * gemm_timing_enable(h, n): each of the next n gemm_run calls on h records a
+ * pair of CUDA events on its stream, immediately before and immediately after
+ * the launch of the tensor-core GEMM kernel (the repack, int8 widening and
+ * split-K reduce kernels fall outside the pair).  The events are created
+ * here, so gemm_run still allocates nothing; n = 0 switches timing off and
+ * destroys them.  Calling it again restarts the count.  Returns GEMM_OK,
+ * GEMM_ERR_INVALID_ARG (n < 0) or GEMM_ERR_CUDA.
+ * gemm_timing_read(h, ms, n): waits for the recorded runs and writes the
+ * kernel duration of the first min(n, runs recorded) of them, in
+ * milliseconds, to the caller's host array ms; returns how many it wrote, or
+ * GEMM_ERR_INVALID_ARG / GEMM_ERR_CUDA.
+ */
+GEMM_API int gemm_timing_enable(gemm_handle_t h, int n);
+GEMM_API int gemm_timing_read(gemm_handle_t h, float* ms, int n);
+
+/*
  * Test hooks (not for production use).
  * gemm_debug_set: flags bit 0 makes the load warp of the next gemm_run skip
  * its first stage fill, so that the consumer's bounded wait expires and the

@@ -155,6 +155,42 @@ def test_side_stream_and_reuse():
         _assert_ok(check_rows(w, inp, D), f"stream run {off}")
 
 
+def test_kernel_timing_hook():
+    """gemm_timing_enable/read: one duration per recorded run, each inside the
+    whole call's events (the split-K reduce of this plan falls outside it),
+    and the result of the timed runs unchanged."""
+    w = WORKLOADS["skinny8192x128x4096_bf16"]
+    inp = make_inputs(w)
+    dev = torch.device("cuda")
+    A, B, C = (logical(inp[k].to(dev), l) for k, l in
+               (("A", w.layout_a), ("B", w.layout_b), ("C", w.layout_c)))
+    D_storage = torch.empty(storage_shape(w.M, w.N, w.layout_d), dtype=torch.bfloat16,
+                            device=dev)
+    D = logical(D_storage, w.layout_d)
+    g = pkg.Gemm.like(A, B, C, D)
+    s = torch.cuda.current_stream()
+    n = 3
+    g.timing_enable(n)
+    outer = []
+    for _ in range(n + 1):  # one run more than recorded
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        g.run(A, B, C, D, s)
+        e1.record(s)
+        outer.append((e0, e1))
+    torch.cuda.synchronize()
+    ms = g.timing_read(8)
+    assert g.status(s) == pkg.GEMM_OK
+    assert len(ms) == n
+    for k, (e0, e1) in zip(ms, outer):
+        assert 0.0 < k <= e0.elapsed_time(e1) * 1.001 + 1e-3
+    g.timing_enable(0)
+    assert g.timing_read(8) == []
+    _assert_ok(check_rows(w, inp, D_storage.cpu(), rows=[0, 127, 128, 4097, w.M - 1]),
+               "timed run")
+    g.close()
+
+
 # ------------------------------------------------------------------ full-size configs
 FULL = [("sq4096_bf16", None), ("sq4096_bf16", "pair=1,bn=256,tail=0"),
         ("sq4096_bf16", "pair=0,bn=256"), ("skinny64x8192x8192_bf16", None),
@@ -173,11 +209,12 @@ def test_full_config_every_element(name, plan):
     print(f"{name}: {rep['n']} elements ok, {rep['n_needed_slack']} needed the fp32 slack [{p}]")
 
 
-@pytest.mark.parametrize("name", ["sq8192_bf16", "sq8192_i8"])
-def test_8192_sampled(name):
+@pytest.mark.parametrize("name,plan", [("sq8192_bf16", None), ("sq8192_i8", None),
+                                       ("sq8192_i8", "pair=0")])
+def test_8192_sampled(name, plan):
     w = WORKLOADS[name]
     inp = make_inputs(w)
-    D, p = run_gpu(w, inp)
+    D, p = run_gpu(w, inp, plan=plan)
     pi, pj = sample_points(w.M, w.N)
     _assert_ok(check_points(w, inp, D, pi.numpy(), pj.numpy()), f"{name} points [{p}]")
     rows = sample_rows(w.M).numpy()
@@ -185,18 +222,25 @@ def test_8192_sampled(name):
 
 
 # ------------------------------------------------------------------ exact int8
+I8_PLANS = [None, "pair=1,ksub=1", "pair=1,ksub=2"]
+
+
+@pytest.mark.parametrize("plan", I8_PLANS)
 @pytest.mark.parametrize("shape", [(300, 200, 1500, ROW, ROW), (129, 257, 2049, COL, COL),
-                                   (64, 384, 600, ROW, COL)])
-def test_int8_exact_small(shape):
+                                   (64, 384, 600, ROW, COL), (520, 640, 4160, ROW, ROW)])
+def test_int8_exact_small(shape, plan):
+    """Exact int8 on both kernels; K spans several 512-wide chunks and ends
+    in a partial one."""
     M, N, K, la, lb = shape
     w = Workload("i8", 51, M, N, K, I8, I32, I32, "int", la, lb)
     inp = make_inputs(w)
-    D, p = run_gpu(w, inp)
+    D, p = run_gpu(w, inp, plan=plan)
     _assert_ok(check_rows(w, inp, D), f"int8 {shape} [{p}]")
 
 
+@pytest.mark.parametrize("plan", I8_PLANS)
 @pytest.mark.parametrize("fill", [-128, 127])
-def test_int8_extremes(fill):
+def test_int8_extremes(fill, plan):
     """All entries at one extreme, K = 8192: |sum| = 2^27 (or 127^2 * 8192)."""
     M, N, K = 256, 256, 8192
     A = torch.full((M, K), fill, dtype=torch.int8)
@@ -205,7 +249,7 @@ def test_int8_extremes(fill):
                       dtype=torch.int32)
     w = Workload("i8x", 52, M, N, K, I8, I32, I32, "int")
     inp = {"A": A, "B": B, "C": C}
-    D, p = run_gpu(w, inp)
+    D, p = run_gpu(w, inp, plan=plan)
     want = (A[0, 0].long() * B[0, 0].long() * K) + C.long()
     assert torch.equal(D.long(), want), p
 
