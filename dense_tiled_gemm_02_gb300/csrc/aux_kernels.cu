@@ -96,6 +96,58 @@ __global__ void repack_kernel(const void* __restrict__ src, int src_type, long l
   }
 }
 
+// 16-bit rows copied between a side whose rows start on 16-byte boundaries
+// (a workspace with its leading dimension rounded up to 8 elements) and a
+// side with arbitrary 2-byte alignment.  A thread moves 8 consecutive
+// elements: one 16-byte access on the aligned side, eight 2-byte accesses on
+// the other (consecutive threads cover consecutive bytes, so a warp access
+// still spans 512 contiguous bytes).  TO_ALIGNED: src arbitrary -> dst
+// aligned; otherwise src aligned -> dst arbitrary.  Elements of the aligned
+// side's last chunk beyond `cols` are written as zeros or not read.
+template <bool TO_ALIGNED>
+__global__ void copy16_kernel(const uint16_t* __restrict__ src, long long ld_src,
+                              uint16_t* __restrict__ dst, long long ld_dst, long long rows,
+                              long long cols) {
+  const long long c8 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c8 * 8 >= cols) return;
+  const long long c0 = c8 * 8;
+  const int nv = cols - c0 < 8 ? static_cast<int>(cols - c0) : 8;
+  constexpr int R = 4;
+  const long long step = static_cast<long long>(gridDim.y) * R;
+  for (long long r0 = static_cast<long long>(blockIdx.y) * R; r0 < rows; r0 += step) {
+    uint4 v[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const long long r = r0 + i;
+      if (r >= rows) break;
+      if (TO_ALIGNED) {
+        uint16_t e[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) e[k] = k < nv ? src[r * ld_src + c0 + k] : uint16_t(0);
+        v[i].x = e[0] | (uint32_t(e[1]) << 16);
+        v[i].y = e[2] | (uint32_t(e[3]) << 16);
+        v[i].z = e[4] | (uint32_t(e[5]) << 16);
+        v[i].w = e[6] | (uint32_t(e[7]) << 16);
+      } else {
+        v[i] = *reinterpret_cast<const uint4*>(src + r * ld_src + c0);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const long long r = r0 + i;
+      if (r >= rows) break;
+      if (TO_ALIGNED) {
+        *reinterpret_cast<uint4*>(dst + r * ld_dst + c0) = v[i];
+      } else {
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (k < nv) dst[r * ld_dst + c0 + k] = static_cast<uint16_t>(w[k / 2] >> (16 * (k & 1)));
+      }
+    }
+  }
+}
+
 // int8 -> bf16 widening, 4 elements per thread (rows whose starts and
 // lengths are multiples of 4 elements), four rows per step.
 __global__ void widen_i8_x4_kernel(const char4* __restrict__ src, long long ld_src4,
@@ -135,25 +187,44 @@ cudaError_t launch_reduce(const KParams& p, int row_order, int num_sms, cudaStre
   return cudaGetLastError();
 }
 
+namespace {
+dim3 copy_grid(long long chunks, long long rows, int num_sms) {
+  const unsigned gx = static_cast<unsigned>((chunks + 255) / 256);
+  long long gy = (static_cast<long long>(num_sms) * 16 + gx - 1) / gx;
+  const long long row_steps = (rows + 3) / 4;  // the copy kernels take four rows a step
+  if (gy > row_steps) gy = row_steps;
+  if (gy > 65535) gy = 65535;
+  if (gy < 1) gy = 1;
+  return dim3(gx, static_cast<unsigned>(gy));
+}
+}  // namespace
+
 cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint16_t* dst,
                           long long ld_dst, long long rows, long long cols, int num_sms,
                           cudaStream_t st) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   const bool x4 = src_type == T_I8 && cols % 4 == 0 && ld_src % 4 == 0 && ld_dst % 4 == 0 &&
                   reinterpret_cast<uintptr_t>(src) % 4 == 0;
-  const long long ccols = x4 ? cols / 4 : cols;
-  const unsigned gx = static_cast<unsigned>((ccols + 255) / 256);
-  long long gy = (static_cast<long long>(num_sms) * 16 + gx - 1) / gx;
-  const long long row_steps = (rows + 3) / 4;  // both kernels take four rows a step
-  if (gy > row_steps) gy = row_steps;
-  if (gy > 65535) gy = 65535;
-  const dim3 grid(gx, static_cast<unsigned>(gy));
-  if (x4)
-    widen_i8_x4_kernel<<<grid, 256, 0, st>>>(static_cast<const char4*>(src), ld_src / 4,
-                                             reinterpret_cast<uint2*>(dst), ld_dst / 4, rows,
-                                             ccols);
-  else
-    repack_kernel<<<grid, 256, 0, st>>>(src, src_type, ld_src, dst, ld_dst, rows, cols);
+  if (x4) {
+    widen_i8_x4_kernel<<<copy_grid(cols / 4, rows, num_sms), 256, 0, st>>>(
+        static_cast<const char4*>(src), ld_src / 4, reinterpret_cast<uint2*>(dst), ld_dst / 4,
+        rows, cols / 4);
+  } else if (src_type != T_I8 && ld_dst % 8 == 0 && reinterpret_cast<uintptr_t>(dst) % 16 == 0) {
+    copy16_kernel<true><<<copy_grid((cols + 7) / 8, rows, num_sms), 256, 0, st>>>(
+        static_cast<const uint16_t*>(src), ld_src, dst, ld_dst, rows, cols);
+  } else {
+    repack_kernel<<<copy_grid(cols, rows, num_sms), 256, 0, st>>>(src, src_type, ld_src, dst,
+                                                                  ld_dst, rows, cols);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_out16(const uint16_t* src, long long ld_src, uint16_t* dst,
+                              long long ld_dst, long long rows, long long cols, int num_sms,
+                              cudaStream_t st) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  copy16_kernel<false><<<copy_grid((cols + 7) / 8, rows, num_sms), 256, 0, st>>>(
+      src, ld_src, dst, ld_dst, rows, cols);
   return cudaGetLastError();
 }
 

@@ -102,6 +102,11 @@ struct gemm_plan {
   size_t ws_bytes = 0;
   size_t ws_partial_off = 0;
   size_t ws_tail_off = 0, ws_flags_off = 0;  // last-wave partials and their flags
+  // 16-bit C / D whose rows are not 16-byte aligned: aligned workspace copies
+  // (leading dimension stage_ld) that the kernel reads / writes instead.
+  bool c_stage = false, d_stage = false;
+  size_t ws_c_off = 0, ws_d_off = 0;
+  int64_t stage_ld = 0;
   uint32_t epoch = 0;                         // flag value of the latest run
   uint32_t* status = nullptr;
   int debug_flags = 0;
@@ -184,7 +189,7 @@ void make_plan_string(gemm_plan* h) {
   std::snprintf(buf, sizeof buf,
                 "M=%lld N=%lld K=%lld swap=%d pair=%d bn=%d ksub=%d stages=%d group_m=%d "
                 "splits=%d kb_per_split=%d tail=%d grid=%d i8x=%d a_mn=%d b_mn=%d repack_a=%d "
-                "repack_b=%d ws_bytes=%zu",
+                "repack_b=%d stage_c=%d stage_d=%d ws_bytes=%zu",
                 (long long)h->desc.M, (long long)h->desc.N, (long long)h->desc.K, h->choice.swap,
                 h->pair ? 1 : 0, h->choice.bn, h->choice.ksub,
                 h->pair ? h->pair->stages : (h->variant ? h->variant->stages : 0), h->kp.group_m,
@@ -192,7 +197,8 @@ void make_plan_string(gemm_plan* h) {
                 h->kp.kb_per_split,
                 h->kp.tail_parts > 1 ? h->kp.tiles_m * h->kp.tiles_n - h->kp.tail_start : 0,
                 h->grid, (int)h->i8x, h->kp.a_mn, h->kp.b_mn,
-                (int)h->a.repack, (int)h->b.repack, h->ws_bytes);
+                (int)h->a.repack, (int)h->b.repack, (int)h->c_stage, (int)h->d_stage,
+                h->ws_bytes);
   h->plan_str = buf;
 }
 
@@ -295,9 +301,10 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   h->choice = choose_plan(d.M, d.N, d.K, d.ab_type, d.layout_a, d.layout_b, sms);
   apply_force_plan(h->choice);
   if (h->i8x) {
-    // The exact-int8 kernels keep 128 columns of int32 sums (tensor memory in
-    // the pair kernel, registers in the single-CTA one) and no K split.
-    h->choice.bn = 128;
+    // The exact-int8 kernels: the pair kernel's 256 x 256 tile or the
+    // single-CTA 128 x 128 tile (each epilogue thread keeps 128 int32 sums in
+    // registers), with no K split.
+    h->choice.bn = h->choice.pair ? 256 : 128;
     h->choice.splits = 1;
     h->choice.tail = 0;
   }
@@ -433,6 +440,28 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     h->ws_flags_off = off;
     off += (size_t)round_up(tail_tiles * 2 * 4, 256);
   }
+  // C and D rows (along the internal N) that are not 16-byte aligned keep
+  // the kernels off their vector and TMA paths; an aligned copy costs one
+  // extra pass over C or D, far less than scattered 2-byte accesses from
+  // the epilogue.  Split-K plans write D from the reduce kernel, which
+  // streams it anyway.
+  auto is16 = [](int t) { return t == GEMM_F16 || t == GEMM_BF16; };
+  if (kp.splits == 1) {
+    h->c_stage = is16(d.c_type) && h->c_layout == GEMM_ROW_MAJOR && (h->ldc * 2) % 16 != 0;
+    h->d_stage = is16(d.d_type) && h->d_layout == GEMM_ROW_MAJOR && (h->ldd * 2) % 16 != 0;
+  }
+  if (h->c_stage || h->d_stage) {
+    h->stage_ld = round_up(std::max<int64_t>(h->N, 1), 8);
+    const size_t bytes = (size_t)round_up(h->stage_ld * h->M * 2, 256);
+    if (h->c_stage) {
+      h->ws_c_off = off;
+      off += bytes;
+    }
+    if (h->d_stage) {
+      h->ws_d_off = off;
+      off += bytes;
+    }
+  }
   h->ws_bytes = off;
   if (off > 0 && cudaMalloc(&h->ws, off) != cudaSuccess) {
     cudaGetLastError();
@@ -483,23 +512,41 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
   kp.timeout_ns = h->timeout_ns;
   kp.debug_flags = h->debug_flags;
   h->debug_flags = 0;  // test hooks apply to one run
-  kp.c_vec = (C && kp.c_cs == 1 && (reinterpret_cast<uintptr_t>(C) % 16) == 0 &&
-              (kp.c_rs * es_c) % 16 == 0) ? 1 : 0;
-  kp.d_vec = (kp.d_cs == 1 && (reinterpret_cast<uintptr_t>(D) % 16) == 0 &&
-              (kp.d_rs * es_d) % 16 == 0) ? 1 : 0;
   const bool row_order = h->d_layout == GEMM_ROW_MAJOR;
+  auto set_vec = [&]() {
+    kp.c_vec = (kp.C && kp.c_cs == 1 && (reinterpret_cast<uintptr_t>(kp.C) % 16) == 0 &&
+                (kp.c_rs * es_c) % 16 == 0) ? 1 : 0;
+    kp.d_vec = (kp.d_cs == 1 && (reinterpret_cast<uintptr_t>(kp.D) % 16) == 0 &&
+                (kp.d_rs * es_d) % 16 == 0) ? 1 : 0;
+  };
+  set_vec();
 
   if (d.K == 0) {  // D = C
     kp.splits = 0;
     return launch_reduce(kp, row_order, h->num_sms, st) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
   }
+  char* ws = static_cast<char*>(h->ws);
+  uint16_t* d_staged = nullptr;
+  if (h->c_stage && C) {
+    uint16_t* cs = reinterpret_cast<uint16_t*>(ws + h->ws_c_off);
+    if (launch_repack(C, d.c_type, kp.c_rs, cs, h->stage_ld, h->M, h->N, h->num_sms, st) !=
+        cudaSuccess)
+      return GEMM_ERR_CUDA;
+    kp.C = cs;
+    kp.c_rs = h->stage_ld;
+  }
+  if (h->d_stage) {
+    d_staged = reinterpret_cast<uint16_t*>(ws + h->ws_d_off);
+    kp.D = d_staged;
+    kp.d_rs = h->stage_ld;
+  }
+  set_vec();
 
   const bool swap = h->choice.swap != 0;
   const void* pa = swap ? B : A;  // storage of A'
   const void* pb = swap ? A : B;  // storage of B'
   const void* ta = pa;
   const void* tb = pb;
-  char* ws = static_cast<char*>(h->ws);
   // Operands the TMA unit cannot read in place go through the workspace.
   for (int which = 0; which < 2; ++which) {
     Operand& o = which == 0 ? h->a : h->b;
@@ -551,14 +598,14 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
   if (kp.d_tma) {
     const CUtensorMap* hit = nullptr;
     for (int i = 0; i < gemm_plan::kMapCache; ++i)
-      if (h->map_ptr[2][i] == D) hit = &h->map[2][i];
+      if (h->map_ptr[2][i] == kp.D) hit = &h->map[2][i];
     if (!hit) {
       const int slot = h->map_next[2];
       h->map_next[2] = (slot + 1) % gemm_plan::kMapCache;
       h->map_ptr[2][slot] = nullptr;
-      if (encode_store_d(&h->map[2][slot], D, kp.d_rs, h->M, h->N) != GEMM_OK)
+      if (encode_store_d(&h->map[2][slot], kp.D, kp.d_rs, h->M, h->N) != GEMM_OK)
         return GEMM_ERR_CUDA;
-      h->map_ptr[2][slot] = D;
+      h->map_ptr[2][slot] = kp.D;
       hit = &h->map[2][slot];
     }
     tmd = hit;
@@ -575,6 +622,9 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
     ++h->timing_used;
   }
   if (kp.splits > 1 && launch_reduce(kp, row_order, h->num_sms, st) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  if (d_staged && launch_copy_out16(d_staged, h->stage_ld, static_cast<uint16_t*>(D), h->ldd,
+                                    h->M, h->N, h->num_sms, st) != cudaSuccess)
     return GEMM_ERR_CUDA;
   return GEMM_OK;
 }

@@ -33,9 +33,30 @@ struct PlanRow {
   PlanChoice choice;
 };
 
-// Measured rows (exact shape match).
+// Measured rows (exact shape match), from interleaved sweeps of the tuning
+// script on one GB300 (median of 5 repeats; the figures are TFLOP/s or TOPS
+// of the whole call).  Layouts: 0 = row-major, 1 = column-major; types as in
+// common.h.
 static const PlanRow kTable[] = {
-    {0, 0, 0, -1, -1, -1, {0, 0, 0, 0, 0, 0, 0, 0}},  // sentinel
+    // 4096^3 bf16, B column-major: pair 256x256 1550, 2 K slices per stage
+    // 1526; the last-wave split is neutral here (1550 vs 1549).
+    {4096, 4096, 4096, T_BF16, 0, 1, {256, 8, 1, 0, 0, 1, 1, 1}},
+    // 8192^3 bf16, B column-major: pair 256x256 1864; pair 256x128 1099
+    // (1453 with 2 K slices per stage); single-CTA 128x256 1486.
+    {8192, 8192, 8192, T_BF16, 0, 1, {256, 8, 1, 0, 0, 1, 1, 1}},
+    // 8192^3 int8: pair 256x256 1209; with 2 K slices per stage 1184;
+    // single-CTA 128x128 858.
+    {8192, 8192, 8192, T_I8, 0, 0, {256, 8, 1, 0, 0, 1, 1, 0}},
+    // (64, 8192, 8192) bf16, all row-major: 128x128 tiles, split 2: 246;
+    // 128x256 split 4: 241; swapped 128x64 split 4: 230, split 2: 211.
+    {64, 8192, 8192, T_BF16, 0, 0, {128, 8, 2, 0, 0, 0, 1, 0}},
+    // (8192, 128, 4096) bf16: 128x64 tiles, no split: 370; 128x128 no
+    // split: 319, split 2: 286; pair 256x128 split 4: 260.
+    {8192, 128, 4096, T_BF16, 0, 0, {64, 8, 1, 0, 0, 0, 1, 0}},
+    // (1000, 1000, 1000) bf16: 128x64: 130; 128x128: 104; pair: 105 / 84.
+    {1000, 1000, 1000, T_BF16, 0, 0, {64, 8, 1, 0, 0, 0, 1, 0}},
+    // 1024^3 fp16: 128x64: 202; 128x128: 174; pair 256x128: 168.
+    {1024, 1024, 1024, T_F16, 0, 0, {64, 8, 1, 0, 0, 0, 1, 0}},
 };
 
 inline int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -62,9 +83,8 @@ inline PlanChoice choose_plan(int64_t M, int64_t N, int64_t K, int ab_type, int 
   else c.bn = 64;
   // Large problems: the CTA-pair 256 x 256 tile when its tiles fill at
   // least one wave of 2-CTA clusters (measured faster than 128 x 256 per SM).
-  // Exact int8 stays on the single-CTA 128 x 128 kernel: at 8192^3 it
-  // measured 851 TOPS against 759 for the pair kernel's 256 x 128 tile.
-  if (ab_type != T_I8 && Ni > 128 && cdiv64(Mi, 256) * cdiv64(Ni, 256) >= num_sms / 2) {
+  // Exact int8 takes the same rule with the pair kernel's int8 variant.
+  if (Ni > 128 && cdiv64(Mi, 256) * cdiv64(Ni, 256) >= num_sms / 2) {
     c.pair = 1;
     c.bn = 256;
     return c;

@@ -41,11 +41,15 @@ struct PairCfg {
   static constexpr uint32_t B_BYTES = KSUB * B_ATOM;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t PAIR_TX = 2 * STAGE_BYTES;      // bytes both CTAs land per stage
-  // Two fp32 accumulators of BN columns; the exact-int8 variant adds BN
-  // columns of int32 running sums.
-  static constexpr uint32_t TMEM_COLS = (!I8X && 2 * BN <= 256) ? 256 : 512;
+  // Two fp32 accumulators of BN columns each.
+  static constexpr uint32_t TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
+  // Epilogue warps: four (one per 32-lane quarter of tensor memory), or
+  // eight for exact int8, where two warps share a quarter and each keeps the
+  // int32 sums of half the tile's columns in registers.
+  static constexpr int EPI_WARPS = I8X ? 8 : 4;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static_assert(BN == 128 || BN == 256, "pair tile width");
-  static_assert(!I8X || 3 * BN <= 512, "int8 sums must fit in tensor memory");
+  static_assert(!I8X || BN == 256, "the int8 pair variant uses 256-wide tiles");
   static_assert(B_ATOM % 1024 == 0, "stage alignment");
 };
 
@@ -103,11 +107,12 @@ __device__ __forceinline__ Unit decode_pair_unit(const KParams& p, int u, int bn
 // beforehand, which is exact for |v| <= 128).  Each run of kb_per_chunk K
 // slices (512 K) is accumulated afresh in fp32, where every partial sum is an
 // integer of magnitude at most 512 * 2^14 = 2^23 and therefore exact; the
-// epilogue converts each finished chunk to int32 and adds it to a running sum
-// kept in tensor memory, while the MMA fills the other accumulator with the
-// next chunk.  The last chunk's sum gets C added and is stored as int32.
+// epilogue converts each finished chunk to int32 and adds it to running sums
+// held in registers (eight epilogue warps, 128 columns each), while the MMA
+// fills the other accumulator with the next chunk.  After the last chunk C is
+// added and the sums are stored as int32.
 template <int BN, int STAGES, int KSUB, bool I8X>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmD, const KParams p) {
@@ -142,7 +147,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), 1);
-      mbar_init(acc_empty(b), 8);  // one arrival per epilogue warp of both CTAs
+      mbar_init(acc_empty(b), 2 * Cfg::EPI_WARPS);  // one arrival per epilogue warp of both CTAs
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -248,45 +253,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       uint32_t s = 0, ph = 0, acc_it = 0;
       bool stop = false;
+      // One pass of the K loop into accumulator buffer `buf`.
+      auto k_loop = [&](const int kc, const int ke, const uint32_t buf) {
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        uint32_t accumulate = 0;
+        for (int kb = kc; kb < ke; kb += KSUB) {
+          if (!bounded_wait(full(s), ph, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
+            stop = true;
+            return;
+          }
+          const uint32_t a_lo = a_lo0 + s * (Cfg::A_BYTES >> 4);
+          const uint32_t b_lo = b_lo0 + s * (Cfg::B_BYTES >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4 * KSUB; ++kk)
+            mma_f16_ss_pair(d_tmem, sdesc(dhi, a_lo + a_off[kk]), sdesc(dhi, b_lo + b_off[kk]),
+                            p.idesc, accumulate | kk);
+          accumulate = 1;
+          mma_commit_pair_both(empty(s));
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      };
       for (int u = cid; u < num_units && !stop; u += ncl) {
         const Unit w = decode_pair_unit<KSUB>(p, u, BN);
-        // One accumulator per unit; the int8 variant takes a fresh one for
-        // every chunk of kb_per_chunk K slices.
-        int kc = w.kb0;
-        do {
-          const int ke = I8X ? min(w.kb1, kc + p.kb_per_chunk) : w.kb1;
-          const uint32_t buf = acc_it & 1u;
-          if (!bounded_wait(acc_empty(buf), ((acc_it >> 1) & 1u) ^ 1u, abort_flag, p.status,
-                            STATUS_TIMEOUT, tmo)) {
-            stop = true;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d_tmem = tmem_base + buf * BN;
-          uint32_t accumulate = 0;
-          for (int kb = kc; kb < ke; kb += KSUB) {
-            if (!bounded_wait(full(s), ph, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
+        if constexpr (I8X) {
+          // a fresh accumulator for every chunk of kb_per_chunk K slices
+          for (int kc = w.kb0; kc < w.kb1 && !stop; kc += p.kb_per_chunk) {
+            const uint32_t buf = acc_it & 1u;
+            if (!bounded_wait(acc_empty(buf), ((acc_it >> 1) & 1u) ^ 1u, abort_flag, p.status,
+                              STATUS_TIMEOUT, tmo)) {
               stop = true;
               break;
             }
-            const uint32_t a_lo = a_lo0 + s * (Cfg::A_BYTES >> 4);
-            const uint32_t b_lo = b_lo0 + s * (Cfg::B_BYTES >> 4);
-#pragma unroll
-            for (int kk = 0; kk < 4 * KSUB; ++kk)
-              mma_f16_ss_pair(d_tmem, sdesc(dhi, a_lo + a_off[kk]),
-                              sdesc(dhi, b_lo + b_off[kk]), p.idesc, accumulate | kk);
-            accumulate = 1;
-            mma_commit_pair_both(empty(s));
-            if (++s == STAGES) {
-              s = 0;
-              ph ^= 1u;
-            }
+            tc_fence_after();
+            k_loop(kc, min(w.kb1, kc + p.kb_per_chunk), buf);
+            if (stop) break;
+            mma_commit_pair_both(acc_full(buf));
+            ++acc_it;
           }
+        } else {
+          const uint32_t buf = acc_it & 1u;
+          if (!bounded_wait(acc_empty(buf), ((acc_it >> 1) & 1u) ^ 1u, abort_flag, p.status,
+                            STATUS_TIMEOUT, tmo))
+            break;
+          tc_fence_after();
+          k_loop(w.kb0, w.kb1, buf);
           if (stop) break;
           mma_commit_pair_both(acc_full(buf));
           ++acc_it;
-          kc = ke;
-        } while (I8X && kc < w.kb1);
+        }
       }
       mma_commit_pair_both(done_bar);
       drain_wait(done_bar, 0, 200000000ull);
@@ -306,55 +323,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const bool ep_leader = threadIdx.x == 64;
     uint32_t acc_it = 0, staged = 0;
     if constexpr (I8X) {
-      // Exact int8: per chunk, convert the fp32 accumulator (integers below
-      // 2^24, so cvt.rni is exact) and add it to the int32 sums kept in
-      // tensor memory columns [2*BN, 3*BN); the last chunk adds C and stores.
-      const uint32_t isum = tmem_base + lane_base + 2 * BN;
+      // Exact int8.  Warps 2-9: warp w reads TMEM lanes 32*(w%4).. and the
+      // columns [HC*half, HC*half + HC) of each accumulator.  Per chunk,
+      // each fp32 value (an integer below 2^24, so cvt.rni is exact) is
+      // added to the thread's int32 sums; after the last chunk C is added
+      // and the row segment stored.
+      constexpr int HC = BN / 2;
+      const int half = (warp - 2) >> 2;
+      const uint32_t col0 = static_cast<uint32_t>(half * HC);
+      int isum[HC];
       bool ok = true;
       for (int u = cid; u < num_units && ok; u += ncl) {
         const Unit w = decode_pair_unit<KSUB>(p, u, BN);
         const int r = w.m0 + BM * static_cast<int>(rank) + row_local;
         const int nch = (w.kb1 - w.kb0 + p.kb_per_chunk - 1) / p.kb_per_chunk;
+#pragma unroll
+        for (int j = 0; j < HC; ++j) isum[j] = 0;
         for (int ch = 0; ch < nch; ++ch) {
           const uint32_t buf = acc_it & 1u;
           if (ep_leader)
             *ep_go = bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status,
                                   STATUS_TIMEOUT, tmo) ? 1 : 0;
-          named_barrier_sync(1, 128);
+          named_barrier_sync(1, 32 * Cfg::EPI_WARPS);
           ok = *ep_go != 0;
-          named_barrier_sync(1, 128);
+          named_barrier_sync(1, 32 * Cfg::EPI_WARPS);
           if (!ok) break;
           tc_fence_after();
-          const bool first = ch == 0, last = ch == nch - 1;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t v[32], sm[32];
-            tmem_ld_32x32b_x32(tmem_base + lane_base + buf * BN + c * 32, v);
-            if (!first) tmem_ld_32x32b_x32(isum + c * 32, sm);
+          // 16 columns at a time: the 128 sums already hold most of the
+          // registers a thread of this 320-thread block may have.
+#pragma unroll
+          for (int c = 0; c < HC / 16; ++c) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(tmem_base + lane_base + buf * BN + col0 + c * 16, v);
             tmem_ld_wait();
-            if (c == BN / 32 - 1) {
+            if (c == HC / 16 - 1) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive_cluster(map_shared_rank(acc_empty(buf), 0));
             }
-            int t[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int x = __float2int_rn(__uint_as_float(v[j]));
-              t[j] = first ? x : static_cast<int>(sm[j]) + x;
-            }
-            if (!last) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) sm[j] = static_cast<uint32_t>(t[j]);
-              tmem_st_32x32b_x32(isum + c * 32, sm);
-            } else {
-              store_d_i32(p, r, w.n0 + c * 32, t);
-            }
+            for (int j = 0; j < 16; ++j) isum[c * 16 + j] += __float2int_rn(__uint_as_float(v[j]));
           }
-          // the next chunk reads these sums back
-          if (!last) tmem_st_wait();
           ++acc_it;
         }
+        if (!ok) break;
+#pragma unroll
+        for (int c = 0; c < HC / 32; ++c)
+          store_d_i32(p, r, w.n0 + static_cast<int>(col0) + c * 32,
+                      *reinterpret_cast<int(*)[32]>(isum + c * 32));
       }
     } else {
     for (int u = cid; u < num_units; u += ncl) {

@@ -48,5 +48,10 @@ cudaError_t launch_reduce(const KParams& p, int row_order, int num_sms, cudaStre
 cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint16_t* dst,
                           long long ld_dst, long long rows, long long cols, int num_sms,
                           cudaStream_t st);
+// 16-bit rows from a 16-byte aligned workspace (ld_src a multiple of 8
+// elements) to a destination of any 2-byte alignment.
+cudaError_t launch_copy_out16(const uint16_t* src, long long ld_src, uint16_t* dst,
+                              long long ld_dst, long long rows, long long cols, int num_sms,
+                              cudaStream_t st);
 
 }  // namespace gb300

@@ -8,11 +8,11 @@
 namespace gb300 {
 
 namespace {
-template <int BN, int STAGES, int KSUB>
+template <int BN, int STAGES, int KSUB, bool I8X>
 cudaLaunchConfig_t pair_config(int grid, cudaStream_t st, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.blockDim = dim3(PairCfg<BN, KSUB, I8X>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = pair_smem_bytes<BN, STAGES, KSUB>();
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -28,7 +28,7 @@ template <int BN, int STAGES, int KSUB, bool I8X>
 cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
                         const KParams& p, int grid, cudaStream_t st) {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pair_config<BN, STAGES, KSUB>(grid, st, attr);
+  cudaLaunchConfig_t cfg = pair_config<BN, STAGES, KSUB, I8X>(grid, st, attr);
   return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, KSUB, I8X>, a, b, d, p);
 }
 
@@ -42,7 +42,7 @@ cudaError_t prepare_pair() {
 template <int BN, int STAGES, int KSUB, bool I8X>
 int max_clusters_pair() {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pair_config<BN, STAGES, KSUB>(2, nullptr, attr);
+  cudaLaunchConfig_t cfg = pair_config<BN, STAGES, KSUB, I8X>(2, nullptr, attr);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<BN, STAGES, KSUB, I8X>, &cfg) !=
       cudaSuccess) {
@@ -60,7 +60,7 @@ int max_clusters_pair() {
 
 const PairVariant kPairVariants[] = {GB_PAIR(256, 6, 1, false), GB_PAIR(256, 3, 2, false),
                                      GB_PAIR(128, 8, 1, false), GB_PAIR(128, 4, 2, false),
-                                     GB_PAIR(128, 8, 1, true),  GB_PAIR(128, 4, 2, true)};
+                                     GB_PAIR(256, 6, 1, true),  GB_PAIR(256, 3, 2, true)};
 const int kNumPairVariants = 6;
 
 }  // namespace gb300

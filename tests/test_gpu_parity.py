@@ -15,8 +15,8 @@ import pytest
 import torch
 
 import dense_tiled_gemm_02_gb300 as pkg
-from gpu_helpers import check_points, check_rows, logical, run_gpu
-from workloads import (BF16, COL, F16, F32, I8, I32, ROW, WORKLOADS, Workload, draw,
+from gpu_helpers import check_points, check_rows, forced_plan, logical, run_gpu
+from workloads import (BF16, COL, F16, F32, I8, I32, ROW, TORCH_DTYPE, WORKLOADS, Workload, draw,
                        make_inputs, sample_points, sample_rows, storage_shape)
 
 pytestmark = pytest.mark.gpu
@@ -117,6 +117,25 @@ def test_ragged_shapes(shape, plan):
     _assert_ok(check_rows(w, inp, D), f"{shape} [{p}]")
 
 
+@pytest.mark.parametrize("plan", [None, "pair=0", "pair=1,bn=128"])
+def test_unaligned_c_d_staged_and_aliased(plan):
+    """16-bit C and D rows that are not 16-byte aligned go through aligned
+    workspace copies (stage_c / stage_d in the plan); D may alias C there."""
+    M, N, K = 390, 301, 200
+    w = Workload("stage", 10, M, N, K, BF16, BF16, BF16, "normal")
+    inp = make_inputs(w)
+    A, B = inp["A"].cuda(), inp["B"].cuda()
+    CD = inp["C"].cuda().clone()  # C in, D out, same buffer (ld = 301)
+    with forced_plan(plan):
+        g = pkg.Gemm.like(A, B, CD, CD)
+    plan_str = g.plan()
+    assert "stage_c=1" in plan_str and "stage_d=1" in plan_str, plan_str
+    g.run(A, B, CD, CD)
+    assert g.status() == pkg.GEMM_OK
+    g.close()
+    _assert_ok(check_rows(w, inp, CD.cpu()), f"aliased [{plan_str}]")
+
+
 def test_k_zero_gives_c():
     w = Workload("k0", 8, 130, 70, 0, BF16, F16, F32, "normal")
     inp = make_inputs(w)
@@ -189,6 +208,37 @@ def test_kernel_timing_hook():
     _assert_ok(check_rows(w, inp, D_storage.cpu(), rows=[0, 127, 128, 4097, w.M - 1]),
                "timed run")
     g.close()
+
+
+# The measured rows of the selection table (csrc/plan_table.h) are the plans
+# these workloads get.
+TABLE_ROWS = {
+    "sq4096_bf16": "pair=1 bn=256 ksub=1",
+    "sq8192_bf16": "pair=1 bn=256 ksub=1",
+    "sq8192_i8": "pair=1 bn=256 ksub=1",
+    "skinny64x8192x8192_bf16": "swap=0 pair=0 bn=128 ksub=1 stages=6",
+    "skinny8192x128x4096_bf16": "swap=0 pair=0 bn=64 ksub=1 stages=8",
+    "rag1000_bf16": "swap=0 pair=0 bn=64",
+    "sq1024_f16": "swap=0 pair=0 bn=64",
+}
+
+
+@pytest.mark.parametrize("name", sorted(TABLE_ROWS))
+def test_plan_table_rows_engage(name):
+    w = WORKLOADS[name]
+    dev = torch.device("cuda")
+    A = torch.empty(storage_shape(w.M, w.K, w.layout_a), dtype=TORCH_DTYPE[w.ab_type], device=dev)
+    B = torch.empty(storage_shape(w.K, w.N, w.layout_b), dtype=TORCH_DTYPE[w.ab_type], device=dev)
+    D = torch.empty(storage_shape(w.M, w.N, w.layout_d), dtype=TORCH_DTYPE[w.d_type], device=dev)
+    C = None if w.c_type is None else torch.empty(storage_shape(w.M, w.N, w.layout_c),
+                                                  dtype=TORCH_DTYPE[w.c_type], device=dev)
+    g = pkg.Gemm.like(logical(A, w.layout_a), logical(B, w.layout_b),
+                      None if C is None else logical(C, w.layout_c), logical(D, w.layout_d))
+    plan = g.plan()
+    g.close()
+    assert TABLE_ROWS[name] in plan, plan
+    want_splits = {"skinny64x8192x8192_bf16": 2}.get(name, 1)
+    assert f" splits={want_splits} " in plan, plan
 
 
 # ------------------------------------------------------------------ full-size configs
