@@ -9,7 +9,8 @@ no CPU fallback.
 Low-level names mirror ``include/gemm.h``: ``gemm_create``, ``gemm_run``,
 ``gemm_get_status``, ``gemm_destroy``, ``gemm_strerror``,
 ``gemm_plan_string``, ``gemm_workspace_bytes``, ``gemm_raster_tile``,
-``gemm_debug_set``, ``gemm_timing_enable``, ``gemm_timing_read``.  ``Gemm`` wraps a handle for torch tensors.
+``gemm_debug_set``, ``gemm_timing_enable``, ``gemm_timing_read``,
+``gemm_pair_schedule``.  ``Gemm`` wraps a handle for torch tensors.
 """
 from __future__ import annotations
 
@@ -32,7 +33,8 @@ GEMM_DEBUG_SKIP_FIRST_FILL = 1
 
 EXPORTED = ["gemm_create", "gemm_run", "gemm_get_status", "gemm_destroy", "gemm_strerror",
             "gemm_plan_string", "gemm_workspace_bytes", "gemm_raster_tile", "gemm_debug_set",
-            "gemm_run_splitk_noalloc", "gemm_timing_enable", "gemm_timing_read"]
+            "gemm_run_splitk_noalloc", "gemm_timing_enable", "gemm_timing_read",
+            "gemm_pair_schedule"]
 GEMM_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
@@ -89,6 +91,8 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
     lib.gemm_debug_set.restype = ci
     lib.gemm_run_splitk_noalloc.argtypes = [ctypes.POINTER(GemmDesc), ci, vp, vp, vp, vp, vp]
     lib.gemm_run_splitk_noalloc.restype = ci
+    lib.gemm_pair_schedule.argtypes = [i64, i64, i64, ci, ci, ci, ci, ci, ci, ctypes.POINTER(i64)]
+    lib.gemm_pair_schedule.restype = ci
     lib.gemm_timing_enable.argtypes = [vp, ci]
     lib.gemm_timing_enable.restype = ci
     lib.gemm_timing_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ci]
@@ -139,6 +143,25 @@ def gemm_raster_tile(t: int, num_pid_m: int, num_pid_n: int, group_m: int):
 
 def gemm_debug_set(h: int, flags: int, timeout_ns: int = 0) -> int:
     return load().gemm_debug_set(h, flags, timeout_ns)
+
+
+def gemm_pair_schedule(tiles_m: int, tiles_n: int, group_m: int, num_kb: int, ksub: int,
+                       clusters: int, stream_k: bool, cid: int) -> list[tuple]:
+    """All units of cluster cid: (tile_row, tile_col, kb0, kb1, shared, part, slot)."""
+    lib = load()
+    n = lib.gemm_pair_schedule(tiles_m, tiles_n, group_m, num_kb, ksub, clusters, int(stream_k),
+                               cid, 0, None)
+    if n < 0:
+        raise GemmError(n, "gemm_pair_schedule")
+    out = (ctypes.c_int64 * 7)()
+    units = []
+    for i in range(n):
+        rc = lib.gemm_pair_schedule(tiles_m, tiles_n, group_m, num_kb, ksub, clusters,
+                                    int(stream_k), cid, i, out)
+        if rc < 0:
+            raise GemmError(rc, "gemm_pair_schedule")
+        units.append(tuple(out))
+    return units
 
 
 def gemm_timing_enable(h: int, n: int) -> int:

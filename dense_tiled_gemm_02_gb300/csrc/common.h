@@ -50,14 +50,17 @@ struct KParams {
   uint32_t* status;              // device status word
   unsigned long long timeout_ns; // bound of every device-side wait
   int debug_flags;
-  // Last-wave split (pair kernel): tiles from tail_start on (in raster
-  // order) are each computed as two K halves by two clusters; the second
-  // half leaves its fp32 partial in tail_ws and raises tail_flags to
-  // epoch, the first half adds it and finishes the tile.
-  int tail_start;                // first split tile (= number of whole tiles)
-  int tail_parts;                // 1 = no split, 2 = split in two K halves
-  float* tail_ws;                // [split tile][CTA half][128 rows][BN] fp32
-  uint32_t* tail_flags;          // [split tile][CTA half]
+  // Stream-K hybrid (pair kernel), when sk_len > 0: cluster c first takes
+  // sk_dp whole tiles (c, c + clusters, ...), then one contiguous run of
+  // K stages over the tiles from sk_start on (sk_len stages, one more for
+  // clusters c < sk_rem), so that every cluster gets the same work.  A tile
+  // whose stages fall to two clusters is finished by the one that reaches
+  // it last (the end of its run); the other (at the start of its run)
+  // leaves its fp32 partial in tail_ws[c] and raises tail_flags[c] to epoch.
+  // sk_len = 0: units are dealt round-robin.
+  int sk_dp, sk_start, sk_len, sk_rem;
+  float* tail_ws;                // [leaving cluster][CTA half][128 rows][BN] fp32
+  uint32_t* tail_flags;          // [leaving cluster][CTA half]
   uint32_t epoch;                // value the flags take during this run
 };
 
@@ -83,6 +86,108 @@ GB_HD void raster_tile(int64_t t, int64_t num_pid_m, int64_t num_pid_n, int64_t 
   const int64_t size_m = rem < group_m ? rem : group_m;
   pid_m = first_m + (t % in_group) % size_m;
   pid_n = (t % in_group) / size_m;
+}
+
+// A piece of work of one CTA (or CTA pair): the output tile at (m0, n0) and
+// the K slices [kb0, kb1).
+struct Unit {
+  int m0, n0, kb0, kb1, split;
+  int tail;  // 1: part of a tile shared by two clusters (pair kernel, stream-K)
+  int part;  // 0: adds the other cluster's partial and finishes the tile;
+             // 1: leaves its partial sums
+  int ti;    // partial-sum slot (the leaving cluster)
+};
+
+// Stream-K hybrid plan (pair kernel): with W = tiles / clusters full waves
+// and a partial last wave, W - 1 waves run as whole tiles and the stages of
+// the remaining tiles are dealt out as equal contiguous runs, one per
+// cluster.  Runs are at least one tile long (the remaining tiles number at
+// least `clusters`), so a tile is shared by at most two clusters.  Leaves
+// the fields zero (round-robin units) when the waves are already full or a
+// run would be shorter than a tile.
+GB_HD void plan_stream_k(int64_t tiles, int clusters, int num_kb, int ksub, KParams& p) {
+  p.sk_dp = p.sk_start = p.sk_len = p.sk_rem = 0;
+  if (clusters <= 0 || tiles < clusters || tiles % clusters == 0 || ksub <= 0 ||
+      num_kb % ksub != 0 || num_kb / ksub < 2)
+    return;
+  const int64_t waves = tiles / clusters;
+  const int64_t sk_tiles = tiles - (waves - 1) * clusters;
+  const int64_t work = sk_tiles * (num_kb / ksub);
+  p.sk_dp = static_cast<int>(waves - 1);
+  p.sk_start = static_cast<int>((waves - 1) * clusters);
+  p.sk_len = static_cast<int>(work / clusters);
+  p.sk_rem = static_cast<int>(work % clusters);
+}
+
+// Work of one cluster.  Round-robin: units u = cid, cid + ncl, ... of the
+// tiles x splits.  Stream-K hybrid: sk_dp whole tiles, then the tile pieces
+// of the cluster's run of K stages [g0, g1) (stages of ksub slices).
+struct PairWork {
+  int n;       // number of units
+  int g0, g1;  // stream-K run (stage indices over the tiles from sk_start)
+};
+
+GB_HD PairWork pair_work(const KParams& p, int ksub, int cid, int ncl) {
+  PairWork pw;
+  if (p.sk_len > 0) {
+    const int nks = p.num_kb / ksub;
+    pw.g0 = cid * p.sk_len + (cid < p.sk_rem ? cid : p.sk_rem);
+    pw.g1 = pw.g0 + p.sk_len + (cid < p.sk_rem ? 1 : 0);
+    pw.n = p.sk_dp + ((pw.g1 - 1) / nks - pw.g0 / nks + 1);
+  } else {
+    const int total = p.tiles_m * p.tiles_n * p.splits;
+    pw.g0 = pw.g1 = 0;
+    pw.n = cid < total ? (total - cid + ncl - 1) / ncl : 0;
+  }
+  return pw;
+}
+
+// The i-th unit of cluster cid; m0 counts rows of 2*BM-row pair tiles.
+GB_HD Unit pair_unit(const KParams& p, const PairWork& pw, int ksub, int cid, int ncl, int i,
+                     int bn) {
+  Unit w;
+  int t;
+  w.split = 0;
+  w.tail = 0;
+  w.part = 0;
+  w.ti = 0;
+  if (p.sk_len > 0 && i >= p.sk_dp) {
+    const int nks = p.num_kb / ksub;
+    const int s = pw.g0 / nks + (i - p.sk_dp);
+    const int st0 = pw.g0 - s * nks > 0 ? pw.g0 - s * nks : 0;
+    const int st1 = pw.g1 - s * nks < nks ? pw.g1 - s * nks : nks;
+    t = p.sk_start + s;
+    w.kb0 = st0 * ksub;
+    w.kb1 = st1 * ksub;
+    // A run is at least one tile long, so a piece cannot both start and
+    // end inside its tile: the first piece of a run that starts mid-tile
+    // leaves its partial (slot cid); the last piece of a run that ends
+    // mid-tile finishes that tile with the next cluster's partial.
+    if (st0 > 0) {
+      w.tail = 1;
+      w.part = 1;
+      w.ti = cid;
+    } else if (st1 < nks) {
+      w.tail = 1;
+      w.part = 0;
+      w.ti = cid + 1;
+    }
+  } else if (p.sk_len > 0) {
+    t = cid + i * ncl;
+    w.kb0 = 0;
+    w.kb1 = p.num_kb;
+  } else {
+    const int u = cid + i * ncl;
+    t = u / p.splits;
+    w.split = u - t * p.splits;
+    w.kb0 = w.split * p.kb_per_split;
+    w.kb1 = w.kb0 + p.kb_per_split < p.num_kb ? w.kb0 + p.kb_per_split : p.num_kb;
+  }
+  int64_t pm, pn;
+  raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
+  w.m0 = static_cast<int>(pm) * (2 * BM);
+  w.n0 = static_cast<int>(pn) * bn;
+  return w;
 }
 
 }  // namespace gb300

@@ -195,7 +195,7 @@ void make_plan_string(gemm_plan* h) {
                 h->pair ? h->pair->stages : (h->variant ? h->variant->stages : 0), h->kp.group_m,
                 h->kp.splits,
                 h->kp.kb_per_split,
-                h->kp.tail_parts > 1 ? h->kp.tiles_m * h->kp.tiles_n - h->kp.tail_start : 0,
+                h->kp.sk_len > 0 ? h->kp.tiles_m * h->kp.tiles_n - h->kp.sk_start : 0,
                 h->grid, (int)h->i8x, h->kp.a_mn, h->kp.b_mn,
                 (int)h->a.repack, (int)h->b.repack, (int)h->c_stage, (int)h->d_stage,
                 h->ws_bytes);
@@ -270,6 +270,33 @@ int gemm_raster_tile(int64_t t, int64_t num_pid_m, int64_t num_pid_n, int64_t gr
   if (t < 0 || t >= num_pid_m * num_pid_n) return GEMM_ERR_INVALID_ARG;
   raster_tile(t, num_pid_m, num_pid_n, group_m, *pid_m, *pid_n);
   return GEMM_OK;
+}
+
+int gemm_pair_schedule(int64_t tiles_m, int64_t tiles_n, int64_t group_m, int num_kb, int ksub,
+                       int clusters, int stream_k, int cid, int i, int64_t* out) {
+  if (tiles_m <= 0 || tiles_n <= 0 || group_m <= 0 || num_kb <= 0 || ksub <= 0 ||
+      clusters <= 0 || cid < 0 || cid >= clusters || i < 0)
+    return GEMM_ERR_INVALID_ARG;
+  KParams p{};
+  p.tiles_m = (int)tiles_m;
+  p.tiles_n = (int)tiles_n;
+  p.group_m = (int)group_m;
+  p.num_kb = num_kb;
+  p.splits = 1;
+  p.kb_per_split = num_kb;
+  if (stream_k) plan_stream_k(tiles_m * tiles_n, clusters, num_kb, ksub, p);
+  const PairWork pw = pair_work(p, ksub, cid, clusters);
+  if (!out) return pw.n;
+  if (i >= pw.n) return GEMM_ERR_INVALID_ARG;
+  const Unit w = pair_unit(p, pw, ksub, cid, clusters, i, 1);
+  out[0] = w.m0 / (2 * BM);  // tile row
+  out[1] = w.n0;             // tile column (bn = 1)
+  out[2] = w.kb0;
+  out[3] = w.kb1;
+  out[4] = w.tail;
+  out[5] = w.part;
+  out[6] = w.ti;
+  return pw.n;
 }
 
 int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
@@ -393,23 +420,18 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     delete h;
     return GEMM_ERR_CUDA;
   }
-  // Last-wave split: when the tiles leave a partial final wave that fits
-  // twice over into the clusters, its tiles are computed as two K halves.
+  // Stream-K hybrid: when the tiles leave a partial last wave, all full
+  // waves but one run as whole tiles and the rest of the tiles' K stages
+  // are dealt out as equal contiguous runs, one per cluster, so that the
+  // clusters finish together.  Each run is at least one tile long, so a
+  // tile is shared by at most two clusters.
   const int64_t tiles = (int64_t)kp.tiles_m * kp.tiles_n;
-  kp.tail_parts = 1;
-  kp.tail_start = (int)tiles;
-  int64_t tail_tiles = 0;
-  if (h->pair && c.tail && kp.splits == 1 && tiles >= clusters && kp.num_kb >= 4 * c.ksub) {
-    const int64_t rem = tiles % clusters;
-    if (rem > 0 && 2 * rem <= clusters) {
-      tail_tiles = rem;
-      kp.tail_parts = 2;
-      kp.tail_start = (int)(tiles - rem);
-    }
-  }
-  const int64_t units_all =
-      kp.tail_parts > 1 ? kp.tail_start + tail_tiles * kp.tail_parts : units;
-  if (h->pair) h->grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(units_all, clusters));
+  kp.sk_dp = kp.sk_start = kp.sk_len = kp.sk_rem = 0;
+  if (h->pair && c.tail && !h->i8x && kp.splits == 1)
+    plan_stream_k(tiles, clusters, kp.num_kb, c.ksub, kp);
+  const int64_t sk_slots = kp.sk_len > 0 ? clusters : 0;
+  if (h->pair) h->grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(
+                                 kp.sk_len > 0 ? clusters : units, clusters));
 
   // Workspace: operand copies the TMA unit can read, split-K partials, and
   // the last-wave partials with their flags.
@@ -434,11 +456,11 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     kp.ws_cs = row ? 1 : h->M;
     kp.ws_split = h->M * h->N;
   }
-  if (tail_tiles > 0) {
+  if (sk_slots > 0) {
     h->ws_tail_off = off;
-    off += (size_t)round_up(tail_tiles * 2 * BM * c.bn * 4, 256);
+    off += (size_t)round_up(sk_slots * 2 * BM * c.bn * 4, 256);
     h->ws_flags_off = off;
-    off += (size_t)round_up(tail_tiles * 2 * 4, 256);
+    off += (size_t)round_up(sk_slots * 2 * 4, 256);
   }
   // C and D rows (along the internal N) that are not 16-byte aligned keep
   // the kernels off their vector and TMA paths; an aligned copy costs one
@@ -468,8 +490,8 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     delete h;
     return GEMM_ERR_ALLOC_FAILED;
   }
-  if (tail_tiles > 0 &&
-      cudaMemset(static_cast<char*>(h->ws) + h->ws_flags_off, 0, tail_tiles * 2 * 4) !=
+  if (sk_slots > 0 &&
+      cudaMemset(static_cast<char*>(h->ws) + h->ws_flags_off, 0, sk_slots * 2 * 4) !=
           cudaSuccess) {
     cudaGetLastError();
     cudaFree(h->ws);
@@ -584,7 +606,7 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
     tm[which] = &h->map[which][slot];
   }
   if (kp.splits > 1) kp.ws = reinterpret_cast<float*>(ws + h->ws_partial_off);
-  if (kp.tail_parts > 1) {
+  if (kp.sk_len > 0) {
     kp.tail_ws = reinterpret_cast<float*>(ws + h->ws_tail_off);
     kp.tail_flags = reinterpret_cast<uint32_t*>(ws + h->ws_flags_off);
     if (++h->epoch == 0) h->epoch = 1;  // flags start at 0: never reuse it

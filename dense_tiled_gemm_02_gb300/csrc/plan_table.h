@@ -38,11 +38,12 @@ struct PlanRow {
 // of the whole call).  Layouts: 0 = row-major, 1 = column-major; types as in
 // common.h.
 static const PlanRow kTable[] = {
-    // 4096^3 bf16, B column-major: pair 256x256 1550, 2 K slices per stage
-    // 1526; the last-wave split is neutral here (1550 vs 1549).
-    {4096, 4096, 4096, T_BF16, 0, 1, {256, 8, 1, 0, 0, 1, 1, 1}},
-    // 8192^3 bf16, B column-major: pair 256x256 1864; pair 256x128 1099
-    // (1453 with 2 K slices per stage); single-CTA 128x256 1486.
+    // 4096^3 bf16, B column-major: pair 256x256 without stream-K 1565,
+    // with it 1547; 2 K slices per stage 1495; GROUP_M 4 / 16: 1551 / 1546.
+    {4096, 4096, 4096, T_BF16, 0, 1, {256, 8, 1, 0, 0, 1, 1, 0}},
+    // 8192^3 bf16, B column-major: pair 256x256 with stream-K 1932, without
+    // 1915; pair 256x128 1099 (1453 with 2 K slices per stage); single-CTA
+    // 128x256 1486.
     {8192, 8192, 8192, T_BF16, 0, 1, {256, 8, 1, 0, 0, 1, 1, 1}},
     // 8192^3 int8: pair 256x256 1209; with 2 K slices per stage 1184;
     // single-CTA 128x128 858.

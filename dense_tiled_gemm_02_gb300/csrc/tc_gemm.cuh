@@ -45,13 +45,6 @@ constexpr uint32_t smem_bytes() {
   return STAGES * TileCfg<BN>::STAGE_TX + 256 + 1024;
 }
 
-struct Unit {
-  int m0, n0, kb0, kb1, split;
-  int tail;  // 1: a K half of a last-wave tile (pair kernel)
-  int part;  // which half: 0 finishes the tile, 1 leaves its partial sums
-  int ti;    // index of the split tile
-};
-
 __device__ __forceinline__ Unit decode_unit(const KParams& p, int u, int bn) {
   Unit w;
   const int t = u / p.splits;

@@ -62,45 +62,6 @@ constexpr uint32_t pair_smem_bytes() {
   return STAGES * PairCfg<BN, KSUB>::STAGE_BYTES + 2 * D_STAGE_BYTES + 256 + 1024;
 }
 
-// Units: whole 256 x BN tiles (or split-K pieces), then, when the last
-// wave is split, two K halves per remaining tile.
-__device__ __forceinline__ int pair_num_units(const KParams& p) {
-  const int tiles = p.tiles_m * p.tiles_n;
-  return p.tail_parts > 1 ? p.tail_start + (tiles - p.tail_start) * p.tail_parts
-                          : tiles * p.splits;
-}
-
-template <int KSUB>
-__device__ __forceinline__ Unit decode_pair_unit(const KParams& p, int u, int bn) {
-  Unit w;
-  int t;
-  if (p.tail_parts > 1 && u >= p.tail_start) {
-    const int v = u - p.tail_start;
-    w.ti = v / p.tail_parts;
-    w.part = v - w.ti * p.tail_parts;
-    w.tail = 1;
-    w.split = 0;
-    t = p.tail_start + w.ti;
-    const int per = (p.num_kb + p.tail_parts - 1) / p.tail_parts;
-    const int half = (per + KSUB - 1) / KSUB * KSUB;  // halves start on stage boundaries
-    w.kb0 = w.part * half;
-    w.kb1 = min(p.num_kb, w.kb0 + half);
-  } else {
-    t = u / p.splits;
-    w.split = u - t * p.splits;
-    w.tail = 0;
-    w.part = 0;
-    w.ti = 0;
-    w.kb0 = w.split * p.kb_per_split;
-    w.kb1 = min(p.num_kb, w.kb0 + p.kb_per_split);
-  }
-  int64_t pm, pn;
-  raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
-  w.m0 = static_cast<int>(pm) * (2 * BM);
-  w.n0 = static_cast<int>(pn) * bn;
-  return w;
-}
-
 // kb0/kb1 count 64-wide K slices; a stage covers KSUB of them.
 //
 // I8X: exact int8 GEMM on the bf16 tensor pipe (operands widened to bf16
@@ -168,9 +129,9 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  const int num_units = pair_num_units(p);
   const int cid = blockIdx.x >> 1;
   const int ncl = gridDim.x >> 1;
+  const PairWork pw = pair_work(p, KSUB, cid, ncl);
   const uint64_t tmo = p.timeout_ns;
 
   if (warp == 0) {
@@ -179,8 +140,8 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
       uint32_t it = 0, s = 0, ph = 0;  // it: stages issued; (s, ph): ring slot and phase
       int64_t skipped = -1;
       bool stop = false;
-      for (int u = cid; u < num_units && !stop; u += ncl) {
-        const Unit w = decode_pair_unit<KSUB>(p, u, BN);
+      for (int i = 0; i < pw.n && !stop; ++i) {
+        const Unit w = pair_unit(p, pw, KSUB, cid, ncl, i, BN);
         const int am = w.m0 + BM * static_cast<int>(rank);
         const int bn0 = w.n0 + Cfg::BNH * static_cast<int>(rank);
         for (int kb = w.kb0; kb < w.kb1; kb += KSUB) {
@@ -276,8 +237,8 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
           }
         }
       };
-      for (int u = cid; u < num_units && !stop; u += ncl) {
-        const Unit w = decode_pair_unit<KSUB>(p, u, BN);
+      for (int i = 0; i < pw.n && !stop; ++i) {
+        const Unit w = pair_unit(p, pw, KSUB, cid, ncl, i, BN);
         if constexpr (I8X) {
           // a fresh accumulator for every chunk of kb_per_chunk K slices
           for (int kc = w.kb0; kc < w.kb1 && !stop; kc += p.kb_per_chunk) {
@@ -333,8 +294,8 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
       const uint32_t col0 = static_cast<uint32_t>(half * HC);
       int isum[HC];
       bool ok = true;
-      for (int u = cid; u < num_units && ok; u += ncl) {
-        const Unit w = decode_pair_unit<KSUB>(p, u, BN);
+      for (int i = 0; i < pw.n && ok; ++i) {
+        const Unit w = pair_unit(p, pw, KSUB, cid, ncl, i, BN);
         const int r = w.m0 + BM * static_cast<int>(rank) + row_local;
         const int nch = (w.kb1 - w.kb0 + p.kb_per_chunk - 1) / p.kb_per_chunk;
 #pragma unroll
@@ -373,8 +334,8 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
                       *reinterpret_cast<int(*)[32]>(isum + c * 32));
       }
     } else {
-    for (int u = cid; u < num_units; u += ncl) {
-      const Unit w = decode_pair_unit<KSUB>(p, u, BN);
+    for (int i = 0; i < pw.n; ++i) {
+      const Unit w = pair_unit(p, pw, KSUB, cid, ncl, i, BN);
       const int r = w.m0 + BM * static_cast<int>(rank) + row_local;
       const bool leaves_partial = w.tail && w.part == 1;
       const bool staged_store = p.d_tma && !leaves_partial && p.splits == 1;

@@ -197,6 +197,23 @@ GEMM_API int gemm_timing_enable(gemm_handle_t h, int n);
 GEMM_API int gemm_timing_read(gemm_handle_t h, float* ms, int n);
 
 /*
+ * gemm_pair_schedule: host-side view of how the CTA-pair kernel deals its
+ * work to clusters (for tests; no device needed).  For a tiles_m x tiles_n
+ * grid of tiles in the grouped order (group_m), num_kb 64-wide K slices,
+ * ring stages of ksub slices and `clusters` clusters, with the stream-K
+ * hybrid when stream_k != 0 and it applies (a partial last wave, at least
+ * one full wave), it returns the number of units of cluster cid; when out
+ * is non-NULL it also writes unit i of that cluster as out[0..6] = tile
+ * row, tile column, first K slice, end K slice, shared-tile flag, part
+ * (1 leaves its fp32 partial, 0 adds the partial and finishes the tile) and
+ * the partial-sum slot.  Returns GEMM_ERR_INVALID_ARG for a bad argument or
+ * i out of range.
+ */
+GEMM_API int gemm_pair_schedule(int64_t tiles_m, int64_t tiles_n, int64_t group_m, int num_kb,
+                                int ksub, int clusters, int stream_k, int cid, int i,
+                                int64_t* out);
+
+/*
  * Test hooks (not for production use).
  * gemm_debug_set: flags bit 0 makes the load warp of the next gemm_run skip
  * its first stage fill, so that the consumer's bounded wait expires and the

@@ -107,3 +107,72 @@ def test_raster_rejects_out_of_range():
     assert pkg.gemm_raster_tile(6, 2, 3, 2)[0] == pkg.GEMM_ERR_INVALID_ARG
     assert pkg.gemm_raster_tile(-1, 2, 3, 2)[0] == pkg.GEMM_ERR_INVALID_ARG
     assert pkg.gemm_raster_tile(0, 2, 3, 0)[0] == pkg.GEMM_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------------ pair-kernel work schedule
+def _schedule(tm, tn, group, nkb, ksub, clusters, sk):
+    return [pkg.gemm_pair_schedule(tm, tn, group, nkb, ksub, clusters, sk, c)
+            for c in range(clusters)]
+
+
+SCHEDULES = [
+    # (tiles_m, tiles_n, group_m, num_kb, ksub, clusters)
+    (16, 16, 8, 64, 1, 76),     # 4096^3 at 256x256 on 152 SMs
+    (32, 32, 8, 128, 1, 76),    # 8192^3
+    (16, 17, 8, 65, 1, 76),     # 4095 x 4097 x 4099
+    (16, 16, 8, 64, 2, 76),     # two K slices per stage
+    (16, 16, 8, 66, 2, 74),
+    (5, 31, 4, 3, 1, 76),       # short K: runs of a few stages
+    (7, 11, 8, 2, 1, 76),       # 77 tiles: one full wave and one tile
+    (10, 16, 8, 9, 1, 76),
+    (4, 4, 2, 64, 1, 16),       # tiles a multiple of the clusters: no stream-K
+    (3, 5, 8, 40, 1, 76),       # fewer tiles than clusters: no stream-K
+]
+
+
+@pytest.mark.parametrize("sk", [False, True])
+@pytest.mark.parametrize("tm,tn,group,nkb,ksub,clusters", SCHEDULES)
+def test_pair_schedule_covers_every_tile_stage_once(tm, tn, group, nkb, ksub, clusters, sk):
+    """Every (tile, K slice) is computed by exactly one unit; a shared tile
+    has exactly one piece that leaves its partial (slot = its cluster) and
+    one that adds that slot's partial and finishes it; the runs of stream-K
+    are balanced to one stage."""
+    sched = _schedule(tm, tn, group, nkb, ksub, clusters, sk)
+    seen = {}
+    pieces = {}
+    for cid, units in enumerate(sched):
+        for (r, c, kb0, kb1, shared, part, slot) in units:
+            assert 0 <= r < tm and 0 <= c < tn and 0 <= kb0 < kb1 <= nkb
+            assert kb0 % ksub == 0 and (kb1 % ksub == 0 or kb1 == nkb)
+            for k in range(kb0, kb1):
+                assert (r, c, k) not in seen, ((r, c, k), seen.get((r, c, k)), cid)
+                seen[(r, c, k)] = cid
+            pieces.setdefault((r, c), []).append((cid, kb0, kb1, shared, part, slot))
+    assert len(seen) == tm * tn * nkb
+    for tile, ps in pieces.items():
+        if len(ps) == 1:
+            cid, kb0, kb1, shared, part, slot = ps[0]
+            assert (kb0, kb1, shared) == (0, nkb, 0)
+            continue
+        assert sk and len(ps) == 2, (tile, ps)
+        first, second = sorted(ps, key=lambda x: x[1])
+        # the K head belongs to the cluster whose run ends there: it finishes
+        assert first[1] == 0 and first[3:5] == (1, 0)
+        assert second[2] == nkb and second[3:5] == (1, 1)
+        assert second[5] == second[0] and first[5] == second[0] == first[0] + 1
+    tiles = tm * tn
+    if sk and tiles >= clusters and tiles % clusters and nkb % ksub == 0 and nkb // ksub >= 2:
+        work = [sum(u[3] - u[2] for u in units) for units in sched]
+        assert max(work) - min(work) <= ksub + (nkb if tiles < 2 * clusters else nkb)
+        # stream-K part alone is balanced to one stage
+        waves = tiles // clusters
+        sk_work = [sum(u[3] - u[2] for u in units[waves - 1:]) for units in sched]
+        assert max(sk_work) - min(sk_work) <= ksub
+        # the leaver of a shared tile reaches it before any piece that waits
+        for cid, units in enumerate(sched):
+            waits = [i for i, u in enumerate(units) if u[4] and u[5] == 0]
+            leaves = [i for i, u in enumerate(units) if u[4] and u[5] == 1]
+            assert all(i == len(units) - 1 for i in waits)
+            assert all(i == waves - 1 for i in leaves)
+    else:
+        assert all(u[4] == 0 for units in sched for u in units)

@@ -80,7 +80,9 @@ def test_identity_plus_c(bn):
                                   "pair=1,bn=128", "pair=1,bn=256,grid=28",
                                   "pair=1,bn=256,grid=28,tail=0", "pair=1,bn=256,splits=2",
                                   "pair=1,bn=128,swap=1", "pair=1,bn=256,ksub=2",
-                                  "pair=1,bn=256,ksub=2,splits=3", "pair=1,bn=128,ksub=2"])
+                                  "pair=1,bn=256,ksub=2,splits=3", "pair=1,bn=128,ksub=2",
+                                  # stream-K runs over a few clusters
+                                  "pair=1,bn=128,grid=20", "pair=1,bn=256,ksub=2,grid=22"])
 def test_small_config(name, plan):
     w = WORKLOADS[name]
     inp = make_inputs(w)
