@@ -14,6 +14,8 @@
 #include <cuda_runtime.h>
 
 #include "common.h"
+#include "ptx.cuh"
+#include "tc_launch.h"
 
 namespace gb300 {
 
@@ -35,6 +37,8 @@ __device__ __forceinline__ void st_f(void* base, int t, long long off, float v) 
 // row_order = 1: element index walks D row by row (D rows contiguous),
 // otherwise column by column.
 __global__ void splitk_reduce_kernel(const KParams p, int row_order) {
+  pdl_wait();
+  pdl_trigger();
   const long long total = static_cast<long long>(p.M) * p.N;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
@@ -69,6 +73,8 @@ __global__ void splitk_reduce_kernel(const KParams p, int row_order) {
 __global__ void repack_kernel(const void* __restrict__ src, int src_type, long long ld_src,
                               uint16_t* __restrict__ dst, long long ld_dst, long long rows,
                               long long cols) {
+  pdl_wait();
+  pdl_trigger();
   const long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c >= cols) return;
   // Four rows per step: their loads are independent, so four are in flight.
@@ -108,6 +114,8 @@ template <bool TO_ALIGNED>
 __global__ void copy16_kernel(const uint16_t* __restrict__ src, long long ld_src,
                               uint16_t* __restrict__ dst, long long ld_dst, long long rows,
                               long long cols) {
+  pdl_wait();
+  pdl_trigger();
   const long long c8 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c8 * 8 >= cols) return;
   const long long c0 = c8 * 8;
@@ -153,6 +161,8 @@ __global__ void copy16_kernel(const uint16_t* __restrict__ src, long long ld_src
 __global__ void widen_i8_x4_kernel(const char4* __restrict__ src, long long ld_src4,
                                    uint2* __restrict__ dst, long long ld_dst4, long long rows,
                                    long long cols4) {
+  pdl_wait();
+  pdl_trigger();
   const long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c >= cols4) return;
   constexpr int R = 4;
@@ -183,8 +193,8 @@ cudaError_t launch_reduce(const KParams& p, int row_order, int num_sms, cudaStre
   long long blocks = (total + 255) / 256;
   const long long cap = static_cast<long long>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
-  splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(p, row_order);
-  return cudaGetLastError();
+  return launch_pdl(splitk_reduce_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+                    p, row_order);
 }
 
 namespace {
@@ -205,27 +215,23 @@ cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint1
   if (rows == 0 || cols == 0) return cudaSuccess;
   const bool x4 = src_type == T_I8 && cols % 4 == 0 && ld_src % 4 == 0 && ld_dst % 4 == 0 &&
                   reinterpret_cast<uintptr_t>(src) % 4 == 0;
-  if (x4) {
-    widen_i8_x4_kernel<<<copy_grid(cols / 4, rows, num_sms), 256, 0, st>>>(
-        static_cast<const char4*>(src), ld_src / 4, reinterpret_cast<uint2*>(dst), ld_dst / 4,
-        rows, cols / 4);
-  } else if (src_type != T_I8 && ld_dst % 8 == 0 && reinterpret_cast<uintptr_t>(dst) % 16 == 0) {
-    copy16_kernel<true><<<copy_grid((cols + 7) / 8, rows, num_sms), 256, 0, st>>>(
-        static_cast<const uint16_t*>(src), ld_src, dst, ld_dst, rows, cols);
-  } else {
-    repack_kernel<<<copy_grid(cols, rows, num_sms), 256, 0, st>>>(src, src_type, ld_src, dst,
-                                                                  ld_dst, rows, cols);
-  }
-  return cudaGetLastError();
+  if (x4)
+    return launch_pdl(widen_i8_x4_kernel, copy_grid(cols / 4, rows, num_sms), dim3(256), 0, st,
+                      static_cast<const char4*>(src), ld_src / 4, reinterpret_cast<uint2*>(dst),
+                      ld_dst / 4, rows, cols / 4);
+  if (src_type != T_I8 && ld_dst % 8 == 0 && reinterpret_cast<uintptr_t>(dst) % 16 == 0)
+    return launch_pdl(copy16_kernel<true>, copy_grid((cols + 7) / 8, rows, num_sms), dim3(256), 0,
+                      st, static_cast<const uint16_t*>(src), ld_src, dst, ld_dst, rows, cols);
+  return launch_pdl(repack_kernel, copy_grid(cols, rows, num_sms), dim3(256), 0, st, src,
+                    src_type, ld_src, dst, ld_dst, rows, cols);
 }
 
 cudaError_t launch_copy_out16(const uint16_t* src, long long ld_src, uint16_t* dst,
                               long long ld_dst, long long rows, long long cols, int num_sms,
                               cudaStream_t st) {
   if (rows == 0 || cols == 0) return cudaSuccess;
-  copy16_kernel<false><<<copy_grid((cols + 7) / 8, rows, num_sms), 256, 0, st>>>(
-      src, ld_src, dst, ld_dst, rows, cols);
-  return cudaGetLastError();
+  return launch_pdl(copy16_kernel<false>, copy_grid((cols + 7) / 8, rows, num_sms), dim3(256), 0,
+                    st, src, ld_src, dst, ld_dst, rows, cols);
 }
 
 }  // namespace gb300

@@ -152,17 +152,36 @@ GB_HD Unit pair_unit(const KParams& p, const PairWork& pw, int ksub, int cid, in
   w.part = 0;
   w.ti = 0;
   if (p.sk_len > 0 && i >= p.sk_dp) {
+    // After its sk_dp whole tiles of the full waves, a cluster takes the
+    // pieces of its stream-K run (k = 0 .. n-1 in K order) as: the piece
+    // that starts mid-tile (it leaves a partial for the cluster whose run
+    // ends in that tile, and waits for nothing), then the piece that ends
+    // mid-tile (it finishes its tile with the next cluster's partial), then
+    // the whole tiles (a run is shorter than two tiles: at most one).  A
+    // finishing piece thus waits only for another run's first piece, and its
+    // epilogue overlaps the whole tile's MMAs.  (Taking the leaving piece
+    // before the full waves was measured slower: it staggers the waves and
+    // loses the grouped raster's L2 reuse.)
     const int nks = p.num_kb / ksub;
-    const int s = pw.g0 / nks + (i - p.sk_dp);
+    const int j = i - p.sk_dp;
+    const int n_sk = pw.n - p.sk_dp;
+    const int has_l = pw.g0 % nks != 0 ? 1 : 0;
+    const int has_f = (pw.g1 % nks != 0 && n_sk > has_l) ? 1 : 0;
+    int k;
+    if (has_l && j == 0)
+      k = 0;
+    else if (has_f && j == has_l)
+      k = n_sk - 1;
+    else
+      k = j - has_f;
+    const int s = pw.g0 / nks + k;
     const int st0 = pw.g0 - s * nks > 0 ? pw.g0 - s * nks : 0;
     const int st1 = pw.g1 - s * nks < nks ? pw.g1 - s * nks : nks;
     t = p.sk_start + s;
     w.kb0 = st0 * ksub;
     w.kb1 = st1 * ksub;
-    // A run is at least one tile long, so a piece cannot both start and
-    // end inside its tile: the first piece of a run that starts mid-tile
-    // leaves its partial (slot cid); the last piece of a run that ends
-    // mid-tile finishes that tile with the next cluster's partial.
+    // A run is at least one tile long, so a piece cannot both start and end
+    // inside its tile.
     if (st0 > 0) {
       w.tail = 1;
       w.part = 1;

@@ -38,11 +38,12 @@ struct PlanRow {
 // of the whole call).  Layouts: 0 = row-major, 1 = column-major; types as in
 // common.h.
 static const PlanRow kTable[] = {
-    // 4096^3 bf16, B column-major: pair 256x256 without stream-K 1565,
-    // with it 1547; 2 K slices per stage 1495; GROUP_M 4 / 16: 1551 / 1546.
-    {4096, 4096, 4096, T_BF16, 0, 1, {256, 8, 1, 0, 0, 1, 1, 0}},
-    // 8192^3 bf16, B column-major: pair 256x256 with stream-K 1932, without
-    // 1915; pair 256x128 1099 (1453 with 2 K slices per stage); single-CTA
+    // 4096^3 bf16, B column-major: pair 256x256 with the stream-K hybrid
+    // 1605, without 1579; 2 K slices per stage 1495; GROUP_M 4 / 16 within
+    // 1 % of 8.
+    {4096, 4096, 4096, T_BF16, 0, 1, {256, 8, 1, 0, 0, 1, 1, 1}},
+    // 8192^3 bf16, B column-major: pair 256x256 with stream-K 1940, without
+    // 1913; pair 256x128 1099 (1453 with 2 K slices per stage); single-CTA
     // 128x256 1486.
     {8192, 8192, 8192, T_BF16, 0, 1, {256, 8, 1, 0, 0, 1, 1, 1}},
     // 8192^3 int8: pair 256x256 1209; with 2 K slices per stage 1184;

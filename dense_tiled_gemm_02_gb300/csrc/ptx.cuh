@@ -269,6 +269,19 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on in
+// its stream have completed and their memory is visible.  Every kernel of a
+// GEMM call is launched so that it may start while the previous kernel in
+// the stream is still running, and calls this before its first global
+// memory access; without the launch attribute it returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next kernel in the stream be scheduled once every block of this
+// grid has started (it still waits in pdl_wait() for this grid to finish).
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- CTA pairs (clusters of 2)
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

@@ -343,6 +343,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // Everything above touches only on-chip state: it overlaps the previous
+  // kernel in the stream; global memory is read and written only after it.
+  pdl_wait();
+  pdl_trigger();
 
   const int num_units = p.tiles_m * p.tiles_n * p.splits;
   const uint64_t tmo = p.timeout_ns;

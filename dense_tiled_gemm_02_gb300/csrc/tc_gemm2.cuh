@@ -128,6 +128,10 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
   cluster_sync_all();  // both CTAs' barriers exist before either signals the other
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // Everything above touches only on-chip state: it overlaps the previous
+  // kernel in the stream; global memory is read and written only after it.
+  pdl_wait();
+  pdl_trigger();
 
   const int cid = blockIdx.x >> 1;
   const int ncl = gridDim.x >> 1;
@@ -348,6 +352,53 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
       // Two slices of C in flight: slice c lives in cb[c & 1] and is
       // reloaded with slice c + 2 once used (a loop unrolled by two keeps the
       // buffers in fixed registers).
+      const uint32_t buf = acc_it & 1u;
+      uint32_t* flag = w.tail ? p.tail_flags + w.ti * 2 + rank : nullptr;
+      // The fp32 partial sums of a shared tile (one CTA half), stored so that
+      // the 128 threads' float4s of each 4-column group are adjacent: a warp
+      // then moves 512 contiguous bytes per access instead of 32 pieces.
+      float4* pbase = w.tail ? reinterpret_cast<float4*>(
+                                   p.tail_ws + static_cast<size_t>(w.ti * 2 + rank) * BM * BN) +
+                                   row_local
+                             : nullptr;
+      // When a unit that finishes a shared tile is the last of its cluster,
+      // the MMA no longer needs the other accumulator buffer: while this
+      // unit's MMAs run, the other cluster's partial is copied into those
+      // tensor-memory columns, and the final epilogue reads both sums there.
+      // Otherwise the partial is read from global memory slice by slice,
+      // while the MMAs of the cluster's next unit run.
+      const bool adds = w.tail && w.part == 0;
+      const bool preloaded = adds && i == pw.n - 1;
+      const uint32_t pcol = tmem_base + lane_base + (buf ^ 1u) * BN;
+      if (adds) {
+        if (ep_leader)
+          *ep_go = bounded_flag_wait(flag, p.epoch, abort_flag, p.status, STATUS_TIMEOUT, tmo)
+                       ? 1 : 0;
+        named_barrier_sync(1, 128);
+        const bool fok = *ep_go != 0;
+        named_barrier_sync(1, 128);
+        if (!fok) break;
+        if (preloaded) {
+          // two 32-column slices per batch: 16 loads in flight per thread
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; c += 2) {
+            uint32_t x[2][32];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 q = pbase[((c + h) * 8 + j) * BM];
+                x[h][4 * j] = __float_as_uint(q.x);
+                x[h][4 * j + 1] = __float_as_uint(q.y);
+                x[h][4 * j + 2] = __float_as_uint(q.z);
+                x[h][4 * j + 3] = __float_as_uint(q.w);
+              }
+            tmem_st_32x32b_x32(pcol + c * 32, x[0]);
+            tmem_st_32x32b_x32(pcol + (c + 1) * 32, x[1]);
+          }
+          tmem_st_wait();
+        }
+      }
       uint4 cb0[4], cb1[4];
       if (c_rows) {
 #pragma unroll
@@ -355,27 +406,24 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) cb1[k] = ld_global_v4_pinned(crow + 32 + 8 * k);
       }
-      const uint32_t buf = acc_it & 1u;
-      uint32_t* flag = w.tail ? p.tail_flags + w.ti * 2 + rank : nullptr;
-      if (ep_leader) {
-        bool ok = bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status,
-                               STATUS_TIMEOUT, tmo);
-        if (ok && w.tail && w.part == 0)
-          ok = bounded_flag_wait(flag, p.epoch, abort_flag, p.status, STATUS_TIMEOUT, tmo);
-        *ep_go = ok ? 1 : 0;
+      // The other cluster's partial, when it is read from global memory:
+      // like C, two slices in flight (slice c in pb[c & 1]).
+      const bool adds_global = adds && !preloaded;
+      float4 pb0[8], pb1[8];
+      if (adds_global) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) pb0[j] = pbase[j * BM];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) pb1[j] = pbase[(8 + j) * BM];
       }
+      if (ep_leader)
+        *ep_go = bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status,
+                              STATUS_TIMEOUT, tmo) ? 1 : 0;
       named_barrier_sync(1, 128);
       const bool go = *ep_go != 0;
       named_barrier_sync(1, 128);
       if (!go) break;
       tc_fence_after();
-      // The split tile's fp32 partial sums (one CTA half), stored so that the
-      // 128 threads' float4s of each 4-column group are adjacent: a warp then
-      // moves 512 contiguous bytes per access instead of 32 scattered pieces.
-      float4* pbase = w.tail ? reinterpret_cast<float4*>(
-                                   p.tail_ws + static_cast<size_t>(w.ti * 2 + rank) * BM * BN) +
-                                   row_local
-                             : nullptr;
       // One 32-column slice; CT/DT are the C and D element types when known
       // at compile time (0: no C), -1 for the generic run-time path.
       // Once slice c's C has been added, its buffer takes slice c + 2.
@@ -385,7 +433,8 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
           for (int k = 0; k < 4; ++k) cbuf[k] = ld_global_v4_pinned(crow + 32 * (c + 2) + 8 * k);
         }
       };
-      auto slice = [&](const int c, uint4 (&cbuf)[4], auto ct_tag, auto dt_tag) {
+      auto slice = [&](const int c, uint4 (&cbuf)[4], float4 (&pbuf)[8], auto ct_tag,
+                       auto dt_tag) {
         constexpr int CT = decltype(ct_tag)::value;
         constexpr int DT = decltype(dt_tag)::value;
         const int h = c & 1;  // which half of a 64-column staging chunk
@@ -416,14 +465,23 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
                                                   f[4 * j + 3]);
           return;
         }
-        if (w.tail) {
+        if (preloaded) {
+          uint32_t q[32];
+          tmem_ld_32x32b_x32(pcol + c * 32, q);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) f[j] += __uint_as_float(q[j]);
+        } else if (adds_global) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float4 x = pbase[(c * 8 + j) * BM];
-            f[4 * j] += x.x;
-            f[4 * j + 1] += x.y;
-            f[4 * j + 2] += x.z;
-            f[4 * j + 3] += x.w;
+            f[4 * j] += pbuf[j].x;
+            f[4 * j + 1] += pbuf[j].y;
+            f[4 * j + 2] += pbuf[j].z;
+            f[4 * j + 3] += pbuf[j].w;
+          }
+          if (c + 2 < BN / 32) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) pbuf[j] = pbase[((c + 2) * 8 + j) * BM];
           }
         }
         if (CT < 0) {
@@ -498,24 +556,24 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
       for (int c = 0; c < BN / 32; c += 2) {
         switch (kind) {
           case 1:
-            slice(c, cb0, IntTag<T_BF16>{}, IntTag<T_BF16>{});
-            slice(c + 1, cb1, IntTag<T_BF16>{}, IntTag<T_BF16>{});
+            slice(c, cb0, pb0, IntTag<T_BF16>{}, IntTag<T_BF16>{});
+            slice(c + 1, cb1, pb1, IntTag<T_BF16>{}, IntTag<T_BF16>{});
             break;
           case 2:
-            slice(c, cb0, IntTag<0>{}, IntTag<T_BF16>{});
-            slice(c + 1, cb1, IntTag<0>{}, IntTag<T_BF16>{});
+            slice(c, cb0, pb0, IntTag<0>{}, IntTag<T_BF16>{});
+            slice(c + 1, cb1, pb1, IntTag<0>{}, IntTag<T_BF16>{});
             break;
           case 3:
-            slice(c, cb0, IntTag<T_F16>{}, IntTag<T_F16>{});
-            slice(c + 1, cb1, IntTag<T_F16>{}, IntTag<T_F16>{});
+            slice(c, cb0, pb0, IntTag<T_F16>{}, IntTag<T_F16>{});
+            slice(c + 1, cb1, pb1, IntTag<T_F16>{}, IntTag<T_F16>{});
             break;
           case 4:
-            slice(c, cb0, IntTag<0>{}, IntTag<T_F16>{});
-            slice(c + 1, cb1, IntTag<0>{}, IntTag<T_F16>{});
+            slice(c, cb0, pb0, IntTag<0>{}, IntTag<T_F16>{});
+            slice(c + 1, cb1, pb1, IntTag<0>{}, IntTag<T_F16>{});
             break;
           default:
-            slice(c, cb0, IntTag<-1>{}, IntTag<-1>{});
-            slice(c + 1, cb1, IntTag<-1>{}, IntTag<-1>{});
+            slice(c, cb0, pb0, IntTag<-1>{}, IntTag<-1>{});
+            slice(c + 1, cb1, pb1, IntTag<-1>{}, IntTag<-1>{});
             break;
         }
       }

@@ -17,8 +17,8 @@ template <int BN, int STAGES, bool I8X>
 cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b, const KParams& p, int grid,
                         cudaStream_t st) {
   constexpr uint32_t smem = smem_bytes<BN, STAGES>();
-  tc_gemm_kernel<BN, STAGES, I8X><<<grid, NUM_THREADS, smem, st>>>(a, b, p);
-  return cudaGetLastError();
+  return launch_pdl(tc_gemm_kernel<BN, STAGES, I8X>, dim3(grid), dim3(NUM_THREADS), smem, st, a,
+                    b, p);
 }
 
 template <int BN, int STAGES, bool I8X>

@@ -8,6 +8,27 @@
 
 namespace gb300 {
 
+// Launch with programmatic stream serialisation allowed: the kernel may be
+// scheduled while the previous kernel in the stream finishes, and waits for
+// it in pdl_wait() before touching global memory (hides launch latency
+// between the kernels of one GEMM call).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+
 struct TcVariant {
   int bn;
   int stages;

@@ -19,15 +19,18 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t st, cudaLaunchAttribute* a
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may start while the previous kernel in the stream finishes (pdl_wait)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cfg;
 }
 
 template <int BN, int STAGES, int KSUB, bool I8X>
 cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
                         const KParams& p, int grid, cudaStream_t st) {
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config<BN, STAGES, KSUB, I8X>(grid, st, attr);
   return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, KSUB, I8X>, a, b, d, p);
 }
@@ -41,7 +44,7 @@ cudaError_t prepare_pair() {
 
 template <int BN, int STAGES, int KSUB, bool I8X>
 int max_clusters_pair() {
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config<BN, STAGES, KSUB, I8X>(2, nullptr, attr);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<BN, STAGES, KSUB, I8X>, &cfg) !=

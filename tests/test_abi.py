@@ -162,17 +162,22 @@ def test_pair_schedule_covers_every_tile_stage_once(tm, tn, group, nkb, ksub, cl
         assert second[5] == second[0] and first[5] == second[0] == first[0] + 1
     tiles = tm * tn
     if sk and tiles >= clusters and tiles % clusters and nkb % ksub == 0 and nkb // ksub >= 2:
+        # every cluster has the same number of full-wave tiles, and the
+        # stream-K runs are equal to one stage
         work = [sum(u[3] - u[2] for u in units) for units in sched]
-        assert max(work) - min(work) <= ksub + (nkb if tiles < 2 * clusters else nkb)
-        # stream-K part alone is balanced to one stage
+        assert max(work) - min(work) <= ksub
         waves = tiles // clusters
-        sk_work = [sum(u[3] - u[2] for u in units[waves - 1:]) for units in sched]
-        assert max(sk_work) - min(sk_work) <= ksub
-        # the leaver of a shared tile reaches it before any piece that waits
+        # after the full-wave tiles: the piece that leaves a partial first (it
+        # waits for nothing), then the piece that finishes a shared tile, so
+        # every wait is for the first piece of another run, and at most one
+        # whole tile follows it (tensor memory holds two accumulators)
         for cid, units in enumerate(sched):
             waits = [i for i, u in enumerate(units) if u[4] and u[5] == 0]
             leaves = [i for i, u in enumerate(units) if u[4] and u[5] == 1]
-            assert all(i == len(units) - 1 for i in waits)
+            assert len(waits) <= 1 and len(leaves) <= 1
             assert all(i == waves - 1 for i in leaves)
+            assert all(i == waves - 1 + len(leaves) for i in waits)
+            if waits:
+                assert len(units) - 1 - waits[0] <= 1
     else:
         assert all(u[4] == 0 for units in sched for u in units)
