@@ -3,12 +3,16 @@
 //  * splitk_reduce_kernel: sums the fp32 partial tiles of a split-K run in a
 //    fixed order (split 0, 1, ...), adds C in fp32 and stores D with one
 //    conversion.  With zero splits it computes D = C (the K = 0 case).
-//  * repack_kernel: copies an operand whose rows are not 16-byte aligned into
-//    a padded workspace that the TMA unit can read; for int8 operands it
-//    also widens every value to bf16 (exact: |v| <= 128 needs 8 bits).
+//  * copy_rows16_kernel: copies 16-bit rows between buffers of any 2-byte
+//    alignment: operands whose rows the TMA unit cannot read in place into a
+//    padded workspace, and C / D rows that are not 16-byte aligned into and
+//    out of aligned workspace rows.
+//  * widen_i8_x4_kernel / repack_kernel: int8 operands widened to bf16 in
+//    the workspace (exact: |v| <= 128 needs 8 bits), four elements a thread
+//    when rows allow it, else one.
 //
-// Both walk their arrays in storage order with consecutive threads on
-// consecutive addresses, in grid-stride loops sized to the SM count.
+// All of them put consecutive threads on consecutive addresses and are
+// launched with programmatic stream serialisation (pdl_wait first).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -39,28 +43,69 @@ __device__ __forceinline__ void st_f(void* base, int t, long long off, float v) 
 __global__ void splitk_reduce_kernel(const KParams p, int row_order) {
   pdl_wait();
   pdl_trigger();
-  const long long total = static_cast<long long>(p.M) * p.N;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += stride) {
-    long long r, c;
-    if (row_order) {
-      r = idx / p.N;
-      c = idx - r * p.N;
-    } else {
-      c = idx / p.M;
-      r = idx - c * p.M;
-    }
-    if (p.d_type == T_I32) {
-      int v = 0;
-      if (p.C) v = static_cast<const int*>(p.C)[r * p.c_rs + c * p.c_cs];
-      static_cast<int*>(p.D)[r * p.d_rs + c * p.d_cs] = v;
+  // D walked along its contiguous dimension: `inner` is N for row-major D
+  // and M otherwise.  Thread t of block x takes inner indices
+  // base + k * 256 + t (k < 8) of the outer lines strided over block y, so
+  // every warp access covers consecutive addresses and all loads of a split
+  // are in flight together.
+  constexpr int EPT = 8;
+  const long long outer = row_order ? p.M : p.N;
+  const long long inner = row_order ? p.N : p.M;
+  const long long base = static_cast<long long>(blockIdx.x) * blockDim.x * EPT + threadIdx.x;
+  if (base >= inner) return;
+  for (long long o = blockIdx.y; o < outer; o += gridDim.y) {
+    auto rc = [&](int k, long long& r, long long& c) {
+      const long long i = base + static_cast<long long>(k) * blockDim.x;
+      r = row_order ? o : i;
+      c = row_order ? i : o;
+    };
+    if (p.d_type == T_I32) {  // K = 0 with int32 C: D = C
+#pragma unroll
+      for (int k = 0; k < EPT; ++k) {
+        long long r, c;
+        rc(k, r, c);
+        if ((row_order ? c : r) >= inner) continue;
+        static_cast<int*>(p.D)[r * p.d_rs + c * p.d_cs] =
+            p.C ? static_cast<const int*>(p.C)[r * p.c_rs + c * p.c_cs] : 0;
+      }
       continue;
     }
-    float acc = 0.f;
-    for (int s = 0; s < p.splits; ++s) acc += p.ws[s * p.ws_split + r * p.ws_rs + c * p.ws_cs];
-    if (p.C) acc += ld_f(p.C, p.c_type, r * p.c_rs + c * p.c_cs);
-    st_f(p.D, p.d_type, r * p.d_rs + c * p.d_cs, acc);
+    // C and up to four splits' partials are all requested before the first
+    // add (the sum itself still runs split 0, 1, ... in order).
+    float cv[EPT], acc[EPT];
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+      long long r, c;
+      rc(k, r, c);
+      cv[k] = (p.C && (row_order ? c : r) < inner) ? ld_f(p.C, p.c_type, r * p.c_rs + c * p.c_cs)
+                                                   : 0.f;
+      acc[k] = 0.f;
+    }
+    for (int s0 = 0; s0 < p.splits; s0 += 4) {
+      float v[4][EPT];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+          long long r, c;
+          rc(k, r, c);
+          v[q][k] = (s0 + q < p.splits && (row_order ? c : r) < inner)
+                        ? p.ws[(s0 + q) * p.ws_split + r * p.ws_rs + c * p.ws_cs]
+                        : 0.f;
+        }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (s0 + q < p.splits)  // (no +0.0 for absent splits: it would turn -0.0 into +0.0)
+#pragma unroll
+          for (int k = 0; k < EPT; ++k) acc[k] += v[q][k];
+    }
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+      long long r, c;
+      rc(k, r, c);
+      if ((row_order ? c : r) >= inner) continue;
+      st_f(p.D, p.d_type, r * p.d_rs + c * p.d_cs, p.C ? acc[k] + cv[k] : acc[k]);
+    }
   }
 }
 
@@ -102,56 +147,31 @@ __global__ void repack_kernel(const void* __restrict__ src, int src_type, long l
   }
 }
 
-// 16-bit rows copied between a side whose rows start on 16-byte boundaries
-// (a workspace with its leading dimension rounded up to 8 elements) and a
-// side with arbitrary 2-byte alignment.  A thread moves 8 consecutive
-// elements: one 16-byte access on the aligned side, eight 2-byte accesses on
-// the other (consecutive threads cover consecutive bytes, so a warp access
-// still spans 512 contiguous bytes).  TO_ALIGNED: src arbitrary -> dst
-// aligned; otherwise src aligned -> dst arbitrary.  Elements of the aligned
-// side's last chunk beyond `cols` are written as zeros or not read.
-template <bool TO_ALIGNED>
-__global__ void copy16_kernel(const uint16_t* __restrict__ src, long long ld_src,
-                              uint16_t* __restrict__ dst, long long ld_dst, long long rows,
-                              long long cols) {
+// 16-bit rows copied between buffers of any 2-byte alignment (into or out
+// of the aligned workspace).  Consecutive lanes take consecutive elements,
+// so every warp access covers 64 contiguous bytes on both sides (2 bytes per
+// lane at a wider stride would touch a sector per lane).  Block x covers
+// 256 * 8 columns of a row band, element k of thread t at column
+// base + k * 256 + t; rows are strided over block y.
+__global__ void copy_rows16_kernel(const uint16_t* __restrict__ src, long long ld_src,
+                                  uint16_t* __restrict__ dst, long long ld_dst, long long rows,
+                                  long long cols) {
   pdl_wait();
   pdl_trigger();
-  const long long c8 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (c8 * 8 >= cols) return;
-  const long long c0 = c8 * 8;
-  const int nv = cols - c0 < 8 ? static_cast<int>(cols - c0) : 8;
-  constexpr int R = 4;
-  const long long step = static_cast<long long>(gridDim.y) * R;
-  for (long long r0 = static_cast<long long>(blockIdx.y) * R; r0 < rows; r0 += step) {
-    uint4 v[R];
+  constexpr int EPT = 8;
+  const long long base = static_cast<long long>(blockIdx.x) * blockDim.x * EPT + threadIdx.x;
+  if (base >= cols) return;
+  for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
+    uint16_t v[EPT];
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const long long r = r0 + i;
-      if (r >= rows) break;
-      if (TO_ALIGNED) {
-        uint16_t e[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) e[k] = k < nv ? src[r * ld_src + c0 + k] : uint16_t(0);
-        v[i].x = e[0] | (uint32_t(e[1]) << 16);
-        v[i].y = e[2] | (uint32_t(e[3]) << 16);
-        v[i].z = e[4] | (uint32_t(e[5]) << 16);
-        v[i].w = e[6] | (uint32_t(e[7]) << 16);
-      } else {
-        v[i] = *reinterpret_cast<const uint4*>(src + r * ld_src + c0);
-      }
+    for (int k = 0; k < EPT; ++k) {
+      const long long c = base + static_cast<long long>(k) * blockDim.x;
+      if (c < cols) v[k] = src[r * ld_src + c];
     }
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const long long r = r0 + i;
-      if (r >= rows) break;
-      if (TO_ALIGNED) {
-        *reinterpret_cast<uint4*>(dst + r * ld_dst + c0) = v[i];
-      } else {
-        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (k < nv) dst[r * ld_dst + c0 + k] = static_cast<uint16_t>(w[k / 2] >> (16 * (k & 1)));
-      }
+    for (int k = 0; k < EPT; ++k) {
+      const long long c = base + static_cast<long long>(k) * blockDim.x;
+      if (c < cols) dst[r * ld_dst + c] = v[k];
     }
   }
 }
@@ -187,17 +207,17 @@ __global__ void widen_i8_x4_kernel(const char4* __restrict__ src, long long ld_s
   }
 }
 
-cudaError_t launch_reduce(const KParams& p, int row_order, int num_sms, cudaStream_t st) {
-  const long long total = static_cast<long long>(p.M) * p.N;
-  if (total == 0) return cudaSuccess;
-  long long blocks = (total + 255) / 256;
-  const long long cap = static_cast<long long>(num_sms) * 8;
-  if (blocks > cap) blocks = cap;
-  return launch_pdl(splitk_reduce_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
-                    p, row_order);
+namespace {
+// copy_rows16_kernel: 2048 columns per block, rows strided over block y.
+dim3 copy_rows_grid(long long rows, long long cols, int num_sms) {
+  const unsigned gx = static_cast<unsigned>((cols + 2047) / 2048);
+  long long gy = (static_cast<long long>(num_sms) * 16 + gx - 1) / gx;
+  if (gy > rows) gy = rows;
+  if (gy > 65535) gy = 65535;
+  if (gy < 1) gy = 1;
+  return dim3(gx, static_cast<unsigned>(gy));
 }
 
-namespace {
 dim3 copy_grid(long long chunks, long long rows, int num_sms) {
   const unsigned gx = static_cast<unsigned>((chunks + 255) / 256);
   long long gy = (static_cast<long long>(num_sms) * 16 + gx - 1) / gx;
@@ -209,6 +229,15 @@ dim3 copy_grid(long long chunks, long long rows, int num_sms) {
 }
 }  // namespace
 
+cudaError_t launch_reduce(const KParams& p, int row_order, int num_sms, cudaStream_t st) {
+  if (static_cast<long long>(p.M) * p.N == 0) return cudaSuccess;
+  const long long outer = row_order ? p.M : p.N;
+  const long long inner = row_order ? p.N : p.M;
+  return launch_pdl(splitk_reduce_kernel, copy_rows_grid(outer, inner, num_sms), dim3(256), 0, st,
+                    p, row_order);
+}
+
+
 cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint16_t* dst,
                           long long ld_dst, long long rows, long long cols, int num_sms,
                           cudaStream_t st) {
@@ -219,9 +248,9 @@ cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint1
     return launch_pdl(widen_i8_x4_kernel, copy_grid(cols / 4, rows, num_sms), dim3(256), 0, st,
                       static_cast<const char4*>(src), ld_src / 4, reinterpret_cast<uint2*>(dst),
                       ld_dst / 4, rows, cols / 4);
-  if (src_type != T_I8 && ld_dst % 8 == 0 && reinterpret_cast<uintptr_t>(dst) % 16 == 0)
-    return launch_pdl(copy16_kernel<true>, copy_grid((cols + 7) / 8, rows, num_sms), dim3(256), 0,
-                      st, static_cast<const uint16_t*>(src), ld_src, dst, ld_dst, rows, cols);
+  if (src_type != T_I8)
+    return launch_pdl(copy_rows16_kernel, copy_rows_grid(rows, cols, num_sms), dim3(256), 0, st,
+                      static_cast<const uint16_t*>(src), ld_src, dst, ld_dst, rows, cols);
   return launch_pdl(repack_kernel, copy_grid(cols, rows, num_sms), dim3(256), 0, st, src,
                     src_type, ld_src, dst, ld_dst, rows, cols);
 }
@@ -230,8 +259,8 @@ cudaError_t launch_copy_out16(const uint16_t* src, long long ld_src, uint16_t* d
                               long long ld_dst, long long rows, long long cols, int num_sms,
                               cudaStream_t st) {
   if (rows == 0 || cols == 0) return cudaSuccess;
-  return launch_pdl(copy16_kernel<false>, copy_grid((cols + 7) / 8, rows, num_sms), dim3(256), 0,
-                    st, src, ld_src, dst, ld_dst, rows, cols);
+  return launch_pdl(copy_rows16_kernel, copy_rows_grid(rows, cols, num_sms), dim3(256), 0, st,
+                    src, ld_src, dst, ld_dst, rows, cols);
 }
 
 }  // namespace gb300

@@ -59,6 +59,10 @@ WORKLOADS = {
                             layout_b=COL),
     "sq8192_bf16": Workload("sq8192_bf16", 31, 8192, 8192, 8192, BF16, BF16, BF16, "normal",
                             layout_b=COL),
+    # 8192^3 with a row-major (N-contiguous) B: the operand layout of the
+    # int8 workload, for comparing the kernels' two B majors at one size
+    "sq8192_bf16_browB": Workload("sq8192_bf16_browB", 32, 8192, 8192, 8192, BF16, BF16, BF16,
+                                  "normal"),
     "rag1000_bf16": Workload("rag1000_bf16", 41, 1000, 1000, 1000, BF16, BF16, BF16, "normal"),
     "skinny64x8192x8192_bf16": Workload("skinny64x8192x8192_bf16", 42, 64, 8192, 8192, BF16,
                                         BF16, BF16, "normal"),
