@@ -77,10 +77,14 @@ KERNEL_SOURCES = {
              "gemm_host.cu", "plan_table.h"),
     "cta1": ("common.h", "ptx.cuh", "tc_gemm.cuh", "tc_launch.cu", "tc_launch.h",
              "gemm_host.cu", "plan_table.h"),
+    "decode": ("common.h", "ptx.cuh", "decode.cu", "tc_launch.h", "gemm_host.cu",
+               "plan_table.h"),
 }
 
 
 def kernel_family(plan: str) -> str:
+    if re.search(r"\bdecode=1\b", plan):
+        return "decode"
     return "pair" if re.search(r"\bpair=1\b", plan) else "cta1"
 
 
@@ -354,21 +358,33 @@ def main():
     e2e = e2e_measure(pkg, g, w, inp, dev, stream, max(3, args.steps // 5), world)
 
     peaks, src = load_peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     events_ms = statistics.mean(kernel_ms)
     single = launches_per_step(g) == 1
     avg_kernel_ms = min(total_ms / args.steps, events_ms) if single else events_ms
-    achieved = w.flops / (avg_kernel_ms * 1e-3) / 1e12
     traffic = profiled_traffic(w.name, kernel_family(g.plan()))
-    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                "peak_source": f"{src} bf16 burst (cuBLAS 8192^3)",
-                "kernel": kernel_name(g.plan()),
-                "kernel_ms_mean": round(avg_kernel_ms, 5),
-                "kernel_ms_events_mean": round(events_ms, 5),
-                "kernel_timing": ("timed region (the step is this one kernel)" if single and
-                                  avg_kernel_ms < events_ms else
-                                  "library events around each launch, second pass of the steps")}
+    # The kernel's roofline: tensor-bound when its arithmetic intensity over
+    # the compulsory bytes (A, B, C and D once) is above the ridge of the two
+    # measured peaks, HBM-bound below it.
+    algo_bytes = algorithmic_bytes(w)
+    if w.flops / algo_bytes >= peak_tf * 1e12 / (peak_bw * 1e9):
+        achieved = w.flops / (avg_kernel_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak_tf,
+                    "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
+                    "peak_source": f"{src} bf16 burst (cuBLAS 8192^3)"}
+    else:
+        achieved = algo_bytes / (avg_kernel_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak_bw,
+                    "unit": "GB/s", "frac": round(achieved / peak_bw, 4),
+                    "peak_source": f"{src} HBM copy bandwidth"}
+    roofline.update({"traffic": traffic, "algorithmic_bytes": algo_bytes,
+                     "kernel": kernel_name(g.plan()),
+                     "kernel_ms_mean": round(avg_kernel_ms, 5),
+                     "kernel_ms_events_mean": round(events_ms, 5),
+                     "kernel_timing": ("timed region (the step is this one kernel)"
+                                       if single and avg_kernel_ms < events_ms else
+                                       "library events around each launch, second pass")})
 
     line = {"metric": metric_name(w), "value": round(value, 1),
             "unit": "TOPS" if w.ab_type == I8 else "TFLOPS", "n_gpus": world,
@@ -392,13 +408,27 @@ def main():
 
 def kernel_name(plan: str) -> str:
     f = dict(kv.split("=") for kv in plan.split() if "=" in kv)
+    if f.get("decode") == "1":
+        return "decode_kn_kernel"
     if f.get("pair") == "1":
         return f"tc_gemm_pair_kernel<{f['bn']}, {f['stages']}, {f.get('ksub', '1')}>"
     return f"tc_gemm_kernel<{f['bn']}, {f['stages']}, {f.get('i8x', '0')}>"
 
 
+def algorithmic_bytes(w) -> int:
+    """Compulsory DRAM bytes of one GEMM: A, B, C (when present) and D once."""
+    from workloads import TORCH_DTYPE
+    es = lambda t: TORCH_DTYPE[t].itemsize
+    n = (w.M * w.K + w.K * w.N) * es(w.ab_type) + w.M * w.N * es(w.d_type)
+    if w.c_type:
+        n += w.M * w.N * es(w.c_type)
+    return n
+
+
 def launches_per_step(g) -> int:
     plan = g.plan()
+    if re.search(r"\bdecode=1\b", plan):
+        return 2  # decode kernel + the reduce that adds its K slices and C
     n = 1
     if re.search(r"splits=(\d+)", plan) and int(re.search(r"splits=(\d+)", plan).group(1)) > 1:
         n += 1

@@ -34,6 +34,7 @@ UNITS = [
     ("tc_launch.cu", ["-DTC_BN=128"], "tc_bn128.o"),
     ("tc_launch.cu", ["-DTC_BN=64"], "tc_bn64.o"),
     ("tc_pair_launch.cu", [], "tc_pair.o"),
+    ("decode.cu", [], "decode.o"),
 ]
 
 

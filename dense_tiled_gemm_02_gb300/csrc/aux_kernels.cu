@@ -45,10 +45,11 @@ __global__ void splitk_reduce_kernel(const KParams p, int row_order) {
   pdl_trigger();
   // D walked along its contiguous dimension: `inner` is N for row-major D
   // and M otherwise.  Thread t of block x takes inner indices
-  // base + k * 256 + t (k < 8) of the outer lines strided over block y, so
+  // base + k * 256 + t (k < EPT) of the outer lines strided over block y, so
   // every warp access covers consecutive addresses and all loads of a split
-  // are in flight together.
-  constexpr int EPT = 8;
+  // are in flight together.  Two elements a thread: a D of a few long lines
+  // (M = 1 .. 64) still spreads over many blocks.
+  constexpr int EPT = 2;
   const long long outer = row_order ? p.M : p.N;
   const long long inner = row_order ? p.N : p.M;
   const long long base = static_cast<long long>(blockIdx.x) * blockDim.x * EPT + threadIdx.x;
@@ -233,7 +234,12 @@ cudaError_t launch_reduce(const KParams& p, int row_order, int num_sms, cudaStre
   if (static_cast<long long>(p.M) * p.N == 0) return cudaSuccess;
   const long long outer = row_order ? p.M : p.N;
   const long long inner = row_order ? p.N : p.M;
-  return launch_pdl(splitk_reduce_kernel, copy_rows_grid(outer, inner, num_sms), dim3(256), 0, st,
+  const unsigned gx = static_cast<unsigned>((inner + 511) / 512);  // 256 threads x 2 elements
+  long long gy = (static_cast<long long>(num_sms) * 16 + gx - 1) / gx;
+  if (gy > outer) gy = outer;
+  if (gy > 65535) gy = 65535;
+  if (gy < 1) gy = 1;
+  return launch_pdl(splitk_reduce_kernel, dim3(gx, static_cast<unsigned>(gy)), dim3(256), 0, st,
                     p, row_order);
 }
 

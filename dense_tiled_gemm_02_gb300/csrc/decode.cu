@@ -1,0 +1,198 @@
+// decode.cu -- the decode regime: D = A*B + C with M <= 4 rows and B's K
+// dimension contiguous (a weight stored N x K).
+//
+// At M <= 4 the multiply is bound by reading B once (2*N*K bytes), not by
+// arithmetic, so this kernel streams B with 16-byte loads on the CUDA cores
+// instead of padding the rows up to a tensor-core tile.  (At 16 rows the
+// CUDA-core arithmetic per B element is no longer small: that case was
+// measured 3x slower here than on the tensor-core path, which it keeps.)  Block (x, y) takes
+// 32 columns of D and the y-th slice of K:
+//   * the slice of A (M rows x kc) is staged in shared memory as 16-bit
+//     values (the same for every column);
+//   * warp w takes columns 4w .. 4w+3 of the block; lane l reads K elements
+//     8l + 256j of each column's row of B (one 512-byte segment per column
+//     and step for the warp) and multiplies them with the matching A
+//     elements of every row, so one A load from shared memory serves four
+//     columns;
+//   * each lane's fp32 sums are added across the warp by a fixed butterfly,
+//     and lane 0 writes the slice's partial sums to the workspace.
+// splitk_reduce_kernel then adds the slices in order, adds C, converts and
+// stores D (deterministic; no atomics).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "common.h"
+#include "ptx.cuh"
+#include "tc_launch.h"
+
+namespace gb300 {
+
+namespace {
+
+constexpr int DEC_THREADS = 256;
+constexpr int DEC_NC = 4;                          // columns per warp
+constexpr int DEC_COLS = DEC_NC * DEC_THREADS / 32;  // columns per block
+
+template <bool BF16>
+__device__ __forceinline__ void widen8(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (BF16) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    } else {
+      const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+      const float2 x = __half22float2(h);
+      f[2 * i] = x.x;
+      f[2 * i + 1] = x.y;
+    }
+  }
+}
+
+// MM: rows the registers are sized for (M <= MM).  kc: K elements of a
+// slice, a multiple of 8; the slice of block y is [y*kc, min(K, y*kc + kc)).
+// VEC: B's rows start on 16-byte boundaries (16-byte loads), else 2-byte
+// loads of the same elements.
+template <int MM, bool BF16, bool VEC>
+__global__ void __launch_bounds__(DEC_THREADS)
+    decode_kn_kernel(const uint16_t* __restrict__ A, long long a_rs, long long a_cs,
+                     const uint16_t* __restrict__ B, long long ldb, int M, int N, int K, int kc,
+                     float* __restrict__ ws, long long ws_split, long long ws_rs,
+                     long long ws_cs) {
+  extern __shared__ __align__(16) uint16_t sA[];  // [MM][kc]
+  pdl_wait();
+  pdl_trigger();
+  const int k0 = blockIdx.y * kc;
+  const int kn = min(kc, K - k0);  // a multiple of 8 (K is)
+  // Stage A's slice (rows M .. MM-1 are zero).
+  for (int i = threadIdx.x; i < MM * kc; i += DEC_THREADS) {
+    const int m = i / kc, kk = i - m * kc;
+    sA[i] = (m < M && kk < kn) ? A[m * a_rs + static_cast<long long>(k0 + kk) * a_cs]
+                               : uint16_t(0);
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * DEC_COLS + warp * DEC_NC;
+  float acc[MM][DEC_NC];
+#pragma unroll
+  for (int m = 0; m < MM; ++m)
+#pragma unroll
+    for (int c = 0; c < DEC_NC; ++c) acc[m][c] = 0.f;
+  const uint16_t* brow[DEC_NC];
+#pragma unroll
+  for (int c = 0; c < DEC_NC; ++c)
+    brow[c] = B + static_cast<long long>(min(n0 + c, N - 1)) * ldb + k0;
+
+  // Four 256-element steps at a time, all their B loads issued before the
+  // first use: one memory round trip per four steps, not per step.
+  constexpr int U = 4;
+  for (int kb = 8 * lane; kb < kn; kb += 256 * U) {
+    uint4 raw[U][DEC_NC];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int kk = kb + 256 * u;
+#pragma unroll
+      for (int c = 0; c < DEC_NC; ++c) {
+        if (kk >= kn) {
+          raw[u][c] = make_uint4(0u, 0u, 0u, 0u);
+        } else if (VEC) {
+          raw[u][c] = ld_global_v4_pinned(brow[c] + kk);
+        } else {
+          uint16_t e[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) e[i] = brow[c][kk + i];
+          raw[u][c] = make_uint4(e[0] | (uint32_t(e[1]) << 16), e[2] | (uint32_t(e[3]) << 16),
+                                 e[4] | (uint32_t(e[5]) << 16), e[6] | (uint32_t(e[7]) << 16));
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int kk = kb + 256 * u;
+      if (kk >= kn) break;
+      float b[DEC_NC][8];
+#pragma unroll
+      for (int c = 0; c < DEC_NC; ++c) widen8<BF16>(raw[u][c], b[c]);
+#pragma unroll
+      for (int m = 0; m < MM; ++m) {
+        float a[8];
+        widen8<BF16>(*reinterpret_cast<const uint4*>(sA + m * kc + kk), a);
+#pragma unroll
+        for (int c = 0; c < DEC_NC; ++c) {
+          float s = acc[m][c];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) s = fmaf(a[e], b[c][e], s);
+          acc[m][c] = s;
+        }
+      }
+    }
+  }
+  // Sum over the warp (fixed butterfly), then lane 0 writes the partials.
+#pragma unroll
+  for (int m = 0; m < MM; ++m)
+#pragma unroll
+    for (int c = 0; c < DEC_NC; ++c) {
+      float v = acc[m][c];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      acc[m][c] = v;
+    }
+  if (lane == 0) {
+    float* out = ws + blockIdx.y * ws_split;
+#pragma unroll
+    for (int m = 0; m < MM; ++m)
+#pragma unroll
+      for (int c = 0; c < DEC_NC; ++c)
+        if (m < M && n0 + c < N) out[m * ws_rs + static_cast<long long>(n0 + c) * ws_cs] = acc[m][c];
+  }
+}
+
+template <int MM, bool BF16, bool VEC>
+cudaError_t launch_mm(const DecodeArgs& d, cudaStream_t st) {
+  const size_t smem = static_cast<size_t>(MM) * d.kc * sizeof(uint16_t);
+  auto kernel = decode_kn_kernel<MM, BF16, VEC>;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>((d.N + DEC_COLS - 1) / DEC_COLS),
+                  static_cast<unsigned>(d.splits));
+  return launch_pdl(kernel, grid, dim3(DEC_THREADS), smem, st, d.A, d.a_rs, d.a_cs, d.B, d.ldb,
+                    d.M, d.N, d.K, d.kc, d.ws, d.ws_split, d.ws_rs, d.ws_cs);
+}
+
+template <bool BF16, bool VEC>
+cudaError_t launch_type(const DecodeArgs& d, cudaStream_t st) {
+  if (d.M <= 1) return launch_mm<1, BF16, VEC>(d, st);
+  if (d.M <= 2) return launch_mm<2, BF16, VEC>(d, st);
+  return launch_mm<4, BF16, VEC>(d, st);
+}
+
+}  // namespace
+
+int decode_columns_per_block() { return DEC_COLS; }
+
+int decode_blocks_per_sm(int M, int kc) {
+  const size_t smem = static_cast<size_t>(M <= 1 ? 1 : M <= 2 ? 2 : 4) * kc * sizeof(uint16_t);
+  int n = 0;
+  const auto k = M <= 1 ? decode_kn_kernel<1, true, true>
+                        : M <= 2 ? decode_kn_kernel<2, true, true> : decode_kn_kernel<4, true, true>;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, DEC_THREADS, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  return n > 0 ? n : 1;
+}
+
+cudaError_t launch_decode(const DecodeArgs& d, cudaStream_t st) {
+  if (d.M < 1 || d.M > kDecodeMaxRows || d.kc % 8 != 0 || d.K % 8 != 0)
+    return cudaErrorInvalidValue;
+  const bool vec = reinterpret_cast<uintptr_t>(d.B) % 16 == 0 && d.ldb % 8 == 0;
+  if (d.bf16) return vec ? launch_type<true, true>(d, st) : launch_type<true, false>(d, st);
+  return vec ? launch_type<false, true>(d, st) : launch_type<false, false>(d, st);
+}
+
+}  // namespace gb300

@@ -102,6 +102,9 @@ struct gemm_plan {
   size_t ws_bytes = 0;
   size_t ws_partial_off = 0;
   size_t ws_tail_off = 0, ws_flags_off = 0;  // last-wave partials and their flags
+  // Decode regime (decode.cu): a handful of rows against a K-contiguous B.
+  bool decode = false;
+  int decode_kc = 0;
   // 16-bit C / D whose rows are not 16-byte aligned: aligned workspace copies
   // (leading dimension stage_ld) that the kernel reads / writes instead.
   bool c_stage = false, d_stage = false;
@@ -179,6 +182,7 @@ void apply_force_plan(PlanChoice& c) {
       else if (k == "pair") c.pair = v;
       else if (k == "ksub") c.ksub = v;
       else if (k == "tail") c.tail = v;
+      else if (k == "decode") c.no_decode = v ? 0 : 1;
     }
     pos = end + 1;
   }
@@ -187,10 +191,11 @@ void apply_force_plan(PlanChoice& c) {
 void make_plan_string(gemm_plan* h) {
   char buf[512];
   std::snprintf(buf, sizeof buf,
-                "M=%lld N=%lld K=%lld swap=%d pair=%d bn=%d ksub=%d stages=%d group_m=%d "
+                "M=%lld N=%lld K=%lld decode=%d swap=%d pair=%d bn=%d ksub=%d stages=%d group_m=%d "
                 "splits=%d kb_per_split=%d tail=%d grid=%d i8x=%d a_mn=%d b_mn=%d repack_a=%d "
                 "repack_b=%d stage_c=%d stage_d=%d ws_bytes=%zu",
-                (long long)h->desc.M, (long long)h->desc.N, (long long)h->desc.K, h->choice.swap,
+                (long long)h->desc.M, (long long)h->desc.N, (long long)h->desc.K, (int)h->decode,
+                h->choice.swap,
                 h->pair ? 1 : 0, h->choice.bn, h->choice.ksub,
                 h->pair ? h->pair->stages : (h->variant ? h->variant->stages : 0), h->kp.group_m,
                 h->kp.splits,
@@ -200,6 +205,65 @@ void make_plan_string(gemm_plan* h) {
                 (int)h->a.repack, (int)h->b.repack, (int)h->c_stage, (int)h->d_stage,
                 h->ws_bytes);
   h->plan_str = buf;
+}
+
+// Plan of the decode kernel (no operand swap, no tensor maps): K split into
+// slices so that about four blocks per SM stream B, the slices' fp32
+// partials in the workspace, finished by the split-K reduce.  Leaves h's
+// workspace and status word allocated, or frees them and returns an error.
+int plan_decode(gemm_plan* h, int sms) {
+  const gemm_desc_t& d = h->desc;
+  h->decode = true;
+  h->M = d.M;
+  h->N = d.N;
+  h->K = d.K;
+  h->c_layout = d.layout_c;
+  h->d_layout = d.layout_d;
+  h->ldc = d.ldc;
+  h->ldd = d.ldd;
+  KParams& kp = h->kp;
+  kp.M = (int)d.M;
+  kp.N = (int)d.N;
+  kp.K = (int)d.K;
+  kp.c_type = d.c_type;
+  kp.d_type = d.d_type;
+  kp.c_rs = d.layout_c == GEMM_ROW_MAJOR ? d.ldc : 1;
+  kp.c_cs = d.layout_c == GEMM_ROW_MAJOR ? 1 : d.ldc;
+  kp.d_rs = d.layout_d == GEMM_ROW_MAJOR ? d.ldd : 1;
+  kp.d_cs = d.layout_d == GEMM_ROW_MAJOR ? 1 : d.ldd;
+  // Slices of kc K elements (a multiple of 256, the width of one warp step;
+  // at most 2048: a slice of A is at most 4 rows x 2048 x 2 bytes of shared
+  // memory), as many as fill one wave of resident blocks: a second, partial
+  // wave would double the time of the ones in it.
+  const int64_t col_blocks = (d.N + decode_columns_per_block() - 1) / decode_columns_per_block();
+  const int64_t slots = (int64_t)sms * decode_blocks_per_sm((int)d.M, 1024);
+  int64_t s = std::max<int64_t>(1, slots / col_blocks);
+  s = std::min<int64_t>(s, std::max<int64_t>(1, d.K / 256));
+  int64_t kc = round_up((d.K + s - 1) / s, 256);
+  kc = std::min<int64_t>(kc, 2048);
+  s = (d.K + kc - 1) / kc;
+  h->decode_kc = (int)kc;
+  kp.splits = (int)s;
+  kp.kb_per_split = 0;
+  const bool row = d.layout_d == GEMM_ROW_MAJOR;
+  kp.ws_rs = row ? d.N : 1;
+  kp.ws_cs = row ? 1 : d.M;
+  kp.ws_split = d.M * d.N;
+  h->ws_partial_off = 0;
+  h->ws_bytes = (size_t)round_up(s * d.M * d.N * 4, 256);
+  h->grid = (int)(col_blocks * s);
+  if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    h->ws = nullptr;
+    return GEMM_ERR_ALLOC_FAILED;
+  }
+  if (cudaMalloc(&h->status, 256) != cudaSuccess || cudaMemset(h->status, 0, 256) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->ws);
+    return GEMM_ERR_ALLOC_FAILED;
+  }
+  make_plan_string(h);
+  return GEMM_OK;
 }
 
 // Build the tiled tensor map of an internal operand (16-bit elements).
@@ -327,6 +391,16 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
 
   h->choice = choose_plan(d.M, d.N, d.K, d.ab_type, d.layout_a, d.layout_b, sms);
   apply_force_plan(h->choice);
+  if (!h->choice.no_decode && (d.ab_type == GEMM_F16 || d.ab_type == GEMM_BF16) && d.M >= 1 &&
+      d.M <= kDecodeMaxRows && d.layout_b == GEMM_COL_MAJOR && d.K % 8 == 0 && d.K >= 256) {
+    const int rc = plan_decode(h, sms);
+    if (rc != GEMM_OK) {
+      delete h;
+      return rc;
+    }
+    *out = h;
+    return GEMM_OK;
+  }
   if (h->i8x) {
     // The exact-int8 kernels: the pair kernel's 256 x 256 tile or the
     // single-CTA 128 x 128 tile (each epilogue thread keeps 128 int32 sums in
@@ -545,6 +619,35 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
 
   if (d.K == 0) {  // D = C
     kp.splits = 0;
+    return launch_reduce(kp, row_order, h->num_sms, st) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  }
+  if (h->decode) {
+    DecodeArgs a;
+    a.A = static_cast<const uint16_t*>(A);
+    a.a_rs = d.layout_a == GEMM_ROW_MAJOR ? d.lda : 1;
+    a.a_cs = d.layout_a == GEMM_ROW_MAJOR ? 1 : d.lda;
+    a.B = static_cast<const uint16_t*>(B);
+    a.ldb = d.ldb;
+    a.M = (int)d.M;
+    a.N = (int)d.N;
+    a.K = (int)d.K;
+    a.kc = h->decode_kc;
+    a.splits = kp.splits;
+    a.bf16 = d.ab_type == GEMM_BF16;
+    a.ws = static_cast<float*>(h->ws);
+    a.ws_split = kp.ws_split;
+    a.ws_rs = kp.ws_rs;
+    a.ws_cs = kp.ws_cs;
+    kp.ws = a.ws;
+    const bool timed = h->timing_used < h->timing_n;
+    if (timed && cudaEventRecord(h->timing_ev[2 * h->timing_used], st) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    if (launch_decode(a, st) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (timed) {
+      if (cudaEventRecord(h->timing_ev[2 * h->timing_used + 1], st) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+      ++h->timing_used;
+    }
     return launch_reduce(kp, row_order, h->num_sms, st) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
   }
   char* ws = static_cast<char*>(h->ws);

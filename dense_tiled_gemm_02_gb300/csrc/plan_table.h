@@ -24,7 +24,8 @@ struct PlanChoice {
   int max_ctas;  // 0 = one CTA per SM
   int pair;      // 1: CTA-pair kernel (cta_group::2), tile 256 x bn
   int ksub;      // pair kernel: 64-wide K slices per ring stage (1 or 2)
-  int tail;      // pair kernel: split the tiles of a partial last wave in two K halves
+  int tail;      // pair kernel: stream-K hybrid for a partial last wave
+  int no_decode; // 1: never take the decode kernel (M <= 16, K-contiguous B)
 };
 
 struct PlanRow {
@@ -70,7 +71,7 @@ inline PlanChoice choose_plan(int64_t M, int64_t N, int64_t K, int ab_type, int 
         (r.layout_a < 0 || r.layout_a == layout_a) && (r.layout_b < 0 || r.layout_b == layout_b))
       return r.choice;
   }
-  PlanChoice c{256, 8, 1, 0, 0, 0, 1, 1};
+  PlanChoice c{256, 8, 1, 0, 0, 0, 1, 1, 0};
   // Skinny M: put the long N dimension on the 128-row tensor-core side.
   if (M < 128 && N >= 2 * M) c.swap = 1;
   const int64_t Mi = c.swap ? N : M;

@@ -69,6 +69,28 @@ cudaError_t launch_reduce(const KParams& p, int row_order, int num_sms, cudaStre
 cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint16_t* dst,
                           long long ld_dst, long long rows, long long cols, int num_sms,
                           cudaStream_t st);
+// Decode regime (decode.cu): M <= kDecodeMaxRows rows, B K-contiguous (element (k, n)
+// at B[n * ldb + k]), K a multiple of 8 (16-byte loads when B is 16-byte
+// aligned and ldb a multiple of 8, else 2-byte loads).  Writes
+// `splits` fp32 partial slices of kc K elements each to ws (slice s at
+// ws + s * ws_split, element (m, n) at m * ws_rs + n * ws_cs), for
+// splitk_reduce_kernel to finish.
+constexpr int kDecodeMaxRows = 4;
+struct DecodeArgs {
+  const uint16_t* A;
+  long long a_rs, a_cs;
+  const uint16_t* B;
+  long long ldb;
+  int M, N, K, kc, splits;
+  bool bf16;
+  float* ws;
+  long long ws_split, ws_rs, ws_cs;
+};
+cudaError_t launch_decode(const DecodeArgs& d, cudaStream_t st);
+int decode_columns_per_block();
+// Resident blocks of the decode kernel per SM for M rows and slices of kc.
+int decode_blocks_per_sm(int M, int kc);
+
 // 16-bit rows from a 16-byte aligned workspace (ld_src a multiple of 8
 // elements) to a destination of any 2-byte alignment.
 cudaError_t launch_copy_out16(const uint16_t* src, long long ld_src, uint16_t* dst,

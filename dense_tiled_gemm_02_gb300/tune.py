@@ -25,6 +25,36 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 L2_BYTES = 129 * 10 ** 6
 
 
+class LibraryReference:
+    """The candidate "cublas": PyTorch's own GEMM on the same operands, timed
+    beside the plans as context (torch.addmm / torch.mm for 16-bit types,
+    torch._int_mm plus C for int8).  Not part of the library."""
+
+    def __init__(self, w):
+        self.w = w
+
+    def run(self, A, B, C, D):
+        import torch
+        if A.dtype == torch.int8:
+            r = torch._int_mm(A, B)
+            torch.add(r, C, out=D) if C is not None else D.copy_(r)
+        elif D.dtype == A.dtype:
+            if C is not None and C.dtype == D.dtype:
+                torch.addmm(C, A, B, out=D)
+            else:
+                torch.mm(A, B, out=D)
+        else:
+            D.copy_(torch.mm(A, B))
+            if C is not None:
+                D.add_(C)
+
+    def plan(self) -> str:
+        return "torch (cuBLAS) reference"
+
+    def close(self) -> None:
+        pass
+
+
 def child(args) -> int:
     sys.path.insert(0, ROOT)
     import torch
@@ -49,6 +79,9 @@ def child(args) -> int:
     cands = [c for c in args.candidates.split(";") if c.strip()]
     handles = []
     for c in cands:
+        if c == "cublas":
+            handles.append(LibraryReference(w))
+            continue
         os.environ["GEMM_FORCE_PLAN"] = c
         handles.append(pkg.Gemm.like(*sets[0]))
     os.environ.pop("GEMM_FORCE_PLAN", None)
@@ -58,11 +91,17 @@ def child(args) -> int:
     def run(g, n, base=0):
         for i in range(n):
             A, B, C, D = sets[(base + i) % nsets]
+            if isinstance(g, LibraryReference):
+                g.run(A, B, C, D)
+                continue
             g.run_ptrs(A.data_ptr(), B.data_ptr(), None if C is None else C.data_ptr(),
                        D.data_ptr(), sp)
 
     for g in handles:
         run(g, 3)
+        if isinstance(g, LibraryReference):
+            torch.cuda.synchronize()
+            continue
         st = g.status(stream)
         if st != pkg.GEMM_OK:
             raise RuntimeError(f"candidate {g.plan()} failed: {pkg.gemm_strerror(st)}")
@@ -77,7 +116,7 @@ def child(args) -> int:
             torch.cuda.synchronize()
             times[ci].append(s.elapsed_time(e) / args.iters)
     for ci, g in enumerate(handles):
-        if g.status(stream) != pkg.GEMM_OK:
+        if not isinstance(g, LibraryReference) and g.status(stream) != pkg.GEMM_OK:
             raise RuntimeError(f"candidate {g.plan()} timed out")
         med = statistics.median(times[ci])
         spread = (max(times[ci]) - min(times[ci])) / med

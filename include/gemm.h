@@ -57,7 +57,7 @@ enum {
   GEMM_OK = 0,
   GEMM_ERR_INVALID_ARG = -1,    /* a size, leading dimension or pointer is invalid */
   GEMM_ERR_UNSUPPORTED = -2,    /* type combination not supported */
-  GEMM_ERR_MISALIGNED = -3,     /* an operand pointer is not aligned to its element size */
+  GEMM_ERR_MISALIGNED = -3,     /* an operand pointer is not aligned as gemm_run requires */
   GEMM_ERR_CUDA = -4,           /* a CUDA runtime/driver call or a launch failed */
   GEMM_ERR_DEVICE_TIMEOUT = -5, /* a bounded device-side wait expired (see gemm_get_status) */
   GEMM_ERR_ALLOC_FAILED = -6,   /* device or host allocation failed */
@@ -82,7 +82,8 @@ typedef void* gemm_stream_t;
 
 /*
  * gemm_create: validate desc, choose a plan (tile, stage count, raster
- * group, split-K, operand swap, repack) from the measured selection table
+ * group, split-K, operand swap, repack, or the decode kernel for M <= 4
+ * rows against a K-contiguous B) from the measured selection table
  * keyed on (M, N, K, types, layouts), and allocate on the current device the
  * workspace and the device status word that the plan needs.  The workspace
  * holds copies of operands whose rows the TMA unit cannot read in place
@@ -94,15 +95,21 @@ typedef void* gemm_stream_t;
  * GEMM_ERR_NO_DEVICE, GEMM_ERR_ALLOC_FAILED or GEMM_ERR_CUDA.
  * Environment: GEMM_LOG=1 prints the chosen plan to stderr;
  * GEMM_FORCE_PLAN="bn=128,splits=2,group=8,swap=1" overrides fields of the
- * plan (for tuning sweeps).
+ * plan (for tuning sweeps; keys bn, splits, group, swap, grid, pair, ksub,
+ * tail, decode).
  */
 GEMM_API int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc);
 
 /*
  * gemm_run: enqueue D = A*B + C on stream.  Never allocates and never
- * synchronises.  A, B, D must be non-NULL device pointers aligned to their
- * element size (more alignment enables faster paths); C may be NULL, which
- * means C = 0 and C is not read.  D may alias C only when both have the same
+ * synchronises.  A, B, C, D must be device pointers aligned to their
+ * element size; C may be NULL, which means C = 0 and C is not read.  The
+ * tensor-core paths read A and B with TMA: when the description's leading
+ * dimension gives rows that are not 16-byte aligned, gemm_create plans an
+ * aligned workspace copy, but a base pointer that is not 16-byte aligned
+ * while its rows are is rejected with GEMM_ERR_MISALIGNED (the handle has
+ * no copy for it).  The decode path (M <= 4, K-contiguous B) and C / D
+ * accept any element-aligned pointer.  D may alias C only when both have the same
  * type, layout and leading dimension; D must not overlap A or B.
  * One handle must not be used by two streams at the same time (its
  * workspace and status word are shared by its calls).

@@ -273,6 +273,61 @@ def test_8192_sampled(name, plan):
     _assert_ok(check_rows(w, inp, D, rows=rows), f"{name} rows [{p}]")
 
 
+@pytest.mark.parametrize("name", ["decode1x4096x4096_bf16", "decode16x4096x4096_bf16",
+                                  "decode1x4096x4096_bf16_brow", "decode16x4096x4096_bf16_brow"])
+def test_decode_shapes_every_element(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    D, p = run_gpu(w, inp)
+    _assert_ok(check_rows(w, inp, D), f"{name} [{p}]")
+
+
+DECODE_CASES = [
+    # (M, N, K, layout_a, ab, c, d, layout_d, B element offset)
+    (3, 1000, 1032, ROW, BF16, BF16, BF16, ROW, 0),
+    (4, 777, 4096, COL, F16, F32, F32, ROW, 0),
+    (2, 512, 264, ROW, BF16, None, BF16, COL, 0),
+    (1, 4096, 4096, ROW, BF16, BF16, BF16, ROW, 1),   # B not 16-byte aligned: 2-byte loads
+    (1, 333, 2312, ROW, F16, F16, F16, ROW, 0),       # K slices not a multiple of 4 steps
+    (4, 64, 8192, ROW, BF16, BF16, BF16, ROW, 0),
+]
+
+
+@pytest.mark.parametrize("plan", [None, "decode=0"])
+@pytest.mark.parametrize("case", DECODE_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}-off{c[8]}"
+                                                   for c in DECODE_CASES])
+def test_decode_kernel(case, plan):
+    """M <= 16 with a K-contiguous B takes the decode kernel (and, with
+    decode=0, the tensor-core path); every element against the oracle."""
+    M, N, K, la, ab, ct, dt, ld, off = case
+    w = Workload("dec", 65, M, N, K, ab, ct, dt, "normal", la, COL, ROW, ld)
+    inp = make_inputs(w)
+    dev = torch.device("cuda")
+    A = logical(inp["A"].to(dev), la)
+    flat = torch.zeros(N * K + 8, dtype=inp["B"].dtype, device=dev)
+    flat[off:off + N * K] = inp["B"].to(dev).reshape(-1)
+    B = flat[off:off + N * K].view(N, K).t()          # K x N, column-major, ldb = K
+    C = None if inp["C"] is None else inp["C"].to(dev)
+    D_storage = torch.zeros(storage_shape(M, N, ld), dtype=TORCH_DTYPE[dt], device=dev)
+    D = logical(D_storage, ld)
+    with forced_plan(plan):
+        g = pkg.Gemm.like(A, B, C, D)
+    p = g.plan()
+    assert ("decode=1" in p) == (plan is None), p
+    if plan is not None and off:
+        # the tensor-core path reads B with TMA: a B base off the 16-byte grid
+        # with 16-byte aligned rows has no workspace copy and is rejected
+        with pytest.raises(pkg.GemmError) as e:
+            g.run(A, B, C, D)
+        assert e.value.code == pkg.GEMM_ERR_MISALIGNED
+        g.close()
+        return
+    g.run(A, B, C, D)
+    assert g.status() == pkg.GEMM_OK
+    g.close()
+    _assert_ok(check_rows(w, inp, D_storage.cpu()), f"{case} [{p}]")
+
+
 # ------------------------------------------------------------------ exact int8
 I8_PLANS = [None, "pair=1,ksub=1", "pair=1,ksub=2"]
 

@@ -71,6 +71,16 @@ WORKLOADS = {
     "rag4095x4097x4099_bf16": Workload("rag4095x4097x4099_bf16", 44, 4095, 4097, 4099, BF16,
                                        BF16, BF16, "normal"),
     "sq8192_i8": Workload("sq8192_i8", 5, 8192, 8192, 8192, I8, I32, I32, "int"),
+    # decode regime (M <= 16, N = K = 4096), with B K-contiguous (a weight
+    # stored N x K) and N-contiguous
+    "decode1x4096x4096_bf16": Workload("decode1x4096x4096_bf16", 61, 1, 4096, 4096, BF16, BF16,
+                                       BF16, "normal", layout_b=COL),
+    "decode16x4096x4096_bf16": Workload("decode16x4096x4096_bf16", 62, 16, 4096, 4096, BF16,
+                                        BF16, BF16, "normal", layout_b=COL),
+    "decode1x4096x4096_bf16_brow": Workload("decode1x4096x4096_bf16_brow", 63, 1, 4096, 4096,
+                                            BF16, BF16, BF16, "normal"),
+    "decode16x4096x4096_bf16_brow": Workload("decode16x4096x4096_bf16_brow", 64, 16, 4096, 4096,
+                                             BF16, BF16, BF16, "normal"),
 }
 
 
