@@ -118,9 +118,9 @@ struct gemm_plan {
   // operand, replaced round-robin): encoding one costs microseconds of host
   // time, which short GEMMs cannot hide.
   static constexpr int kMapCache = 8;
-  const void* map_ptr[3][kMapCache] = {};  // A', B', D
-  CUtensorMap map[3][kMapCache] = {};
-  int map_next[3] = {0, 0, 0};
+  const void* map_ptr[4][kMapCache] = {};  // A', B', D, C
+  CUtensorMap map[4][kMapCache] = {};
+  int map_next[4] = {0, 0, 0, 0};
   std::string plan_str;
   // Kernel timing: event pairs recorded around the tensor-core launch of the
   // next timing_n runs (created by gemm_timing_enable, never by gemm_run).
@@ -308,6 +308,35 @@ int encode_store_d(CUtensorMap* tm, void* base, int64_t ld, int64_t M, int64_t N
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// Tensor map of a row-contiguous int32 C or D (internal coordinates): dims
+// {N, M}, box {32, 32} (128 bytes x 32 rows) with 128-byte swizzle, for the
+// exact-int8 pair kernel's per-warp C loads and D stores.
+int encode_i32_tile(CUtensorMap* tm, const void* base, int64_t ld, int64_t M, int64_t N) {
+  EncodeFn enc = get_encode();
+  if (!enc) return GEMM_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// The cached tensor map of slot `which` for base (encoded on a miss).
+template <typename Enc>
+const CUtensorMap* cached_map(gemm_plan* h, int which, const void* base, Enc encode) {
+  for (int i = 0; i < gemm_plan::kMapCache; ++i)
+    if (h->map_ptr[which][i] == base) return &h->map[which][i];
+  const int slot = h->map_next[which];
+  h->map_next[which] = (slot + 1) % gemm_plan::kMapCache;
+  h->map_ptr[which][slot] = nullptr;
+  if (encode(&h->map[which][slot]) != GEMM_OK) return nullptr;
+  h->map_ptr[which][slot] = base;
+  return &h->map[which][slot];
 }
 
 }  // namespace
@@ -716,29 +745,44 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
     kp.epoch = h->epoch;
   }
   // The pair kernel stores a 16-bit, row-contiguous D with TMA from swizzled
-  // shared memory (rows 16-byte aligned, as TMA requires).
-  const CUtensorMap* tmd = tm[0];  // placeholder argument when D is stored directly
-  kp.d_tma = (h->pair && kp.splits == 1 && kp.d_vec && (d.d_type == GEMM_BF16 ||
-                                                         d.d_type == GEMM_F16)) ? 1 : 0;
-  if (kp.d_tma) {
-    const CUtensorMap* hit = nullptr;
-    for (int i = 0; i < gemm_plan::kMapCache; ++i)
-      if (h->map_ptr[2][i] == kp.D) hit = &h->map[2][i];
-    if (!hit) {
-      const int slot = h->map_next[2];
-      h->map_next[2] = (slot + 1) % gemm_plan::kMapCache;
-      h->map_ptr[2][slot] = nullptr;
-      if (encode_store_d(&h->map[2][slot], kp.D, kp.d_rs, h->M, h->N) != GEMM_OK)
-        return GEMM_ERR_CUDA;
-      h->map_ptr[2][slot] = kp.D;
-      hit = &h->map[2][slot];
+  // shared memory (rows 16-byte aligned, as TMA requires); its exact-int8
+  // mode moves an int32 C and D that way.
+  const CUtensorMap* tmd = tm[0];  // placeholder arguments when unused
+  const CUtensorMap* tmc = tm[0];
+  if (h->i8x) {
+    kp.d_tma = (h->pair && kp.splits == 1 && kp.d_vec && (!C || kp.c_vec)) ? 1 : 0;
+    if (kp.d_tma) {
+      void* dp = kp.D;
+      const int64_t drs = kp.d_rs;
+      tmd = cached_map(h, 2, dp, [&](CUtensorMap* m) {
+        return encode_i32_tile(m, dp, drs, h->M, h->N);
+      });
+      if (!tmd) return GEMM_ERR_CUDA;
+      if (C) {
+        const void* cp = kp.C;
+        const int64_t crs = kp.c_rs;
+        tmc = cached_map(h, 3, cp, [&](CUtensorMap* m) {
+          return encode_i32_tile(m, cp, crs, h->M, h->N);
+        });
+        if (!tmc) return GEMM_ERR_CUDA;
+      }
     }
-    tmd = hit;
+  } else {
+    kp.d_tma = (h->pair && kp.splits == 1 && kp.d_vec &&
+                (d.d_type == GEMM_BF16 || d.d_type == GEMM_F16)) ? 1 : 0;
+    if (kp.d_tma) {
+      void* dp = kp.D;
+      const int64_t drs = kp.d_rs;
+      tmd = cached_map(h, 2, dp, [&](CUtensorMap* m) {
+        return encode_store_d(m, dp, drs, h->M, h->N);
+      });
+      if (!tmd) return GEMM_ERR_CUDA;
+    }
   }
   const bool timed = h->timing_used < h->timing_n;
   if (timed && cudaEventRecord(h->timing_ev[2 * h->timing_used], st) != cudaSuccess)
     return GEMM_ERR_CUDA;
-  const cudaError_t le = h->pair ? h->pair->launch(*tm[0], *tm[1], *tmd, kp, h->grid, st)
+  const cudaError_t le = h->pair ? h->pair->launch(*tm[0], *tm[1], *tmd, *tmc, kp, h->grid, st)
                                  : h->variant->launch(*tm[0], *tm[1], kp, h->grid, st);
   if (le != cudaSuccess) return GEMM_ERR_CUDA;
   if (timed) {

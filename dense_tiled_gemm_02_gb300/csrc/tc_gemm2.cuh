@@ -54,12 +54,18 @@ struct PairCfg {
 };
 
 // Staging for the TMA store of D: two buffers of 128 rows x 64 16-bit
-// columns (one 128-byte swizzle row each).
+// columns (one 128-byte swizzle row each).  The exact-int8 variant has four:
+// two 4 KB buffers (32 rows x 32 int32) per epilogue warp for C and D.
 constexpr uint32_t D_STAGE_BYTES = BM * 64 * 2;
 
-template <int BN, int STAGES, int KSUB>
+template <bool I8X>
+__host__ __device__ constexpr uint32_t pair_stage_bytes() {
+  return (I8X ? 4 : 2) * D_STAGE_BYTES;
+}
+
+template <int BN, int STAGES, int KSUB, bool I8X = false>
 constexpr uint32_t pair_smem_bytes() {
-  return STAGES * PairCfg<BN, KSUB>::STAGE_BYTES + 2 * D_STAGE_BYTES + 256 + 1024;
+  return STAGES * PairCfg<BN, KSUB>::STAGE_BYTES + pair_stage_bytes<I8X>() + 512 + 1024;
 }
 
 // kb0/kb1 count 64-wide K slices; a stage covers KSUB of them.
@@ -76,16 +82,20 @@ template <int BN, int STAGES, int KSUB, bool I8X>
 __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmD, const KParams p) {
+                        const __grid_constant__ CUtensorMap tmD,
+                        const __grid_constant__ CUtensorMap tmC, const KParams p) {
   using Cfg = PairCfg<BN, KSUB, I8X>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
-  uint8_t* sD = sB + STAGES * Cfg::B_BYTES;  // 2 x D_STAGE_BYTES, 1024-aligned
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sD + 2 * D_STAGE_BYTES);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint8_t* sD = sB + STAGES * Cfg::B_BYTES;  // staging buffers, 1024-aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sD + pair_stage_bytes<I8X>());
+  // ring full/empty, accumulator full/empty, done; int8: C-load barriers of
+  // the 8 epilogue warps' two staging buffers
+  constexpr int NBARS = 2 * STAGES + 5 + (I8X ? 2 * Cfg::EPI_WARPS : 0);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* ep_go = abort_flag + 1;  // the epilogue leader's verdict for its warps
 
@@ -95,6 +105,7 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
   auto acc_full = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + b); };
   auto acc_empty = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto cbar = [&](int e, int b) { return bar0 + 8u * (2 * STAGES + 5 + 2 * e + b); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -111,6 +122,11 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
       mbar_init(acc_empty(b), 2 * Cfg::EPI_WARPS);  // one arrival per epilogue warp of both CTAs
     }
     mbar_init(done_bar, 1);
+    if constexpr (I8X)
+      for (int e = 0; e < Cfg::EPI_WARPS; ++e) {
+        mbar_init(cbar(e, 0), 1);
+        mbar_init(cbar(e, 1), 1);
+      }
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -119,6 +135,7 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (p.d_tma) tma_prefetch_desc(&tmD);
+    if (I8X && p.d_tma && p.C) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_holder), Cfg::TMEM_COLS);
@@ -296,16 +313,38 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
       constexpr int HC = BN / 2;
       const int half = (warp - 2) >> 2;
       const uint32_t col0 = static_cast<uint32_t>(half * HC);
+      // With p.d_tma the tile's C and D move through two 4 KB shared-memory
+      // buffers of this warp (32 rows x 32 int32, 128-byte swizzle) by TMA:
+      // per-thread row accesses would put 32 rows in every warp access.
+      const int e = warp - 2;
+      uint8_t* const stg = sD + e * 8192;
+      uint32_t cph[2] = {0u, 0u};      // parity of the next completion of cbar(e, b)
+      bool c_pending[2] = {false, false};
+      auto load_c = [&](int b, int gx, int gy) {  // lane 0: slice into buffer b
+        bulk_wait_read_all();                       // earlier stores have read it
+        mbar_arrive_expect_tx(cbar(e, b), 32 * 32 * 4);
+        tma_load_2d(smem_u32(stg + b * 4096), &tmC, gx, gy, cbar(e, b));
+      };
       int isum[HC];
       bool ok = true;
       for (int i = 0; i < pw.n && ok; ++i) {
         const Unit w = pair_unit(p, pw, KSUB, cid, ncl, i, BN);
         const int r = w.m0 + BM * static_cast<int>(rank) + row_local;
         const int nch = (w.kb1 - w.kb0 + p.kb_per_chunk - 1) / p.kb_per_chunk;
+        const int gy = w.m0 + BM * static_cast<int>(rank) + 32 * q;  // this warp's rows
+        const int gx0 = w.n0 + static_cast<int>(col0);
 #pragma unroll
         for (int j = 0; j < HC; ++j) isum[j] = 0;
         for (int ch = 0; ch < nch; ++ch) {
           const uint32_t buf = acc_it & 1u;
+          if (p.d_tma && p.C && ch == nch - 1) {
+            // C of the tile's first two slices, while the last chunk runs
+            if (lane == 0) {
+              load_c(0, gx0, gy);
+              load_c(1, gx0 + 32, gy);
+            }
+            c_pending[0] = c_pending[1] = true;
+          }
           if (ep_leader)
             *ep_go = bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status,
                                   STATUS_TIMEOUT, tmo) ? 1 : 0;
@@ -332,10 +371,59 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
           ++acc_it;
         }
         if (!ok) break;
+        if (p.d_tma) {
 #pragma unroll
-        for (int c = 0; c < HC / 32; ++c)
-          store_d_i32(p, r, w.n0 + static_cast<int>(col0) + c * 32,
-                      *reinterpret_cast<int(*)[32]>(isum + c * 32));
+          for (int c = 0; c < HC / 32; ++c) {
+            const int b = c & 1;
+            uint8_t* const sbuf = stg + b * 4096;
+            const int gx = gx0 + 32 * c;
+            if (!p.C) {
+              // the store issued from this buffer two slices ago has read it
+              if (lane == 0) bulk_wait_read_le1();
+              __syncwarp();
+            } else {
+              if (!bounded_wait(cbar(e, b), cph[b], abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
+                ok = false;
+                break;
+              }
+              cph[b] ^= 1u;
+              c_pending[b] = false;
+            }
+            // this thread's row: 8 units of 16 bytes, unit u at (u ^ row % 8)
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              int4* const ptr = reinterpret_cast<int4*>(sbuf + lane * 128 + ((u ^ (lane & 7)) * 16));
+              int4 x = p.C ? *ptr : make_int4(0, 0, 0, 0);
+              x.x += isum[c * 32 + 4 * u];
+              x.y += isum[c * 32 + 4 * u + 1];
+              x.z += isum[c * 32 + 4 * u + 2];
+              x.w += isum[c * 32 + 4 * u + 3];
+              *ptr = x;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (gx < p.N && gy < p.M)  // boxes entirely outside D are skipped
+                tma_store_2d(&tmD, smem_u32(sbuf), gx, gy);
+              bulk_commit();
+              if (p.C && c + 2 < HC / 32) load_c(b, gx + 64, gy);
+            }
+            if (p.C && c + 2 < HC / 32) c_pending[b] = true;
+          }
+          if (!ok) break;
+        } else {
+#pragma unroll
+          for (int c = 0; c < HC / 32; ++c)
+            store_d_i32(p, r, w.n0 + static_cast<int>(col0) + c * 32,
+                        *reinterpret_cast<int(*)[32]>(isum + c * 32));
+        }
+      }
+      // C loads still in flight (after a timeout) land before the CTA
+      // leaves, and so do the stores that read the staging buffers.
+      if (lane == 0) {
+        for (int b = 0; b < 2; ++b)
+          if (c_pending[b]) drain_wait(cbar(e, b), cph[b], 200000000ull);
+        bulk_wait_all();
       }
     } else {
     for (int i = 0; i < pw.n; ++i) {

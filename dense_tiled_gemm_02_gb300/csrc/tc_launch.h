@@ -55,9 +55,9 @@ struct PairVariant {
   int ksub;  // 64-wide K slices per ring stage
   bool i8x;  // exact int8 (bf16-widened operands, chunked int32 sums)
   uint32_t smem;
-  // tensor maps of A, B and (when KParams::d_tma) D
+  // tensor maps of A, B and, when KParams::d_tma, D and (exact int8) C
   cudaError_t (*launch)(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                        const KParams&, int grid, cudaStream_t);
+                        const CUtensorMap&, const KParams&, int grid, cudaStream_t);
   cudaError_t (*prepare)();
   int (*max_clusters)();
 };

@@ -13,7 +13,7 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t st, cudaLaunchAttribute* a
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(PairCfg<BN, KSUB, I8X>::THREADS, 1, 1);
-  cfg.dynamicSmemBytes = pair_smem_bytes<BN, STAGES, KSUB>();
+  cfg.dynamicSmemBytes = pair_smem_bytes<BN, STAGES, KSUB, I8X>();
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -29,17 +29,17 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t st, cudaLaunchAttribute* a
 
 template <int BN, int STAGES, int KSUB, bool I8X>
 cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
-                        const KParams& p, int grid, cudaStream_t st) {
+                        const CUtensorMap& c, const KParams& p, int grid, cudaStream_t st) {
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config<BN, STAGES, KSUB, I8X>(grid, st, attr);
-  return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, KSUB, I8X>, a, b, d, p);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, KSUB, I8X>, a, b, d, c, p);
 }
 
 template <int BN, int STAGES, int KSUB, bool I8X>
 cudaError_t prepare_pair() {
   return cudaFuncSetAttribute(tc_gemm_pair_kernel<BN, STAGES, KSUB, I8X>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              pair_smem_bytes<BN, STAGES, KSUB>());
+                              pair_smem_bytes<BN, STAGES, KSUB, I8X>());
 }
 
 template <int BN, int STAGES, int KSUB, bool I8X>
@@ -57,13 +57,13 @@ int max_clusters_pair() {
 }  // namespace
 
 #define GB_PAIR(BN_, ST_, KS_, I8_)                                                 \
-  PairVariant{BN_, ST_, KS_, I8_, pair_smem_bytes<BN_, ST_, KS_>(),                 \
+  PairVariant{BN_, ST_, KS_, I8_, pair_smem_bytes<BN_, ST_, KS_, I8_>(),            \
               &launch_pair<BN_, ST_, KS_, I8_>, &prepare_pair<BN_, ST_, KS_, I8_>, \
               &max_clusters_pair<BN_, ST_, KS_, I8_>}
 
 const PairVariant kPairVariants[] = {GB_PAIR(256, 6, 1, false), GB_PAIR(256, 3, 2, false),
                                      GB_PAIR(128, 8, 1, false), GB_PAIR(128, 4, 2, false),
-                                     GB_PAIR(256, 6, 1, true),  GB_PAIR(256, 3, 2, true)};
-const int kNumPairVariants = 6;
+                                     GB_PAIR(256, 5, 1, true)};
+const int kNumPairVariants = 5;
 
 }  // namespace gb300

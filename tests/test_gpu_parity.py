@@ -346,6 +346,16 @@ def test_int8_exact_small(shape, plan):
 
 
 @pytest.mark.parametrize("plan", I8_PLANS)
+def test_int8_without_c(plan):
+    """C absent: D = A*B exactly (the pair kernel stages D alone)."""
+    M, N, K = 520, 640, 2112
+    w = Workload("i8n", 53, M, N, K, I8, None, I32, "int")
+    inp = make_inputs(w)
+    D, p = run_gpu(w, inp, plan=plan)
+    _assert_ok(check_rows(w, inp, D), f"int8 no C [{p}]")
+
+
+@pytest.mark.parametrize("plan", I8_PLANS)
 @pytest.mark.parametrize("fill", [-128, 127])
 def test_int8_extremes(fill, plan):
     """All entries at one extreme, K = 8192: |sum| = 2^27 (or 127^2 * 8192)."""
