@@ -428,7 +428,7 @@ def algorithmic_bytes(w) -> int:
 def launches_per_step(g) -> int:
     plan = g.plan()
     if re.search(r"\bdecode=1\b", plan):
-        return 2  # decode kernel + the reduce that adds its K slices and C
+        return 1  # the decode kernel finishes D itself
     n = 1
     if re.search(r"splits=(\d+)", plan) and int(re.search(r"splits=(\d+)", plan).group(1)) > 1:
         n += 1

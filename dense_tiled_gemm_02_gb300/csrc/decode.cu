@@ -15,9 +15,12 @@
 //     elements of every row, so one A load from shared memory serves four
 //     columns;
 //   * each lane's fp32 sums are added across the warp by a fixed butterfly,
-//     and lane 0 writes the slice's partial sums to the workspace.
-// splitk_reduce_kernel then adds the slices in order, adds C, converts and
-// stores D (deterministic; no atomics).
+//     and lane 0 writes the slice's partial sums to the workspace;
+//   * the block that finishes last among the K slices of its columns (a
+//     per-column-block counter) adds the slices' partials in slice order,
+//     adds C, converts and stores D, and resets the counter.  The sum's
+//     order does not depend on which block is last: deterministic, and no
+//     second kernel.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -33,6 +36,21 @@ namespace {
 constexpr int DEC_THREADS = 256;
 constexpr int DEC_NC = 4;                          // columns per warp
 constexpr int DEC_COLS = DEC_NC * DEC_THREADS / 32;  // columns per block
+
+__device__ __forceinline__ float dec_load(const void* base, int t, long long off) {
+  if (t == T_BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[off]);
+  if (t == T_F16) return __half2float(static_cast<const __half*>(base)[off]);
+  return static_cast<const float*>(base)[off];
+}
+
+__device__ __forceinline__ void dec_store(void* base, int t, long long off, float v) {
+  if (t == T_BF16)
+    static_cast<__nv_bfloat16*>(base)[off] = __float2bfloat16_rn(v);
+  else if (t == T_F16)
+    static_cast<__half*>(base)[off] = __float2half_rn(v);
+  else
+    static_cast<float*>(base)[off] = v;
+}
 
 template <bool BF16>
 __device__ __forceinline__ void widen8(const uint4 v, float (&f)[8]) {
@@ -57,10 +75,11 @@ __device__ __forceinline__ void widen8(const uint4 v, float (&f)[8]) {
 // loads of the same elements.
 template <int MM, bool BF16, bool VEC>
 __global__ void __launch_bounds__(DEC_THREADS)
-    decode_kn_kernel(const uint16_t* __restrict__ A, long long a_rs, long long a_cs,
-                     const uint16_t* __restrict__ B, long long ldb, int M, int N, int K, int kc,
-                     float* __restrict__ ws, long long ws_split, long long ws_rs,
-                     long long ws_cs) {
+    decode_kn_kernel(const DecodeArgs d) {
+  const uint16_t* __restrict__ A = d.A;
+  const uint16_t* __restrict__ B = d.B;
+  const long long a_rs = d.a_rs, a_cs = d.a_cs, ldb = d.ldb;
+  const int M = d.M, N = d.N, K = d.K, kc = d.kc;
   extern __shared__ __align__(16) uint16_t sA[];  // [MM][kc]
   pdl_wait();
   pdl_trigger();
@@ -141,13 +160,36 @@ __global__ void __launch_bounds__(DEC_THREADS)
       acc[m][c] = v;
     }
   if (lane == 0) {
-    float* out = ws + blockIdx.y * ws_split;
+    float* out = d.ws + blockIdx.y * d.ws_split;
 #pragma unroll
     for (int m = 0; m < MM; ++m)
 #pragma unroll
       for (int c = 0; c < DEC_NC; ++c)
-        if (m < M && n0 + c < N) out[m * ws_rs + static_cast<long long>(n0 + c) * ws_cs] = acc[m][c];
+        if (m < M && n0 + c < N)
+          out[m * d.ws_rs + static_cast<long long>(n0 + c) * d.ws_cs] = acc[m][c];
   }
+  // The last block of this column block's K slices finishes the columns.
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned old = atomicAdd(d.counters + blockIdx.x, 1u);
+    last = old == static_cast<unsigned>(d.splits) - 1u;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const int nb = blockIdx.x * DEC_COLS;
+  for (int i = threadIdx.x; i < M * DEC_COLS; i += DEC_THREADS) {
+    const int m = i / DEC_COLS, n = nb + (i - m * DEC_COLS);
+    if (n >= N) continue;
+    float v = 0.f;
+    for (int sl = 0; sl < d.splits; ++sl)
+      v += d.ws[sl * d.ws_split + m * d.ws_rs + static_cast<long long>(n) * d.ws_cs];
+    if (d.C) v += dec_load(d.C, d.c_type, m * d.c_rs + static_cast<long long>(n) * d.c_cs);
+    dec_store(d.D, d.d_type, m * d.d_rs + static_cast<long long>(n) * d.d_cs, v);
+  }
+  if (threadIdx.x == 0) d.counters[blockIdx.x] = 0u;  // ready for the next call
 }
 
 template <int MM, bool BF16, bool VEC>
@@ -160,8 +202,7 @@ cudaError_t launch_mm(const DecodeArgs& d, cudaStream_t st) {
     return cudaGetLastError();
   const dim3 grid(static_cast<unsigned>((d.N + DEC_COLS - 1) / DEC_COLS),
                   static_cast<unsigned>(d.splits));
-  return launch_pdl(kernel, grid, dim3(DEC_THREADS), smem, st, d.A, d.a_rs, d.a_cs, d.B, d.ldb,
-                    d.M, d.N, d.K, d.kc, d.ws, d.ws_split, d.ws_rs, d.ws_cs);
+  return launch_pdl(kernel, grid, dim3(DEC_THREADS), smem, st, d);
 }
 
 template <bool BF16, bool VEC>

@@ -250,12 +250,19 @@ int plan_decode(gemm_plan* h, int sms) {
   kp.ws_cs = row ? 1 : d.M;
   kp.ws_split = d.M * d.N;
   h->ws_partial_off = 0;
-  h->ws_bytes = (size_t)round_up(s * d.M * d.N * 4, 256);
+  h->ws_flags_off = (size_t)round_up(s * d.M * d.N * 4, 256);  // per-column-block counters
+  h->ws_bytes = h->ws_flags_off + (size_t)round_up(col_blocks * 4, 256);
   h->grid = (int)(col_blocks * s);
   if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
     h->ws = nullptr;
     return GEMM_ERR_ALLOC_FAILED;
+  }
+  if (cudaMemset(static_cast<char*>(h->ws) + h->ws_flags_off, 0, col_blocks * 4) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->ws);
+    return GEMM_ERR_CUDA;
   }
   if (cudaMalloc(&h->status, 256) != cudaSuccess || cudaMemset(h->status, 0, 256) != cudaSuccess) {
     cudaGetLastError();
@@ -667,7 +674,15 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
     a.ws_split = kp.ws_split;
     a.ws_rs = kp.ws_rs;
     a.ws_cs = kp.ws_cs;
-    kp.ws = a.ws;
+    a.counters = reinterpret_cast<unsigned*>(static_cast<char*>(h->ws) + h->ws_flags_off);
+    a.C = C;
+    a.c_type = d.c_type;
+    a.c_rs = kp.c_rs;
+    a.c_cs = kp.c_cs;
+    a.D = D;
+    a.d_type = d.d_type;
+    a.d_rs = kp.d_rs;
+    a.d_cs = kp.d_cs;
     const bool timed = h->timing_used < h->timing_n;
     if (timed && cudaEventRecord(h->timing_ev[2 * h->timing_used], st) != cudaSuccess)
       return GEMM_ERR_CUDA;
@@ -677,7 +692,7 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
         return GEMM_ERR_CUDA;
       ++h->timing_used;
     }
-    return launch_reduce(kp, row_order, h->num_sms, st) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    return GEMM_OK;
   }
   char* ws = static_cast<char*>(h->ws);
   uint16_t* d_staged = nullptr;

@@ -71,10 +71,12 @@ cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint1
                           cudaStream_t st);
 // Decode regime (decode.cu): M <= kDecodeMaxRows rows, B K-contiguous (element (k, n)
 // at B[n * ldb + k]), K a multiple of 8 (16-byte loads when B is 16-byte
-// aligned and ldb a multiple of 8, else 2-byte loads).  Writes
-// `splits` fp32 partial slices of kc K elements each to ws (slice s at
-// ws + s * ws_split, element (m, n) at m * ws_rs + n * ws_cs), for
-// splitk_reduce_kernel to finish.
+// aligned and ldb a multiple of 8, else 2-byte loads).  Each block writes
+// the fp32 partial sums of its K slice (kc elements) to ws (slice s at
+// ws + s * ws_split, element (m, n) at m * ws_rs + n * ws_cs); the last of a
+// column block's `splits` blocks adds them in slice order, adds C and
+// stores D.  counters: one per block of decode_columns_per_block()
+// columns, zero between calls.
 constexpr int kDecodeMaxRows = 4;
 struct DecodeArgs {
   const uint16_t* A;
@@ -85,6 +87,13 @@ struct DecodeArgs {
   bool bf16;
   float* ws;
   long long ws_split, ws_rs, ws_cs;
+  unsigned* counters;
+  const void* C;  // may be null
+  int c_type;
+  long long c_rs, c_cs;
+  void* D;
+  int d_type;
+  long long d_rs, d_cs;
 };
 cudaError_t launch_decode(const DecodeArgs& d, cudaStream_t st);
 int decode_columns_per_block();
