@@ -48,9 +48,29 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="sq4096_bf16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="target CPU time of the whole reference-arm run (the oracle)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
     return ap.parse_args()
+
+
+def job_step_ms(total_ms: float, steps: int, world: int) -> float:
+    """Per-step time of the whole job: the slowest rank's timed region (every
+    rank holds one replica, so the job ends with the last of them)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], dtype=torch.float64,
+                         device="cuda" if dist.get_backend() == "nccl" else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms / steps
+
+
+def job_value(flops_per_step: float, step_ms: float, world: int) -> float:
+    """Aggregate throughput (TFLOP/s or TOPS) of `world` replicas."""
+    return flops_per_step / (step_ms * 1e-3) / 1e12 * world
 
 
 def dist_env():
@@ -183,7 +203,7 @@ def run_reference(args, w):
     from workloads import I8, make_inputs
     inp = make_inputs(w)
     total_steps = max(1, args.steps + args.warmup)
-    per_step_s = min(10.0, max(0.2, 120.0 / total_steps))
+    per_step_s = min(10.0, max(0.02, args.ref_seconds / total_steps))
     run, threads = oracle_rows_runner(w, inp)
     rows_per_step = calibrate_rows(run, w.M, per_step_s)
     for i in range(args.warmup):
@@ -347,12 +367,9 @@ def main():
         raise RuntimeError(f"kernel timing run failed: {pkg.gemm_strerror(st)}")
     if len(kernel_ms) != args.steps:
         raise RuntimeError(f"kernel timing recorded {len(kernel_ms)} of {args.steps} launches")
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms = total_ms / args.steps
-    value = w.flops / (ms * 1e-3) / 1e12 * world
+    ms = job_step_ms(total_ms, args.steps, world)
+    total_ms = ms * args.steps
+    value = job_value(w.flops, ms, world)
 
     # ---- end to end through the same call, host buffers
     e2e = e2e_measure(pkg, g, w, inp, dev, stream, max(3, args.steps // 5), world)
@@ -466,8 +483,8 @@ def e2e_measure(pkg, g, w, inp, dev, stream, steps, world):
         one()
     e.record(stream)
     torch.cuda.synchronize(dev)
-    ms = s.elapsed_time(e) / steps
-    return {"value": round(w.flops / (ms * 1e-3) / 1e12 * world, 1),
+    ms = job_step_ms(s.elapsed_time(e), steps, world)
+    return {"value": round(job_value(w.flops, ms, world), 1),
             "unit": "TOPS" if w.ab_type == 4 else "TFLOPS", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
 
