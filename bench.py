@@ -449,9 +449,13 @@ def launches_per_step(g) -> int:
     n = 1
     if re.search(r"splits=(\d+)", plan) and int(re.search(r"splits=(\d+)", plan).group(1)) > 1:
         n += 1
-    for key in ("repack_a", "repack_b", "stage_c", "stage_d"):
-        n += int(re.search(key + r"=(\d)", plan).group(1))
-    return n
+    flag = {k: int(re.search(k + r"=(\d)", plan).group(1))
+            for k in ("repack_a", "repack_b", "stage_c", "stage_d", "i8x")}
+    if flag["i8x"]:  # int8 operands are widened by one launch each
+        n += flag["repack_a"] + flag["repack_b"]
+    elif flag["repack_a"] or flag["repack_b"] or flag["stage_c"]:
+        n += 1  # the 16-bit copies before the GEMM share one launch
+    return n + flag["stage_d"]
 
 
 def e2e_measure(pkg, g, w, inp, dev, stream, steps, world):

@@ -153,26 +153,31 @@ __global__ void repack_kernel(const void* __restrict__ src, int src_type, long l
 // so every warp access covers 64 contiguous bytes on both sides (2 bytes per
 // lane at a wider stride would touch a sector per lane).  Block x covers
 // 256 * 8 columns of a row band, element k of thread t at column
-// base + k * 256 + t; rows are strided over block y.
-__global__ void copy_rows16_kernel(const uint16_t* __restrict__ src, long long ld_src,
-                                  uint16_t* __restrict__ dst, long long ld_dst, long long rows,
-                                  long long cols) {
+// base + k * 256 + t; rows are strided over block y.  (Sixteen elements a
+// thread, with half the blocks, measured slower.)
+constexpr int kCopyEpt = 8;  // elements of a row per thread
+
+// Up to kMaxCopyJobs copies in one launch, job blockIdx.z: the operand
+// copies and the C staging of a call overlap instead of each waiting for
+// the tail of the one before.
+__global__ void copy_rows16_kernel(const CopyJobs16 jobs) {
   pdl_wait();
   pdl_trigger();
-  constexpr int EPT = 8;
+  const CopyJob16 j = jobs.job[blockIdx.z];
+  constexpr int EPT = kCopyEpt;
   const long long base = static_cast<long long>(blockIdx.x) * blockDim.x * EPT + threadIdx.x;
-  if (base >= cols) return;
-  for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
+  if (base >= j.cols) return;
+  for (long long r = blockIdx.y; r < j.rows; r += gridDim.y) {
     uint16_t v[EPT];
 #pragma unroll
     for (int k = 0; k < EPT; ++k) {
       const long long c = base + static_cast<long long>(k) * blockDim.x;
-      if (c < cols) v[k] = src[r * ld_src + c];
+      if (c < j.cols) v[k] = j.src[r * j.ld_src + c];
     }
 #pragma unroll
     for (int k = 0; k < EPT; ++k) {
       const long long c = base + static_cast<long long>(k) * blockDim.x;
-      if (c < cols) dst[r * ld_dst + c] = v[k];
+      if (c < j.cols) j.dst[r * j.ld_dst + c] = v[k];
     }
   }
 }
@@ -210,13 +215,13 @@ __global__ void widen_i8_x4_kernel(const char4* __restrict__ src, long long ld_s
 
 namespace {
 // copy_rows16_kernel: 2048 columns per block, rows strided over block y.
-dim3 copy_rows_grid(long long rows, long long cols, int num_sms) {
-  const unsigned gx = static_cast<unsigned>((cols + 2047) / 2048);
+dim3 copy_rows_grid(long long rows, long long cols, int num_sms, int njobs) {
+  const unsigned gx = static_cast<unsigned>((cols + 256 * kCopyEpt - 1) / (256 * kCopyEpt));
   long long gy = (static_cast<long long>(num_sms) * 16 + gx - 1) / gx;
   if (gy > rows) gy = rows;
   if (gy > 65535) gy = 65535;
   if (gy < 1) gy = 1;
-  return dim3(gx, static_cast<unsigned>(gy));
+  return dim3(gx, static_cast<unsigned>(gy), static_cast<unsigned>(njobs));
 }
 
 dim3 copy_grid(long long chunks, long long rows, int num_sms) {
@@ -254,19 +259,35 @@ cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint1
     return launch_pdl(widen_i8_x4_kernel, copy_grid(cols / 4, rows, num_sms), dim3(256), 0, st,
                       static_cast<const char4*>(src), ld_src / 4, reinterpret_cast<uint2*>(dst),
                       ld_dst / 4, rows, cols / 4);
-  if (src_type != T_I8)
-    return launch_pdl(copy_rows16_kernel, copy_rows_grid(rows, cols, num_sms), dim3(256), 0, st,
-                      static_cast<const uint16_t*>(src), ld_src, dst, ld_dst, rows, cols);
+  if (src_type != T_I8) {
+    const CopyJob16 j{static_cast<const uint16_t*>(src), ld_src, dst, ld_dst, rows, cols};
+    return launch_copy16(&j, 1, num_sms, st);
+  }
   return launch_pdl(repack_kernel, copy_grid(cols, rows, num_sms), dim3(256), 0, st, src,
                     src_type, ld_src, dst, ld_dst, rows, cols);
+}
+
+cudaError_t launch_copy16(const CopyJob16* jobs, int n, int num_sms, cudaStream_t st) {
+  if (n < 1 || n > kMaxCopyJobs) return cudaErrorInvalidValue;
+  CopyJobs16 js{};
+  long long rows = 0, cols = 0;
+  int m = 0;
+  for (int i = 0; i < n; ++i) {
+    if (jobs[i].rows == 0 || jobs[i].cols == 0) continue;
+    js.job[m++] = jobs[i];
+    rows = jobs[i].rows > rows ? jobs[i].rows : rows;
+    cols = jobs[i].cols > cols ? jobs[i].cols : cols;
+  }
+  if (m == 0) return cudaSuccess;
+  return launch_pdl(copy_rows16_kernel, copy_rows_grid(rows, cols, num_sms, m), dim3(256), 0, st,
+                    js);
 }
 
 cudaError_t launch_copy_out16(const uint16_t* src, long long ld_src, uint16_t* dst,
                               long long ld_dst, long long rows, long long cols, int num_sms,
                               cudaStream_t st) {
-  if (rows == 0 || cols == 0) return cudaSuccess;
-  return launch_pdl(copy_rows16_kernel, copy_rows_grid(rows, cols, num_sms), dim3(256), 0, st,
-                    src, ld_src, dst, ld_dst, rows, cols);
+  const CopyJob16 j{src, ld_src, dst, ld_dst, rows, cols};
+  return launch_copy16(&j, 1, num_sms, st);
 }
 
 }  // namespace gb300

@@ -551,7 +551,10 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     const int64_t outer = o.layout == GEMM_ROW_MAJOR ? o.rows : o.cols;
     o.repack = h->i8x || ((o.ld * in_es) % 16 != 0);
     if (!o.repack) return;
-    o.ws_ld = round_up(std::max<int64_t>(inner, 1), 8);
+    // Rows start on 128-byte lines: a TMA row of 128 bytes then reads four
+    // 32-byte sectors, not five (measured: a B whose rows sat 16 bytes off
+    // the line cost 10 % of the kernel time at 4096 x 4097 x 4096).
+    o.ws_ld = round_up(std::max<int64_t>(inner, 1), 64);
     o.ws_off = off;
     off += (size_t)round_up(o.ws_ld * outer * 2, 256);
   };
@@ -575,15 +578,17 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   // C and D rows (along the internal N) that are not 16-byte aligned keep
   // the kernels off their vector and TMA paths; an aligned copy costs one
   // extra pass over C or D, far less than scattered 2-byte accesses from
-  // the epilogue.  Split-K plans write D from the reduce kernel, which
-  // streams it anyway.
+  // the epilogue (measured: the pair kernel moving such rows itself, one
+  // row per warp access through its staging chunks, took 306 us at
+  // 4095 x 4097 x 4099 against 121 us plus the copies).  Split-K plans
+  // write D from the reduce kernel, which streams it anyway.
   auto is16 = [](int t) { return t == GEMM_F16 || t == GEMM_BF16; };
   if (kp.splits == 1) {
     h->c_stage = is16(d.c_type) && h->c_layout == GEMM_ROW_MAJOR && (h->ldc * 2) % 16 != 0;
     h->d_stage = is16(d.d_type) && h->d_layout == GEMM_ROW_MAJOR && (h->ldd * 2) % 16 != 0;
   }
   if (h->c_stage || h->d_stage) {
-    h->stage_ld = round_up(std::max<int64_t>(h->N, 1), 8);
+    h->stage_ld = round_up(std::max<int64_t>(h->N, 1), 64);  // 128-byte rows, as above
     const size_t bytes = (size_t)round_up(h->stage_ld * h->M * 2, 256);
     if (h->c_stage) {
       h->ws_c_off = off;
@@ -696,11 +701,14 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
   }
   char* ws = static_cast<char*>(h->ws);
   uint16_t* d_staged = nullptr;
+  // The 16-bit copies before the GEMM (C staging, operand copies) go out
+  // as one launch.
+  CopyJob16 jobs[kMaxCopyJobs];
+  int njobs = 0;
   if (h->c_stage && C) {
     uint16_t* cs = reinterpret_cast<uint16_t*>(ws + h->ws_c_off);
-    if (launch_repack(C, d.c_type, kp.c_rs, cs, h->stage_ld, h->M, h->N, h->num_sms, st) !=
-        cudaSuccess)
-      return GEMM_ERR_CUDA;
+    jobs[njobs++] = CopyJob16{static_cast<const uint16_t*>(C), kp.c_rs, cs, h->stage_ld, h->M,
+                              h->N};
     kp.C = cs;
     kp.c_rs = h->stage_ld;
   }
@@ -726,11 +734,18 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
     const int64_t inner = o.layout == GEMM_ROW_MAJOR ? o.cols : o.rows;
     const int64_t outer = o.layout == GEMM_ROW_MAJOR ? o.rows : o.cols;
     uint16_t* dst = reinterpret_cast<uint16_t*>(ws + o.ws_off);
-    if (launch_repack(src, d.ab_type, o.ld, dst, o.ws_ld, outer, inner, h->num_sms, st) !=
-        cudaSuccess)
-      return GEMM_ERR_CUDA;
+    if (d.ab_type == GEMM_I8) {  // widened to bf16 on the way
+      if (launch_repack(src, d.ab_type, o.ld, dst, o.ws_ld, outer, inner, h->num_sms, st) !=
+          cudaSuccess)
+        return GEMM_ERR_CUDA;
+    } else {
+      jobs[njobs++] = CopyJob16{static_cast<const uint16_t*>(src), o.ld, dst, o.ws_ld, outer,
+                                inner};
+    }
     (which == 0 ? ta : tb) = dst;
   }
+  if (njobs > 0 && launch_copy16(jobs, njobs, h->num_sms, st) != cudaSuccess)
+    return GEMM_ERR_CUDA;
   const int64_t lda_eff = h->a.repack ? h->a.ws_ld : h->a.ld;
   const int64_t ldb_eff = h->b.repack ? h->b.ws_ld : h->b.ld;
 
@@ -764,8 +779,14 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
   // mode moves an int32 C and D that way.
   const CUtensorMap* tmd = tm[0];  // placeholder arguments when unused
   const CUtensorMap* tmc = tm[0];
+  // A TMA store writes whole 16-byte units at the right edge of the tensor
+  // (measured: a 700-column bf16 D in rows of 704 had columns 700-703
+  // written).  The 16-bit path stores the chunk that crosses such an N by
+  // rows instead (in the kernel); the int32 path of exact int8 takes TMA
+  // only when N fills whole units.
   if (h->i8x) {
-    kp.d_tma = (h->pair && kp.splits == 1 && kp.d_vec && (!C || kp.c_vec)) ? 1 : 0;
+    kp.d_tma = (h->pair && kp.splits == 1 && kp.d_vec && (!C || kp.c_vec) && h->N % 4 == 0) ? 1
+                                                                                            : 0;
     if (kp.d_tma) {
       void* dp = kp.D;
       const int64_t drs = kp.d_rs;

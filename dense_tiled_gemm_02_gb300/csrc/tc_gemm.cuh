@@ -169,25 +169,31 @@ __device__ __forceinline__ void add_c_f(const KParams& p, int r, int c0, float (
   }
 }
 
-// C of one thread's whole tile row (16-bit C, rows contiguous and 16-byte
-// aligned, tile inside N), loaded before the accumulator is ready so that
-// its latency hides under the main loop; ok = false selects the per-chunk
-// path above.
-template <int BN>
-struct CRow {
-  uint4 v[BN / 8];
-  bool ok;
-};
-
-template <int BN>
-__device__ __forceinline__ void prefetch_c_row(const KParams& p, int r, int n0, CRow<BN>& c) {
-  c.ok = p.C != nullptr && p.splits == 1 && p.c_vec && p.c_type != T_F32 && r < p.M &&
-         n0 + BN <= p.N;
-  if (!c.ok) return;
-  const uint4* src =
-      reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.C) + r * p.c_rs + n0);
+// Eight 16-bit C values of one row, columns col .. col+7 of the tile, of
+// which the first ncols lie inside N: one 16-byte load when all eight do,
+// else element loads of those inside and zeros for the rest (the row starts
+// on a 16-byte boundary, so col, a multiple of 8, does too).
+__device__ __forceinline__ uint4 ld_c8(const uint16_t* row, int col, int ncols) {
+  if (col + 8 <= ncols) return ld_global_v4_pinned(row + col);
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-  for (int i = 0; i < BN / 8; ++i) c.v[i] = ld_global_v4_pinned(src + i);
+  for (int i = 0; i < 8; ++i)
+    if (col + i < ncols) w[i >> 1] |= static_cast<uint32_t>(row[col + i]) << (16 * (i & 1));
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Stores eight 16-bit outputs at columns col .. col+7 of a row (16-byte
+// aligned at col): one 16-byte store when all lie inside N, else element
+// stores of those that do.
+__device__ __forceinline__ void st_d8(uint16_t* row, int col, int n, const uint4 x) {
+  if (col + 8 <= n) {
+    *reinterpret_cast<uint4*>(row + col) = x;
+    return;
+  }
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (col + i < n) row[col + i] = static_cast<uint16_t>(w[i >> 1] >> (16 * (i & 1)));
 }
 
 // f += the 32 prefetched C values starting at uint4 index q (8 values each).
@@ -479,17 +485,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // C of a slice as four 16-byte loads of this thread's row, two
         // slices in flight (slice c in cb[c & 1]); the loop over slices is
         // kept rolled so that its code stays in the instruction cache.
+        // In a tile that crosses N the groups past N are masked (ld_c8).
         const bool c_rows = p.splits == 1 && p.C != nullptr && p.c_vec && p.c_type != T_F32 &&
-                            r < p.M && w.n0 + BN <= p.N;
+                            r < p.M;
+        const int c_ncols = min(BN, p.N - w.n0);
         const uint16_t* crow =
             c_rows ? static_cast<const uint16_t*>(p.C) + r * p.c_rs + w.n0 : nullptr;
         uint4 cb0[4], cb1[4];
         if (c_rows) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) cb0[k] = ld_global_v4_pinned(crow + 8 * k);
+          for (int k = 0; k < 4; ++k) cb0[k] = ld_c8(crow, 8 * k, c_ncols);
           if (BN >= 64) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) cb1[k] = ld_global_v4_pinned(crow + 32 + 8 * k);
+            for (int k = 0; k < 4; ++k) cb1[k] = ld_c8(crow, 32 + 8 * k, c_ncols);
           }
         }
         const uint32_t buf = acc_it & 1u;
@@ -499,17 +507,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         tc_fence_after();
-        // Typed fast path: 16-bit D rows contiguous and 16-byte aligned, the
-        // tile inside N, C absent or of D's type read by rows.  Every slice
-        // starts with a warp-wide tcgen05.ld, so the path must be the same
-        // for all threads: it may depend on the tile, never on the thread's
-        // row (a C tile takes the typed path only when all 128 rows are
-        // inside M, where c_rows holds for every thread).
-        const bool band_inside = w.m0 + BM <= p.M;
-        const bool typed = p.splits == 1 && p.d_vec && w.n0 + BN <= p.N &&
+        // Typed fast path: 16-bit D rows contiguous and 16-byte aligned, C
+        // absent or of D's type read by rows.  Every slice starts with a
+        // warp-wide tcgen05.ld, so the path must be the same for all
+        // threads: it depends on the call only.  Ragged tiles take it too: a
+        // row past M adds no C and stores nothing, columns past N are masked.
+        const bool typed = p.splits == 1 && p.d_vec &&
                            (p.d_type == T_BF16 || p.d_type == T_F16) &&
-                           (p.C == nullptr ||
-                            (band_inside && p.c_vec && p.c_type == p.d_type));
+                           (p.C == nullptr || (p.c_vec && p.c_type == p.d_type));
         const int kind = !typed ? 0 : (p.C ? 1 : 2) + (p.d_type == T_F16 ? 2 : 0);
         auto slice = [&](const int c, uint4 (&cbuf)[4], auto ct_tag, auto dt_tag) {
           constexpr int CT = decltype(ct_tag)::value;
@@ -547,8 +552,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (c + 2 < BN / 32) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                cbuf[k] = ld_global_v4_pinned(crow + 32 * (c + 2) + 8 * k);
+              for (int k = 0; k < 4; ++k) cbuf[k] = ld_c8(crow, 32 * (c + 2) + 8 * k, c_ncols);
             }
           } else if (CT < 0) {
             add_c_f(p, r, c0, f);
@@ -556,8 +560,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if constexpr (DT < 0) {
             store_d_f(p, r, c0, f);
           } else {
-            if (r >= p.M) return;
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.D) + r * p.d_rs + c0);
+            if (r >= p.M || c0 >= p.N) return;
+            uint16_t* drow = static_cast<uint16_t*>(p.D) + r * p.d_rs;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               uint4 x;
@@ -565,7 +569,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               x.y = pack2_t<DT>(f[8 * k + 2], f[8 * k + 3]);
               x.z = pack2_t<DT>(f[8 * k + 4], f[8 * k + 5]);
               x.w = pack2_t<DT>(f[8 * k + 6], f[8 * k + 7]);
-              dst[k] = x;
+              st_d8(drow, c0 + 8 * k, p.N, x);
             }
           }
         };

@@ -68,6 +68,38 @@ constexpr uint32_t pair_smem_bytes() {
   return STAGES * PairCfg<BN, KSUB>::STAGE_BYTES + pair_stage_bytes<I8X>() + 512 + 1024;
 }
 
+// ---------------------------------------------------------------- the chunk that crosses N
+// A TMA store writes whole 16-byte units at the right edge of the tensor: a
+// D whose N is not a multiple of 8 (16-bit) but whose rows are padded to
+// one would get up to 7 elements of its padding overwritten.  The staged
+// 32 x 64 chunk that crosses N is therefore stored by the warp itself, by
+// rows: lane l takes columns 2l and 2l+1 of every row, so each warp access
+// covers 128 contiguous bytes of one row, with element masks at N.
+
+// Byte offset, in a swizzled chunk, of row i's columns 2*lane and 2*lane+1.
+__device__ __forceinline__ uint32_t chunk_off(int i, int lane) {
+  return static_cast<uint32_t>(i * 128 + (((lane >> 2) ^ (i & 7)) * 16) + (lane & 3) * 4);
+}
+
+// The warp's staged 32 x 64 D chunk to global memory at (y0, x0), masked to
+// M x N; a word store where the row's address allows it, else two halves.
+__device__ __forceinline__ void st_d_chunk_rows(const uint8_t* chunk, uint16_t* D, long long d_rs,
+                                                int y0, int x0, int M, int N, int lane) {
+  const int col = x0 + 2 * lane;
+#pragma unroll 4
+  for (int i = 0; i < 32; ++i) {
+    if (y0 + i >= M) break;
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(chunk + chunk_off(i, lane));
+    uint16_t* dst = D + static_cast<long long>(y0 + i) * d_rs + col;
+    if (col + 1 < N && (reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+      *reinterpret_cast<uint32_t*>(dst) = w;
+    } else {
+      if (col < N) dst[0] = static_cast<uint16_t>(w);
+      if (col + 1 < N) dst[1] = static_cast<uint16_t>(w >> 16);
+    }
+  }
+}
+
 // kb0/kb1 count 64-wide K slices; a stage covers KSUB of them.
 //
 // I8X: exact int8 GEMM on the bf16 tensor pipe (operands widened to bf16
@@ -431,10 +463,14 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
       const int r = w.m0 + BM * static_cast<int>(rank) + row_local;
       const bool leaves_partial = w.tail && w.part == 1;
       const bool staged_store = p.d_tma && !leaves_partial && p.splits == 1;
+      const int y0w = w.m0 + BM * static_cast<int>(rank) + 32 * q;  // the warp's first row
       // C of a slice comes as four 16-byte loads of this thread's row, issued
-      // one slice ahead (the first one before the accumulator wait).
+      // one slice ahead (the first one before the accumulator wait); in a
+      // tile that crosses N the groups past N are masked (ld_c8), and a row
+      // past M reads nothing and adds zeros.
       const bool c_rows = !leaves_partial && p.C != nullptr && p.c_vec && p.c_type != T_F32 &&
-                          r < p.M && w.n0 + BN <= p.N;
+                          r < p.M;
+      const int c_ncols = min(BN, p.N - w.n0);
       const uint16_t* crow =
           c_rows ? static_cast<const uint16_t*>(p.C) + r * p.c_rs + w.n0 : nullptr;
       // Two slices of C in flight: slice c lives in cb[c & 1] and is
@@ -490,9 +526,12 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
       uint4 cb0[4], cb1[4];
       if (c_rows) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) cb0[k] = ld_global_v4_pinned(crow + 8 * k);
+        for (int k = 0; k < 4; ++k) cb0[k] = ld_c8(crow, 8 * k, c_ncols);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) cb1[k] = ld_global_v4_pinned(crow + 32 + 8 * k);
+        for (int k = 0; k < 4; ++k) cb1[k] = ld_c8(crow, 32 + 8 * k, c_ncols);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) cb0[k] = cb1[k] = make_uint4(0u, 0u, 0u, 0u);
       }
       // The other cluster's partial, when it is read from global memory:
       // like C, two slices in flight (slice c in pb[c & 1]).
@@ -516,9 +555,9 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
       // at compile time (0: no C), -1 for the generic run-time path.
       // Once slice c's C has been added, its buffer takes slice c + 2.
       auto reload_c = [&](const int c, uint4 (&cbuf)[4]) {
-        if (c + 2 < BN / 32) {
+        if (c_rows && c + 2 < BN / 32) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) cbuf[k] = ld_global_v4_pinned(crow + 32 * (c + 2) + 8 * k);
+          for (int k = 0; k < 4; ++k) cbuf[k] = ld_c8(crow, 32 * (c + 2) + 8 * k, c_ncols);
         }
       };
       auto slice = [&](const int c, uint4 (&cbuf)[4], float4 (&pbuf)[8], auto ct_tag,
@@ -622,23 +661,30 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
           *reinterpret_cast<uint4*>(stage + row_local * 128 + unit * 16) = x;
         }
         if (h == 1) {
-          fence_proxy_async_smem();
-          __syncwarp();
-          const int x0 = w.n0 + 32 * (c - 1), y0 = w.m0 + BM * static_cast<int>(rank) + 32 * q;
-          if (lane == 0 && x0 < p.N && y0 < p.M)  // boxes entirely outside D are skipped
-            tma_store_2d(&tmD, smem_u32(stage + q * 32 * 128), x0, y0);
-          if (lane == 0) bulk_commit();
+          const int x0 = w.n0 + 32 * (c - 1);
+          if (x0 + 64 <= p.N || (p.N & 7) == 0) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && x0 < p.N && y0w < p.M)  // boxes entirely outside D are skipped
+              tma_store_2d(&tmD, smem_u32(stage + q * 32 * 128), x0, y0w);
+            if (lane == 0) bulk_commit();
+          } else {
+            __syncwarp();
+            st_d_chunk_rows(stage + q * 32 * 128, static_cast<uint16_t*>(p.D), p.d_rs, y0w, x0,
+                            p.M, p.N, lane);
+            __syncwarp();  // read out before the buffer takes a later chunk
+          }
           ++staged;
         }
       };
       // Typed paths: staged 16-bit D with C of the same type read by rows,
       // or no C; everything else takes the generic path.  The choice must be
-      // the same for all 128 threads (the slices hold warp-wide barriers), so
-      // it only depends on the CTA's row band lying inside M.
-      const bool band_inside = w.m0 + BM * static_cast<int>(rank) + BM <= p.M;
-      const bool c_typed = p.C != nullptr && p.c_vec && p.c_type == p.d_type &&
-                           w.n0 + BN <= p.N && band_inside;
-      const bool typed = staged_store && p.splits == 1 && (p.C == nullptr || c_typed);
+      // the same for all 128 threads (the slices hold warp-wide barriers):
+      // it depends on the call only, and ragged tiles take it too (their C
+      // loads are masked; D is clipped at M by the TMA store and at N by the
+      // TMA store or, for the chunk that crosses an N off 16 bytes, by rows).
+      const bool c_typed = p.C != nullptr && p.c_vec && p.c_type == p.d_type;
+      const bool typed = staged_store && (p.C == nullptr || c_typed);
       const int kind = !typed ? 0 : (p.C ? 1 : 2) + (p.d_type == T_F16 ? 2 : 0);
 #pragma unroll 1
       for (int c = 0; c < BN / 32; c += 2) {

@@ -100,6 +100,22 @@ int decode_columns_per_block();
 // Resident blocks of the decode kernel per SM for M rows and slices of kc.
 int decode_blocks_per_sm(int M, int kc);
 
+// Copies of 16-bit rows between buffers of any 2-byte alignment (rows x
+// cols elements, row strides in elements); up to kMaxCopyJobs in one
+// launch.  Jobs with no elements are skipped.
+constexpr int kMaxCopyJobs = 3;
+struct CopyJob16 {
+  const uint16_t* src;
+  long long ld_src;
+  uint16_t* dst;
+  long long ld_dst;
+  long long rows, cols;
+};
+struct CopyJobs16 {
+  CopyJob16 job[kMaxCopyJobs];
+};
+cudaError_t launch_copy16(const CopyJob16* jobs, int n, int num_sms, cudaStream_t st);
+
 // 16-bit rows from a 16-byte aligned workspace (ld_src a multiple of 8
 // elements) to a destination of any 2-byte alignment.
 cudaError_t launch_copy_out16(const uint16_t* src, long long ld_src, uint16_t* dst,

@@ -87,9 +87,10 @@ typedef void* gemm_stream_t;
  * keyed on (M, N, K, types, layouts), and allocate on the current device the
  * workspace and the device status word that the plan needs.  The workspace
  * holds copies of operands whose rows the TMA unit cannot read in place
- * (rows not 16-byte aligned, or int8 widened to bf16), aligned copies of
- * 16-bit C and D with unaligned rows (C is copied in and D copied out by
- * extra kernels of gemm_run), split-K partial sums and last-wave partials.
+ * (rows not 16-byte aligned, or int8 widened to bf16; copy rows start on
+ * 128-byte lines), aligned copies of 16-bit C and D with unaligned rows (C
+ * is copied in and D copied out by extra kernels of gemm_run), split-K
+ * partial sums and last-wave partials.
  *   out:  receives the handle (untouched on failure).
  * Returns GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED,
  * GEMM_ERR_NO_DEVICE, GEMM_ERR_ALLOC_FAILED or GEMM_ERR_CUDA.

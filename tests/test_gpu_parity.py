@@ -108,7 +108,7 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("plan", [None, "pair=1", "pair=1,ksub=2"])
+@pytest.mark.parametrize("plan", [None, "pair=1,bn=256", "pair=1,bn=128", "pair=1,bn=256,ksub=2"])
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"{s[0]}x{s[1]}x{s[2]}-{s[3]}{s[4]}{s[5]}{s[6]}"
                                                for s in SHAPES])
 def test_ragged_shapes(shape, plan):
@@ -119,8 +119,8 @@ def test_ragged_shapes(shape, plan):
     _assert_ok(check_rows(w, inp, D), f"{shape} [{p}]")
 
 
-@pytest.mark.parametrize("plan", [None, "pair=0", "pair=1,bn=128"])
-def test_unaligned_c_d_staged_and_aliased(plan):
+@pytest.mark.parametrize("plan", [None, "pair=0", "pair=1,bn=256", "pair=1,bn=128", "pair=1,bn=256,ksub=2"])
+def test_unaligned_c_d_rows_and_aliased(plan):
     """16-bit C and D rows that are not 16-byte aligned go through aligned
     workspace copies (stage_c / stage_d in the plan); D may alias C there."""
     M, N, K = 390, 301, 200
@@ -136,6 +136,93 @@ def test_unaligned_c_d_staged_and_aliased(plan):
     assert g.status() == pkg.GEMM_OK
     g.close()
     _assert_ok(check_rows(w, inp, CD.cpu()), f"aliased [{plan_str}]")
+
+
+def _placed(t: torch.Tensor, ld: int, off: int, fill: float) -> tuple[torch.Tensor, torch.Tensor]:
+    """A device view of the rows x cols tensor t at column offset off of a
+    (rows + 2) x ld buffer filled with `fill` (row 0 and the last row are
+    guard rows); returns (view, buffer)."""
+    rows, cols = t.shape
+    buf = torch.full((rows + 2, ld), fill, dtype=t.dtype, device="cuda")
+    view = buf[1:1 + rows, off:off + cols]
+    view.copy_(t.cuda())
+    return view, buf
+
+
+# (M, N, K, type, C (ld, offset) or None, D (ld, offset)): rows off 16 bytes
+# through the stride (odd ld) or the base (offset 1 with an aligned ld), for
+# C alone, D alone and both, and aligned rows padded past an N that is not
+# a multiple of 8; ragged tiles in M and N.
+ROWS_CASES = [
+    (600, 700, 300, BF16, (701, 0), (704, 0)),      # C rows off, D by TMA
+    (600, 700, 300, BF16, (704, 0), (703, 0)),      # C by vectors, D rows off
+    (600, 700, 300, F16, (705, 3), (709, 5)),       # both off, f16
+    (513, 515, 130, BF16, (528, 1), (528, 1)),      # aligned ld, base off by one element
+    (520, 300, 64, F16, None, (301, 0)),            # no C, D rows off
+    (257, 1000, 520, BF16, (1001, 0), (1001, 0)),   # stream-K tail, both off
+]
+
+
+@pytest.mark.parametrize("plan", ["pair=1,bn=256", "pair=1,bn=128", "pair=1,bn=256,tail=1,grid=8"])
+@pytest.mark.parametrize("case", ROWS_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}-{i}"
+                                                  for i, c in enumerate(ROWS_CASES)])
+def test_pair_c_d_placements(case, plan):
+    """C and D placed in padded buffers, rows aligned or not: every element
+    against the oracle, and nothing written outside D's view (the pair
+    kernel's TMA store, its by-rows store of the chunk crossing N, and the
+    staged copies)."""
+    M, N, K, t, cspec, dspec = case
+    w = Workload("rows", 12, M, N, K, t, t if cspec else None, t, "normal")
+    inp = make_inputs(w, seed_offset=M + N)
+    A, B = inp["A"].cuda(), inp["B"].cuda()
+    C = None
+    if cspec:
+        C, _ = _placed(inp["C"], cspec[0], cspec[1], 0.0)
+    D, dbuf = _placed(torch.zeros(M, N, dtype=TORCH_DTYPE[t]), dspec[0], dspec[1], 768.0)
+    dbuf.fill_(768.0)  # exact in bf16 and fp16
+    with forced_plan(plan):
+        g = pkg.Gemm.like(A, B, C, D)
+    plan_str = g.plan()
+    assert "pair=1" in plan_str, plan_str
+    g.run(A, B, C, D)
+    assert g.status() == pkg.GEMM_OK
+    g.close()
+    host = dbuf.cpu()
+    mask = torch.ones_like(host, dtype=torch.bool)
+    mask[1:1 + M, dspec[1]:dspec[1] + N] = False
+    assert torch.all(host[mask] == 768.0), f"write outside D [{plan_str}]"
+    _assert_ok(check_rows(w, inp, D.cpu().contiguous()), f"{case} [{plan_str}]")
+
+
+@pytest.mark.parametrize("plan", [None, "pair=0,bn=128", "pair=0,bn=64", "pair=1,bn=256",
+                                  "pair=1,bn=128"])
+@pytest.mark.parametrize("lb", [ROW, COL], ids=["Brow", "Bcol"])
+def test_padding_never_read_or_written(plan, lb):
+    """Operands read in place (rows 16-byte aligned) whose rows are padded
+    past K or N with NaN: the padding must not reach D (the TMA loads and the
+    C loads stop at K and N), and D's own padding past N keeps its sentinel."""
+    M, N, K = 300, 260, 203  # K and N not multiples of 8; leading dimensions are
+    w = Workload("pad", 13, M, N, K, BF16, BF16, BF16, "normal", ROW, lb)
+    inp = make_inputs(w)
+    nan = float("nan")
+    A, _ = _placed(inp["A"], 208, 0, nan)
+    Bs, _ = _placed(inp["B"], 208 if lb == COL else 264, 0, nan)
+    B = Bs.t() if lb == COL else Bs
+    C, _ = _placed(inp["C"], 264, 0, nan)
+    D, dbuf = _placed(torch.zeros(M, N, dtype=torch.bfloat16), 264, 0, 768.0)
+    dbuf.fill_(768.0)
+    with forced_plan(plan):
+        g = pkg.Gemm.like(A, B, C, D)
+    plan_str = g.plan()
+    assert "repack_a=0" in plan_str and "repack_b=0" in plan_str, plan_str
+    g.run(A, B, C, D)
+    assert g.status() == pkg.GEMM_OK
+    g.close()
+    host = dbuf.cpu()
+    mask = torch.ones_like(host, dtype=torch.bool)
+    mask[1:1 + M, :N] = False
+    assert torch.all(host[mask] == 768.0), f"write outside D [{plan_str}]"
+    _assert_ok(check_rows(w, inp, D.cpu().contiguous()), f"padded [{plan_str}]")
 
 
 def test_k_zero_gives_c():
