@@ -93,8 +93,9 @@ def load_peaks():
 # and the host planner that picks its launch); a profile's figures stand only
 # while these files are unchanged.
 KERNEL_SOURCES = {
-    "pair": ("common.h", "ptx.cuh", "tc_gemm2.cuh", "tc_pair_launch.cu", "tc_launch.h",
-             "gemm_host.cu", "plan_table.h"),
+    # tc_gemm2.cuh includes tc_gemm.cuh (epilogue helpers)
+    "pair": ("common.h", "ptx.cuh", "tc_gemm.cuh", "tc_gemm2.cuh", "tc_pair_launch.cu",
+             "tc_launch.h", "gemm_host.cu", "plan_table.h"),
     "cta1": ("common.h", "ptx.cuh", "tc_gemm.cuh", "tc_launch.cu", "tc_launch.h",
              "gemm_host.cu", "plan_table.h"),
     "decode": ("common.h", "ptx.cuh", "decode.cu", "tc_launch.h", "gemm_host.cu",
