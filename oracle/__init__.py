@@ -12,11 +12,12 @@ compiler and exposes it through ctypes over numpy arrays:
   plus the sum of absolute products used by the error bound.
 * ``gemm_i64_rows`` / ``gemm_i64_points``: int8 operands, int32 C, int64 sum.
 * ``round_bits`` / ``widen_bits``: one correct round-to-nearest-even from fp64
-  to fp16/bf16, and the exact inverse widening.
+  to fp16/bf16, and the exact inverse widening; ``widen_bits8`` the exact
+  widening of the 8-bit float encodings.
 
-Type codes: 1 fp16, 2 bf16, 3 fp32, 4 int8, 5 int32.  Layout flags: 0 row-
-major, 1 column-major.  fp16/bf16 arrays are passed as their uint16 bit
-patterns.
+Type codes: 1 fp16, 2 bf16, 3 fp32, 4 int8, 5 int32, 6 E4M3, 7 E5M2 (OCP
+OFP8).  Layout flags: 0 row-major, 1 column-major.  fp16/bf16 arrays are
+passed as their uint16 bit patterns, E4M3/E5M2 arrays as uint8 patterns.
 """
 from __future__ import annotations
 
@@ -27,7 +28,7 @@ import tempfile
 
 import numpy as np
 
-F16, BF16, F32, I8, I32 = 1, 2, 3, 4, 5
+F16, BF16, F32, I8, I32, E4M3, E5M2 = 1, 2, 3, 4, 5, 6, 7
 ROW, COL = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -77,6 +78,7 @@ class Oracle:
         self.path = path
         self._lib = lib
         lib.oracle_widen.argtypes = [_vp, _i64, _int, _vp]
+        lib.oracle_widen8.argtypes = [_vp, _i64, _int, _vp]
         lib.oracle_round.argtypes = [_vp, _i64, _int, _vp]
         lib.oracle_threads.argtypes = []
         lib.oracle_gemm_f64_rows.argtypes = [_i64, _i64, _i64, _int, _int, _int, _int, _int,
@@ -103,6 +105,13 @@ class Oracle:
         bits = np.ascontiguousarray(bits, dtype=np.uint16)
         out = np.empty(bits.shape, dtype=np.float64)
         if self._lib.oracle_widen(_ptr(bits), bits.size, t, _ptr(out)) != 0:
+            raise ValueError("bad type")
+        return out
+
+    def widen_bits8(self, bits, t: int) -> np.ndarray:
+        bits = np.ascontiguousarray(bits, dtype=np.uint8)
+        out = np.empty(bits.shape, dtype=np.float64)
+        if self._lib.oracle_widen8(_ptr(bits), bits.size, t, _ptr(out)) != 0:
             raise ValueError("bad type")
         return out
 

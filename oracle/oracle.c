@@ -20,6 +20,14 @@
  *
  * Floating point: fp16/bf16 operands are widened exactly to fp64 and the
  * whole sum is formed in fp64 (every fp16/bf16 product is exact in fp64).
+ * The same holds for the two 8-bit float operand types, E4M3 and E5M2: the
+ * pages name a scaled low-precision matrix product (mfma_scaled) as the
+ * next data type without defining the encodings, so the encodings are the
+ * ones of the OCP 8-bit floating point specification (OFP8): E4M3 has 4
+ * exponent bits (bias 7) and 3 fraction bits, no infinities, and only the
+ * all-ones pattern S.1111.111 is NaN (largest finite 448); E5M2 has 5
+ * exponent bits (bias 15) and 2 fraction bits with IEEE 754 infinities and
+ * NaNs (largest finite 57344).
  * Integer: int8 operands, int32 C, and the sum is formed in int64 (exact).
  *
  * Indexing follows the storage order of each operand.  Row-major X[r,c] is
@@ -48,6 +56,8 @@
 #define OR_F32 3
 #define OR_I8 4
 #define OR_I32 5
+#define OR_E4M3 6
+#define OR_E5M2 7
 
 /* Fault-planting hook for the oracle's own self-tests: a build with
  * -DORACLE_MUTANT=n plants one plausible mistake so that the tests can show
@@ -57,24 +67,35 @@
  *   4: last k dropped       5: rounding ties away from zero
  *   6: integer sum starts at k = 1
  *   7: subnormal scale off by a factor of two in the widening
- *   8: A's k index reversed (A[i, K-1-k] paired with B[k, j]) */
+ *   8: A's k index reversed (A[i, K-1-k] paired with B[k, j])
+ *   9: E4M3 read with IEEE specials (exponent field 15 as inf / NaN) */
 #ifndef ORACLE_MUTANT
 #define ORACLE_MUTANT 0
 #endif
 
 /* ---------------------------------------------------------------------------
- * Binary16 and bfloat16 encodings.
+ * Binary16, bfloat16 and the two OFP8 encodings.
  *   binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits.
  *   bfloat16: 1 sign, 8 exponent (bias 127), 7 fraction bits.
+ *   E5M2:     1 sign, 5 exponent (bias 15), 2 fraction bits, IEEE specials.
+ *   E4M3:     1 sign, 4 exponent (bias 7), 3 fraction bits; the all-ones
+ *             exponent holds normal numbers except S.1111.111 (NaN).
  * ------------------------------------------------------------------------- */
 typedef struct {
   int frac_bits; /* stored fraction bits */
   int exp_bits;
   int bias;
+  int ieee_specials; /* all-ones exponent = inf (fraction 0) or NaN */
 } or_format;
 
-static const or_format FMT_F16 = {10, 5, 15};
-static const or_format FMT_BF16 = {7, 8, 127};
+static const or_format FMT_F16 = {10, 5, 15, 1};
+static const or_format FMT_BF16 = {7, 8, 127, 1};
+static const or_format FMT_E5M2 = {2, 5, 15, 1};
+#if ORACLE_MUTANT == 9
+static const or_format FMT_E4M3 = {3, 4, 7, 1};
+#else
+static const or_format FMT_E4M3 = {3, 4, 7, 0};
+#endif
 
 /* Exact value of an encoding. */
 static double widen_bits(uint32_t bits, or_format f) {
@@ -84,8 +105,10 @@ static double widen_bits(uint32_t bits, or_format f) {
   const uint32_t e = (bits >> f.frac_bits) & exp_mask;
   const int neg = (int)((bits >> (f.frac_bits + f.exp_bits)) & 1u);
   double v;
-  if (e == exp_mask) {
+  if (e == exp_mask && f.ieee_specials) {
     v = frac ? NAN : INFINITY;
+  } else if (e == exp_mask && frac == frac_mask) {
+    v = NAN; /* E4M3: the only NaN pattern; no infinities */
   } else if (e == 0) {
     /* subnormal: frac * 2^(1 - bias - frac_bits) */
 #if ORACLE_MUTANT == 7
@@ -152,6 +175,14 @@ int oracle_widen(const uint16_t* bits, int64_t n, int t, double* out) {
   return 0;
 }
 
+/* Exported: exact widening of n 8-bit float encodings (OR_E4M3/OR_E5M2). */
+int oracle_widen8(const uint8_t* bits, int64_t n, int t, double* out) {
+  if (t != OR_E4M3 && t != OR_E5M2) return -1;
+  const or_format f = (t == OR_E4M3) ? FMT_E4M3 : FMT_E5M2;
+  for (int64_t i = 0; i < n; ++i) out[i] = widen_bits(bits[i], f);
+  return 0;
+}
+
 /* Exported: one round-to-nearest-even of each fp64 value to type t. */
 int oracle_round(const double* x, int64_t n, int t, uint16_t* out_bits) {
   if (t != OR_F16 && t != OR_BF16) return -1;
@@ -192,6 +223,8 @@ static double load_f(const void* base, int t, int64_t idx) {
     case OR_F16: return widen_bits(((const uint16_t*)base)[idx], FMT_F16);
     case OR_BF16: return widen_bits(((const uint16_t*)base)[idx], FMT_BF16);
     case OR_F32: return (double)((const float*)base)[idx];
+    case OR_E4M3: return widen_bits(((const uint8_t*)base)[idx], FMT_E4M3);
+    case OR_E5M2: return widen_bits(((const uint8_t*)base)[idx], FMT_E5M2);
     default: return NAN;
   }
 }
@@ -216,7 +249,8 @@ static int64_t k_end(int64_t K) {
 }
 
 static int fp_types_ok(int ab_type, int c_type, const void* C) {
-  if (ab_type != OR_F16 && ab_type != OR_BF16) return 0;
+  if (ab_type != OR_F16 && ab_type != OR_BF16 && ab_type != OR_E4M3 && ab_type != OR_E5M2)
+    return 0;
   if (C && c_type != OR_F16 && c_type != OR_BF16 && c_type != OR_F32) return 0;
   return 1;
 }

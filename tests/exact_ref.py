@@ -4,7 +4,8 @@ Pure Python over ``fractions.Fraction``; it shares nothing with the C oracle:
 
 * decoding uses the standard library's IEEE binary16 codec (``struct`` 'e')
   and, for bfloat16, the binary32 codec on the bits shifted into the upper
-  half of a float;
+  half of a float; the 8-bit float types (E4M3, E5M2) are decoded by
+  torch's own float8 dtypes;
 * rounding to fp16/bf16 is a nearest-neighbour search over the sorted table
   of every non-negative encoding (ties go to the even encoding; the encoding
   after the largest finite value is infinity, with value 2^(emax+1), which
@@ -18,7 +19,13 @@ import struct
 from fractions import Fraction
 from functools import lru_cache
 
-F16, BF16, F32 = 1, 2, 3
+F16, BF16, F32, E4M3, E5M2 = 1, 2, 3, 6, 7
+
+
+def _decode8(bits: int, t: int) -> float:
+    import torch
+    dt = torch.float8_e4m3fn if t == E4M3 else torch.float8_e5m2
+    return float(torch.tensor([bits], dtype=torch.uint8).view(dt).float()[0])
 
 
 def decode(bits: int, t: int) -> Fraction | float:
@@ -26,6 +33,8 @@ def decode(bits: int, t: int) -> Fraction | float:
         v = struct.unpack("<e", struct.pack("<H", bits))[0]
     elif t == BF16:
         v = struct.unpack("<f", struct.pack("<I", bits << 16))[0]
+    elif t in (E4M3, E5M2):
+        v = _decode8(bits, t)
     else:
         raise ValueError(t)
     if v != v or v in (float("inf"), float("-inf")):

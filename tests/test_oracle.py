@@ -7,13 +7,16 @@ least one pin fails for every mistake.
 
 What pins what:
 * widening: the standard library's / numpy's IEEE binary16 and binary32
-  decoders, over all 65536 encodings;
+  decoders, over all 65536 encodings; torch's float8 dtypes over all 256
+  E4M3 and E5M2 encodings, and the OFP8 specification's named values;
 * rounding: every midpoint between neighbouring fp16/bf16 values (ties to
   even) and one double either side, numpy's float64->float16 conversion,
   torch's float32->bfloat16 conversion, and an exact rational search;
 * the GEMM: an exact rational evaluation of the definition on every shape in
   {1,2,3}^3 and every layout, closed forms (identity, permutation, rank-1,
-  all-ones, linearity), and torch's CPU int64 matmul for int8.
+  all-ones, linearity), and torch's CPU int64 matmul for int8; for the
+  8-bit float types, the exact rational evaluation on tiny shapes and the
+  identity and all-ones closed forms.
 """
 from __future__ import annotations
 
@@ -29,7 +32,7 @@ import torch
 
 import exact_ref
 import oracle
-from oracle import BF16, F16, F32
+from oracle import BF16, E4M3, E5M2, F16, F32
 
 INF_BITS = {F16: 0x7C00, BF16: 0x7F80}
 EMAX1 = {F16: 16, BF16: 128}
@@ -64,6 +67,79 @@ def pin_widen_exhaustive(orc):
         got = orc.widen_bits(allb, t)
         same = (got == ref) | (np.isnan(got) & np.isnan(ref))
         assert same.all(), f"widen type {t}: first bad encoding {np.argmax(~same):#06x}"
+
+
+# 8-bit floats (OCP OFP8): torch's float8 dtypes decode every encoding, and
+# the specification's named values are checked by their closed forms.
+FP8_TORCH = {E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
+
+
+def fp8_bits(x, t) -> np.ndarray:
+    """Encodings of values exactly representable in the 8-bit type t."""
+    xt = torch.as_tensor(np.asarray(x, dtype=np.float32))
+    b = xt.to(FP8_TORCH[t])
+    assert torch.equal(b.float(), xt), "value not representable"
+    return b.view(torch.uint8).numpy()
+
+
+def pin_widen_fp8(orc):
+    allb = np.arange(256, dtype=np.uint8)
+    for t, dt in FP8_TORCH.items():
+        ref = torch.from_numpy(allb).view(dt).to(torch.float64).numpy()
+        got = orc.widen_bits8(allb, t)
+        same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+        assert same.all(), f"widen type {t}: first bad encoding {np.argmax(~same):#04x}"
+    e4 = orc.widen_bits8(np.array([0x7E, 0x7F, 0xFE, 0x01, 0x08, 0x38, 0x78], np.uint8), E4M3)
+    assert e4[0] == 448.0 and np.isnan(e4[1]) and e4[2] == -448.0
+    assert e4[3] == 2.0 ** -9 and e4[4] == 2.0 ** -6 and e4[5] == 1.0 and e4[6] == 256.0
+    e5 = orc.widen_bits8(np.array([0x7B, 0x7C, 0x7D, 0x01, 0x04, 0x3C], np.uint8), E5M2)
+    assert e5[0] == 57344.0 and e5[1] == np.inf and np.isnan(e5[2])
+    assert e5[3] == 2.0 ** -16 and e5[4] == 2.0 ** -14 and e5[5] == 1.0
+
+
+def _rand_fp8(rng, shape, t):
+    """Random finite encodings of t (normal and subnormal alike) and their
+    values as decoded by torch."""
+    codes = rng.integers(0, 256, size=shape).astype(np.uint8)
+    vals = torch.from_numpy(codes).view(FP8_TORCH[t]).to(torch.float64).numpy()
+    # finite, and |v| < 2^8, so that the exact sums of the tiny shapes below
+    # still fit fp64's 53 bits (the test compares for equality)
+    bad = ~np.isfinite(vals) | (np.abs(vals) >= 256.0)
+    codes[bad] = codes[bad] & 0x83  # exponent field cleared: a finite (subnormal) code
+    vals = torch.from_numpy(codes).view(FP8_TORCH[t]).to(torch.float64).numpy()
+    assert np.isfinite(vals).all()
+    return vals, codes
+
+
+def pin_fp8_gemm(orc):
+    rng = np.random.default_rng(17)
+    for t in (E4M3, E5M2):
+        for (M, N, K), (a_col, b_col) in itertools.product(
+                [(1, 1, 1), (2, 3, 1), (3, 2, 5), (4, 4, 17)], itertools.product((0, 1), repeat=2)):
+            A, Ab = _rand_fp8(rng, (M, K), t)
+            B, Bb = _rand_fp8(rng, (K, N), t)
+            C = (rng.integers(-64, 64, size=(M, N)) / 16).astype(np.float32)
+            D, S = orc.gemm_f64_rows(M, N, K, to_storage(Ab, a_col), to_storage(Bb, b_col), C,
+                                     ab_type=t, c_type=F32, a_col=a_col, b_col=b_col)
+            Af = [[exact_ref.decode(int(v), t) for v in r] for r in Ab]
+            Bf = [[exact_ref.decode(int(v), t) for v in r] for r in Bb]
+            Cf = [[Fraction(float(v)) for v in r] for r in C]
+            ex = exact_ref.exact_gemm(Af, Bf, Cf)
+            for i in range(M):
+                for j in range(N):
+                    assert Fraction(float(D[i, j])) == ex[i][j], (t, M, N, K, i, j)
+                    assert Fraction(float(S[i, j])) == sum(abs(Af[i][k] * Bf[k][j])
+                                                           for k in range(K))
+        # identity: D = B + C; all ones: D = K + C
+        n, N = 24, 20
+        B, Bb = _rand_fp8(rng, (n, N), t)
+        C = rng.standard_normal((n, N)).astype(np.float32)
+        D, _ = orc.gemm_f64_rows(n, N, n, fp8_bits(np.eye(n), t), Bb, C, ab_type=t, c_type=F32)
+        assert np.array_equal(D, B + C.astype(np.float64))
+        for K in (1, 9, 300):
+            D, S = orc.gemm_f64_rows(3, 2, K, fp8_bits(np.ones((3, K)), t),
+                                     fp8_bits(np.ones((K, 2)), t), None, ab_type=t)
+            assert np.all(D == K) and np.all(S == K)
 
 
 # ----------------------------------------------------------------------------- rounding
@@ -267,7 +343,8 @@ def pin_int8(orc):
 
 
 PINS = [pin_widen_exhaustive, pin_round_midpoints, pin_round_vs_libraries, pin_round_vs_exact,
-        pin_brute_force_tiny, pin_closed_forms, pin_views_agree, pin_int8]
+        pin_brute_force_tiny, pin_closed_forms, pin_views_agree, pin_int8, pin_widen_fp8,
+        pin_fp8_gemm]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -288,7 +365,7 @@ def test_oracle_threads(orc):
     assert orc.threads() >= 1
 
 
-@pytest.mark.parametrize("mutant", range(1, 9))
+@pytest.mark.parametrize("mutant", range(1, 10))
 def test_pins_catch_planted_mistakes(mutant):
     with tempfile.TemporaryDirectory() as d:
         path = oracle.compile_library(os.path.join(d, f"liboracle_m{mutant}.so"), mutant=mutant)
