@@ -20,6 +20,7 @@ import os
 from . import build as _build
 
 GEMM_F16, GEMM_BF16, GEMM_F32, GEMM_I8, GEMM_I32 = 1, 2, 3, 4, 5
+GEMM_E4M3, GEMM_E5M2 = 6, 7  # OCP OFP8 8-bit float operands
 GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
 GEMM_OK = 0
 GEMM_ERR_INVALID_ARG = -1
@@ -185,7 +186,8 @@ def gemm_run_splitk_noalloc(desc: GemmDesc, splits: int, A: int, B: int, C: int 
 def _torch_type(dtype) -> int:
     import torch
     return {torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16, torch.float32: GEMM_F32,
-            torch.int8: GEMM_I8, torch.int32: GEMM_I32}[dtype]
+            torch.int8: GEMM_I8, torch.int32: GEMM_I32, torch.float8_e4m3fn: GEMM_E4M3,
+            torch.float8_e5m2: GEMM_E5M2}[dtype]
 
 
 def layout_of(t) -> tuple[int, int]:

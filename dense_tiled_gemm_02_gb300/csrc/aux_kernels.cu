@@ -182,6 +182,31 @@ __global__ void copy_rows16_kernel(const CopyJobs16 jobs) {
   }
 }
 
+// 8-bit rows (8-bit float operands) copied into the aligned workspace, the
+// 16-bit kernel's pattern with bytes.
+__global__ void copy_rows8_kernel(const uint8_t* __restrict__ src, long long ld_src,
+                                  uint8_t* __restrict__ dst, long long ld_dst, long long rows,
+                                  long long cols) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int EPT = 2 * kCopyEpt;
+  const long long base = static_cast<long long>(blockIdx.x) * blockDim.x * EPT + threadIdx.x;
+  if (base >= cols) return;
+  for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
+    uint8_t v[EPT];
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+      const long long c = base + static_cast<long long>(k) * blockDim.x;
+      if (c < cols) v[k] = src[r * ld_src + c];
+    }
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+      const long long c = base + static_cast<long long>(k) * blockDim.x;
+      if (c < cols) dst[r * ld_dst + c] = v[k];
+    }
+  }
+}
+
 // int8 -> bf16 widening, 4 elements per thread (rows whose starts and
 // lengths are multiples of 4 elements), four rows per step.
 __global__ void widen_i8_x4_kernel(const char4* __restrict__ src, long long ld_src4,
@@ -259,6 +284,11 @@ cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint1
     return launch_pdl(widen_i8_x4_kernel, copy_grid(cols / 4, rows, num_sms), dim3(256), 0, st,
                       static_cast<const char4*>(src), ld_src / 4, reinterpret_cast<uint2*>(dst),
                       ld_dst / 4, rows, cols / 4);
+  if (src_type == T_E4M3 || src_type == T_E5M2) {  // bytes into a byte workspace
+    const dim3 g = copy_rows_grid(rows, (cols + 1) / 2, num_sms, 1);
+    return launch_pdl(copy_rows8_kernel, g, dim3(256), 0, st, static_cast<const uint8_t*>(src),
+                      ld_src, reinterpret_cast<uint8_t*>(dst), ld_dst, rows, cols);
+  }
   if (src_type != T_I8) {
     const CopyJob16 j{static_cast<const uint16_t*>(src), ld_src, dst, ld_dst, rows, cols};
     return launch_copy16(&j, 1, num_sms, st);

@@ -12,7 +12,7 @@
 namespace gb300 {
 
 // Element type codes (the values of gemm_dtype_t).
-enum : int { T_F16 = 1, T_BF16 = 2, T_F32 = 3, T_I8 = 4, T_I32 = 5 };
+enum : int { T_F16 = 1, T_BF16 = 2, T_F32 = 3, T_I8 = 4, T_I32 = 5, T_E4M3 = 6, T_E5M2 = 7 };
 
 // Tile geometry of the tcgen05 kernels: one CTA owns a BM x BN output tile
 // and walks K in BK-wide slices (BK 16-bit elements = one 128-byte row).
@@ -35,6 +35,7 @@ struct KParams {
   int kb_per_chunk;              // k-blocks accumulated in one TMEM pass (exact-int8 mode)
   int a_mn, b_mn;                // operand majors: 0 = K-major, 1 = MN-major
   uint32_t idesc;                // tcgen05 instruction descriptor
+  int f8;                        // 8-bit float operands: kind::f8f6f4, 128 K a slice
   // epilogue (internal coordinates: row r < M, column c < N)
   const void* C;
   int c_type;
@@ -64,10 +65,11 @@ struct KParams {
   uint32_t epoch;                // value the flags take during this run
 };
 
-// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator
-// (bits 4-5 = 1), A/B element type (bits 7-9, 10-12: 0 fp16, 1 bf16),
-// operand majors (bit 15 A, bit 16 B: 0 K-major, 1 MN-major), N/8 in bits
-// 17-22 and M/16 in bits 24-28.
+// Instruction descriptor of tcgen05.mma kind::f16 and kind::f8f6f4: fp32
+// accumulator (bits 4-5 = 1), A/B element type (bits 7-9, 10-12: 0 fp16,
+// 1 bf16 for kind::f16; 0 E4M3, 1 E5M2 for kind::f8f6f4), operand majors
+// (bit 15 A, bit 16 B: 0 K-major, 1 MN-major), N/8 in bits 17-22 and M/16
+// in bits 24-28.
 GB_HD constexpr uint32_t idesc_f16(uint32_t bf16, uint32_t a_mn, uint32_t b_mn,
                                                  uint32_t m, uint32_t n) {
   return (1u << 4) | (bf16 << 7) | (bf16 << 10) | (a_mn << 15) | (b_mn << 16) |

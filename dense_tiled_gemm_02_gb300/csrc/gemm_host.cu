@@ -29,12 +29,15 @@ int elem_size(int t) {
     case T_BF16: return 2;
     case T_F32:
     case T_I32: return 4;
-    case T_I8: return 1;
+    case T_I8:
+    case T_E4M3:
+    case T_E5M2: return 1;
     default: return 0;
   }
 }
 
 bool is_f16ish(int t) { return t == T_F16 || t == T_BF16; }
+bool is_f8(int t) { return t == T_E4M3 || t == T_E5M2; }
 
 // One operand as the kernel sees it: storage pointer (user's or workspace),
 // storage layout and leading dimension, logical rows x cols.
@@ -91,6 +94,7 @@ struct gemm_plan {
   const TcVariant* variant = nullptr;
   const PairVariant* pair = nullptr;  // set when the CTA-pair kernel runs the plan
   bool i8x = false;
+  bool f8 = false;              // 8-bit float operands (kind::f8f6f4, K-major)
   int mab_type = T_BF16;        // type the tensor cores read (bf16 for int8 input)
   int64_t M = 0, N = 0, K = 0;  // internal problem
   Operand a{}, b{};
@@ -150,6 +154,11 @@ int validate(const gemm_desc_t& d) {
     if (!(is_f16ish(c) || c == T_F32 || c == 0)) return GEMM_ERR_UNSUPPORTED;
   } else if (ab == T_I8) {
     if (o != T_I32 || !(c == T_I32 || c == 0)) return GEMM_ERR_UNSUPPORTED;
+  } else if (is_f8(ab)) {
+    // 8-bit float operands, read K-major only (A row-major, B column-major)
+    if (!(is_f16ish(o) || o == T_F32)) return GEMM_ERR_UNSUPPORTED;
+    if (!(is_f16ish(c) || c == T_F32 || c == 0)) return GEMM_ERR_UNSUPPORTED;
+    if (d.layout_a != GEMM_ROW_MAJOR || d.layout_b != GEMM_COL_MAJOR) return GEMM_ERR_UNSUPPORTED;
   } else {
     return GEMM_ERR_UNSUPPORTED;
   }
@@ -273,12 +282,13 @@ int plan_decode(gemm_plan* h, int sms) {
   return GEMM_OK;
 }
 
-// Build the tiled tensor map of an internal operand (16-bit elements).
-// K-major storage: dims {K, rows}, box {BK, box_rows}; MN-major storage:
-// dims {MN, K}, box {64, BK}; 128-byte swizzle; reads outside the tensor
-// return zeros.
+// Build the tiled tensor map of an internal operand (es-byte elements: 2,
+// or 1 for 8-bit floats, which are K-major only).  K-major storage: dims
+// {K, rows}, box {128 / es, box_rows} (one 128-byte row of K); MN-major
+// storage (16-bit): dims {MN, K}, box {64, BK}; 128-byte swizzle; reads
+// outside the tensor return zeros.
 int encode_operand(CUtensorMap* tm, const void* base, int64_t ld, bool k_major, int64_t mn,
-                   int64_t K, int box_rows) {
+                   int64_t K, int box_rows, int es) {
   EncodeFn enc = get_encode();
   if (!enc) return GEMM_ERR_CUDA;
   cuuint64_t dims[2], strides[1];
@@ -286,7 +296,7 @@ int encode_operand(CUtensorMap* tm, const void* base, int64_t ld, bool k_major, 
   if (k_major) {
     dims[0] = (cuuint64_t)K;
     dims[1] = (cuuint64_t)mn;
-    box[0] = BK;
+    box[0] = (cuuint32_t)(128 / es);
     box[1] = (cuuint32_t)box_rows;
   } else {
     dims[0] = (cuuint64_t)mn;
@@ -294,8 +304,9 @@ int encode_operand(CUtensorMap* tm, const void* base, int64_t ld, bool k_major, 
     box[0] = 64;
     box[1] = BK;
   }
-  strides[0] = (cuuint64_t)ld * 2;
-  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides,
+  strides[0] = (cuuint64_t)ld * es;
+  CUresult r = enc(tm, es == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+                   const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
@@ -423,6 +434,7 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   h->device = dev;
   h->num_sms = sms;
   h->i8x = (static_cast<int>(d.ab_type) == T_I8);
+  h->f8 = is_f8(static_cast<int>(d.ab_type));
   h->mab_type = h->i8x ? static_cast<int>(T_BF16) : static_cast<int>(d.ab_type);
 
   h->choice = choose_plan(d.M, d.N, d.K, d.ab_type, d.layout_a, d.layout_b, sms);
@@ -493,7 +505,9 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   kp.tiles_m = (int)((h->M + tile_m - 1) / tile_m);
   kp.tiles_n = (int)((h->N + c.bn - 1) / c.bn);
   kp.group_m = std::max(1, std::min(c.group_m, kp.tiles_m));
-  kp.num_kb = (int)((h->K + BK - 1) / BK);
+  const int bk_el = h->f8 ? 2 * BK : BK;  // K per 128-byte row
+  kp.num_kb = (int)((h->K + bk_el - 1) / bk_el);
+  kp.f8 = h->f8 ? 1 : 0;
   int splits = std::max(1, std::min(c.splits, std::max(1, kp.num_kb)));
   kp.kb_per_split = kp.num_kb > 0 ? (kp.num_kb + splits - 1) / splits : 0;
   // a ring stage covers ksub K slices: splits start on stage boundaries
@@ -504,8 +518,9 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   kp.kb_per_chunk = h->i8x ? 8 : std::max(1, kp.num_kb);  // int8: 512 K per exact fp32 pass
   kp.a_mn = h->a.layout == GEMM_COL_MAJOR ? 1 : 0;  // A' contiguous along M'
   kp.b_mn = h->b.layout == GEMM_ROW_MAJOR ? 1 : 0;  // B' contiguous along N'
-  kp.idesc = idesc_f16(h->mab_type == T_BF16 ? 1u : 0u, (uint32_t)kp.a_mn, (uint32_t)kp.b_mn,
-                       (uint32_t)tile_m, (uint32_t)c.bn);
+  // element type code 1: bf16 (kind::f16) or E5M2 (kind::f8f6f4)
+  kp.idesc = idesc_f16(h->mab_type == T_BF16 || h->mab_type == T_E5M2 ? 1u : 0u,
+                       (uint32_t)kp.a_mn, (uint32_t)kp.b_mn, (uint32_t)tile_m, (uint32_t)c.bn);
   kp.c_type = d.c_type;
   kp.d_type = d.d_type;
   kp.c_rs = h->c_layout == GEMM_ROW_MAJOR ? h->ldc : 1;
@@ -551,12 +566,13 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     const int64_t outer = o.layout == GEMM_ROW_MAJOR ? o.rows : o.cols;
     o.repack = h->i8x || ((o.ld * in_es) % 16 != 0);
     if (!o.repack) return;
+    const int64_t ws_es = h->f8 ? 1 : 2;  // bf16 (16-bit or widened int8) or 8-bit copies
     // Rows start on 128-byte lines: a TMA row of 128 bytes then reads four
     // 32-byte sectors, not five (measured: a B whose rows sat 16 bytes off
     // the line cost 10 % of the kernel time at 4096 x 4097 x 4096).
-    o.ws_ld = round_up(std::max<int64_t>(inner, 1), 64);
+    o.ws_ld = round_up(std::max<int64_t>(inner, 1), 128 / ws_es);
     o.ws_off = off;
-    off += (size_t)round_up(o.ws_ld * outer * 2, 256);
+    off += (size_t)round_up(o.ws_ld * outer * ws_es, 256);
   };
   const int64_t in_es = elem_size(d.ab_type);
   plan_copy(h->a, in_es);
@@ -734,7 +750,7 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
     const int64_t inner = o.layout == GEMM_ROW_MAJOR ? o.cols : o.rows;
     const int64_t outer = o.layout == GEMM_ROW_MAJOR ? o.rows : o.cols;
     uint16_t* dst = reinterpret_cast<uint16_t*>(ws + o.ws_off);
-    if (d.ab_type == GEMM_I8) {  // widened to bf16 on the way
+    if (d.ab_type == GEMM_I8 || h->f8) {  // int8 widened to bf16; 8-bit floats as bytes
       if (launch_repack(src, d.ab_type, o.ld, dst, o.ws_ld, outer, inner, h->num_sms, st) !=
           cudaSuccess)
         return GEMM_ERR_CUDA;
@@ -760,9 +776,10 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
     h->map_next[which] = (slot + 1) % gemm_plan::kMapCache;
     h->map_ptr[which][slot] = nullptr;
     const int rc = which == 0
-                       ? encode_operand(&h->map[0][slot], ta, lda_eff, kp.a_mn == 0, h->M, h->K, BM)
+                       ? encode_operand(&h->map[0][slot], ta, lda_eff, kp.a_mn == 0, h->M, h->K, BM,
+                                        h->f8 ? 1 : 2)
                        : encode_operand(&h->map[1][slot], tb, ldb_eff, kp.b_mn == 0, h->N, h->K,
-                                        b_box);
+                                        b_box, h->f8 ? 1 : 2);
     if (rc != GEMM_OK) return GEMM_ERR_CUDA;
     h->map_ptr[which][slot] = base;
     tm[which] = &h->map[which][slot];

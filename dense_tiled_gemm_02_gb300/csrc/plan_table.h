@@ -94,7 +94,7 @@ inline PlanChoice choose_plan(int64_t M, int64_t N, int64_t K, int ab_type, int 
   }
   const int64_t tiles = tm * cdiv64(Ni, c.bn);
   // Split K when the tiles alone leave most SMs idle and K is long.
-  const int64_t kb = cdiv64(K, 64);
+  const int64_t kb = cdiv64(K, ab_type == T_E4M3 || ab_type == T_E5M2 ? 128 : 64);  // K slices
   if (tiles * 2 <= num_sms && kb >= 16) {
     int64_t s = num_sms / tiles;
     if (s > kb / 8) s = kb / 8;

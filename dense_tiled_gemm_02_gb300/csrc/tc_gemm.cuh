@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive_expect_tx(full(s), Cfg::STAGE_TX);
           const uint32_t a_dst = smem_u32(sA + s * Cfg::A_BYTES);
           const uint32_t b_dst = smem_u32(sB + s * Cfg::B_BYTES);
-          const int k0 = kb * BK;
+          const int k0 = kb * (p.f8 ? 2 * BK : BK);  // a 128-byte row: 64 or 128 K
           if (!p.a_mn) {
             tma_load_2d(a_dst, &tmA, k0, w.m0, full(s));
           } else {
@@ -429,6 +429,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       uint32_t s = 0, ph = 0, acc_it = 0;
       bool stop = false;
+      const bool f8 = !I8X && p.f8 != 0;
       for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
         const Unit w = decode_unit(p, u, BN);
         // One accumulation pass per chunk of kb_per_chunk K slices (the whole
@@ -451,10 +452,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             const uint32_t a_lo = a_lo0 + s * (Cfg::A_BYTES >> 4);
             const uint32_t b_lo = b_lo0 + s * (Cfg::B_BYTES >> 4);
+            // 8-bit operands: the same four 32-byte steps along the row,
+            // 32 K each (both operands K-major)
+            if (f8) {
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              mma_f16_ss(d_tmem, sdesc(dhi, a_lo + a_off[kk]), sdesc(dhi, b_lo + b_off[kk]),
-                         p.idesc, accumulate | kk);
+              for (int kk = 0; kk < BK / 16; ++kk)
+                mma_f8_ss(d_tmem, sdesc(dhi, a_lo + a_off[kk]), sdesc(dhi, b_lo + b_off[kk]),
+                          p.idesc, accumulate | kk);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk)
+                mma_f16_ss(d_tmem, sdesc(dhi, a_lo + a_off[kk]), sdesc(dhi, b_lo + b_off[kk]),
+                           p.idesc, accumulate | kk);
+            }
             accumulate = 1;
             mma_commit(empty(s));
             if (++s == STAGES) {

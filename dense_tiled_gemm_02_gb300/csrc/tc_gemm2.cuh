@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
 #pragma unroll
             for (int j = 0; j < KSUB; ++j) {
               // a K slice past the end still lands (as zeros) and is counted
-              const int k0 = (kb + j) * BK;
+              const int k0 = (kb + j) * (p.f8 ? 2 * BK : BK);  // a 128-byte row: 64 or 128 K
               const uint32_t a_dst = smem_u32(sA + s * Cfg::A_BYTES + j * Cfg::A_ATOM);
               const uint32_t b_dst = smem_u32(sB + s * Cfg::B_BYTES + j * Cfg::B_ATOM);
               if (!p.a_mn) {
@@ -267,6 +267,7 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
       }
       uint32_t s = 0, ph = 0, acc_it = 0;
       bool stop = false;
+      const bool f8 = !I8X && p.f8 != 0;
       // One pass of the K loop into accumulator buffer `buf`.
       auto k_loop = [&](const int kc, const int ke, const uint32_t buf) {
         const uint32_t d_tmem = tmem_base + buf * BN;
@@ -278,10 +279,17 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
           }
           const uint32_t a_lo = a_lo0 + s * (Cfg::A_BYTES >> 4);
           const uint32_t b_lo = b_lo0 + s * (Cfg::B_BYTES >> 4);
+          if (f8) {  // 8-bit operands: 32 K per 32-byte step (both K-major)
 #pragma unroll
-          for (int kk = 0; kk < 4 * KSUB; ++kk)
-            mma_f16_ss_pair(d_tmem, sdesc(dhi, a_lo + a_off[kk]), sdesc(dhi, b_lo + b_off[kk]),
-                            p.idesc, accumulate | kk);
+            for (int kk = 0; kk < 4 * KSUB; ++kk)
+              mma_f8_ss_pair(d_tmem, sdesc(dhi, a_lo + a_off[kk]), sdesc(dhi, b_lo + b_off[kk]),
+                             p.idesc, accumulate | kk);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4 * KSUB; ++kk)
+              mma_f16_ss_pair(d_tmem, sdesc(dhi, a_lo + a_off[kk]), sdesc(dhi, b_lo + b_off[kk]),
+                              p.idesc, accumulate | kk);
+          }
           accumulate = 1;
           mma_commit_pair_both(empty(s));
           if (++s == STAGES) {

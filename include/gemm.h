@@ -20,6 +20,14 @@
  *       C widened to fp32 and added to the fp32 sum, one round-to-nearest-
  *       even conversion to d_type.
  *   (I8, I32 or C absent, I32): exact integer result (int32).
+ *   (E4M3|E5M2, F16|BF16|F32 or C absent, F16|BF16|F32): 8-bit float
+ *       operands in the OCP OFP8 encodings (E4M3: 4 exponent bits, bias 7,
+ *       no infinities; E5M2: 5 exponent bits, bias 15, IEEE specials), read
+ *       by the tensor core natively (tcgen05 kind::f8f6f4); fp32
+ *       accumulation and the output path of the 16-bit types.  The pages
+ *       name a scaled low-precision matrix product (mfma_scaled) as the next
+ *       data type; this is its unscaled form.  A must be row-major and B
+ *       column-major (both contiguous along K), else GEMM_ERR_UNSUPPORTED.
  *
  * Device pointers, caller-owned.  Every call is asynchronous on the given
  * stream.  All sizes are element counts.
@@ -46,7 +54,9 @@ typedef enum {
   GEMM_BF16 = 2,
   GEMM_F32 = 3,
   GEMM_I8 = 4,
-  GEMM_I32 = 5
+  GEMM_I32 = 5,
+  GEMM_E4M3 = 6, /* OCP OFP8 E4M3 (operands only) */
+  GEMM_E5M2 = 7  /* OCP OFP8 E5M2 (operands only) */
 } gemm_dtype_t;
 
 /* Storage order: row-major X[r,c] = X[r*ld + c]; column-major X[r + c*ld]. */

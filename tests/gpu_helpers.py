@@ -9,9 +9,9 @@ import torch
 
 import oracle
 from oracle import compare
-from workloads import F32, I8, I32, ROW, Workload, bits_u16, storage_shape
+from workloads import F32, I8, I32, ROW, TORCH_DTYPE, Workload, bits_of, bits_u16, storage_shape
 
-TYPE_TORCH = {1: torch.float16, 2: torch.bfloat16, 3: torch.float32, 4: torch.int8, 5: torch.int32}
+TYPE_TORCH = TORCH_DTYPE
 
 
 def logical(storage: torch.Tensor, layout: int) -> torch.Tensor:
@@ -61,8 +61,8 @@ def _oracle_args(w: Workload, inp: dict):
         B = inp["B"].numpy()
         C = None if inp["C"] is None else inp["C"].numpy()
     else:
-        A = bits_u16(inp["A"])
-        B = bits_u16(inp["B"])
+        A = bits_of(inp["A"])
+        B = bits_of(inp["B"])
         C = None
         if inp["C"] is not None:
             C = inp["C"].numpy() if w.c_type == F32 else bits_u16(inp["C"])

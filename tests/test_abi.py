@@ -55,6 +55,12 @@ def _desc(**kw):
     (dict(d_type=pkg.GEMM_I32), pkg.GEMM_ERR_UNSUPPORTED),
     (dict(ab_type=pkg.GEMM_I8, c_type=pkg.GEMM_BF16, d_type=pkg.GEMM_I32),
      pkg.GEMM_ERR_UNSUPPORTED),
+    # 8-bit float operands: K-major A and B only, 16/32-bit float C and D
+    (dict(ab_type=pkg.GEMM_E4M3), pkg.GEMM_ERR_UNSUPPORTED),           # B row-major
+    (dict(ab_type=pkg.GEMM_E5M2, layout_a=1, layout_b=1), pkg.GEMM_ERR_UNSUPPORTED),
+    (dict(ab_type=pkg.GEMM_E4M3, layout_b=1, d_type=pkg.GEMM_I32), pkg.GEMM_ERR_UNSUPPORTED),
+    (dict(ab_type=pkg.GEMM_E4M3, layout_b=1, d_type=pkg.GEMM_E4M3), pkg.GEMM_ERR_UNSUPPORTED),
+    (dict(ab_type=pkg.GEMM_E5M2, layout_b=1, c_type=pkg.GEMM_I32), pkg.GEMM_ERR_UNSUPPORTED),
 ])
 def test_create_rejects_bad_descriptions(kw, code):
     rc, h = pkg.gemm_create(_desc(**kw))
@@ -66,6 +72,9 @@ def test_create_without_gpu_reports_no_device():
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     rc, h = pkg.gemm_create(_desc())
+    assert rc == pkg.GEMM_ERR_NO_DEVICE and h is None
+    # a valid 8-bit float description passes validation and reaches the device check
+    rc, h = pkg.gemm_create(_desc(ab_type=pkg.GEMM_E4M3, layout_b=1, d_type=pkg.GEMM_F32))
     assert rc == pkg.GEMM_ERR_NO_DEVICE and h is None
 
 

@@ -16,7 +16,8 @@ import torch
 
 import dense_tiled_gemm_02_gb300 as pkg
 from gpu_helpers import check_points, check_rows, forced_plan, logical, run_gpu
-from workloads import (BF16, COL, F16, F32, I8, I32, ROW, TORCH_DTYPE, WORKLOADS, Workload, draw,
+from workloads import (BF16, COL, E4M3, E5M2, F16, F32, I8, I32, ROW, TORCH_DTYPE, WORKLOADS,
+                       Workload, draw,
                        make_inputs, sample_points, sample_rows, storage_shape)
 
 pytestmark = pytest.mark.gpu
@@ -331,7 +332,7 @@ def test_plan_table_rows_engage(name):
 
 
 # ------------------------------------------------------------------ full-size configs
-FULL = [("sq4096_bf16", None), ("sq4096_bf16", "pair=1,bn=256,tail=0"),
+FULL = [("sq4096_bf16", None), ("sq4096_bf16", "pair=1,bn=256,tail=0"), ("sq4096_e4m3", None),
         ("sq4096_bf16", "pair=0,bn=256"), ("skinny64x8192x8192_bf16", None),
         ("skinny8192x128x4096_bf16", None), ("rag4095x4097x4099_bf16", None),
         ("rag4095x4097x4099_bf16", "pair=1,bn=256"), ("sq4096_bf16", "pair=1,bn=256,ksub=2"),
@@ -349,7 +350,7 @@ def test_full_config_every_element(name, plan):
 
 
 @pytest.mark.parametrize("name,plan", [("sq8192_bf16", None), ("sq8192_i8", None),
-                                       ("sq8192_i8", "pair=0")])
+                                       ("sq8192_i8", "pair=0"), ("sq8192_e4m3", None)])
 def test_8192_sampled(name, plan):
     w = WORKLOADS[name]
     inp = make_inputs(w)
@@ -358,6 +359,50 @@ def test_8192_sampled(name, plan):
     _assert_ok(check_points(w, inp, D, pi.numpy(), pj.numpy()), f"{name} points [{p}]")
     rows = sample_rows(w.M).numpy()
     _assert_ok(check_rows(w, inp, D, rows=rows), f"{name} rows [{p}]")
+
+
+# ------------------------------------------------------------------ 8-bit float operands
+# (M, N, K, C type or None, D type); A row-major, B column-major (K-major).
+F8_CASES = [
+    (128, 128, 128, BF16, BF16),
+    (300, 520, 200, BF16, BF16),    # rows of 200 bytes: copied to 128-byte workspace rows
+    (129, 257, 72, None, F32),
+    (1000, 1000, 1000, F16, F16),
+    (513, 770, 4096, F32, BF16),
+    (64, 2048, 4096, BF16, BF16),   # skinny
+    (3, 512, 1024, BF16, F32),      # below the decode kernel's types: the tensor path
+]
+F8_PLANS = [None, "pair=0,bn=64", "pair=0,bn=128", "pair=0,bn=256", "pair=1,bn=256",
+            "pair=1,bn=128", "pair=1,bn=256,ksub=2", "pair=1,bn=256,grid=8,tail=1",
+            "pair=0,bn=128,splits=3"]
+
+
+@pytest.mark.parametrize("plan", F8_PLANS)
+@pytest.mark.parametrize("t", [E4M3, E5M2], ids=["e4m3", "e5m2"])
+@pytest.mark.parametrize("case", F8_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}" for c in F8_CASES])
+def test_fp8_every_element(case, t, plan):
+    """kind::f8f6f4 on both kernels (split-K, stream-K, two K slices a stage)
+    against the oracle's exact widening of the OFP8 encodings."""
+    M, N, K, ct, dt = case
+    w = Workload("f8", 14, M, N, K, t, ct, dt, "normal", ROW, COL)
+    inp = make_inputs(w, seed_offset=M + K)
+    D, p = run_gpu(w, inp, plan=plan)
+    _assert_ok(check_rows(w, inp, D), f"{case} {t} [{p}]")
+
+
+def test_fp8_special_values():
+    """E4M3's largest finite (448), subnormals and signed zeros pass through
+    unchanged: A = diag of specials, B = I, so D = A exactly."""
+    vals = torch.tensor([448.0, -448.0, 2.0 ** -9, -(2.0 ** -9), 2.0 ** -6, 0.0, -0.0, 1.0],
+                        dtype=torch.float32)
+    n = 128
+    A = torch.zeros(n, n, dtype=torch.float32)
+    A[torch.arange(n), torch.arange(n)] = vals.repeat(n // vals.numel())
+    w = Workload("f8s", 15, n, n, n, E4M3, None, F32, "normal", ROW, COL)
+    inp = {"A": A.to(torch.float8_e4m3fn), "B": torch.eye(n).to(torch.float8_e4m3fn).t()
+           .contiguous(), "C": None}
+    D, p = run_gpu(w, inp)
+    assert torch.equal(D, torch.diag(vals.repeat(n // vals.numel()))), p
 
 
 @pytest.mark.parametrize("name", ["decode1x4096x4096_bf16", "decode16x4096x4096_bf16",

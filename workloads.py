@@ -10,6 +10,8 @@ transpose; the entries are i.i.d., so nothing depends on that choice):
 * uniform[-1, 1]: fp32 ``rand * 2 - 1`` rounded once to fp16
 * normal(0, 1):   fp32 ``randn`` rounded once to bf16
 * int8:           ``randint(-128, 128)``; int32 C: ``randint(-2**20, 2**20 + 1)``
+* E4M3 / E5M2 operands (8-bit floats): fp32 ``randn`` rounded once by
+  torch's float8 conversion (nearest even; |x| < 448 always fits)
 
 Seeds: ``seed = 1000 * idx + {0: A, 1: B, 2: C}`` with the workload index
 below.  The shapes and distributions are the ones the pages' workloads use
@@ -22,12 +24,15 @@ from dataclasses import dataclass, field
 
 import torch
 
-F16, BF16, F32, I8, I32 = 1, 2, 3, 4, 5
+F16, BF16, F32, I8, I32, E4M3, E5M2 = 1, 2, 3, 4, 5, 6, 7
 ROW, COL = 0, 1
+F8 = (E4M3, E5M2)
 
 TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32,
-               I8: torch.int8, I32: torch.int32}
-TYPE_NAME = {F16: "f16", BF16: "bf16", F32: "f32", I8: "i8", I32: "i32"}
+               I8: torch.int8, I32: torch.int32, E4M3: torch.float8_e4m3fn,
+               E5M2: torch.float8_e5m2}
+TYPE_NAME = {F16: "f16", BF16: "bf16", F32: "f32", I8: "i8", I32: "i32", E4M3: "e4m3",
+             E5M2: "e5m2"}
 
 
 @dataclass(frozen=True)
@@ -71,6 +76,12 @@ WORKLOADS = {
     "rag4095x4097x4099_bf16": Workload("rag4095x4097x4099_bf16", 44, 4095, 4097, 4099, BF16,
                                        BF16, BF16, "normal"),
     "sq8192_i8": Workload("sq8192_i8", 5, 8192, 8192, 8192, I8, I32, I32, "int"),
+    # 8-bit float operands (K-major A and B, as the kind::f8f6f4 path reads
+    # them), bf16 C and D
+    "sq4096_e4m3": Workload("sq4096_e4m3", 51, 4096, 4096, 4096, E4M3, BF16, BF16, "normal",
+                            layout_b=COL),
+    "sq8192_e4m3": Workload("sq8192_e4m3", 52, 8192, 8192, 8192, E4M3, BF16, BF16, "normal",
+                            layout_b=COL),
     # decode regime (M <= 16, N = K = 4096), with B K-contiguous (a weight
     # stored N x K) and N-contiguous
     "decode1x4096x4096_bf16": Workload("decode1x4096x4096_bf16", 61, 1, 4096, 4096, BF16, BF16,
@@ -131,6 +142,14 @@ def sample_rows(M: int, n: int = 64, seed: int = 0x5EED + 1):
     perm = torch.randperm(M, generator=g).tolist()
     rest = [r for r in perm if r not in fixed][: max(0, n - len(fixed))]
     return torch.tensor(fixed + rest, dtype=torch.int64)
+
+
+def bits_of(t: torch.Tensor):
+    """Bit patterns of a 16-bit (uint16) or 8-bit float (uint8) CPU tensor,
+    the oracle's input form."""
+    if t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
+        return t.contiguous().view(torch.uint8).numpy()
+    return bits_u16(t)
 
 
 def bits_u16(t: torch.Tensor):
