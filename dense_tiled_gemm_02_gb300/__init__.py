@@ -10,7 +10,8 @@ Low-level names mirror ``include/gemm.h``: ``gemm_create``, ``gemm_run``,
 ``gemm_get_status``, ``gemm_destroy``, ``gemm_strerror``,
 ``gemm_plan_string``, ``gemm_workspace_bytes``, ``gemm_raster_tile``,
 ``gemm_debug_set``, ``gemm_timing_enable``, ``gemm_timing_read``,
-``gemm_pair_schedule``.  ``Gemm`` wraps a handle for torch tensors.
+``gemm_host_io_enable``, ``gemm_run_host_batch``, ``gemm_pair_schedule``.
+``Gemm`` wraps a handle for torch tensors.
 """
 from __future__ import annotations
 
@@ -35,7 +36,7 @@ GEMM_DEBUG_SKIP_FIRST_FILL = 1
 EXPORTED = ["gemm_create", "gemm_run", "gemm_get_status", "gemm_destroy", "gemm_strerror",
             "gemm_plan_string", "gemm_workspace_bytes", "gemm_raster_tile", "gemm_debug_set",
             "gemm_run_splitk_noalloc", "gemm_timing_enable", "gemm_timing_read",
-            "gemm_pair_schedule"]
+            "gemm_host_io_enable", "gemm_run_host_batch", "gemm_pair_schedule"]
 GEMM_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
@@ -98,6 +99,11 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
     lib.gemm_timing_enable.restype = ci
     lib.gemm_timing_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ci]
     lib.gemm_timing_read.restype = ci
+    lib.gemm_host_io_enable.argtypes = [vp]
+    lib.gemm_host_io_enable.restype = ci
+    lib.gemm_run_host_batch.argtypes = [vp, ci, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                        ctypes.POINTER(vp), ctypes.POINTER(vp), vp]
+    lib.gemm_run_host_batch.restype = ci
     _lib = lib
     return lib
 
@@ -175,6 +181,19 @@ def gemm_timing_read(h: int, n: int) -> tuple[int, list[float]]:
     return rc, [buf[i] for i in range(max(rc, 0))]
 
 
+def gemm_host_io_enable(h: int) -> int:
+    return load().gemm_host_io_enable(h)
+
+
+def gemm_run_host_batch(h: int, A: list, B: list, C: list | None, D: list,
+                        stream: int | None) -> int:
+    """D[i] = A[i]*B[i] + C[i] for lists of host addresses (C None or entries None: C = 0)."""
+    n = len(A)
+    arr = ctypes.c_void_p * max(n, 1)
+    c_arr = None if C is None else arr(*C)
+    return load().gemm_run_host_batch(h, n, arr(*A), arr(*B), c_arr, arr(*D), stream)
+
+
 def gemm_run_splitk_noalloc(desc: GemmDesc, splits: int, A: int, B: int, C: int | None, D: int,
                             stream: int | None) -> int:
     """Split-K GEMM for callers that cannot allocate device memory (scratch is a
@@ -245,6 +264,30 @@ class Gemm:
         rc = gemm_run(self.handle, A, B, C, D, stream)
         if rc != GEMM_OK:
             raise GemmError(rc, "gemm_run")
+
+    def host_io_enable(self) -> None:
+        """Allocate the device copies and streams that run_host_batch uses."""
+        rc = gemm_host_io_enable(self.handle)
+        if rc != GEMM_OK:
+            raise GemmError(rc, "gemm_host_io_enable")
+
+    def run_host_batch(self, As, Bs, Cs, Ds, stream=None) -> None:
+        """Enqueue Ds[i] = As[i]*Bs[i] + Cs[i] for host (ideally pinned) tensors,
+        each in the storage order of the description; copies overlap the GEMMs."""
+        if stream is None:
+            import torch
+            stream = torch.cuda.current_stream()
+        s = getattr(stream, "cuda_stream", stream)
+        for t in list(As) + list(Bs) + list(Ds) + [c for c in (Cs or []) if c is not None]:
+            if t.is_cuda:
+                raise ValueError("run_host_batch takes host tensors")
+        rc = gemm_run_host_batch(self.handle, [a.data_ptr() for a in As],
+                                 [b.data_ptr() for b in Bs],
+                                 None if Cs is None else
+                                 [None if c is None else c.data_ptr() for c in Cs],
+                                 [d.data_ptr() for d in Ds], s)
+        if rc != GEMM_OK:
+            raise GemmError(rc, "gemm_run_host_batch")
 
     def status(self, stream=None) -> int:
         s = getattr(stream, "cuda_stream", stream)

@@ -130,6 +130,17 @@ struct gemm_plan {
   // next timing_n runs (created by gemm_timing_enable, never by gemm_run).
   std::vector<cudaEvent_t> timing_ev;
   int timing_n = 0, timing_used = 0;
+  // Host-buffer calls (gemm_host_io_enable / gemm_run_host_batch): two sets
+  // of device copies of A, B, C, D, and three streams (copies in, GEMM,
+  // copy out) with per-set events, so that one call's input copies overlap
+  // the previous call's GEMM and output copy.
+  bool io_ready = false;
+  void* io_buf[2][4] = {};  // [set][A, B, C, D]
+  size_t io_bytes[4] = {};
+  cudaStream_t io_stream[3] = {};
+  cudaEvent_t io_ev[2][3] = {};  // [set][inputs landed, GEMM done, D copied out]
+  cudaEvent_t io_start = nullptr, io_end = nullptr;
+  uint64_t io_calls = 0;
 };
 
 namespace {
@@ -869,8 +880,99 @@ int gemm_destroy(gemm_handle_t h) {
   if (h->ws) cudaFree(h->ws);
   if (h->status) cudaFree(h->status);
   for (cudaEvent_t e : h->timing_ev) cudaEventDestroy(e);
+  for (auto& set : h->io_buf)
+    for (void* b : set)
+      if (b) cudaFree(b);
+  for (cudaStream_t s : h->io_stream)
+    if (s) cudaStreamDestroy(s);
+  for (auto& set : h->io_ev)
+    for (cudaEvent_t e : set)
+      if (e) cudaEventDestroy(e);
+  if (h->io_start) cudaEventDestroy(h->io_start);
+  if (h->io_end) cudaEventDestroy(h->io_end);
   delete h;
   return rc;
+}
+
+namespace {
+// Bytes from an operand's first element to one past its last, in storage
+// order (rows x cols, leading dimension ld).
+size_t span_bytes(int layout, int64_t rows, int64_t cols, int64_t ld, int es) {
+  if (rows <= 0 || cols <= 0) return 0;
+  const int64_t outer = layout == GEMM_ROW_MAJOR ? rows : cols;
+  const int64_t inner = layout == GEMM_ROW_MAJOR ? cols : rows;
+  return (size_t)((outer - 1) * ld + inner) * (size_t)es;
+}
+}  // namespace
+
+int gemm_host_io_enable(gemm_handle_t h) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  if (h->io_ready) return GEMM_OK;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) return GEMM_ERR_INVALID_ARG;
+  const gemm_desc_t& d = h->desc;
+  h->io_bytes[0] = span_bytes(d.layout_a, d.M, d.K, d.lda, elem_size(d.ab_type));
+  h->io_bytes[1] = span_bytes(d.layout_b, d.K, d.N, d.ldb, elem_size(d.ab_type));
+  h->io_bytes[2] = d.c_type ? span_bytes(d.layout_c, d.M, d.N, d.ldc, elem_size(d.c_type)) : 0;
+  h->io_bytes[3] = span_bytes(d.layout_d, d.M, d.N, d.ldd, elem_size(d.d_type));
+  bool ok = true;
+  for (int s = 0; s < 2 && ok; ++s)
+    for (int k = 0; k < 4 && ok; ++k)
+      if (h->io_bytes[k]) ok = cudaMalloc(&h->io_buf[s][k], h->io_bytes[k]) == cudaSuccess;
+  for (int k = 0; k < 3 && ok; ++k)
+    ok = cudaStreamCreateWithFlags(&h->io_stream[k], cudaStreamNonBlocking) == cudaSuccess;
+  for (int s = 0; s < 2 && ok; ++s)
+    for (int k = 0; k < 3 && ok; ++k)
+      ok = cudaEventCreateWithFlags(&h->io_ev[s][k], cudaEventDisableTiming) == cudaSuccess;
+  if (ok) ok = cudaEventCreateWithFlags(&h->io_start, cudaEventDisableTiming) == cudaSuccess;
+  if (ok) ok = cudaEventCreateWithFlags(&h->io_end, cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    return GEMM_ERR_ALLOC_FAILED;  // what was created is released by gemm_destroy
+  }
+  h->io_ready = true;
+  return GEMM_OK;
+}
+
+int gemm_run_host_batch(gemm_handle_t h, int n, const void* const* A, const void* const* B,
+                        const void* const* C, void* const* D, gemm_stream_t stream) {
+  if (!h || n < 0 || (n > 0 && (!A || !B || !D))) return GEMM_ERR_INVALID_ARG;
+  if (!h->io_ready) return GEMM_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i)  // nothing is enqueued unless every pointer is there
+    if (!A[i] || !B[i] || !D[i]) return GEMM_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStream_t s_in = h->io_stream[0], s_gemm = h->io_stream[1], s_out = h->io_stream[2];
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  // Everything enqueued on `stream` before this call comes first.
+  if (!ok(cudaEventRecord(h->io_start, st)) || !ok(cudaStreamWaitEvent(s_in, h->io_start, 0)))
+    return GEMM_ERR_CUDA;
+  for (int i = 0; i < n; ++i) {
+    const int set = (int)(h->io_calls++ & 1u);
+    void* const* buf = h->io_buf[set];
+    cudaEvent_t* ev = h->io_ev[set];
+    const void* hc = (C && h->io_bytes[2]) ? C[i] : nullptr;
+    // The set's inputs are free once the GEMM that read them is done, its D
+    // once that D has been copied out (an event never recorded is complete).
+    if (!ok(cudaStreamWaitEvent(s_in, ev[1], 0))) return GEMM_ERR_CUDA;
+    if (!ok(cudaMemcpyAsync(buf[0], A[i], h->io_bytes[0], cudaMemcpyHostToDevice, s_in)) ||
+        !ok(cudaMemcpyAsync(buf[1], B[i], h->io_bytes[1], cudaMemcpyHostToDevice, s_in)))
+      return GEMM_ERR_CUDA;
+    if (hc && !ok(cudaMemcpyAsync(buf[2], hc, h->io_bytes[2], cudaMemcpyHostToDevice, s_in)))
+      return GEMM_ERR_CUDA;
+    if (!ok(cudaEventRecord(ev[0], s_in)) || !ok(cudaStreamWaitEvent(s_gemm, ev[0], 0)) ||
+        !ok(cudaStreamWaitEvent(s_gemm, ev[2], 0)))
+      return GEMM_ERR_CUDA;
+    const int rc = gemm_run(h, buf[0], buf[1], hc ? buf[2] : nullptr, buf[3], s_gemm);
+    if (rc != GEMM_OK) return rc;
+    if (!ok(cudaEventRecord(ev[1], s_gemm)) || !ok(cudaStreamWaitEvent(s_out, ev[1], 0)) ||
+        !ok(cudaMemcpyAsync(D[i], buf[3], h->io_bytes[3], cudaMemcpyDeviceToHost, s_out)) ||
+        !ok(cudaEventRecord(ev[2], s_out)))
+      return GEMM_ERR_CUDA;
+  }
+  // `stream` continues once the last output copy has landed.
+  if (!ok(cudaEventRecord(h->io_end, s_out)) || !ok(cudaStreamWaitEvent(st, h->io_end, 0)))
+    return GEMM_ERR_CUDA;
+  return GEMM_OK;
 }
 
 int gemm_plan_string(gemm_handle_t h, char* buf, size_t n) {

@@ -215,6 +215,38 @@ GEMM_API int gemm_timing_enable(gemm_handle_t h, int n);
 GEMM_API int gemm_timing_read(gemm_handle_t h, float* ms, int n);
 
 /*
+ * Host buffers.  The same operation, for operands that live in host memory;
+ * the pages have no counterpart (their timings start from operands already
+ * on the device).
+ * gemm_host_io_enable(h): allocates on h's device two sets of device copies
+ * of A, B, C and D (each the span of the operand in the description's
+ * layout and leading dimension) and three streams owned by h.  Call once;
+ * freed by gemm_destroy.  Returns GEMM_OK, GEMM_ERR_INVALID_ARG (h null or
+ * another device current) or GEMM_ERR_ALLOC_FAILED.
+ * gemm_run_host_batch(h, n, A, B, C, D, stream): n products D[i] = A[i] *
+ * B[i] + C[i], every operand in host memory (arrays of n host pointers laid
+ * out as the description says; C may be NULL, or C[i] NULL, for C = 0,
+ * and is ignored when the description has no C type).
+ * Host memory should be page-locked (cudaHostAlloc / cudaHostRegister);
+ * pageable memory works but its copies do not overlap.  For each i: the
+ * host-to-device copies of A[i], B[i], C[i] into one device set, gemm_run
+ * on it, and the device-to-host copy of D into D[i].  The sets alternate,
+ * so the input copies of product i+1 overlap the GEMM of product i and the
+ * output copy of product i-1 (copies in and out use separate streams).
+ * The call only enqueues: it starts after the work already on `stream` and
+ * `stream` waits for the last output copy, so synchronising `stream` (or
+ * gemm_get_status on it) completes every D[i].  Products of one call
+ * overlap; a second call on the same stream starts after the first one's
+ * last output copy, so pass a stream of products in one call.  The caller keeps the host
+ * buffers untouched until then.  Returns GEMM_OK, GEMM_ERR_INVALID_ARG (no
+ * gemm_host_io_enable, a null pointer), or what gemm_run returns.
+ */
+GEMM_API int gemm_host_io_enable(gemm_handle_t h);
+GEMM_API int gemm_run_host_batch(gemm_handle_t h, int n, const void* const* A,
+                                 const void* const* B, const void* const* C, void* const* D,
+                                 gemm_stream_t stream);
+
+/*
  * gemm_pair_schedule: host-side view of how the CTA-pair kernel deals its
  * work to clusters (for tests; no device needed).  For a tiles_m x tiles_n
  * grid of tiles in the grouped order (group_m), num_kb 64-wide K slices,

@@ -86,6 +86,9 @@ def test_null_handles():
     assert lib.gemm_plan_string(None, None, 0) == pkg.GEMM_ERR_INVALID_ARG
     assert lib.gemm_workspace_bytes(None) == -1
     assert lib.gemm_create(None, None) == pkg.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_host_io_enable(None) == pkg.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_run_host_batch(None, 0, None, None, None, None, None) == \
+        pkg.GEMM_ERR_INVALID_ARG
 
 
 # ------------------------------------------------------------------ grouped raster
