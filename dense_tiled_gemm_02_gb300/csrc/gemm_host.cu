@@ -109,6 +109,10 @@ struct gemm_plan {
   // Decode regime (decode.cu): a handful of rows against a K-contiguous B.
   bool decode = false;
   int decode_kc = 0;
+  // Bulk-copy form of the decode kernel (taken at run time when A and B are
+  // 16-byte aligned; otherwise the split-K form planned beside it runs).
+  bool decode_bulk = false;
+  int decode_cpb = 0, decode_stages = 0;
   // 16-bit C / D whose rows are not 16-byte aligned: aligned workspace copies
   // (leading dimension stage_ld) that the kernel reads / writes instead.
   bool c_stage = false, d_stage = false;
@@ -203,6 +207,7 @@ void apply_force_plan(PlanChoice& c) {
       else if (k == "ksub") c.ksub = v;
       else if (k == "tail") c.tail = v;
       else if (k == "decode") c.no_decode = v ? 0 : 1;
+      else if (k == "dbulk") c.no_dbulk = v ? -1 : 1;
     }
     pos = end + 1;
   }
@@ -211,10 +216,11 @@ void apply_force_plan(PlanChoice& c) {
 void make_plan_string(gemm_plan* h) {
   char buf[512];
   std::snprintf(buf, sizeof buf,
-                "M=%lld N=%lld K=%lld decode=%d swap=%d pair=%d bn=%d ksub=%d stages=%d group_m=%d "
-                "splits=%d kb_per_split=%d tail=%d grid=%d i8x=%d a_mn=%d b_mn=%d repack_a=%d "
-                "repack_b=%d stage_c=%d stage_d=%d ws_bytes=%zu",
+                "M=%lld N=%lld K=%lld decode=%d dbulk=%d swap=%d pair=%d bn=%d ksub=%d stages=%d "
+                "group_m=%d splits=%d kb_per_split=%d tail=%d grid=%d i8x=%d a_mn=%d b_mn=%d "
+                "repack_a=%d repack_b=%d stage_c=%d stage_d=%d ws_bytes=%zu",
                 (long long)h->desc.M, (long long)h->desc.N, (long long)h->desc.K, (int)h->decode,
+                (int)h->decode_bulk,
                 h->choice.swap,
                 h->pair ? 1 : 0, h->choice.bn, h->choice.ksub,
                 h->pair ? h->pair->stages : (h->variant ? h->variant->stages : 0), h->kp.group_m,
@@ -264,6 +270,22 @@ int plan_decode(gemm_plan* h, int sms) {
   s = (d.K + kc - 1) / kc;
   h->decode_kc = (int)kc;
   kp.splits = (int)s;
+  // Bulk-copy form: when A's and B's rows are K-contiguous with strides of
+  // whole 16-byte units, and N gives every SM at least four columns (below
+  // that, the split-K form's parallelism over K wins), blocks of cpb whole
+  // columns, as many as make whole waves of one block per SM.
+  const bool a_k_rows = (d.layout_a == GEMM_ROW_MAJOR && (d.M == 1 || d.lda % 8 == 0)) ||
+                        (d.M == 1 && d.layout_a == GEMM_COL_MAJOR && d.lda == 1);
+  const int bulk_stages = decode_bulk_stages((int)d.M, d.K);
+  if (h->choice.no_dbulk != 1 && a_k_rows && d.ldb % 8 == 0 && bulk_stages >= 2 &&
+      (h->choice.no_dbulk == -1 || d.N >= 4 * (int64_t)sms)) {
+    const int64_t cmax = 32;  // four stages of eight columns
+    const int64_t waves = (d.N + cmax * sms - 1) / (cmax * sms);
+    const int64_t cpb = std::min<int64_t>(cmax, (d.N + sms * waves - 1) / (sms * waves));
+    h->decode_bulk = true;
+    h->decode_cpb = (int)cpb;
+    h->decode_stages = bulk_stages;
+  }
   kp.kb_per_split = 0;
   const bool row = d.layout_d == GEMM_ROW_MAJOR;
   kp.ws_rs = row ? d.N : 1;
@@ -715,6 +737,13 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
     a.d_type = d.d_type;
     a.d_rs = kp.d_rs;
     a.d_cs = kp.d_cs;
+    a.bulk = h->decode_bulk && reinterpret_cast<uintptr_t>(A) % 16 == 0 &&
+             reinterpret_cast<uintptr_t>(B) % 16 == 0;
+    a.cpb = h->decode_cpb;
+    a.stages = h->decode_stages;
+    a.status = h->status;
+    a.timeout_ns = h->timeout_ns;
+    a.debug_flags = kp.debug_flags;
     const bool timed = h->timing_used < h->timing_n;
     if (timed && cudaEventRecord(h->timing_ev[2 * h->timing_used], st) != cudaSuccess)
       return GEMM_ERR_CUDA;

@@ -26,6 +26,8 @@ struct PlanChoice {
   int ksub;      // pair kernel: 64-wide K slices per ring stage (1 or 2)
   int tail;      // pair kernel: stream-K hybrid for a partial last wave
   int no_decode; // 1: never take the decode kernel (M <= 16, K-contiguous B)
+  int no_dbulk;  // 1: never take the decode kernel's bulk-copy form; -1: take it
+                 // whenever the operands allow, whatever N (0: the planner decides)
 };
 
 struct PlanRow {

@@ -147,6 +147,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+// 1-D bulk copy of `bytes` bytes (a multiple of 16; both addresses 16-byte
+// aligned) from global to shared memory; completion is signalled as
+// transaction bytes on bar.
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // 2-D tiled store of a shared-memory box to global memory (elements outside
 // the tensor are not written), tracked as a bulk async group of this thread.
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x,

@@ -107,7 +107,8 @@ typedef void* gemm_stream_t;
  * Environment: GEMM_LOG=1 prints the chosen plan to stderr;
  * GEMM_FORCE_PLAN="bn=128,splits=2,group=8,swap=1" overrides fields of the
  * plan (for tuning sweeps; keys bn, splits, group, swap, grid, pair, ksub,
- * tail, decode).
+ * tail, decode, dbulk: 1 takes the decode kernel's bulk-copy form whenever
+ * A's and B's rows allow it, 0 never).
  */
 GEMM_API int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc);
 
@@ -265,8 +266,9 @@ GEMM_API int gemm_pair_schedule(int64_t tiles_m, int64_t tiles_n, int64_t group_
 
 /*
  * Test hooks (not for production use).
- * gemm_debug_set: flags bit 0 makes the load warp of the next gemm_run skip
- * its first stage fill, so that the consumer's bounded wait expires and the
+ * gemm_debug_set: flags bit 0 makes the load warp of the next gemm_run (the
+ * copy thread, in the decode kernel's bulk-copy form) skip its first stage
+ * fill, so that the consumer's bounded wait expires and the
  * kernel exits with GEMM_ERR_DEVICE_TIMEOUT; timeout_ns (0 = default, two
  * seconds) bounds every device-side wait of later runs.
  */

@@ -425,12 +425,14 @@ DECODE_CASES = [
 ]
 
 
-@pytest.mark.parametrize("plan", [None, "decode=0"])
+@pytest.mark.parametrize("plan", [None, "decode=0", "dbulk=1", "dbulk=0"])
 @pytest.mark.parametrize("case", DECODE_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}-off{c[8]}"
                                                    for c in DECODE_CASES])
 def test_decode_kernel(case, plan):
-    """M <= 16 with a K-contiguous B takes the decode kernel (and, with
-    decode=0, the tensor-core path); every element against the oracle."""
+    """M <= 4 with a K-contiguous B takes the decode kernel (with decode=0,
+    the tensor-core path; dbulk=1 / dbulk=0 force its bulk-copy form on or
+    off, the form falling back to the split-K one at run time when A or B is
+    off the 16-byte grid); every element against the oracle."""
     M, N, K, la, ab, ct, dt, ld, off = case
     w = Workload("dec", 65, M, N, K, ab, ct, dt, "normal", la, COL, ROW, ld)
     inp = make_inputs(w)
@@ -445,8 +447,13 @@ def test_decode_kernel(case, plan):
     with forced_plan(plan):
         g = pkg.Gemm.like(A, B, C, D)
     p = g.plan()
-    assert ("decode=1" in p) == (plan is None), p
-    if plan is not None and off:
+    assert ("decode=1" in p) == (plan != "decode=0"), p
+    k_rows = la == ROW or M == 1  # A's rows K-contiguous (ld a multiple of 8 here)
+    if plan == "dbulk=1" and k_rows and K <= 4096:  # A and two stages of B fit
+        assert "dbulk=1" in p, p
+    if plan == "dbulk=0" or not k_rows:
+        assert "dbulk=0" in p, p
+    if plan == "decode=0" and off:
         # the tensor-core path reads B with TMA: a B base off the 16-byte grid
         # with 16-byte aligned rows has no workspace copy and is rejected
         with pytest.raises(pkg.GemmError) as e:
@@ -458,6 +465,20 @@ def test_decode_kernel(case, plan):
     assert g.status() == pkg.GEMM_OK
     g.close()
     _assert_ok(check_rows(w, inp, D_storage.cpu()), f"{case} [{p}]")
+
+
+def test_decode_bulk_form_engages_at_4096_columns():
+    w = WORKLOADS["decode1x4096x4096_bf16"]
+    dev = torch.device("cuda")
+    inp = make_inputs(w)
+    A = logical(inp["A"].to(dev), w.layout_a)
+    B = logical(inp["B"].to(dev), w.layout_b)
+    D = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
+    g = pkg.Gemm.like(A, B, None, D)
+    try:
+        assert "decode=1 dbulk=1" in g.plan(), g.plan()
+    finally:
+        g.close()
 
 
 # ------------------------------------------------------------------ exact int8
@@ -517,6 +538,30 @@ def test_bounded_wait_reports_timeout_and_context_survives(plan):
     with forced_plan(plan):
         g = pkg.Gemm.like(A, B, C, D)
     assert ("pair=1" in g.plan()) == plan.startswith("pair=1"), g.plan()
+    assert pkg.gemm_debug_set(g.handle, pkg.GEMM_DEBUG_SKIP_FIRST_FILL, 50_000_000) == 0
+    g.run(A, B, C, D)
+    assert g.status() == pkg.GEMM_ERR_DEVICE_TIMEOUT
+    assert pkg.gemm_debug_set(g.handle, 0, 0) == 0
+    g.run(A, B, C, D)
+    assert g.status() == pkg.GEMM_OK
+    g.close()
+    _assert_ok(check_rows(w, inp, D.cpu()), "after timeout")
+
+
+def test_decode_bulk_wait_reports_timeout_and_context_survives():
+    """The decode kernel's bulk-copy form with its first ring stage never
+    filled: the consumers' waits expire, the producer waits for the copies it
+    did issue, the status word reports the timeout, and the next call on the
+    same handle is correct."""
+    w = WORKLOADS["decode1x4096x4096_bf16"]
+    inp = make_inputs(w)
+    dev = torch.device("cuda")
+    A = logical(inp["A"].to(dev), w.layout_a)
+    B = logical(inp["B"].to(dev), w.layout_b)
+    C = logical(inp["C"].to(dev), w.layout_c)
+    D = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
+    g = pkg.Gemm.like(A, B, C, D)
+    assert "dbulk=1" in g.plan(), g.plan()
     assert pkg.gemm_debug_set(g.handle, pkg.GEMM_DEBUG_SKIP_FIRST_FILL, 50_000_000) == 0
     g.run(A, B, C, D)
     assert g.status() == pkg.GEMM_ERR_DEVICE_TIMEOUT
