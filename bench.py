@@ -438,7 +438,7 @@ def main():
 def kernel_name(plan: str) -> str:
     f = dict(kv.split("=") for kv in plan.split() if "=" in kv)
     if f.get("decode") == "1":
-        return "decode_kn_kernel"
+        return "decode_bulk_kernel" if f.get("dbulk") == "1" else "decode_kn_kernel"
     if f.get("pair") == "1":
         return f"tc_gemm_pair_kernel<{f['bn']}, {f['stages']}, {f.get('ksub', '1')}>"
     return f"tc_gemm_kernel<{f['bn']}, {f['stages']}, {f.get('i8x', '0')}>"
