@@ -202,38 +202,41 @@ __global__ void __launch_bounds__(DEC_THREADS)
 // chosen so that the grid is whole waves of one block per SM; there is no
 // split-K tail.  Warp 8, lane 0, copies A's M rows into shared memory once
 // and then streams the block's columns of B (column n's K elements are
-// contiguous) through a ring of stages of eight whole columns, one 1-D bulk
-// copy of 2K bytes per column; warp w of 0-7 takes the w-th column of each
-// stage, adds its K products (lane l: elements 8l + 256i) with a fixed
-// butterfly, adds C and stores D.  Full and empty barriers hand the stages
+// contiguous) through a ring of stages of cps whole columns, one 1-D bulk
+// copy of 2K bytes per column; warp w of 0-7 takes the block's columns w,
+// w + 8, ..., adds its K products (lane l: elements 8l + 256i) with a fixed
+// butterfly, adds C and stores D.  Either every column has a stage slot of
+// its own (stages * cps >= cpb: all copies in flight at once, no stage
+// reused) or cps = 8, so that a warp waits on every fill of every stage in
+// turn and its parity waits cannot run a phase ahead.  Full and empty barriers hand the stages
 // over; every wait is bounded, and on a timeout the producer still waits
 // (bounded) for the copies it issued before the block exits.
 constexpr int DB_CWARPS = 8;                       // consumer warps = columns per stage
 constexpr int DB_THREADS = 32 * (DB_CWARPS + 1);
-constexpr int DB_BAR_BYTES = 256;  // full[8], empty[8], A's barrier, abort flag at the end
-constexpr int DB_MAX_STAGES = 8;
+constexpr int DB_BAR_BYTES = 256;  // full[12], empty[12], A's barrier, abort flag at the end
+constexpr int DB_MAX_STAGES = 12;
 constexpr int DB_SMEM_BUDGET = 227 * 1024;
 
 template <int MM, bool BF16>
 __global__ void __launch_bounds__(DB_THREADS) decode_bulk_kernel(const DecodeArgs d) {
   extern __shared__ __align__(128) unsigned char dsm[];
-  const int S = d.stages, cpb = d.cpb;
+  const int S = d.stages, cpb = d.cpb, cps = d.cps;
   const int M = d.M, N = d.N, K = d.K;
   const int n0 = blockIdx.x * cpb;
   const int ncols = min(cpb, N - n0);
-  const int ngroups = (ncols + DB_CWARPS - 1) / DB_CWARPS;
+  const int ngroups = (ncols + cps - 1) / cps;
   const uint32_t row_bytes = static_cast<uint32_t>(K) * 2u;
   const uint32_t bars = smem_u32(dsm);  // full[0, S), empty[S, 2S), A at 2 * DB_MAX_STAGES
   const uint32_t a_bar = bars + 8 * (2 * DB_MAX_STAGES);
   const uint32_t a_smem = bars + DB_BAR_BYTES;
   const uint32_t ring = a_smem + MM * row_bytes;
-  const uint32_t stage_bytes = DB_CWARPS * row_bytes;
+  const uint32_t stage_bytes = cps * row_bytes;
   volatile int* abort = reinterpret_cast<volatile int*>(dsm + DB_BAR_BYTES - 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(bars + 8 * i, 1);
-      mbar_init(bars + 8 * (S + i), DB_CWARPS);
+      mbar_init(bars + 8 * (S + i), cps);  // one arrival per column of a full stage
     }
     mbar_init(a_bar, 1);
     *abort = 0;
@@ -259,13 +262,12 @@ __global__ void __launch_bounds__(DB_THREADS) decode_bulk_kernel(const DecodeArg
         break;
       issued = j + 1;
       if (j == 0 && skip_first) continue;  // test hook: a stage never filled
-      const int ng = min(DB_CWARPS, ncols - j * DB_CWARPS);
+      const int ng = min(cps, ncols - j * cps);
       mbar_arrive_expect_tx(full, static_cast<uint32_t>(ng) * row_bytes);
       const uint32_t st = ring + s * stage_bytes;
       for (int c = 0; c < ng; ++c)
-        bulk_load_1d(st + c * row_bytes,
-                     d.B + static_cast<long long>(n0 + j * DB_CWARPS + c) * d.ldb, row_bytes,
-                     full);
+        bulk_load_1d(st + c * row_bytes, d.B + static_cast<long long>(n0 + j * cps + c) * d.ldb,
+                     row_bytes, full);
     }
     // The block's shared memory must outlive every copy issued into it: wait
     // for A and for the last fill of each stage (no later phase was armed).
@@ -275,60 +277,58 @@ __global__ void __launch_bounds__(DB_THREADS) decode_bulk_kernel(const DecodeArg
     return;
   }
 
-  // consumers: warp w takes column w of every stage
+  // consumers: warp w takes the block's columns w, w + 8, ...; a column's
+  // stage is freed once each of its cps columns has been read.
   if (!bounded_wait(a_bar, 0, abort, d.status, STATUS_TIMEOUT, d.timeout_ns)) return;
   const uint16_t* sA = reinterpret_cast<const uint16_t*>(dsm + DB_BAR_BYTES);
-  for (int j = 0; j < ngroups; ++j) {
-    const int s = j % S;
+  for (int col = warp; col < ncols; col += DB_CWARPS) {
+    const int j = col / cps, s = j % S;
     if (!bounded_wait(bars + 8 * s, (j / S) & 1, abort, d.status, STATUS_TIMEOUT, d.timeout_ns))
       return;
-    const int col = j * DB_CWARPS + warp;  // within the block
-    if (col < ncols) {
-      const uint16_t* sB = reinterpret_cast<const uint16_t*>(
-          dsm + DB_BAR_BYTES + MM * static_cast<size_t>(row_bytes) +
-          static_cast<size_t>(s) * stage_bytes + static_cast<size_t>(warp) * row_bytes);
-      float acc[MM];
+    const uint16_t* sB = reinterpret_cast<const uint16_t*>(
+        dsm + DB_BAR_BYTES + MM * static_cast<size_t>(row_bytes) +
+        static_cast<size_t>(s) * stage_bytes + static_cast<size_t>(col - j * cps) * row_bytes);
+    float acc[MM];
 #pragma unroll
-      for (int m = 0; m < MM; ++m) acc[m] = 0.f;
-      for (int kk = 8 * lane; kk < K; kk += 256) {
-        float b[8];
-        widen8<BF16>(*reinterpret_cast<const uint4*>(sB + kk), b);
+    for (int m = 0; m < MM; ++m) acc[m] = 0.f;
+    for (int kk = 8 * lane; kk < K; kk += 256) {
+      float b[8];
+      widen8<BF16>(*reinterpret_cast<const uint4*>(sB + kk), b);
 #pragma unroll
-        for (int m = 0; m < MM; ++m) {
-          if (m < M) {
-            float a[8];
-            widen8<BF16>(*reinterpret_cast<const uint4*>(sA + m * K + kk), a);
-            float v = acc[m];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v = fmaf(a[e], b[e], v);
-            acc[m] = v;
-          }
-        }
-      }
-#pragma unroll
-      for (int m = 0; m < MM; ++m)
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
-      if (lane == 0) {
-        const long long n = n0 + col;
-#pragma unroll
-        for (int m = 0; m < MM; ++m) {
-          if (m >= M) continue;
+      for (int m = 0; m < MM; ++m) {
+        if (m < M) {
+          float a[8];
+          widen8<BF16>(*reinterpret_cast<const uint4*>(sA + m * K + kk), a);
           float v = acc[m];
-          if (d.C) v += dec_load(d.C, d.c_type, m * d.c_rs + n * d.c_cs);
-          dec_store(d.D, d.d_type, m * d.d_rs + n * d.d_cs, v);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v = fmaf(a[e], b[e], v);
+          acc[m] = v;
         }
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(bars + 8 * (S + s));
+    if (lane == 0) mbar_arrive(bars + 8 * (S + s));  // the column has been read
+#pragma unroll
+    for (int m = 0; m < MM; ++m)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
+    if (lane == 0) {
+      const long long n = n0 + col;
+#pragma unroll
+      for (int m = 0; m < MM; ++m) {
+        if (m >= M) continue;
+        float v = acc[m];
+        if (d.C) v += dec_load(d.C, d.c_type, m * d.c_rs + n * d.c_cs);
+        dec_store(d.D, d.d_type, m * d.d_rs + n * d.d_cs, v);
+      }
+    }
   }
 }
 
 template <int MM, bool BF16>
 cudaError_t launch_bulk_mm(const DecodeArgs& d, cudaStream_t st) {
   const size_t row = static_cast<size_t>(d.K) * sizeof(uint16_t);
-  const size_t smem = DB_BAR_BYTES + MM * row + static_cast<size_t>(d.stages) * DB_CWARPS * row;
+  const size_t smem = DB_BAR_BYTES + MM * row + static_cast<size_t>(d.stages) * d.cps * row;
   auto kernel = decode_bulk_kernel<MM, BF16>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
@@ -380,12 +380,20 @@ int decode_blocks_per_sm(int M, int kc) {
   return n > 0 ? n : 1;
 }
 
-int decode_bulk_stages(int M, long long K) {
+int decode_bulk_ring(int M, long long K, int cpb, int* cps) {
   const long long mm = M <= 1 ? 1 : M <= 2 ? 2 : 4;
   const long long row = K * static_cast<long long>(sizeof(uint16_t));
   const long long left = DB_SMEM_BUDGET - DB_BAR_BYTES - mm * row;
-  if (row <= 0 || left <= 0) return 0;
-  return static_cast<int>(std::min<long long>(DB_MAX_STAGES, left / (DB_CWARPS * row)));
+  *cps = DB_CWARPS;
+  if (row <= 0 || left <= 0 || cpb < 1) return 0;
+  const long long fit = left / row;  // whole columns of B beside A
+  const int c = (cpb + DB_MAX_STAGES - 1) / DB_MAX_STAGES;
+  const int st = (cpb + c - 1) / c;
+  if (static_cast<long long>(st) * c <= fit) {  // a slot for every column: one round trip
+    *cps = c;
+    return st;
+  }
+  return static_cast<int>(std::min<long long>(DB_MAX_STAGES, fit / DB_CWARPS));
 }
 
 cudaError_t launch_decode(const DecodeArgs& d, cudaStream_t st) {
@@ -397,8 +405,11 @@ cudaError_t launch_decode(const DecodeArgs& d, cudaStream_t st) {
     const bool aligned = reinterpret_cast<uintptr_t>(d.B) % 16 == 0 && d.ldb % 8 == 0 &&
                          reinterpret_cast<uintptr_t>(d.A) % 16 == 0 &&
                          d.a_cs == 1 && (d.M == 1 || d.a_rs % 8 == 0);
-    if (!aligned || d.K <= 0 || d.cpb < 1 || d.cpb > 4 * DB_CWARPS || d.stages < 2 ||
-        d.stages > decode_bulk_stages(d.M, d.K) || d.status == nullptr)
+    int cps = 0;
+    const int stages = decode_bulk_ring(d.M, d.K, d.cpb, &cps);
+    if (!aligned || d.K <= 0 || d.cpb < 1 || d.cpb > 4 * DB_CWARPS || d.stages < 1 ||
+        d.stages != stages || d.cps != cps || (d.stages * d.cps < d.cpb && d.stages < 2) ||
+        d.status == nullptr)
       return cudaErrorInvalidValue;
     return d.bf16 ? launch_bulk<true>(d, st) : launch_bulk<false>(d, st);
   }

@@ -112,7 +112,7 @@ struct gemm_plan {
   // Bulk-copy form of the decode kernel (taken at run time when A and B are
   // 16-byte aligned; otherwise the split-K form planned beside it runs).
   bool decode_bulk = false;
-  int decode_cpb = 0, decode_stages = 0;
+  int decode_cpb = 0, decode_stages = 0, decode_cps = 0;
   // 16-bit C / D whose rows are not 16-byte aligned: aligned workspace copies
   // (leading dimension stage_ld) that the kernel reads / writes instead.
   bool c_stage = false, d_stage = false;
@@ -276,15 +276,18 @@ int plan_decode(gemm_plan* h, int sms) {
   // columns, as many as make whole waves of one block per SM.
   const bool a_k_rows = (d.layout_a == GEMM_ROW_MAJOR && (d.M == 1 || d.lda % 8 == 0)) ||
                         (d.M == 1 && d.layout_a == GEMM_COL_MAJOR && d.lda == 1);
-  const int bulk_stages = decode_bulk_stages((int)d.M, d.K);
-  if (h->choice.no_dbulk != 1 && a_k_rows && d.ldb % 8 == 0 && bulk_stages >= 2 &&
+  const int64_t cmax = 32;  // columns per block: four per consumer warp at most
+  const int64_t waves = (d.N + cmax * sms - 1) / (cmax * sms);
+  const int64_t cpb = std::min<int64_t>(cmax, (d.N + sms * waves - 1) / (sms * waves));
+  int cps = 0;
+  const int stages = decode_bulk_ring((int)d.M, d.K, (int)cpb, &cps);
+  if (h->choice.no_dbulk != 1 && a_k_rows && d.ldb % 8 == 0 &&
+      (stages * cps >= cpb || stages >= 2) &&
       (h->choice.no_dbulk == -1 || d.N >= 4 * (int64_t)sms)) {
-    const int64_t cmax = 32;  // four stages of eight columns
-    const int64_t waves = (d.N + cmax * sms - 1) / (cmax * sms);
-    const int64_t cpb = std::min<int64_t>(cmax, (d.N + sms * waves - 1) / (sms * waves));
     h->decode_bulk = true;
     h->decode_cpb = (int)cpb;
-    h->decode_stages = bulk_stages;
+    h->decode_stages = stages;
+    h->decode_cps = cps;
   }
   kp.kb_per_split = 0;
   const bool row = d.layout_d == GEMM_ROW_MAJOR;
@@ -741,6 +744,7 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
              reinterpret_cast<uintptr_t>(B) % 16 == 0;
     a.cpb = h->decode_cpb;
     a.stages = h->decode_stages;
+    a.cps = h->decode_cps;
     a.status = h->status;
     a.timeout_ns = h->timeout_ns;
     a.debug_flags = kp.debug_flags;

@@ -96,19 +96,21 @@ struct DecodeArgs {
   long long d_rs, d_cs;
   // Bulk-copy form (bulk = true): blocks of cpb whole columns over all of K;
   // A's rows copied once, B's columns streamed through a ring of `stages`
-  // stages of eight whole columns; the bound and status word of its waits,
-  // test hooks.
+  // stages of cps whole columns (from decode_bulk_ring); the bound and
+  // status word of its waits, test hooks.
   bool bulk = false;
-  int cpb = 0, stages = 0;
+  int cpb = 0, stages = 0, cps = 0;
   uint32_t* status = nullptr;
   unsigned long long timeout_ns = 0;
   int debug_flags = 0;
 };
 cudaError_t launch_decode(const DecodeArgs& d, cudaStream_t st);
-// Ring stages of the bulk-copy form for M rows of K elements: stages of
-// eight whole columns that fit beside A in the shared memory it may use
-// (the form needs at least two).
-int decode_bulk_stages(int M, long long K);
+// Ring of the bulk-copy form for M rows of K elements and cpb columns per
+// block, in the shared memory it may use beside A: when all cpb columns fit,
+// a slot for each (stages * *cps >= cpb, one round trip, no stage reused);
+// otherwise stages of *cps = 8 columns.  Returns the stage count (the form
+// needs every column to fit, or at least two stages).
+int decode_bulk_ring(int M, long long K, int cpb, int* cps);
 int decode_columns_per_block();
 // Resident blocks of the decode kernel per SM for M rows and slices of kc.
 int decode_blocks_per_sm(int M, int kc);
