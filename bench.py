@@ -112,7 +112,7 @@ def kernel_family(plan: str) -> str:
 
 
 def kernel_source_hash(family: str) -> str:
-    """Hash of the sources of one kernel family; profile figures apply only to this build."""
+    """Hash of the sources of one kernel family; profile figures apply only while it matches."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_tiled_gemm_02_gb300", "csrc")
     for name in KERNEL_SOURCES[family]:
@@ -123,7 +123,7 @@ def kernel_source_hash(family: str) -> str:
 
 
 def profiled_traffic(workload: str, family: str):
-    """DRAM bytes per launch from the committed ncu summary of this build, or None."""
+    """DRAM bytes per launch from the committed ncu summary of these sources, or None."""
     path = os.path.join(ROOT, "profiles", f"tc_gemm_{workload}.md")
     try:
         text = open(path).read()

@@ -10,7 +10,7 @@ its spread (max - min) / median.  A difference smaller than the spreads is
 not a result (the "Tuning Triton" skill page, section 2: compare a win to
 the noise floor).  Each workload runs in a child process, so a candidate
 that fails cannot take the sweep down with it (same page: probe abort-prone
-configurations in subprocesses and judge them by exit code).
+configurations in subprocesses and rate them by exit code).
 """
 from __future__ import annotations
 
