@@ -987,8 +987,11 @@ int gemm_run_host_batch(gemm_handle_t h, int n, const void* const* A, const void
     // The set's inputs are free once the GEMM that read them is done, its D
     // once that D has been copied out (an event never recorded is complete).
     if (!ok(cudaStreamWaitEvent(s_in, ev[1], 0))) return GEMM_ERR_CUDA;
-    if (!ok(cudaMemcpyAsync(buf[0], A[i], h->io_bytes[0], cudaMemcpyHostToDevice, s_in)) ||
-        !ok(cudaMemcpyAsync(buf[1], B[i], h->io_bytes[1], cudaMemcpyHostToDevice, s_in)))
+    // An empty operand (M, N or K zero) has no device copy and is not copied.
+    if ((h->io_bytes[0] &&
+         !ok(cudaMemcpyAsync(buf[0], A[i], h->io_bytes[0], cudaMemcpyHostToDevice, s_in))) ||
+        (h->io_bytes[1] &&
+         !ok(cudaMemcpyAsync(buf[1], B[i], h->io_bytes[1], cudaMemcpyHostToDevice, s_in))))
       return GEMM_ERR_CUDA;
     if (hc && !ok(cudaMemcpyAsync(buf[2], hc, h->io_bytes[2], cudaMemcpyHostToDevice, s_in)))
       return GEMM_ERR_CUDA;
@@ -998,7 +1001,8 @@ int gemm_run_host_batch(gemm_handle_t h, int n, const void* const* A, const void
     const int rc = gemm_run(h, buf[0], buf[1], hc ? buf[2] : nullptr, buf[3], s_gemm);
     if (rc != GEMM_OK) return rc;
     if (!ok(cudaEventRecord(ev[1], s_gemm)) || !ok(cudaStreamWaitEvent(s_out, ev[1], 0)) ||
-        !ok(cudaMemcpyAsync(D[i], buf[3], h->io_bytes[3], cudaMemcpyDeviceToHost, s_out)) ||
+        (h->io_bytes[3] &&
+         !ok(cudaMemcpyAsync(D[i], buf[3], h->io_bytes[3], cudaMemcpyDeviceToHost, s_out))) ||
         !ok(cudaEventRecord(ev[2], s_out)))
       return GEMM_ERR_CUDA;
   }
