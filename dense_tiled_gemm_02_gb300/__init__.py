@@ -10,7 +10,8 @@ Low-level names mirror ``include/gemm.h``: ``gemm_create``, ``gemm_run``,
 ``gemm_get_status``, ``gemm_destroy``, ``gemm_strerror``,
 ``gemm_plan_string``, ``gemm_workspace_bytes``, ``gemm_raster_tile``,
 ``gemm_debug_set``, ``gemm_timing_enable``, ``gemm_timing_read``,
-``gemm_host_io_enable``, ``gemm_run_host_batch``, ``gemm_pair_schedule``.
+``gemm_host_io_enable``, ``gemm_run_host_batch``, ``gemm_pair_schedule``,
+``gemm_decode_ring``.
 ``Gemm`` wraps a handle for torch tensors.
 """
 from __future__ import annotations
@@ -36,7 +37,8 @@ GEMM_DEBUG_SKIP_FIRST_FILL = 1
 EXPORTED = ["gemm_create", "gemm_run", "gemm_get_status", "gemm_destroy", "gemm_strerror",
             "gemm_plan_string", "gemm_workspace_bytes", "gemm_raster_tile", "gemm_debug_set",
             "gemm_run_splitk_noalloc", "gemm_timing_enable", "gemm_timing_read",
-            "gemm_host_io_enable", "gemm_run_host_batch", "gemm_pair_schedule"]
+            "gemm_host_io_enable", "gemm_run_host_batch", "gemm_pair_schedule",
+            "gemm_decode_ring"]
 GEMM_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
@@ -99,6 +101,8 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
     lib.gemm_timing_enable.restype = ci
     lib.gemm_timing_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ci]
     lib.gemm_timing_read.restype = ci
+    lib.gemm_decode_ring.argtypes = [ci, i64, ci, ctypes.POINTER(ci), ctypes.POINTER(i64)]
+    lib.gemm_decode_ring.restype = ci
     lib.gemm_host_io_enable.argtypes = [vp]
     lib.gemm_host_io_enable.restype = ci
     lib.gemm_run_host_batch.argtypes = [vp, ci, ctypes.POINTER(vp), ctypes.POINTER(vp),
@@ -169,6 +173,14 @@ def gemm_pair_schedule(tiles_m: int, tiles_n: int, group_m: int, num_kb: int, ks
             raise GemmError(rc, "gemm_pair_schedule")
         units.append(tuple(out))
     return units
+
+
+def gemm_decode_ring(M: int, K: int, cpb: int) -> tuple[int, int, int]:
+    """(stages, columns per stage, shared-memory bytes) of the decode kernel's
+    bulk-copy ring; stages < 0 is an error code."""
+    cps, smem = ctypes.c_int(), ctypes.c_int64()
+    rc = load().gemm_decode_ring(M, K, cpb, ctypes.byref(cps), ctypes.byref(smem))
+    return rc, cps.value, smem.value
 
 
 def gemm_timing_enable(h: int, n: int) -> int:

@@ -327,8 +327,7 @@ __global__ void __launch_bounds__(DB_THREADS) decode_bulk_kernel(const DecodeArg
 
 template <int MM, bool BF16>
 cudaError_t launch_bulk_mm(const DecodeArgs& d, cudaStream_t st) {
-  const size_t row = static_cast<size_t>(d.K) * sizeof(uint16_t);
-  const size_t smem = DB_BAR_BYTES + MM * row + static_cast<size_t>(d.stages) * d.cps * row;
+  const size_t smem = static_cast<size_t>(decode_bulk_smem(d.M, d.K, d.stages, d.cps));
   auto kernel = decode_bulk_kernel<MM, BF16>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
@@ -378,6 +377,12 @@ int decode_blocks_per_sm(int M, int kc) {
     return 1;
   }
   return n > 0 ? n : 1;
+}
+
+long long decode_bulk_smem(int M, long long K, int stages, int cps) {
+  const long long mm = M <= 1 ? 1 : M <= 2 ? 2 : 4;  // A rows the kernel is sized for
+  const long long row = K * static_cast<long long>(sizeof(uint16_t));
+  return DB_BAR_BYTES + mm * row + static_cast<long long>(stages) * cps * row;
 }
 
 int decode_bulk_ring(int M, long long K, int cpb, int* cps) {

@@ -419,6 +419,14 @@ int gemm_raster_tile(int64_t t, int64_t num_pid_m, int64_t num_pid_n, int64_t gr
   return GEMM_OK;
 }
 
+int gemm_decode_ring(int M, int64_t K, int cpb, int* cps, int64_t* smem_bytes) {
+  if (M < 1 || M > kDecodeMaxRows || K <= 0 || cpb < 1 || cpb > 32 || !cps || !smem_bytes)
+    return GEMM_ERR_INVALID_ARG;
+  const int stages = decode_bulk_ring(M, K, cpb, cps);
+  *smem_bytes = decode_bulk_smem(M, K, stages, *cps);
+  return stages;
+}
+
 int gemm_pair_schedule(int64_t tiles_m, int64_t tiles_n, int64_t group_m, int num_kb, int ksub,
                        int clusters, int stream_k, int cid, int i, int64_t* out) {
   if (tiles_m <= 0 || tiles_n <= 0 || group_m <= 0 || num_kb <= 0 || ksub <= 0 ||

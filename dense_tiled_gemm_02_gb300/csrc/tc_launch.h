@@ -111,6 +111,8 @@ cudaError_t launch_decode(const DecodeArgs& d, cudaStream_t st);
 // otherwise stages of *cps = 8 columns.  Returns the stage count (the form
 // needs every column to fit, or at least two stages).
 int decode_bulk_ring(int M, long long K, int cpb, int* cps);
+// Dynamic shared memory of one block of the bulk-copy form.
+long long decode_bulk_smem(int M, long long K, int stages, int cps);
 int decode_columns_per_block();
 // Resident blocks of the decode kernel per SM for M rows and slices of kc.
 int decode_blocks_per_sm(int M, int kc);

@@ -265,6 +265,18 @@ GEMM_API int gemm_pair_schedule(int64_t tiles_m, int64_t tiles_n, int64_t group_
                                 int64_t* out);
 
 /*
+ * gemm_decode_ring: host-side view of the shared-memory ring of the decode
+ * kernel's bulk-copy form (for tests; no device needed).  For M rows
+ * (1..4) of K elements and cpb columns per block it returns the number of
+ * ring stages and writes the columns per stage to *cps and the dynamic
+ * shared memory a block requests to *smem_bytes.  The form is taken only
+ * when stages * cps >= cpb (every column has a slot: one round trip) or
+ * stages >= 2 with cps = 8.  Returns GEMM_ERR_INVALID_ARG for M outside
+ * 1..4, K <= 0, cpb outside 1..32 or a null output pointer.
+ */
+GEMM_API int gemm_decode_ring(int M, int64_t K, int cpb, int* cps, int64_t* smem_bytes);
+
+/*
  * Test hooks (not for production use).
  * gemm_debug_set: flags bit 0 makes the load warp of the next gemm_run (the
  * copy thread, in the decode kernel's bulk-copy form) skip its first stage

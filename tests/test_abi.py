@@ -193,3 +193,36 @@ def test_pair_schedule_covers_every_tile_stage_once(tm, tn, group, nkb, ksub, cl
                 assert len(units) - 1 - waits[0] <= 1
     else:
         assert all(u[4] == 0 for units in sched for u in units)
+
+
+# ------------------------------------------------------------------ decode ring
+def test_decode_ring_fits_and_never_lets_a_warp_run_a_phase_ahead():
+    """The bulk-copy decode form's ring, over every row count, K (multiples
+    of 8 up to 20 000) and columns per block: a block's shared memory stays
+    within the 227 KB a CTA may have, stage fills stay below the mbarrier's
+    transaction limit, and either every column has a slot of its own or the
+    stages are eight columns wide (one per consumer warp), so that a warp's
+    parity waits see every phase in turn."""
+    n_taken = 0
+    for M in (1, 2, 3, 4):
+        mm = 1 if M == 1 else 2 if M == 2 else 4
+        for K in range(8, 20001, 8):
+            for cpb in (1, 2, 3, 5, 8, 9, 16, 17, 25, 27, 31, 32):
+                stages, cps, smem = pkg.gemm_decode_ring(M, K, cpb)
+                assert stages >= 0
+                if not (stages * cps >= cpb or stages >= 2):
+                    continue  # the planner keeps the split-K form
+                n_taken += 1
+                assert smem == 256 + mm * 2 * K + stages * cps * 2 * K
+                assert smem <= 227 * 1024, (M, K, cpb, stages, cps)
+                assert 1 <= stages <= 12
+                assert stages * cps >= cpb or cps == 8, (M, K, cpb, stages, cps)
+                assert cps * 2 * K < 1 << 20 and M * 2 * K < 1 << 20
+    assert n_taken > 50_000
+    # the 4096-column decode shape: 27 columns per block, one slot each
+    assert pkg.gemm_decode_ring(1, 4096, 27)[:2] == (9, 3)
+
+
+def test_decode_ring_rejects_bad_arguments():
+    for args in ((0, 4096, 27), (5, 4096, 27), (1, 0, 27), (1, 4096, 0), (1, 4096, 33)):
+        assert pkg.gemm_decode_ring(*args)[0] == pkg.GEMM_ERR_INVALID_ARG
