@@ -10,6 +10,8 @@ compiler and exposes it through ctypes over numpy arrays:
 
 * ``gemm_f64_rows`` / ``gemm_f64_points``: fp16/bf16 operands, the sum in fp64,
   plus the sum of absolute products used by the error bound.
+* ``gemm_mx_rows``: the block-scaled form of the 8-bit float product (one
+  E8M0 power-of-two scale per 32 K elements of each row of A and column of B).
 * ``gemm_i64_rows`` / ``gemm_i64_points``: int8 operands, int32 C, int64 sum.
 * ``round_bits`` / ``widen_bits``: one correct round-to-nearest-even from fp64
   to fp16/bf16, and the exact inverse widening; ``widen_bits8`` the exact
@@ -86,6 +88,9 @@ class Oracle:
         lib.oracle_gemm_f64_points.argtypes = [_i64, _i64, _i64, _int, _int, _int, _int, _int,
                                                _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _i64,
                                                _vp, _vp]
+        lib.oracle_gemm_mx_rows.argtypes = [_i64, _i64, _i64, _int, _int, _int, _int, _int,
+                                            _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp,
+                                            _i64, _vp, _vp]
         lib.oracle_gemm_i64_rows.argtypes = [_i64, _i64, _i64, _int, _int, _int,
                                              _i64, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp]
         lib.oracle_gemm_i64_points.argtypes = [_i64, _i64, _i64, _int, _int, _int,
@@ -137,6 +142,33 @@ class Oracle:
                                             _ptr(rows_a), nr, _ptr(D), _ptr(S))
         if rc != 0:
             raise ValueError(f"oracle_gemm_f64_rows failed ({rc})")
+        return D, S
+
+    def gemm_mx_rows(self, M, N, K, A, B, C, SA, SB, *, ab_type, c_type=BF16, a_col=0,
+                     b_col=0, c_col=0, lda=None, ldb=None, ldc=None, rows=None):
+        """Block-scaled 8-bit float product: D (and S = sum |scaled a * scaled b|)
+        for the listed rows.  SA is M x ceil(K/32), SB is N x ceil(K/32), both
+        uint8 E8M0 exponents (scale 2^(e-127)) of 32-element K blocks."""
+        lda = lda if lda is not None else (M if a_col else K)
+        ldb = ldb if ldb is not None else (K if b_col else N)
+        ldc = ldc if ldc is not None else (M if c_col else N)
+        nb = (K + 31) // 32
+        SA = np.ascontiguousarray(SA, dtype=np.uint8)
+        SB = np.ascontiguousarray(SB, dtype=np.uint8)
+        if SA.shape != (M, nb) or SB.shape != (N, nb):
+            raise ValueError(f"scale shapes {SA.shape}, {SB.shape}; want {(M, nb)}, {(N, nb)}")
+        rows_a = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        nr = M if rows_a is None else rows_a.size
+        D = np.empty((nr, N), dtype=np.float64)
+        S = np.empty((nr, N), dtype=np.float64)
+        A = np.ascontiguousarray(A)
+        B = np.ascontiguousarray(B)
+        C = None if C is None else np.ascontiguousarray(C)
+        rc = self._lib.oracle_gemm_mx_rows(M, N, K, ab_type, c_type, a_col, b_col, c_col,
+                                           lda, ldb, ldc, _ptr(A), _ptr(B), _ptr(C), _ptr(SA),
+                                           _ptr(SB), _ptr(rows_a), nr, _ptr(D), _ptr(S))
+        if rc != 0:
+            raise ValueError(f"oracle_gemm_mx_rows failed ({rc})")
         return D, S
 
     def gemm_f64_points(self, M, N, K, A, B, C, pi, pj, *, ab_type, c_type=BF16, a_col=0,

@@ -68,7 +68,11 @@
  *   6: integer sum starts at k = 1
  *   7: subnormal scale off by a factor of two in the widening
  *   8: A's k index reversed (A[i, K-1-k] paired with B[k, j])
- *   9: E4M3 read with IEEE specials (exponent field 15 as inf / NaN) */
+ *   9: E4M3 read with IEEE specials (exponent field 15 as inf / NaN)
+ *  10: block-scaled product with blocks of 16 K elements instead of 32
+ *  11: E8M0 scale read with bias 128 instead of 127
+ *  12: block-scaled product ignores B's scales
+ *  13: block-scaled product applies each row's first block scale to all K */
 #ifndef ORACLE_MUTANT
 #define ORACLE_MUTANT 0
 #endif
@@ -341,6 +345,111 @@ int oracle_gemm_f64_points(int64_t M, int64_t N, int64_t K, int ab_type, int c_t
     D[q] = d;
     if (S) S[q] = s;
   }
+  return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Block-scaled 8-bit float product (microscaling).
+ *
+ * The pages name a scaled low-precision matrix product (the mfma_scaled
+ * entry point of the "Tuning Triton" page, section 6, for the microscaled
+ * data types) without defining the scaling.  The plain reading is the OCP
+ * Microscaling (MX) definition: along K, every block of 32 consecutive
+ * elements of a row of A (and of a column of B) shares one scale X, stored
+ * as an 8-bit power-of-two exponent (E8M0: X = 2^(e - 127), e = 255 is NaN);
+ * the element's value is X times its 8-bit float value.  So
+ *
+ *   D[i,j] = C[i,j] + sum_k (XA[i, k/32] A[i,k]) * (XB[j, k/32] B[k,j])
+ *
+ * with k ascending and C added after the sum, as above.  Every product is
+ * exact in fp64 (8-bit floats times powers of two within 2^+-254).  A last
+ * block shorter than 32 (K not a multiple of 32) keeps its own scale.
+ *   SA: M x nb scale exponents, row-major (SA[i*nb + b]), nb = ceil(K/32);
+ *   SB: N x nb scale exponents, row-major (SB[j*nb + b]) -- per column of B.
+ * Rows variant only (D, S, rows, C as in oracle_gemm_f64_rows).
+ * ------------------------------------------------------------------------- */
+/* Scale block of element k (nb blocks per row). */
+static int64_t mx_block(int64_t k, int64_t nb) {
+#if ORACLE_MUTANT == 10
+  return (k / 16) % nb; /* kept inside the row's nb scales */
+#else
+  (void)nb;
+  return k / 32;
+#endif
+}
+
+static double e8m0(uint8_t e) {
+  if (e == 255) return NAN;
+#if ORACLE_MUTANT == 11
+  return ldexp(1.0, (int)e - 128);
+#else
+  return ldexp(1.0, (int)e - 127);
+#endif
+}
+
+int oracle_gemm_mx_rows(int64_t M, int64_t N, int64_t K, int ab_type, int c_type,
+                        int a_col, int b_col, int c_col,
+                        int64_t lda, int64_t ldb, int64_t ldc,
+                        const void* A, const void* B, const void* C,
+                        const uint8_t* SA, const uint8_t* SB,
+                        const int64_t* rows, int64_t nrows, double* D, double* S) {
+  if (M < 0 || N < 0 || K < 0 || (ab_type != OR_E4M3 && ab_type != OR_E5M2) ||
+      !fp_types_ok(ab_type, c_type, C) || (K > 0 && (!SA || !SB)))
+    return -1;
+  const int64_t nr = rows ? nrows : M;
+  for (int64_t q = 0; q < nr; ++q)
+    if (rows && (rows[q] < 0 || rows[q] >= M)) return -1;
+  if (nr == 0 || N == 0) return 0;
+  const int64_t nb = (K + 31) / 32; /* scale blocks per row (the stored layout) */
+
+  /* B widened and scaled once: Bw[k*N + j] = XB[j, k/32] * B[k,j]. */
+  double* Bw = (double*)malloc((size_t)(K > 0 ? K : 1) * (size_t)N * sizeof(double));
+  double* Aw = (double*)malloc((size_t)(K > 0 ? K : 1) * (size_t)nr * sizeof(double));
+  if (!Bw || !Aw) {
+    free(Bw);
+    free(Aw);
+    return -2;
+  }
+#pragma omp parallel for schedule(static)
+  for (int64_t k = 0; k < K; ++k)
+    for (int64_t j = 0; j < N; ++j) {
+#if ORACLE_MUTANT == 12
+      const double xb = 1.0;
+#else
+      const double xb = e8m0(SB[j * nb + mx_block(k, nb)]);
+#endif
+      Bw[k * N + j] = xb * load_f(B, ab_type, at(k, j, b_col, ldb));
+    }
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t q = 0; q < nr; ++q) {
+    const int64_t i = rows ? rows[q] : q;
+    double* a = Aw + q * K;
+    double* d = D + q * N;
+    double* s = S ? S + q * N : NULL;
+    for (int64_t k = 0; k < K; ++k) {
+#if ORACLE_MUTANT == 13
+      const double xa = e8m0(SA[i * nb]);
+#else
+      const double xa = e8m0(SA[i * nb + mx_block(k, nb)]);
+#endif
+      a[k] = xa * load_f(A, ab_type, at_a(i, k, M, K, a_col, lda));
+    }
+    for (int64_t j = 0; j < N; ++j) d[j] = 0.0;
+    if (s)
+      for (int64_t j = 0; j < N; ++j) s[j] = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      const double aik = a[k];
+      const double* brow = Bw + k * N;
+      for (int64_t j = 0; j < N; ++j) d[j] += aik * brow[j];
+      if (s)
+        for (int64_t j = 0; j < N; ++j) s[j] += fabs(aik * brow[j]);
+    }
+    if (C)
+      for (int64_t j = 0; j < N; ++j) d[j] = add_c(d[j], load_f(C, c_type, at(i, j, c_col, ldc)));
+  }
+  free(Bw);
+  free(Aw);
   return 0;
 }
 

@@ -16,7 +16,10 @@ What pins what:
   {1,2,3}^3 and every layout, closed forms (identity, permutation, rank-1,
   all-ones, linearity), and torch's CPU int64 matmul for int8; for the
   8-bit float types, the exact rational evaluation on tiny shapes and the
-  identity and all-ones closed forms.
+  identity and all-ones closed forms; for their block-scaled form, the
+  unscaled product at unit scales, the exact rational value of the
+  microscaling definition, power-of-two scaling of a row or column, and NaN
+  scales.
 """
 from __future__ import annotations
 
@@ -140,6 +143,91 @@ def pin_fp8_gemm(orc):
             D, S = orc.gemm_f64_rows(3, 2, K, fp8_bits(np.ones((3, K)), t),
                                      fp8_bits(np.ones((K, 2)), t), None, ab_type=t)
             assert np.all(D == K) and np.all(S == K)
+
+
+def _mx_exact(Ab, Bb, SA, SB, C, t):
+    """Exact rational value and magnitude sum of the block-scaled product from
+    the microscaling definition: element (i, k) of A is 2^(SA[i, k//32] - 127)
+    times its 8-bit float value, element (k, j) of B 2^(SB[j, k//32] - 127)
+    times its value (decoded by exact_ref, independently of the oracle)."""
+    M, K = Ab.shape
+    N = Bb.shape[1]
+    x = lambda e: Fraction(2) ** (int(e) - 127)
+    A = [[x(SA[i, k // 32]) * exact_ref.decode(int(Ab[i, k]), t) for k in range(K)]
+         for i in range(M)]
+    B = [[x(SB[j, k // 32]) * exact_ref.decode(int(Bb[k, j]), t) for j in range(N)]
+         for k in range(K)]
+    D = [[sum((A[i][k] * B[k][j] for k in range(K)), Fraction(0)) +
+          (Fraction(float(C[i, j])) if C is not None else 0) for j in range(N)] for i in range(M)]
+    S = [[sum((abs(A[i][k] * B[k][j]) for k in range(K)), Fraction(0)) for j in range(N)]
+         for i in range(M)]
+    return D, S
+
+
+def pin_mx_gemm(orc):
+    """Block-scaled 8-bit float product.  (1) With every scale 2^0 (exponent
+    127) it is the unscaled product, bit for bit; (2) on tiny shapes with
+    random scales and K across block boundaries it matches the exact rational
+    value of the microscaling definition within fp64's summation bound;
+    (3) raising all of a row's (a column's) scales by t multiplies that row
+    (column) of D - C by 2^t exactly; (4) a NaN scale (exponent 255) makes
+    its row NaN."""
+    rng = np.random.default_rng(29)
+    for t in (E4M3, E5M2):
+        # (1) unit scales reduce to the unscaled product
+        for (M, N, K), (a_col, b_col) in itertools.product(
+                [(3, 5, 1), (4, 3, 33), (2, 6, 70), (5, 4, 96)], itertools.product((0, 1), repeat=2)):
+            _, Ab = _rand_fp8(rng, (M, K), t)
+            _, Bb = _rand_fp8(rng, (K, N), t)
+            C = (rng.integers(-64, 64, size=(M, N)) / 16).astype(np.float32)
+            nb = (K + 31) // 32
+            one_a = np.full((M, nb), 127, np.uint8)
+            one_b = np.full((N, nb), 127, np.uint8)
+            a, b = to_storage(Ab, a_col), to_storage(Bb, b_col)
+            D, S = orc.gemm_mx_rows(M, N, K, a, b, C, one_a, one_b, ab_type=t, c_type=F32,
+                                    a_col=a_col, b_col=b_col)
+            D0, S0 = orc.gemm_f64_rows(M, N, K, a, b, C, ab_type=t, c_type=F32, a_col=a_col,
+                                       b_col=b_col)
+            assert np.array_equal(D, D0) and np.array_equal(S, S0), (t, M, N, K)
+        # (2) exact rational value, random scales
+        for (M, N, K), (a_col, b_col) in itertools.product(
+                [(1, 1, 1), (2, 3, 31), (3, 2, 32), (2, 2, 33), (3, 3, 70)],
+                itertools.product((0, 1), repeat=2)):
+            _, Ab = _rand_fp8(rng, (M, K), t)
+            _, Bb = _rand_fp8(rng, (K, N), t)
+            C = (rng.integers(-64, 64, size=(M, N)) / 16).astype(np.float32)
+            nb = (K + 31) // 32
+            SA = rng.integers(118, 137, size=(M, nb)).astype(np.uint8)
+            SB = rng.integers(118, 137, size=(N, nb)).astype(np.uint8)
+            D, S = orc.gemm_mx_rows(M, N, K, to_storage(Ab, a_col), to_storage(Bb, b_col), C,
+                                    SA, SB, ab_type=t, c_type=F32, a_col=a_col, b_col=b_col)
+            ex, exs = _mx_exact(Ab, Bb, SA, SB, C, t)
+            for i in range(M):
+                for j in range(N):
+                    bound = Fraction(K + 1, 2 ** 52) * (exs[i][j] + abs(Fraction(float(C[i, j]))))
+                    assert abs(Fraction(float(D[i, j])) - ex[i][j]) <= bound, (t, M, N, K, i, j)
+                    assert abs(Fraction(float(S[i, j])) - exs[i][j]) <= bound, (t, M, N, K, i, j)
+        # (3) a row's / a column's scales raised by t2: that row / column times 2^t2
+        M, N, K = 4, 5, 100
+        _, Ab = _rand_fp8(rng, (M, K), t)
+        _, Bb = _rand_fp8(rng, (K, N), t)
+        SA = rng.integers(120, 135, size=(M, 4)).astype(np.uint8)
+        SB = rng.integers(120, 135, size=(N, 4)).astype(np.uint8)
+        D, _ = orc.gemm_mx_rows(M, N, K, Ab, Bb, None, SA, SB, ab_type=t)
+        SA2 = SA.copy()
+        SA2[2] += 3
+        D2, _ = orc.gemm_mx_rows(M, N, K, Ab, Bb, None, SA2, SB, ab_type=t)
+        assert np.array_equal(D2[2], D[2] * 8) and np.array_equal(np.delete(D2, 2, 0),
+                                                                  np.delete(D, 2, 0))
+        SB2 = SB.copy()
+        SB2[4] -= 2
+        D3, _ = orc.gemm_mx_rows(M, N, K, Ab, Bb, None, SA, SB2, ab_type=t)
+        assert np.array_equal(D3[:, 4], D[:, 4] / 4) and np.array_equal(D3[:, :4], D[:, :4])
+        # (4) a NaN scale poisons its row (every column reads that block)
+        SA3 = SA.copy()
+        SA3[1, 3] = 255
+        D4, _ = orc.gemm_mx_rows(M, N, K, Ab, Bb, None, SA3, SB, ab_type=t)
+        assert np.isnan(D4[1]).all() and np.array_equal(np.delete(D4, 1, 0), np.delete(D, 1, 0))
 
 
 # ----------------------------------------------------------------------------- rounding
@@ -344,7 +432,7 @@ def pin_int8(orc):
 
 PINS = [pin_widen_exhaustive, pin_round_midpoints, pin_round_vs_libraries, pin_round_vs_exact,
         pin_brute_force_tiny, pin_closed_forms, pin_views_agree, pin_int8, pin_widen_fp8,
-        pin_fp8_gemm]
+        pin_fp8_gemm, pin_mx_gemm]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -365,7 +453,7 @@ def test_oracle_threads(orc):
     assert orc.threads() >= 1
 
 
-@pytest.mark.parametrize("mutant", range(1, 10))
+@pytest.mark.parametrize("mutant", range(1, 14))
 def test_pins_catch_planted_mistakes(mutant):
     with tempfile.TemporaryDirectory() as d:
         path = oracle.compile_library(os.path.join(d, f"liboracle_m{mutant}.so"), mutant=mutant)
