@@ -422,6 +422,9 @@ DECODE_CASES = [
     (1, 4096, 4096, ROW, BF16, BF16, BF16, ROW, 1),   # B not 16-byte aligned: 2-byte loads
     (1, 333, 2312, ROW, F16, F16, F16, ROW, 0),       # K slices not a multiple of 4 steps
     (4, 64, 8192, ROW, BF16, BF16, BF16, ROW, 0),
+    (4, 4096, 4096, ROW, BF16, BF16, BF16, ROW, 0),   # bulk form: 8-column stages, reused
+    (1, 8192, 4096, ROW, BF16, None, BF16, ROW, 0),   # bulk form: two waves of blocks
+    (2, 4096, 2048, ROW, F16, F16, F32, COL, 0),      # bulk form: a slot per column, fp32 D
 ]
 
 
