@@ -311,6 +311,7 @@ int plan_decode(gemm_plan* h, int sms) {
   }
   if (cudaMalloc(&h->status, 256) != cudaSuccess || cudaMemset(h->status, 0, 256) != cudaSuccess) {
     cudaGetLastError();
+    if (h->status) cudaFree(h->status);
     cudaFree(h->ws);
     return GEMM_ERR_ALLOC_FAILED;
   }
@@ -675,6 +676,7 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   }
   if (cudaMalloc(&h->status, 256) != cudaSuccess || cudaMemset(h->status, 0, 256) != cudaSuccess) {
     cudaGetLastError();
+    if (h->status) cudaFree(h->status);
     if (h->ws) cudaFree(h->ws);
     delete h;
     return GEMM_ERR_ALLOC_FAILED;
