@@ -482,6 +482,24 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   h->f8 = is_f8(static_cast<int>(d.ab_type));
   h->mab_type = h->i8x ? static_cast<int>(T_BF16) : static_cast<int>(d.ab_type);
 
+  if (d.M == 0 || d.N == 0) {
+    // An empty D: nothing to read, compute or store (gemm_run returns at
+    // once).  No plan, no workspace; the status word keeps gemm_get_status
+    // uniform.  The planners below divide by tile and column-block counts.
+    h->M = d.M;
+    h->N = d.N;
+    h->K = d.K;
+    if (cudaMalloc(&h->status, 256) != cudaSuccess ||
+        cudaMemset(h->status, 0, 256) != cudaSuccess) {
+      cudaGetLastError();
+      if (h->status) cudaFree(h->status);
+      delete h;
+      return GEMM_ERR_ALLOC_FAILED;
+    }
+    make_plan_string(h);
+    *out = h;
+    return GEMM_OK;
+  }
   h->choice = choose_plan(d.M, d.N, d.K, d.ab_type, d.layout_a, d.layout_b, sms);
   apply_force_plan(h->choice);
   if (!h->choice.no_decode && (d.ab_type == GEMM_F16 || d.ab_type == GEMM_BF16) && d.M >= 1 &&
@@ -690,7 +708,9 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
 
 int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
              gemm_stream_t stream) {
-  if (!h || !D || (h->desc.K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  if (h->desc.M == 0 || h->desc.N == 0) return GEMM_OK;  // an empty D: nothing to do
+  if (!D || (h->desc.K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
   const gemm_desc_t& d = h->desc;
   const int es_ab = elem_size(d.ab_type);
   const int es_c = elem_size(d.c_type);
@@ -702,7 +722,6 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) return GEMM_ERR_INVALID_ARG;
-  if (d.M == 0 || d.N == 0) return GEMM_OK;
 
   KParams kp = h->kp;
   kp.C = C;
@@ -958,6 +977,8 @@ int gemm_host_io_enable(gemm_handle_t h) {
   h->io_bytes[1] = span_bytes(d.layout_b, d.K, d.N, d.ldb, elem_size(d.ab_type));
   h->io_bytes[2] = d.c_type ? span_bytes(d.layout_c, d.M, d.N, d.ldc, elem_size(d.c_type)) : 0;
   h->io_bytes[3] = span_bytes(d.layout_d, d.M, d.N, d.ldd, elem_size(d.d_type));
+  if (d.M == 0 || d.N == 0)  // an empty D reads nothing: no operand is copied
+    for (size_t& b : h->io_bytes) b = 0;
   bool ok = true;
   for (int s = 0; s < 2 && ok; ++s)
     for (int k = 0; k < 4 && ok; ++k)
@@ -981,8 +1002,9 @@ int gemm_run_host_batch(gemm_handle_t h, int n, const void* const* A, const void
                         const void* const* C, void* const* D, gemm_stream_t stream) {
   if (!h || n < 0 || (n > 0 && (!A || !B || !D))) return GEMM_ERR_INVALID_ARG;
   if (!h->io_ready) return GEMM_ERR_INVALID_ARG;
-  for (int i = 0; i < n; ++i)  // nothing is enqueued unless every pointer is there
-    if (!A[i] || !B[i] || !D[i]) return GEMM_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i)  // nothing is enqueued unless every pointer needed is there
+    if ((h->io_bytes[0] && !A[i]) || (h->io_bytes[1] && !B[i]) || (h->io_bytes[3] && !D[i]))
+      return GEMM_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaStream_t s_in = h->io_stream[0], s_gemm = h->io_stream[1], s_out = h->io_stream[2];
   auto ok = [](cudaError_t e) { return e == cudaSuccess; };

@@ -121,7 +121,9 @@ GEMM_API int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc);
  * aligned workspace copy, but a base pointer that is not 16-byte aligned
  * while its rows are is rejected with GEMM_ERR_MISALIGNED (the handle has
  * no copy for it).  The decode path (M <= 4, K-contiguous B) and C / D
- * accept any element-aligned pointer.  D may alias C only when both have the same
+ * accept any element-aligned pointer.  An empty D (M or N zero) returns
+ * GEMM_OK at once without looking at the pointers; K zero gives D = C
+ * (A and B may then be NULL).  D may alias C only when both have the same
  * type, layout and leading dimension; D must not overlap A or B.
  * One handle must not be used by two streams at the same time (its
  * workspace and status word are shared by its calls).
@@ -240,7 +242,8 @@ GEMM_API int gemm_timing_read(gemm_handle_t h, float* ms, int n);
  * overlap; a second call on the same stream starts after the first one's
  * last output copy, so pass a stream of products in one call.  The caller keeps the host
  * buffers untouched until then.  Returns GEMM_OK, GEMM_ERR_INVALID_ARG (no
- * gemm_host_io_enable, a null pointer), or what gemm_run returns.
+ * gemm_host_io_enable, a null pointer for an operand with elements), or
+ * what gemm_run returns.
  */
 GEMM_API int gemm_host_io_enable(gemm_handle_t h);
 GEMM_API int gemm_run_host_batch(gemm_handle_t h, int n, const void* const* A,

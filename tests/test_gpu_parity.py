@@ -233,6 +233,38 @@ def test_k_zero_gives_c():
     assert torch.equal(D, inp["C"].float())
 
 
+@pytest.mark.parametrize("M,N,K,b_col", [(0, 100, 2048, ROW), (1, 0, 4096, COL), (0, 0, 0, ROW),
+                                         (3, 0, 300, COL), (0, 4096, 4096, COL)])
+def test_empty_output(M, N, K, b_col):
+    """M or N zero: planning succeeds (the decode and split-K planners are
+    not reached), gemm_run and the host-buffer batch return at once, the
+    status is clean, and the next handle on the context works."""
+    dev = torch.device("cuda")
+    A = torch.zeros(M, K, dtype=torch.bfloat16, device=dev)
+    Bs = torch.zeros((N, K) if b_col else (K, N), dtype=torch.bfloat16, device=dev)
+    B = Bs.t() if b_col else Bs
+    C = torch.zeros(M, N, dtype=torch.bfloat16, device=dev)
+    D = torch.zeros(M, N, dtype=torch.bfloat16, device=dev)
+    desc = pkg.GemmDesc(M, N, K, pkg.GEMM_BF16, pkg.GEMM_BF16, pkg.GEMM_BF16, pkg.GEMM_ROW_MAJOR,
+                        b_col, pkg.GEMM_ROW_MAJOR, pkg.GEMM_ROW_MAJOR, max(K, 1),
+                        max(K, 1) if b_col else max(N, 1), max(N, 1), max(N, 1))
+    g = pkg.Gemm(desc)
+    try:
+        assert pkg.gemm_workspace_bytes(g.handle) == 0, g.plan()
+        assert pkg.gemm_run(g.handle, A.data_ptr(), B.data_ptr(), C.data_ptr(), D.data_ptr(),
+                            None) == pkg.GEMM_OK
+        assert pkg.gemm_run(g.handle, None, None, None, None, None) == pkg.GEMM_OK
+        g.host_io_enable()
+        assert pkg.gemm_run_host_batch(g.handle, [None], [None], None, [None], None) == pkg.GEMM_OK
+        assert g.status(torch.cuda.current_stream()) == pkg.GEMM_OK
+    finally:
+        g.close()
+    w = WORKLOADS["rag1000_bf16"]
+    inp = make_inputs(w)
+    Dn, p = run_gpu(w, inp)
+    _assert_ok(check_rows(w, inp, Dn, rows=[0, 999]), p)
+
+
 def test_guard_bands_untouched():
     """D written into a larger buffer (ldd > N, extra rows): canaries survive."""
     M, N, K = 200, 300, 130
