@@ -142,8 +142,9 @@ GEMM_API int gemm_run(gemm_handle_t h, const void* A, const void* B, const void*
  */
 GEMM_API int gemm_get_status(gemm_handle_t h, gemm_stream_t stream);
 
-/* gemm_destroy: free the handle's workspace and status word (after
- * synchronising the device work that may still use them).  NULL is a no-op. */
+/* gemm_destroy: free the handle's workspace and status word, and the device
+ * copies, streams and events of gemm_host_io_enable (after synchronising the
+ * device work that may still use them).  NULL is a no-op. */
 GEMM_API int gemm_destroy(gemm_handle_t h);
 
 /* gemm_strerror: static description of a status code. */
