@@ -72,7 +72,12 @@
  *  10: block-scaled product with blocks of 16 K elements instead of 32
  *  11: E8M0 scale read with bias 128 instead of 127
  *  12: block-scaled product ignores B's scales
- *  13: block-scaled product applies each row's first block scale to all K */
+ *  13: block-scaled product applies each row's first block scale to all K
+ *  14: C's storage order ignored (C always read row-major)
+ *  15: a square B read transposed
+ *  16: the rows variant ignores its row list (output row q from A's row q)
+ *  17: the points variant swaps the coordinates of square problems
+ *  18: the magnitude sum S adds signed products */
 #ifndef ORACLE_MUTANT
 #define ORACLE_MUTANT 0
 #endif
@@ -233,6 +238,66 @@ static double load_f(const void* base, int t, int64_t idx) {
   }
 }
 
+/* Element (i, j) of C. */
+static int64_t at_c(int64_t i, int64_t j, int col_major, int64_t ld) {
+#if ORACLE_MUTANT == 14
+  (void)col_major;
+  return at(i, j, 0, ld);
+#else
+  return at(i, j, col_major, ld);
+#endif
+}
+
+/* Element (k, j) of B, a K x N operand. */
+static int64_t at_b(int64_t k, int64_t j, int64_t K, int64_t N, int col_major, int64_t ld) {
+#if ORACLE_MUTANT == 15
+  if (K == N) return at(j, k, col_major, ld);
+#endif
+  (void)K;
+  (void)N;
+  return at(k, j, col_major, ld);
+}
+
+/* |p| for the magnitude sum S of the error bound. */
+static double mag(double p) {
+#if ORACLE_MUTANT == 18
+  return p;
+#else
+  return fabs(p);
+#endif
+}
+
+/* Output row of entry q of a rows call (rows == NULL: every row). */
+static int64_t row_of(const int64_t* rows, int64_t q, int64_t M) {
+#if ORACLE_MUTANT == 16
+  return rows ? q % M : q;
+#else
+  (void)M;
+  return rows ? rows[q] : q;
+#endif
+}
+
+/* Coordinates of point q of a points call. */
+static int64_t point_row(const int64_t* pi, const int64_t* pj, int64_t q, int64_t M, int64_t N) {
+#if ORACLE_MUTANT == 17
+  if (M == N) return pj[q];
+#endif
+  (void)pj;
+  (void)M;
+  (void)N;
+  return pi[q];
+}
+
+static int64_t point_col(const int64_t* pi, const int64_t* pj, int64_t q, int64_t M, int64_t N) {
+#if ORACLE_MUTANT == 17
+  if (M == N) return pi[q];
+#endif
+  (void)pi;
+  (void)M;
+  (void)N;
+  return pj[q];
+}
+
 static double add_c(double sum, double c) {
 #if ORACLE_MUTANT == 2
   (void)c;
@@ -288,11 +353,11 @@ int oracle_gemm_f64_rows(int64_t M, int64_t N, int64_t K, int ab_type, int c_typ
   }
 #pragma omp parallel for schedule(static)
   for (int64_t k = 0; k < K; ++k)
-    for (int64_t j = 0; j < N; ++j) Bw[k * N + j] = load_f(B, ab_type, at(k, j, b_col, ldb));
+    for (int64_t j = 0; j < N; ++j) Bw[k * N + j] = load_f(B, ab_type, at_b(k, j, K, N, b_col, ldb));
 
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t q = 0; q < nr; ++q) {
-    const int64_t i = rows ? rows[q] : q;
+    const int64_t i = row_of(rows, q, M);
     double* a = Aw + q * K;
     double* d = D + q * N;
     double* s = S ? S + q * N : NULL;
@@ -306,10 +371,10 @@ int oracle_gemm_f64_rows(int64_t M, int64_t N, int64_t K, int ab_type, int c_typ
       const double* brow = Bw + k * N;
       for (int64_t j = 0; j < N; ++j) d[j] += aik * brow[j];
       if (s)
-        for (int64_t j = 0; j < N; ++j) s[j] += fabs(aik * brow[j]);
+        for (int64_t j = 0; j < N; ++j) s[j] += mag(aik * brow[j]);
     }
     if (C)
-      for (int64_t j = 0; j < N; ++j) d[j] = add_c(d[j], load_f(C, c_type, at(i, j, c_col, ldc)));
+      for (int64_t j = 0; j < N; ++j) d[j] = add_c(d[j], load_f(C, c_type, at_c(i, j, c_col, ldc)));
   }
   free(Bw);
   free(Aw);
@@ -332,16 +397,16 @@ int oracle_gemm_f64_points(int64_t M, int64_t N, int64_t K, int ab_type, int c_t
     if (pi[q] < 0 || pi[q] >= M || pj[q] < 0 || pj[q] >= N) return -1;
 #pragma omp parallel for schedule(static)
   for (int64_t q = 0; q < npts; ++q) {
-    const int64_t i = pi[q], j = pj[q];
+    const int64_t i = point_row(pi, pj, q, M, N), j = point_col(pi, pj, q, M, N);
     double d = 0.0, s = 0.0;
     const int64_t ke = k_end(K);
     for (int64_t k = 0; k < ke; ++k) {
       const double p = load_f(A, ab_type, at_a(i, k, M, K, a_col, lda)) *
-                       load_f(B, ab_type, at(k, j, b_col, ldb));
+                       load_f(B, ab_type, at_b(k, j, K, N, b_col, ldb));
       d += p;
-      s += fabs(p);
+      s += mag(p);
     }
-    if (C) d = add_c(d, load_f(C, c_type, at(i, j, c_col, ldc)));
+    if (C) d = add_c(d, load_f(C, c_type, at_c(i, j, c_col, ldc)));
     D[q] = d;
     if (S) S[q] = s;
   }
@@ -418,12 +483,12 @@ int oracle_gemm_mx_rows(int64_t M, int64_t N, int64_t K, int ab_type, int c_type
 #else
       const double xb = e8m0(SB[j * nb + mx_block(k, nb)]);
 #endif
-      Bw[k * N + j] = xb * load_f(B, ab_type, at(k, j, b_col, ldb));
+      Bw[k * N + j] = xb * load_f(B, ab_type, at_b(k, j, K, N, b_col, ldb));
     }
 
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t q = 0; q < nr; ++q) {
-    const int64_t i = rows ? rows[q] : q;
+    const int64_t i = row_of(rows, q, M);
     double* a = Aw + q * K;
     double* d = D + q * N;
     double* s = S ? S + q * N : NULL;
@@ -443,10 +508,10 @@ int oracle_gemm_mx_rows(int64_t M, int64_t N, int64_t K, int ab_type, int c_type
       const double* brow = Bw + k * N;
       for (int64_t j = 0; j < N; ++j) d[j] += aik * brow[j];
       if (s)
-        for (int64_t j = 0; j < N; ++j) s[j] += fabs(aik * brow[j]);
+        for (int64_t j = 0; j < N; ++j) s[j] += mag(aik * brow[j]);
     }
     if (C)
-      for (int64_t j = 0; j < N; ++j) d[j] = add_c(d[j], load_f(C, c_type, at(i, j, c_col, ldc)));
+      for (int64_t j = 0; j < N; ++j) d[j] = add_c(d[j], load_f(C, c_type, at_c(i, j, c_col, ldc)));
   }
   free(Bw);
   free(Aw);
@@ -478,11 +543,11 @@ int oracle_gemm_i64_rows(int64_t M, int64_t N, int64_t K, int a_col, int b_col, 
   if (!Bw) return -2;
 #pragma omp parallel for schedule(static)
   for (int64_t k = 0; k < K; ++k)
-    for (int64_t j = 0; j < N; ++j) Bw[k * N + j] = B[at(k, j, b_col, ldb)];
+    for (int64_t j = 0; j < N; ++j) Bw[k * N + j] = B[at_b(k, j, K, N, b_col, ldb)];
 
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t q = 0; q < nr; ++q) {
-    const int64_t i = rows ? rows[q] : q;
+    const int64_t i = row_of(rows, q, M);
     int64_t* d = D + q * N;
     for (int64_t j = 0; j < N; ++j) d[j] = 0;
     for (int64_t k = int_k_begin(); k < K; ++k) {
@@ -491,7 +556,7 @@ int oracle_gemm_i64_rows(int64_t M, int64_t N, int64_t K, int a_col, int b_col, 
       for (int64_t j = 0; j < N; ++j) d[j] += aik * brow[j];
     }
     if (C)
-      for (int64_t j = 0; j < N; ++j) d[j] += C[at(i, j, c_col, ldc)];
+      for (int64_t j = 0; j < N; ++j) d[j] += C[at_c(i, j, c_col, ldc)];
   }
   free(Bw);
   return 0;
@@ -506,11 +571,11 @@ int oracle_gemm_i64_points(int64_t M, int64_t N, int64_t K, int a_col, int b_col
     if (pi[q] < 0 || pi[q] >= M || pj[q] < 0 || pj[q] >= N) return -1;
 #pragma omp parallel for schedule(static)
   for (int64_t q = 0; q < npts; ++q) {
-    const int64_t i = pi[q], j = pj[q];
+    const int64_t i = point_row(pi, pj, q, M, N), j = point_col(pi, pj, q, M, N);
     int64_t d = 0;
     for (int64_t k = int_k_begin(); k < K; ++k)
-      d += (int64_t)A[at_a(i, k, M, K, a_col, lda)] * (int64_t)B[at(k, j, b_col, ldb)];
-    if (C) d += C[at(i, j, c_col, ldc)];
+      d += (int64_t)A[at_a(i, k, M, K, a_col, lda)] * (int64_t)B[at_b(k, j, K, N, b_col, ldb)];
+    if (C) d += C[at_c(i, j, c_col, ldc)];
     D[q] = d;
   }
   return 0;

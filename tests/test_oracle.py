@@ -403,6 +403,14 @@ def pin_views_agree(orc):
     Dp, Sp = orc.gemm_f64_points(M, N, K, bits_of(A, t), bits_of(B, t), C, pi, pj, ab_type=t,
                                  c_type=F32)
     assert np.array_equal(Dp, D[pi, pj]) and np.array_equal(Sp, S[pi, pj])
+    # a square problem (the 8192^3 checks sample points of one): (i, j) is not (j, i)
+    n = 31
+    A = _rand_values(rng, (n, K), t)
+    B = _rand_values(rng, (K, n), t)
+    D, _ = orc.gemm_f64_rows(n, n, K, bits_of(A, t), bits_of(B, t), None, ab_type=t)
+    pi, pj = rng.integers(0, n, 300), rng.integers(0, n, 300)
+    Dp, _ = orc.gemm_f64_points(n, n, K, bits_of(A, t), bits_of(B, t), None, pi, pj, ab_type=t)
+    assert np.array_equal(Dp, D[pi, pj])
 
 
 def pin_int8(orc):
@@ -419,6 +427,12 @@ def pin_int8(orc):
     pi, pj = np.array([0, 22, 7]), np.array([18, 0, 9])
     Dp = orc.gemm_i64_points(M, N, K, A.numpy(), B.numpy(), C.numpy(), pi, pj)
     assert np.array_equal(Dp, ref[pi, pj])
+    # square: points (i, j) and (j, i) differ
+    Aq, Bq = A[:19], B
+    refq = (Aq.long() @ Bq.long()).numpy()
+    pi, pj = np.array([0, 18, 3, 7]), np.array([18, 0, 11, 2])
+    Dq = orc.gemm_i64_points(19, 19, K, Aq.contiguous().numpy(), Bq.numpy(), None, pi, pj)
+    assert np.array_equal(Dq, refq[pi, pj])
     D0 = orc.gemm_i64_rows(M, N, K, A.numpy(), B.numpy(), None)
     assert np.array_equal(D0, (A.long() @ B.long()).numpy())
     # worst case: all -128, K = 8192 -> 2^27 + C
@@ -453,7 +467,7 @@ def test_oracle_threads(orc):
     assert orc.threads() >= 1
 
 
-@pytest.mark.parametrize("mutant", range(1, 14))
+@pytest.mark.parametrize("mutant", range(1, 19))
 def test_pins_catch_planted_mistakes(mutant):
     with tempfile.TemporaryDirectory() as d:
         path = oracle.compile_library(os.path.join(d, f"liboracle_m{mutant}.so"), mutant=mutant)
