@@ -83,6 +83,7 @@ class Oracle:
         lib.oracle_widen8.argtypes = [_vp, _i64, _int, _vp]
         lib.oracle_round.argtypes = [_vp, _i64, _int, _vp]
         lib.oracle_threads.argtypes = []
+        lib.oracle_set_threads.argtypes = [_int]
         lib.oracle_gemm_f64_rows.argtypes = [_i64, _i64, _i64, _int, _int, _int, _int, _int,
                                              _i64, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp, _vp]
         lib.oracle_gemm_f64_points.argtypes = [_i64, _i64, _i64, _int, _int, _int, _int, _int,
@@ -122,6 +123,10 @@ class Oracle:
 
     def threads(self) -> int:
         return int(self._lib.oracle_threads())
+
+    def set_threads(self, n: int) -> int:
+        """Threads of the parallel loops (for timing on one core or all)."""
+        return int(self._lib.oracle_set_threads(int(n)))
 
     # -- floating point -------------------------------------------------------
     def gemm_f64_rows(self, M, N, K, A, B, C, *, ab_type, c_type=BF16, a_col=0, b_col=0,

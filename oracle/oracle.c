@@ -209,6 +209,19 @@ int oracle_threads(void) {
 #endif
 }
 
+/* Exported: set the number of threads of the parallel loops below (n >= 1);
+ * used only to time the oracle on one core and on all of them.  Returns the
+ * count now in effect. */
+int oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+  return omp_get_max_threads();
+#else
+  (void)n;
+  return 1;
+#endif
+}
+
 /* Element (r, c) of an operand stored with leading dimension ld. */
 static int64_t at(int64_t r, int64_t c, int col_major, int64_t ld) {
   return col_major ? r + c * ld : r * ld + c;

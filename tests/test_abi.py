@@ -115,6 +115,32 @@ def test_raster_is_a_bijection_with_grouped_columns(npm, npn, g):
             assert len(cols) == 1
 
 
+def _grouped_tile(t, num_pid_m, num_pid_n, group_m):
+    """The grouped mapping of the FlagGems "Hygon optimization" page, section
+    "Grouped scheduling: improve L2 data reuse", written out step by step:
+    a group spans GROUP_M tile rows and every tile column; the tile's group
+    is t // (GROUP_M * num_pid_n); the last group is clamped to the tile rows
+    that remain; inside a group the row index runs fastest."""
+    num_pid_in_group = group_m * num_pid_n
+    group_id = t // num_pid_in_group
+    first_pid_m = group_id * group_m
+    group_size_m = min(num_pid_m - first_pid_m, group_m)
+    pid_m = first_pid_m + (t % num_pid_in_group) % group_size_m
+    pid_n = (t % num_pid_in_group) // group_size_m
+    return pid_m, pid_n
+
+
+@pytest.mark.parametrize("npm,npn,g", [(1, 1, 1), (5, 3, 2), (32, 16, 8), (7, 9, 4), (3, 11, 8),
+                                       (16, 1, 8), (1, 16, 8), (64, 64, 1), (33, 17, 8),
+                                       (16, 16, 8), (13, 5, 16), (12, 40, 5)])
+def test_raster_equals_the_grouped_formula(npm, npn, g):
+    """Tile for tile, the library's order is the page's formula (a reordered
+    walk that is still grouped would pass the bijection test above)."""
+    for t in range(npm * npn):
+        rc, pm, pn = pkg.gemm_raster_tile(t, npm, npn, g)
+        assert rc == 0 and (pm, pn) == _grouped_tile(t, npm, npn, g), (t, pm, pn)
+
+
 def test_raster_rejects_out_of_range():
     assert pkg.gemm_raster_tile(6, 2, 3, 2)[0] == pkg.GEMM_ERR_INVALID_ARG
     assert pkg.gemm_raster_tile(-1, 2, 3, 2)[0] == pkg.GEMM_ERR_INVALID_ARG

@@ -40,7 +40,9 @@ def _rank_main(rank, world, port, local_ms, out):
 def test_job_time_is_max_over_two_gloo_ranks():
     world, port = 2, free_port()
     local_ms = [3.0, 5.0]  # total timed ms of 10 steps on each rank
-    with mp.Manager() as man:
+    # the manager process is started by spawn too: a fork of this process,
+    # which may already run the oracle's OpenMP threads, can deadlock
+    with mp.get_context("spawn").Manager() as man:
         out = man.dict()
         mp.spawn(_rank_main, args=(world, port, local_ms, out), nprocs=world, join=True)
         res = dict(out)
