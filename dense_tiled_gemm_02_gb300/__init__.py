@@ -11,7 +11,8 @@ Low-level names mirror ``include/gemm.h``: ``gemm_create``, ``gemm_run``,
 ``gemm_plan_string``, ``gemm_workspace_bytes``, ``gemm_raster_tile``,
 ``gemm_debug_set``, ``gemm_timing_enable``, ``gemm_timing_read``,
 ``gemm_host_io_enable``, ``gemm_run_host_batch``, ``gemm_pair_schedule``,
-``gemm_decode_ring``.
+``gemm_cta_schedule``, ``gemm_decode_ring``, ``gemm_run_splitk_noalloc``,
+``gemm_noalloc_status``.
 ``Gemm`` wraps a handle for torch tensors.
 """
 from __future__ import annotations
@@ -36,9 +37,9 @@ GEMM_DEBUG_SKIP_FIRST_FILL = 1
 
 EXPORTED = ["gemm_create", "gemm_run", "gemm_get_status", "gemm_destroy", "gemm_strerror",
             "gemm_plan_string", "gemm_workspace_bytes", "gemm_raster_tile", "gemm_debug_set",
-            "gemm_run_splitk_noalloc", "gemm_timing_enable", "gemm_timing_read",
+            "gemm_run_splitk_noalloc", "gemm_noalloc_status", "gemm_timing_enable", "gemm_timing_read",
             "gemm_host_io_enable", "gemm_run_host_batch", "gemm_pair_schedule",
-            "gemm_decode_ring"]
+            "gemm_cta_schedule", "gemm_decode_ring"]
 GEMM_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
@@ -95,8 +96,12 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
     lib.gemm_debug_set.restype = ci
     lib.gemm_run_splitk_noalloc.argtypes = [ctypes.POINTER(GemmDesc), ci, vp, vp, vp, vp, vp]
     lib.gemm_run_splitk_noalloc.restype = ci
+    lib.gemm_noalloc_status.argtypes = [vp]
+    lib.gemm_noalloc_status.restype = ci
     lib.gemm_pair_schedule.argtypes = [i64, i64, i64, ci, ci, ci, ci, ci, ci, ctypes.POINTER(i64)]
     lib.gemm_pair_schedule.restype = ci
+    lib.gemm_cta_schedule.argtypes = [i64, i64, i64, ci, ci, ci, ci, ci, ci, ctypes.POINTER(i64)]
+    lib.gemm_cta_schedule.restype = ci
     lib.gemm_timing_enable.argtypes = [vp, ci]
     lib.gemm_timing_enable.restype = ci
     lib.gemm_timing_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ci]
@@ -175,6 +180,26 @@ def gemm_pair_schedule(tiles_m: int, tiles_n: int, group_m: int, num_kb: int, ks
     return units
 
 
+def gemm_cta_schedule(tiles_m: int, tiles_n: int, group_m: int, num_kb: int, splits: int,
+                      grid: int, stream_k: bool, cta: int) -> list[tuple]:
+    """All units of CTA `cta` of the single-CTA kernel: (tile, tile_row, tile_col,
+    kb0, kb1, pieces, piece, slot written, slot read for this piece)."""
+    lib = load()
+    n = lib.gemm_cta_schedule(tiles_m, tiles_n, group_m, num_kb, splits, grid, int(stream_k),
+                              cta, 0, None)
+    if n < 0:
+        raise GemmError(n, "gemm_cta_schedule")
+    out = (ctypes.c_int64 * 9)()
+    units = []
+    for i in range(n):
+        rc = lib.gemm_cta_schedule(tiles_m, tiles_n, group_m, num_kb, splits, grid,
+                                   int(stream_k), cta, i, out)
+        if rc < 0:
+            raise GemmError(rc, "gemm_cta_schedule")
+        units.append(tuple(out))
+    return units
+
+
 def gemm_decode_ring(M: int, K: int, cpb: int) -> tuple[int, int, int]:
     """(stages, columns per stage, shared-memory bytes) of the decode kernel's
     bulk-copy ring; stages < 0 is an error code."""
@@ -211,6 +236,11 @@ def gemm_run_splitk_noalloc(desc: GemmDesc, splits: int, A: int, B: int, C: int 
     """Split-K GEMM for callers that cannot allocate device memory (scratch is a
     static device array; see include/gemm.h)."""
     return load().gemm_run_splitk_noalloc(ctypes.byref(desc), splits, A, B, C, D, stream)
+
+
+def gemm_noalloc_status(stream: int | None) -> int:
+    """Status word left by the latest no-allocation call on the current device."""
+    return load().gemm_noalloc_status(stream)
 
 
 # ---------------------------------------------------------------- torch convenience

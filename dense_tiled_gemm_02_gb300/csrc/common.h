@@ -33,6 +33,7 @@ struct KParams {
   int tiles_m, tiles_n, group_m; // output tile grid and raster group
   int splits, kb_per_split, num_kb;
   int kb_per_chunk;              // k-blocks accumulated in one TMEM pass (exact-int8 mode)
+  int kgroup;                    // single-CTA kernel: K slices loaded as one group (1, 2, 4)
   int a_mn, b_mn;                // operand majors: 0 = K-major, 1 = MN-major
   uint32_t idesc;                // tcgen05 instruction descriptor
   int f8;                        // 8-bit float operands: kind::f8f6f4, 128 K a slice
@@ -63,6 +64,18 @@ struct KParams {
   float* tail_ws;                // [leaving cluster][CTA half][128 rows][BN] fp32
   uint32_t* tail_flags;          // [leaving cluster][CTA half]
   uint32_t epoch;                // value the flags take during this run
+  // Stream-K over the single-CTA kernel's tiles (sk1 = 1): CTA c of G takes
+  // the contiguous run [c*T/G, (c+1)*T/G) of the T = tiles * num_kb
+  // (tile, K slice) iterations.  A tile split over several CTAs is finished
+  // by the CTA holding its first K slice: that piece is the last of its
+  // CTA's run, while every other piece of the tile is the first of its own
+  // CTA's run.  Those leave their fp32 partials in fix_ws[c] and raise
+  // fix_flag[c] to `epoch`; the finishing CTA waits for them (they wait for
+  // nothing), adds them up into its idle accumulator buffer while its own
+  // MMAs run, then adds its accumulator and C and stores D.
+  int sk1;
+  float* fix_ws;                 // [G][BM * BN] fp32, interleaved (see tc_gemm.cuh)
+  uint32_t* fix_flag;            // [G], the epoch of the run that wrote fix_ws[c]
 };
 
 // Instruction descriptor of tcgen05.mma kind::f16 and kind::f8f6f4: fp32
@@ -94,10 +107,13 @@ GB_HD void raster_tile(int64_t t, int64_t num_pid_m, int64_t num_pid_n, int64_t 
 // the K slices [kb0, kb1).
 struct Unit {
   int m0, n0, kb0, kb1, split;
-  int tail;  // 1: part of a tile shared by two clusters (pair kernel, stream-K)
+  int tail;  // 1: part of a tile shared by two clusters (pair kernel, stream-K) or
+             // by several CTAs (single-CTA stream-K)
   int part;  // 0: adds the other cluster's partial and finishes the tile;
              // 1: leaves its partial sums
-  int ti;    // partial-sum slot (the leaving cluster)
+  int ti;    // partial-sum slot (the leaving cluster; single-CTA stream-K: this piece's)
+  int tile;  // tile index in the grouped order
+  int pieces, piece;  // single-CTA stream-K: pieces of the tile, this one's K rank
 };
 
 // Stream-K hybrid plan (pair kernel): with W = tiles / clusters full waves
@@ -208,6 +224,85 @@ GB_HD Unit pair_unit(const KParams& p, const PairWork& pw, int ksub, int cid, in
   raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
   w.m0 = static_cast<int>(pm) * (2 * BM);
   w.n0 = static_cast<int>(pn) * bn;
+  w.tile = t;
+  w.pieces = 1;
+  w.piece = 0;
+  return w;
+}
+
+// ---------------------------------------------------------------- single-CTA stream-K
+// First iteration of CTA c's run, and the CTA whose run holds iteration i
+// (T iterations over G CTAs, T >= G so that no run is empty).
+GB_HD int64_t sk_start(int64_t c, int64_t T, int64_t G) { return c * T / G; }
+GB_HD int64_t sk_owner(int64_t i, int64_t T, int64_t G) { return ((i + 1) * G - 1) / T; }
+
+// The units of one CTA of the single-CTA kernel: round-robin over the
+// tiles x splits, or (sk1) the pieces of its stream-K run [s, e).
+struct CtaWork {
+  int n;
+  int64_t s, e;
+};
+
+GB_HD CtaWork cta_work(const KParams& p, int c, int G, bool allow_sk = true) {
+  CtaWork cw;
+  if (allow_sk && p.sk1) {
+    const int64_t T = static_cast<int64_t>(p.tiles_m) * p.tiles_n * p.num_kb;
+    cw.s = sk_start(c, T, G);
+    cw.e = sk_start(c + 1, T, G);
+    cw.n = cw.e > cw.s ? static_cast<int>((cw.e - 1) / p.num_kb - cw.s / p.num_kb + 1) : 0;
+  } else {
+    const int total = p.tiles_m * p.tiles_n * p.splits;
+    cw.s = cw.e = 0;
+    cw.n = c < total ? (total - c + G - 1) / G : 0;
+  }
+  return cw;
+}
+
+// The CTA that computes piece j (in K order) of tile t; for j >= 1 that
+// piece starts the CTA's run, so its partial sits in slot (and flag) of
+// that CTA.
+GB_HD int sk_piece_cta(const KParams& p, int t, int j, int G) {
+  const int64_t T = static_cast<int64_t>(p.tiles_m) * p.tiles_n * p.num_kb;
+  return static_cast<int>(sk_owner(static_cast<int64_t>(t) * p.num_kb, T, G) + j);
+}
+
+// Unit i of CTA c (of G); bm x bn tiles.  allow_sk = false compiles the
+// stream-K arm out (kernels that never take it).
+GB_HD Unit cta_unit(const KParams& p, const CtaWork& cw, int c, int G, int i, int bm, int bn,
+                    bool allow_sk = true) {
+  Unit w;
+  int t;
+  w.split = 0;
+  w.tail = 0;
+  w.part = 0;
+  w.ti = 0;
+  w.pieces = 1;
+  w.piece = 0;
+  if (allow_sk && p.sk1) {
+    const int64_t nkb = p.num_kb;
+    const int64_t T = static_cast<int64_t>(p.tiles_m) * p.tiles_n * nkb;
+    t = static_cast<int>(cw.s / nkb + i);
+    const int64_t t0 = static_cast<int64_t>(t) * nkb, t1 = t0 + nkb;
+    w.kb0 = static_cast<int>((cw.s > t0 ? cw.s : t0) - t0);
+    w.kb1 = static_cast<int>((cw.e < t1 ? cw.e : t1) - t0);
+    const int64_t cf = sk_owner(t0, T, G), cl = sk_owner(t1 - 1, T, G);
+    w.pieces = static_cast<int>(cl - cf + 1);
+    w.piece = static_cast<int>(c - cf);
+    w.tail = w.pieces > 1 ? 1 : 0;
+    w.part = w.piece > 0 ? 1 : 0;  // 1: leaves its partial; 0: finishes the tile
+    w.ti = c;
+  } else {
+    const int u = c + i * G;
+    t = u / p.splits;
+    w.split = u - t * p.splits;
+    w.kb0 = w.split * p.kb_per_split;
+    w.kb1 = w.kb0 + p.kb_per_split < p.num_kb ? w.kb0 + p.kb_per_split : p.num_kb;
+  }
+  int64_t pm, pn;
+  raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
+  w.m0 = static_cast<int>(pm) * bm;
+  w.n0 = static_cast<int>(pn) * bn;
+  w.tile = t;
   return w;
 }
 

@@ -106,6 +106,10 @@ struct gemm_plan {
   size_t ws_bytes = 0;
   size_t ws_partial_off = 0;
   size_t ws_tail_off = 0, ws_flags_off = 0;  // last-wave partials and their flags
+  size_t ws_fix_off = 0, ws_fixflag_off = 0;  // single-CTA stream-K partials and their flags
+  // Native int8 (i8_mma.cu): the integer mma.sync kernel; A and B read
+  // K-contiguous, copied so first when stored otherwise (a.repack, b.repack).
+  bool native_i8 = false;
   // Decode regime (decode.cu): a handful of rows against a K-contiguous B.
   bool decode = false;
   int decode_kc = 0;
@@ -208,6 +212,9 @@ void apply_force_plan(PlanChoice& c) {
       else if (k == "tail") c.tail = v;
       else if (k == "decode") c.no_decode = v ? 0 : 1;
       else if (k == "dbulk") c.no_dbulk = v ? -1 : 1;
+      else if (k == "native_i8") c.native_i8 = v;
+      else if (k == "sk") c.sk = v;
+      else if (k == "kgroup") c.kgroup = v;
     }
     pos = end + 1;
   }
@@ -218,7 +225,8 @@ void make_plan_string(gemm_plan* h) {
   std::snprintf(buf, sizeof buf,
                 "M=%lld N=%lld K=%lld decode=%d dbulk=%d swap=%d pair=%d bn=%d ksub=%d stages=%d "
                 "group_m=%d splits=%d kb_per_split=%d tail=%d grid=%d i8x=%d a_mn=%d b_mn=%d "
-                "repack_a=%d repack_b=%d stage_c=%d stage_d=%d ws_bytes=%zu",
+                "repack_a=%d repack_b=%d stage_c=%d stage_d=%d ws_bytes=%zu native_i8=%d "
+                "sk=%d kgroup=%d",
                 (long long)h->desc.M, (long long)h->desc.N, (long long)h->desc.K, (int)h->decode,
                 (int)h->decode_bulk,
                 h->choice.swap,
@@ -229,7 +237,7 @@ void make_plan_string(gemm_plan* h) {
                 h->kp.sk_len > 0 ? h->kp.tiles_m * h->kp.tiles_n - h->kp.sk_start : 0,
                 h->grid, (int)h->i8x, h->kp.a_mn, h->kp.b_mn,
                 (int)h->a.repack, (int)h->b.repack, (int)h->c_stage, (int)h->d_stage,
-                h->ws_bytes);
+                h->ws_bytes, (int)h->native_i8, h->kp.sk1, h->kp.kgroup);
   h->plan_str = buf;
 }
 
@@ -313,6 +321,85 @@ int plan_decode(gemm_plan* h, int sms) {
     cudaGetLastError();
     if (h->status) cudaFree(h->status);
     cudaFree(h->ws);
+    return GEMM_ERR_ALLOC_FAILED;
+  }
+  make_plan_string(h);
+  return GEMM_OK;
+}
+
+// Plan of the native int8 kernel: 128 x 128 tiles in the grouped order, no
+// split and no swap; A (M x K) and B (read as N rows of K) copied to
+// K-contiguous workspace rows (128-byte lines) unless they already are
+// K-contiguous with 16-byte rows.  Leaves h's workspace and status word
+// allocated, or returns an error with nothing held.
+int plan_native_i8(gemm_plan* h) {
+  const gemm_desc_t& d = h->desc;
+  PlanChoice& c = h->choice;
+  h->native_i8 = true;
+  c.swap = 0;
+  c.pair = 0;
+  c.splits = 1;
+  c.tail = 0;
+  c.bn = 128;
+  c.ksub = 1;
+  h->M = d.M;
+  h->N = d.N;
+  h->K = d.K;
+  h->c_layout = d.layout_c;
+  h->d_layout = d.layout_d;
+  h->ldc = d.ldc;
+  h->ldd = d.ldd;
+  h->a = Operand{d.layout_a, d.lda, d.M, d.K, false, 0, 0};
+  h->b = Operand{d.layout_b, d.ldb, d.K, d.N, false, 0, 0};
+  h->a.repack = !(d.layout_a == GEMM_ROW_MAJOR && d.lda % 16 == 0);
+  h->b.repack = !(d.layout_b == GEMM_COL_MAJOR && d.ldb % 16 == 0);
+  const int64_t ldk = round_up(std::max<int64_t>(d.K, 1), 128);
+  size_t off = 0;
+  if (h->a.repack) {
+    h->a.ws_ld = ldk;
+    h->a.ws_off = off;
+    off += (size_t)round_up(ldk * d.M, 256);
+  }
+  if (h->b.repack) {
+    h->b.ws_ld = ldk;
+    h->b.ws_off = off;
+    off += (size_t)round_up(ldk * d.N, 256);
+  }
+  KParams& kp = h->kp;
+  kp.M = (int)d.M;
+  kp.N = (int)d.N;
+  kp.K = (int)d.K;
+  const int64_t tm = (d.M + 127) / 128, tn = (d.N + 127) / 128;
+  if (tm * tn > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+  kp.tiles_m = (int)tm;
+  kp.tiles_n = (int)tn;
+  kp.group_m = std::max(1, std::min(c.group_m, kp.tiles_m));
+  kp.splits = 1;
+  kp.num_kb = (int)((d.K + 63) / 64);
+  kp.kb_per_split = kp.num_kb;
+  kp.c_type = d.c_type;
+  kp.d_type = d.d_type;
+  kp.c_rs = d.layout_c == GEMM_ROW_MAJOR ? d.ldc : 1;
+  kp.c_cs = d.layout_c == GEMM_ROW_MAJOR ? 1 : d.ldc;
+  kp.d_rs = d.layout_d == GEMM_ROW_MAJOR ? d.ldd : 1;
+  kp.d_cs = d.layout_d == GEMM_ROW_MAJOR ? 1 : d.ldd;
+  h->grid = (int)(tm * tn);
+  if (prepare_i8_mma() != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  h->ws_bytes = off;
+  if (off > 0 && cudaMalloc(&h->ws, off) != cudaSuccess) {
+    cudaGetLastError();
+    h->ws = nullptr;
+    return GEMM_ERR_ALLOC_FAILED;
+  }
+  if (cudaMalloc(&h->status, 256) != cudaSuccess || cudaMemset(h->status, 0, 256) != cudaSuccess) {
+    cudaGetLastError();
+    if (h->status) cudaFree(h->status);
+    if (h->ws) cudaFree(h->ws);
+    h->ws = nullptr;
+    h->status = nullptr;
     return GEMM_ERR_ALLOC_FAILED;
   }
   make_plan_string(h);
@@ -455,6 +542,36 @@ int gemm_pair_schedule(int64_t tiles_m, int64_t tiles_n, int64_t group_m, int nu
   return pw.n;
 }
 
+int gemm_cta_schedule(int64_t tiles_m, int64_t tiles_n, int64_t group_m, int num_kb, int splits,
+                      int grid, int stream_k, int cta, int i, int64_t* out) {
+  if (tiles_m <= 0 || tiles_n <= 0 || group_m <= 0 || num_kb <= 0 || splits <= 0 ||
+      grid <= 0 || cta < 0 || cta >= grid || i < 0 || tiles_m * tiles_n > INT32_MAX / num_kb)
+    return GEMM_ERR_INVALID_ARG;
+  KParams p{};
+  p.tiles_m = (int)tiles_m;
+  p.tiles_n = (int)tiles_n;
+  p.group_m = (int)group_m;
+  p.num_kb = num_kb;
+  p.sk1 = stream_k ? 1 : 0;
+  p.splits = stream_k ? 1 : splits;
+  p.kb_per_split = (num_kb + p.splits - 1) / p.splits;
+  if (p.sk1 && (int64_t)grid > tiles_m * tiles_n * num_kb) return GEMM_ERR_INVALID_ARG;
+  const CtaWork cw = cta_work(p, cta, grid);
+  if (!out) return cw.n;
+  if (i >= cw.n) return GEMM_ERR_INVALID_ARG;
+  const Unit w = cta_unit(p, cw, cta, grid, i, 1, 1);
+  out[0] = w.tile;
+  out[1] = w.m0;  // tile row (bm = 1)
+  out[2] = w.n0;  // tile column (bn = 1)
+  out[3] = w.kb0;
+  out[4] = w.kb1;
+  out[5] = w.pieces;
+  out[6] = w.piece;
+  out[7] = (w.tail && w.part == 1) ? w.ti : -1;
+  out[8] = w.tail ? sk_piece_cta(p, w.tile, w.piece, grid) : -1;
+  return cw.n;
+}
+
 int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   if (!out || !desc) return GEMM_ERR_INVALID_ARG;
   gemm_desc_t d = *desc;
@@ -509,6 +626,17 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
       delete h;
       return rc;
     }
+    *out = h;
+    return GEMM_OK;
+  }
+  if (h->i8x && h->choice.native_i8) {
+    const int rc = plan_native_i8(h);
+    if (rc != GEMM_OK) {
+      delete h;
+      return rc;
+    }
+    const char* lg = std::getenv("GEMM_LOG");
+    if (lg && lg[0] == '1') std::fprintf(stderr, "[gemm] plan: %s\n", h->plan_str.c_str());
     *out = h;
     return GEMM_OK;
   }
@@ -579,6 +707,8 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   kp.splits = splits;
   c.splits = splits;
   kp.kb_per_chunk = h->i8x ? 8 : std::max(1, kp.num_kb);  // int8: 512 K per exact fp32 pass
+  kp.kgroup = (c.kgroup == 2 || c.kgroup == 4) ? c.kgroup : 1;
+  c.kgroup = kp.kgroup;
   kp.a_mn = h->a.layout == GEMM_COL_MAJOR ? 1 : 0;  // A' contiguous along M'
   kp.b_mn = h->b.layout == GEMM_ROW_MAJOR ? 1 : 0;  // B' contiguous along N'
   // element type code 1: bf16 (kind::f16) or E5M2 (kind::f8f6f4)
@@ -590,9 +720,23 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   kp.c_cs = h->c_layout == GEMM_ROW_MAJOR ? 1 : h->ldc;
   kp.d_rs = h->d_layout == GEMM_ROW_MAJOR ? h->ldd : 1;
   kp.d_cs = h->d_layout == GEMM_ROW_MAJOR ? 1 : h->ldd;
-  const int64_t units = (int64_t)kp.tiles_m * kp.tiles_n * kp.splits;
   int max_ctas = sms;
   if (c.max_ctas > 0) max_ctas = std::min(max_ctas, c.max_ctas);
+  // Single-CTA stream-K: one equal run of (tile, K slice) iterations per
+  // CTA over every SM (at most one CTA per iteration, so no run is empty).
+  kp.sk1 = 0;
+  if (!c.pair && c.sk && !h->i8x) {
+    const int64_t iters = (int64_t)kp.tiles_m * kp.tiles_n * std::max(1, kp.num_kb);
+    if (iters <= INT32_MAX && kp.num_kb > 0) {
+      kp.sk1 = 1;
+      splits = 1;
+      kp.splits = 1;
+      c.splits = 1;
+      kp.kb_per_split = kp.num_kb;
+    }
+  }
+  const int64_t units = (int64_t)kp.tiles_m * kp.tiles_n *
+                        (kp.sk1 ? std::max(1, kp.num_kb) : kp.splits);
   if (!c.pair) h->grid = (int)std::max<int64_t>(1, std::min<int64_t>(units, max_ctas));
 
   // Kernel attributes and, for the pair kernel, how many 2-CTA clusters
@@ -648,6 +792,12 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     kp.ws_cs = row ? 1 : h->M;
     kp.ws_split = h->M * h->N;
   }
+  if (kp.sk1) {
+    h->ws_fix_off = off;
+    off += (size_t)round_up((int64_t)h->grid * BM * c.bn * 4, 256);
+    h->ws_fixflag_off = off;
+    off += (size_t)round_up((int64_t)h->grid * 4, 256);
+  }
   if (sk_slots > 0) {
     h->ws_tail_off = off;
     off += (size_t)round_up(sk_slots * 2 * BM * c.bn * 4, 256);
@@ -684,9 +834,11 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     delete h;
     return GEMM_ERR_ALLOC_FAILED;
   }
-  if (sk_slots > 0 &&
-      cudaMemset(static_cast<char*>(h->ws) + h->ws_flags_off, 0, sk_slots * 2 * 4) !=
-          cudaSuccess) {
+  if ((sk_slots > 0 &&
+       cudaMemset(static_cast<char*>(h->ws) + h->ws_flags_off, 0, sk_slots * 2 * 4) !=
+           cudaSuccess) ||
+      (kp.sk1 && cudaMemset(static_cast<char*>(h->ws) + h->ws_fixflag_off, 0,
+                            (size_t)h->grid * 4) != cudaSuccess)) {
     cudaGetLastError();
     cudaFree(h->ws);
     delete h;
@@ -742,6 +894,61 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
   if (d.K == 0) {  // D = C
     kp.splits = 0;
     return launch_reduce(kp, row_order, h->num_sms, st) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  }
+  if (h->native_i8) {
+    // A as M rows of K, B as N rows of K; copied K-contiguous when planned so.
+    char* ws = static_cast<char*>(h->ws);
+    const int8_t* ka = static_cast<const int8_t*>(A);
+    const int8_t* kb = static_cast<const int8_t*>(B);
+    if (h->a.repack) {
+      int8_t* dst = reinterpret_cast<int8_t*>(ws + h->a.ws_off);
+      const bool row = d.layout_a == GEMM_ROW_MAJOR;
+      if (launch_to_kmajor_i8(ka, row ? d.lda : 1, row ? 1 : d.lda, d.M, d.K, dst, h->a.ws_ld,
+                              st) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+      ka = dst;
+    } else if (mis(A, 16)) {
+      return GEMM_ERR_MISALIGNED;
+    }
+    if (h->b.repack) {
+      int8_t* dst = reinterpret_cast<int8_t*>(ws + h->b.ws_off);
+      const bool col = d.layout_b == GEMM_COL_MAJOR;  // element (k, n) at B[k + n * ldb]
+      if (launch_to_kmajor_i8(kb, col ? d.ldb : 1, col ? 1 : d.ldb, d.N, d.K, dst, h->b.ws_ld,
+                              st) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+      kb = dst;
+    } else if (mis(B, 16)) {
+      return GEMM_ERR_MISALIGNED;
+    }
+    I8Params ip;
+    ip.M = kp.M;
+    ip.N = kp.N;
+    ip.K = kp.K;
+    ip.tiles_m = kp.tiles_m;
+    ip.tiles_n = kp.tiles_n;
+    ip.group_m = kp.group_m;
+    ip.A = ka;
+    ip.lda = h->a.repack ? h->a.ws_ld : d.lda;
+    ip.B = kb;
+    ip.ldb = h->b.repack ? h->b.ws_ld : d.ldb;
+    ip.C = static_cast<const int32_t*>(C);
+    ip.c_rs = kp.c_rs;
+    ip.c_cs = kp.c_cs;
+    ip.D = static_cast<int32_t*>(D);
+    ip.d_rs = kp.d_rs;
+    ip.d_cs = kp.d_cs;
+    ip.vec = (kp.d_cs == 1 && kp.d_rs % 2 == 0 && !mis(D, 8) &&
+              (!C || (kp.c_cs == 1 && kp.c_rs % 2 == 0 && !mis(C, 8)))) ? 1 : 0;
+    const bool timed = h->timing_used < h->timing_n;
+    if (timed && cudaEventRecord(h->timing_ev[2 * h->timing_used], st) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    if (launch_i8_mma(ip, st) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (timed) {
+      if (cudaEventRecord(h->timing_ev[2 * h->timing_used + 1], st) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+      ++h->timing_used;
+    }
+    return GEMM_OK;
   }
   if (h->decode) {
     DecodeArgs a;
@@ -858,6 +1065,12 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
     tm[which] = &h->map[which][slot];
   }
   if (kp.splits > 1) kp.ws = reinterpret_cast<float*>(ws + h->ws_partial_off);
+  if (kp.sk1) {
+    kp.fix_ws = reinterpret_cast<float*>(ws + h->ws_fix_off);
+    kp.fix_flag = reinterpret_cast<uint32_t*>(ws + h->ws_fixflag_off);
+    if (++h->epoch == 0) h->epoch = 1;  // flags start at 0: never reuse it
+    kp.epoch = h->epoch;
+  }
   if (kp.sk_len > 0) {
     kp.tail_ws = reinterpret_cast<float*>(ws + h->ws_tail_off);
     kp.tail_flags = reinterpret_cast<uint32_t*>(ws + h->ws_flags_off);

@@ -154,6 +154,7 @@ extern "C" GEMM_API int gemm_run_splitk_noalloc(const gemm_desc_t* desc, int spl
   kp.kb_per_split = (kp.num_kb + s_req - 1) / s_req;
   kp.splits = (kp.num_kb + kp.kb_per_split - 1) / kp.kb_per_split;
   kp.kb_per_chunk = kp.num_kb;
+  kp.kgroup = 1;
   kp.a_mn = d.layout_a == GEMM_COL_MAJOR ? 1 : 0;
   kp.b_mn = d.layout_b == GEMM_ROW_MAJOR ? 1 : 0;
   const uint32_t bf16 = static_cast<int>(d.ab_type) == T_BF16 ? 1u : 0u;
@@ -206,4 +207,18 @@ extern "C" GEMM_API int gemm_run_splitk_noalloc(const gemm_desc_t* desc, int spl
   if (kp.splits > 1 && launch_reduce(kp, row_d ? 1 : 0, sms, st) != cudaSuccess)
     return GEMM_ERR_CUDA;
   return GEMM_OK;
+}
+
+// The status word lives at the start of the same static array; reading it
+// back allocates nothing (a 4-byte copy into the caller's stack).
+extern "C" GEMM_API int gemm_noalloc_status(gemm_stream_t stream) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_NO_DEVICE;
+  const uint32_t* word = static_cast<const uint32_t*>(scratch_address(dev));
+  if (!word) return GEMM_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
+  return (v & STATUS_TIMEOUT) ? GEMM_ERR_DEVICE_TIMEOUT : GEMM_OK;
 }

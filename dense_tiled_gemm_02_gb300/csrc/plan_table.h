@@ -28,6 +28,11 @@ struct PlanChoice {
   int no_decode; // 1: never take the decode kernel (M <= 16, K-contiguous B)
   int no_dbulk;  // 1: never take the decode kernel's bulk-copy form; -1: take it
                  // whenever the operands allow, whatever N (0: the planner decides)
+  int native_i8; // int8: 1 runs the native integer mma.sync kernel instead of the
+                 // exact bf16 emulation on the tcgen05 tensor cores
+  int sk;        // single-CTA kernel: stream-K over all SMs, shared tiles finished
+                 // in the kernel by their last piece (no split-K reduce launch)
+  int kgroup;    // single-CTA kernel: consecutive K slices loaded together (0 = 1)
 };
 
 struct PlanRow {

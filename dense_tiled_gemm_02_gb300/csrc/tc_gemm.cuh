@@ -45,22 +45,6 @@ constexpr uint32_t smem_bytes() {
   return STAGES * TileCfg<BN>::STAGE_TX + 256 + 1024;
 }
 
-__device__ __forceinline__ Unit decode_unit(const KParams& p, int u, int bn) {
-  Unit w;
-  const int t = u / p.splits;
-  w.split = u - t * p.splits;
-  int64_t pm, pn;
-  raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
-  w.m0 = static_cast<int>(pm) * BM;
-  w.n0 = static_cast<int>(pn) * bn;
-  w.kb0 = w.split * p.kb_per_split;
-  w.kb1 = min(p.num_kb, w.kb0 + p.kb_per_split);
-  w.tail = 0;
-  w.part = 0;
-  w.ti = 0;
-  return w;
-}
-
 // ------------------------------------------------------------------ epilogue helpers
 __device__ __forceinline__ float load_elem_f(const void* base, int t, long long off) {
   if (t == T_BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[off]);
@@ -312,6 +296,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * Cfg::B_BYTES);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* ep_go = abort_flag + 1;  // the epilogue leader's verdict for its warps
 
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](uint32_t s) { return bar0 + 8u * s; };
@@ -354,7 +339,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   pdl_wait();
   pdl_trigger();
 
-  const int num_units = p.tiles_m * p.tiles_n * p.splits;
+  const CtaWork cw = cta_work(p, blockIdx.x, gridDim.x, !I8X);
   const uint64_t tmo = p.timeout_ns;
 
   if (warp == 0) {
@@ -363,10 +348,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t it = 0, s = 0, ph = 0;  // it: slices issued; (s, ph): ring slot and phase
       int64_t skipped = -1;
       bool stop = false;
-      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
-        const Unit w = decode_unit(p, u, BN);
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!bounded_wait(empty(s), ph ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
+      for (int i = 0; i < cw.n && !stop; ++i) {
+        const Unit w = cta_unit(p, cw, blockIdx.x, gridDim.x, i, BM, BN, !I8X);
+        for (int kb = w.kb0; kb < w.kb1 && !stop; ++kb) {
+          // Slices are issued in groups of kgroup consecutive K slices once
+          // that many stages are free, so that each row of a K-major operand
+          // is requested as one run of kgroup * 128 bytes rather than as
+          // 128-byte pieces a stage apart.
+          const int kg = max(1, p.kgroup);
+          const int g = ((kb - w.kb0) % kg == 0) ? min(kg, w.kb1 - kb) : 0;
+          if (g > 1) {
+            uint32_t s2 = s, ph2 = ph;
+            for (int j = 0; j < g; ++j) {
+              if (!bounded_wait(empty(s2), ph2 ^ 1u, abort_flag, p.status, STATUS_TIMEOUT,
+                                tmo)) {
+                stop = true;
+                break;
+              }
+              if (++s2 == STAGES) {
+                s2 = 0;
+                ph2 ^= 1u;
+              }
+            }
+            if (stop) break;
+          } else if (!bounded_wait(empty(s), ph ^ 1u, abort_flag, p.status, STATUS_TIMEOUT,
+                                   tmo)) {
             stop = true;
             break;
           }
@@ -430,8 +436,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t s = 0, ph = 0, acc_it = 0;
       bool stop = false;
       const bool f8 = !I8X && p.f8 != 0;
-      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
-        const Unit w = decode_unit(p, u, BN);
+      for (int i = 0; i < cw.n && !stop; ++i) {
+        const Unit w = cta_unit(p, cw, blockIdx.x, gridDim.x, i, BM, BN, !I8X);
         // One accumulation pass per chunk of kb_per_chunk K slices (the whole
         // K range except in exact-int8 mode).
         for (int c0 = w.kb0; c0 < w.kb1 && !stop; c0 += p.kb_per_chunk) {
@@ -488,16 +494,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     uint32_t acc_it = 0;
     bool stop = false;
-    for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
-      const Unit w = decode_unit(p, u, BN);
-      const int r = w.m0 + q * 32 + lane;
+    const int row_local = q * 32 + lane;
+    for (int i = 0; i < cw.n && !stop; ++i) {
+      const Unit w = cta_unit(p, cw, blockIdx.x, gridDim.x, i, BM, BN, !I8X);
+      const int r = w.m0 + row_local;
       if constexpr (!I8X) {
         // C of a slice as four 16-byte loads of this thread's row, two
         // slices in flight (slice c in cb[c & 1]); the loop over slices is
         // kept rolled so that its code stays in the instruction cache.
         // In a tile that crosses N the groups past N are masked (ld_c8).
-        const bool c_rows = p.splits == 1 && p.C != nullptr && p.c_vec && p.c_type != T_F32 &&
-                            r < p.M;
+        const bool c_rows = p.splits == 1 && !(w.tail && w.part == 1) && p.C != nullptr &&
+                            p.c_vec && p.c_type != T_F32 && r < p.M;
         const int c_ncols = min(BN, p.N - w.n0);
         const uint16_t* crow =
             c_rows ? static_cast<const uint16_t*>(p.C) + r * p.c_rs + w.n0 : nullptr;
@@ -511,8 +518,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         const uint32_t buf = acc_it & 1u;
-        if (!bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status,
-                          STATUS_TIMEOUT, tmo)) {
+        // Stream-K: the piece that finishes a shared tile is its CTA's last
+        // unit, so the other accumulator buffer is idle while this piece's
+        // MMAs run: the other pieces' partials (K order) are summed into it.
+        const bool finishes = w.tail && w.part == 0;
+        if (finishes) {
+          if (threadIdx.x == 64) {
+            bool ok = true;
+            for (int j = 1; j < w.pieces && ok; ++j)
+              ok = bounded_flag_wait(p.fix_flag + sk_piece_cta(p, w.tile, j, gridDim.x), p.epoch,
+                                     abort_flag, p.status, STATUS_TIMEOUT, tmo);
+            *ep_go = ok ? 1 : 0;
+          }
+          named_barrier_sync(1, 128);
+          const bool fok = *ep_go != 0;
+          named_barrier_sync(1, 128);
+          if (!fok) {
+            stop = true;
+            break;
+          }
+          const uint32_t pcol = tmem_base + lane_base + (buf ^ 1u) * BN;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float f[32];
+#pragma unroll 1
+            for (int j = 1; j < w.pieces; ++j) {
+              const float4* pb =
+                  reinterpret_cast<const float4*>(
+                      p.fix_ws + static_cast<size_t>(sk_piece_cta(p, w.tile, j, gridDim.x)) *
+                                     BM * BN) +
+                  row_local;
+              float4 v[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) v[k] = __ldcg(pb + (c * 8 + k) * BM);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                f[4 * k] = j == 1 ? v[k].x : f[4 * k] + v[k].x;
+                f[4 * k + 1] = j == 1 ? v[k].y : f[4 * k + 1] + v[k].y;
+                f[4 * k + 2] = j == 1 ? v[k].z : f[4 * k + 2] + v[k].z;
+                f[4 * k + 3] = j == 1 ? v[k].w : f[4 * k + 3] + v[k].w;
+              }
+            }
+            uint32_t x[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) x[k] = __float_as_uint(f[k]);
+            tmem_st_32x32b_x32(pcol + c * 32, x);
+          }
+          tmem_st_wait();
+        }
+        // One thread waits and tells the other 127, so that all of them take
+        // the same path through the named barriers below.
+        if (threadIdx.x == 64)
+          *ep_go = bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status,
+                                STATUS_TIMEOUT, tmo) ? 1 : 0;
+        named_barrier_sync(1, 128);
+        const bool go = *ep_go != 0;
+        named_barrier_sync(1, 128);
+        if (!go) {
           stop = true;
           break;
         }
@@ -540,6 +602,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
           const int c0 = w.n0 + c * 32;
+          if (w.tail && w.part == 1) {
+            // A piece that leaves its fp32 partial: the 128 threads' float4s
+            // of each 4-column group adjacent (a warp moves 512 contiguous
+            // bytes per access)
+            float4* pb = reinterpret_cast<float4*>(p.fix_ws + static_cast<size_t>(w.ti) * BM * BN) +
+                         row_local;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              pb[(c * 8 + k) * BM] = make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+            return;
+          }
+          if (w.tail) {
+            // the finishing piece: its sum plus the other pieces' sum
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(tmem_base + lane_base + (buf ^ 1u) * BN + c * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) f[j] += __uint_as_float(o[j]);
+          }
           if (p.splits > 1) {
             store_partial(p, r, c0, w.split, f);
             return;
@@ -609,6 +690,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         ++acc_it;
+        if (w.tail && w.part == 1) {
+          // Publish: every epilogue thread of this CTA has written its rows.
+          __threadfence();
+          named_barrier_sync(1, 128);
+          if (threadIdx.x == 64) {
+            __threadfence();
+            st_release_gpu(p.fix_flag + w.ti, p.epoch);
+          }
+        }
       } else {
         int isum[BN];
 #pragma unroll

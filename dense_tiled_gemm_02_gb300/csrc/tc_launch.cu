@@ -37,10 +37,10 @@ cudaError_t prepare_impl() {
 const TcVariant kVariantsBN256[] = {GB_VARIANT(256, 4, false)};
 const int kNumVariantsBN256 = 1;
 #elif TC_BN == 128
-const TcVariant kVariantsBN128[] = {GB_VARIANT(128, 6, false), GB_VARIANT(128, 6, true)};
+const TcVariant kVariantsBN128[] = {GB_VARIANT(128, 7, false), GB_VARIANT(128, 6, true)};
 const int kNumVariantsBN128 = 2;
 #elif TC_BN == 64
-const TcVariant kVariantsBN64[] = {GB_VARIANT(64, 8, false)};
+const TcVariant kVariantsBN64[] = {GB_VARIANT(64, 9, false)};
 const int kNumVariantsBN64 = 1;
 #endif
 

@@ -66,6 +66,30 @@ extern const PairVariant kPairVariants[];
 extern const int kNumPairVariants;
 
 cudaError_t launch_reduce(const KParams& p, int row_order, int num_sms, cudaStream_t st);
+
+// Native int8 GEMM (i8_mma.cu): A and B K-contiguous (element (m, k) of A at
+// A[m * lda + k], element (k, n) of B at B[n * ldb + k]; rows and bases
+// 16-byte aligned), int32 C (may be null) and D with element strides; 128 x
+// 128 tiles in the grouped order, one block each.  vec: C (when present)
+// and D have unit column strides, even row strides and 8-byte aligned bases.
+struct I8Params {
+  int M, N, K;
+  int tiles_m, tiles_n, group_m;
+  const int8_t* A;
+  long long lda;
+  const int8_t* B;
+  long long ldb;
+  const int32_t* C;
+  long long c_rs, c_cs;
+  int32_t* D;
+  long long d_rs, d_cs;
+  int vec;
+};
+cudaError_t prepare_i8_mma();
+cudaError_t launch_i8_mma(const I8Params& p, cudaStream_t st);
+// dst[r * ld_dst + k] = src[r * rs + k * ks] (int8, r < rows, k < cols).
+cudaError_t launch_to_kmajor_i8(const int8_t* src, long long rs, long long ks, long long rows,
+                                long long cols, int8_t* dst, long long ld_dst, cudaStream_t st);
 cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint16_t* dst,
                           long long ld_dst, long long rows, long long cols, int num_sms,
                           cudaStream_t st);

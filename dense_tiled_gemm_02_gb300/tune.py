@@ -1,9 +1,10 @@
 """Measured plan sweep for the selection table (csrc/plan_table.h).
 
     python -m dense_tiled_gemm_02_gb300.tune --workload sq4096_bf16 \
-        --candidates "bn=256;bn=128;bn=256,group=4" [--repeats 7] [--iters 20]
+        --candidates "default;bn=256;bn=128;bn=256,group=4;cublas" [--repeats 7] [--iters 20]
 
-Every candidate plan (a GEMM_FORCE_PLAN string) gets its own handle; the
+Every candidate plan (a GEMM_FORCE_PLAN string; "default" for the plan the
+library picks, "cublas" for PyTorch's GEMM as context) gets its own handle; the
 candidates are timed interleaved, repeat after repeat, so that clock and
 power drift hit them alike, and each result is the median over repeats with
 its spread (max - min) / median.  A difference smaller than the spreads is
@@ -82,7 +83,10 @@ def child(args) -> int:
         if c == "cublas":
             handles.append(LibraryReference(w))
             continue
-        os.environ["GEMM_FORCE_PLAN"] = c
+        if c == "default":  # the plan the library picks by itself
+            os.environ.pop("GEMM_FORCE_PLAN", None)
+        else:
+            os.environ["GEMM_FORCE_PLAN"] = c
         handles.append(pkg.Gemm.like(*sets[0]))
     os.environ.pop("GEMM_FORCE_PLAN", None)
     stream = torch.cuda.current_stream()

@@ -107,8 +107,12 @@ typedef void* gemm_stream_t;
  * Environment: GEMM_LOG=1 prints the chosen plan to stderr;
  * GEMM_FORCE_PLAN="bn=128,splits=2,group=8,swap=1" overrides fields of the
  * plan (for tuning sweeps; keys bn, splits, group, swap, grid, pair, ksub,
- * tail, decode, dbulk: 1 takes the decode kernel's bulk-copy form whenever
- * A's and B's rows allow it, 0 never).
+ * tail, sk (1: the single-CTA kernel's stream-K schedule, shared tiles
+ * finished in the kernel), decode, dbulk: 1 takes the decode kernel's bulk-copy form whenever
+ * A's and B's rows allow it, 0 never; native_i8: 1 runs an int8 problem on
+ * the integer mma.sync kernel, which reads A and B contiguous along K and
+ * copies them so first when they are stored otherwise, instead of the exact
+ * emulation on the bf16 tensor cores).
  */
 GEMM_API int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc);
 
@@ -193,13 +197,29 @@ GEMM_API int gemm_raster_tile(int64_t t, int64_t num_pid_m, int64_t num_pid_n, i
  * [1, 16], or when splits * M * N * 4 bytes of partial sums exceed
  * GEMM_NOALLOC_SCRATCH_BYTES - 256; GEMM_ERR_UNSUPPORTED for other types;
  * GEMM_ERR_MISALIGNED; GEMM_ERR_NO_DEVICE; GEMM_ERR_CUDA.  A bounded
- * device-side wait that expires leaves D undefined; this entry point keeps
- * no handle through which to report it.
+ * device-side wait that expires leaves D undefined and sets the array's
+ * status word, which gemm_noalloc_status reads.
+ *
+ * The cached address belongs to the device's primary context: after
+ * cudaDeviceReset (or any reset of that context) it no longer points at the
+ * array, and this entry point must not be called again in that process.
  */
 #define GEMM_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 GEMM_API int gemm_run_splitk_noalloc(const gemm_desc_t* desc, int splits, const void* A,
                                      const void* B, const void* C, void* D,
                                      gemm_stream_t stream);
+
+/*
+ * gemm_noalloc_status: synchronise stream, then return the status word that
+ * the latest gemm_run_splitk_noalloc call on the current device left in the
+ * static array: GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT when one of its kernels
+ * gave up a bounded wait (its D is then undefined).  Allocates nothing and
+ * does not clear the word (the next call clears it).  Returns
+ * GEMM_ERR_NO_DEVICE or GEMM_ERR_CUDA when the device, the synchronisation
+ * or the 4-byte read fails.  The pages have no counterpart to this entry
+ * point.
+ */
+GEMM_API int gemm_noalloc_status(gemm_stream_t stream);
 
 /*
  * Kernel timing (a measurement hook; the operation is unchanged).
@@ -267,6 +287,25 @@ GEMM_API int gemm_run_host_batch(gemm_handle_t h, int n, const void* const* A,
 GEMM_API int gemm_pair_schedule(int64_t tiles_m, int64_t tiles_n, int64_t group_m, int num_kb,
                                 int ksub, int clusters, int stream_k, int cid, int i,
                                 int64_t* out);
+
+/*
+ * gemm_cta_schedule: host-side view of how the single-CTA kernel deals its
+ * work to `grid` CTAs (for tests; no device needed).  For a tiles_m x
+ * tiles_n grid of tiles in the grouped order (group_m) and num_kb 64-wide K
+ * slices: round-robin over the tiles x splits, or with stream_k != 0 one
+ * contiguous run of (tile, K slice) iterations per CTA (grid at most
+ * tiles_m * tiles_n * num_kb), a tile split over several CTAs being finished
+ * by the CTA that holds its first K slice, after the other pieces (each the
+ * first of its CTA's run) have left their fp32 partials.  Returns the number
+ * of units of CTA `cta`; when out is non-NULL it also writes unit i as
+ * out[0..8] = tile index, tile row, tile column, first K slice, end K slice,
+ * pieces of the tile, this piece's rank in K order, the partial-sum slot it
+ * writes (-1 for a whole tile and for the finishing piece) and the CTA that
+ * the finishing CTA expects to hold this rank (-1 for a whole tile).
+ * Returns GEMM_ERR_INVALID_ARG for a bad argument or i out of range.
+ */
+GEMM_API int gemm_cta_schedule(int64_t tiles_m, int64_t tiles_n, int64_t group_m, int num_kb,
+                               int splits, int grid, int stream_k, int cta, int i, int64_t* out);
 
 /*
  * gemm_decode_ring: host-side view of the shared-memory ring of the decode

@@ -252,3 +252,67 @@ def test_decode_ring_fits_and_never_lets_a_warp_run_a_phase_ahead():
 def test_decode_ring_rejects_bad_arguments():
     for args in ((0, 4096, 27), (5, 4096, 27), (1, 0, 27), (1, 4096, 0), (1, 4096, 33)):
         assert pkg.gemm_decode_ring(*args)[0] == pkg.GEMM_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------------ single-CTA kernel work schedule
+CTA_SCHEDULES = [  # tiles_m, tiles_n, group, num_kb, splits, grid, stream_k
+    (64, 1, 8, 64, 1, 152, True),     # (8192, 128, 4096) at 128 x 128 tiles
+    (1, 64, 8, 128, 1, 152, True),    # (64, 8192, 8192)
+    (8, 16, 8, 16, 1, 152, True),     # 1000^3 at 128 x 64 tiles
+    (3, 5, 2, 7, 1, 100, True),       # at most one CTA per iteration
+    (3, 5, 2, 7, 1, 105, True),       # exactly one iteration per CTA
+    (2, 2, 8, 4, 1, 5, True),         # runs longer than a tile
+    (10, 10, 4, 2, 1, 152, True),     # 200 iterations over 152 CTAs
+    (4, 4, 8, 10, 3, 20, False),      # round-robin split-K
+    (5, 3, 2, 9, 1, 7, False),        # round-robin, several waves
+]
+
+
+@pytest.mark.parametrize("tm,tn,g,nkb,splits,grid,sk", CTA_SCHEDULES)
+def test_cta_schedule_covers_every_slice_once(tm, tn, g, nkb, splits, grid, sk):
+    """Every (tile, K slice) is computed exactly once; a tile's pieces are
+    ranked in K order and all know how many there are; the finishing piece
+    (rank 0) is the last unit of its CTA, every other piece is the first
+    unit of its CTA (so it waits for nothing) and writes that CTA's slot,
+    and the finishing CTA looks for each rank at the CTA that holds it."""
+    seen = {}
+    pieces = {}
+    slots = set()
+    for c in range(grid):
+        units = pkg.gemm_cta_schedule(tm, tn, g, nkb, splits, grid, sk, c)
+        if sk:
+            assert len(units) >= 1  # no CTA is left without work
+        for i, (t, pm, pn, kb0, kb1, n, j, ws, pc) in enumerate(units):
+            assert 0 <= t < tm * tn and 0 <= kb0 < kb1 <= nkb
+            rc, em, en = pkg.gemm_raster_tile(t, tm, tn, min(g, tm))
+            assert rc == 0 and (em, en) == (pm, pn)
+            for kb in range(kb0, kb1):
+                assert (t, kb) not in seen
+                seen[(t, kb)] = c
+            pieces.setdefault(t, []).append((kb0, kb1, n, j, ws, pc, c))
+            if n > 1:
+                assert pc == c
+                if j == 0:
+                    assert ws == -1 and i == len(units) - 1
+                else:
+                    assert ws == c and i == 0 and ws not in slots
+                    slots.add(ws)
+            else:
+                assert ws == -1 and pc == -1
+    assert len(seen) == tm * tn * nkb
+    for t, ps in pieces.items():
+        ps.sort()
+        n = len(ps)
+        if not sk:
+            continue
+        for j, (kb0, kb1, n_, j_, ws, pc, c) in enumerate(ps):
+            assert n_ == n and j_ == j
+        assert ps[0][0] == 0 and ps[-1][1] == nkb
+        assert all(ps[i][1] == ps[i + 1][0] for i in range(n - 1))
+
+
+def test_cta_schedule_rejects_bad_arguments():
+    assert pkg.load().gemm_cta_schedule(2, 2, 8, 4, 1, 17, 1, 0, 0, None) == \
+        pkg.GEMM_ERR_INVALID_ARG  # more CTAs than iterations
+    assert pkg.load().gemm_cta_schedule(2, 2, 8, 4, 1, 4, 1, 4, 0, None) == \
+        pkg.GEMM_ERR_INVALID_ARG

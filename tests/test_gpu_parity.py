@@ -83,7 +83,13 @@ def test_identity_plus_c(bn):
                                   "pair=1,bn=128,swap=1", "pair=1,bn=256,ksub=2",
                                   "pair=1,bn=256,ksub=2,splits=3", "pair=1,bn=128,ksub=2",
                                   # stream-K runs over a few clusters
-                                  "pair=1,bn=128,grid=20", "pair=1,bn=256,ksub=2,grid=22"])
+                                  "pair=1,bn=128,grid=20", "pair=1,bn=256,ksub=2,grid=22",
+                                  # single-CTA stream-K, shared tiles finished in the kernel
+                                  "pair=0,bn=128,sk=1", "pair=0,bn=64,sk=1",
+                                  "pair=0,bn=256,sk=1,grid=37", "pair=0,bn=64,sk=1,swap=1",
+                                  # K slices loaded in groups of 2 and 4
+                                  "pair=0,bn=64,kgroup=2", "pair=0,bn=128,kgroup=4,splits=3",
+                                  "pair=0,bn=64,kgroup=4,sk=1"])
 def test_small_config(name, plan):
     w = WORKLOADS[name]
     inp = make_inputs(w)
@@ -109,7 +115,9 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("plan", [None, "pair=1,bn=256", "pair=1,bn=128", "pair=1,bn=256,ksub=2"])
+@pytest.mark.parametrize("plan", [None, "pair=1,bn=256", "pair=1,bn=128", "pair=1,bn=256,ksub=2",
+                                  "pair=0,bn=128,sk=1", "pair=0,bn=64,sk=1,grid=150",
+                                  "pair=0,bn=64,kgroup=2"])
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"{s[0]}x{s[1]}x{s[2]}-{s[3]}{s[4]}{s[5]}{s[6]}"
                                                for s in SHAPES])
 def test_ragged_shapes(shape, plan):
@@ -120,7 +128,8 @@ def test_ragged_shapes(shape, plan):
     _assert_ok(check_rows(w, inp, D), f"{shape} [{p}]")
 
 
-@pytest.mark.parametrize("plan", [None, "pair=0", "pair=1,bn=256", "pair=1,bn=128", "pair=1,bn=256,ksub=2"])
+@pytest.mark.parametrize("plan", [None, "pair=0", "pair=1,bn=256", "pair=1,bn=128", "pair=1,bn=256,ksub=2",
+                                  "pair=0,bn=128,sk=1"])
 def test_unaligned_c_d_rows_and_aliased(plan):
     """16-bit C and D rows that are not 16-byte aligned go through aligned
     workspace copies (stage_c / stage_d in the plan); D may alias C there."""
@@ -338,8 +347,8 @@ TABLE_ROWS = {
     "sq4096_bf16": "pair=1 bn=256 ksub=1",
     "sq8192_bf16": "pair=1 bn=256 ksub=1",
     "sq8192_i8": "pair=1 bn=256 ksub=1",
-    "skinny64x8192x8192_bf16": "swap=0 pair=0 bn=128 ksub=1 stages=6",
-    "skinny8192x128x4096_bf16": "swap=0 pair=0 bn=64 ksub=1 stages=8",
+    "skinny64x8192x8192_bf16": "swap=0 pair=0 bn=128 ksub=1 stages=7",
+    "skinny8192x128x4096_bf16": "swap=0 pair=0 bn=64 ksub=1 stages=9",
     "rag1000_bf16": "swap=0 pair=0 bn=64",
     "sq1024_f16": "swap=0 pair=0 bn=64",
 }
@@ -368,7 +377,13 @@ FULL = [("sq4096_bf16", None), ("sq4096_bf16", "pair=1,bn=256,tail=0"), ("sq4096
         ("sq4096_bf16", "pair=0,bn=256"), ("skinny64x8192x8192_bf16", None),
         ("skinny8192x128x4096_bf16", None), ("rag4095x4097x4099_bf16", None),
         ("rag4095x4097x4099_bf16", "pair=1,bn=256"), ("sq4096_bf16", "pair=1,bn=256,ksub=2"),
-        ("rag4095x4097x4099_bf16", "pair=1,bn=256,ksub=2")]
+        ("rag4095x4097x4099_bf16", "pair=1,bn=256,ksub=2"),
+        ("skinny64x8192x8192_bf16", "pair=0,bn=128,sk=1"),
+        ("skinny64x8192x8192_bf16", "pair=0,bn=64,sk=1,swap=1"),
+        ("skinny8192x128x4096_bf16", "pair=0,bn=128,sk=1"),
+        ("skinny8192x128x4096_bf16", "pair=0,bn=64,sk=1"),
+        ("skinny8192x128x4096_bf16", "pair=0,bn=64,kgroup=4"),
+        ("skinny64x8192x8192_bf16", "pair=0,bn=128,splits=2,kgroup=2")]
 
 
 @pytest.mark.parametrize("name,plan", FULL, ids=[f"{n}-{p}" for n, p in FULL])
@@ -382,7 +397,8 @@ def test_full_config_every_element(name, plan):
 
 
 @pytest.mark.parametrize("name,plan", [("sq8192_bf16", None), ("sq8192_i8", None),
-                                       ("sq8192_i8", "pair=0"), ("sq8192_e4m3", None)])
+                                       ("sq8192_i8", "pair=0"), ("sq8192_i8", "native_i8=1"),
+                                       ("sq8192_e4m3", None)])
 def test_8192_sampled(name, plan):
     w = WORKLOADS[name]
     inp = make_inputs(w)
@@ -517,7 +533,7 @@ def test_decode_bulk_form_engages_at_4096_columns():
 
 
 # ------------------------------------------------------------------ exact int8
-I8_PLANS = [None, "pair=1,ksub=1", "pair=1,ksub=2"]
+I8_PLANS = [None, "pair=1,ksub=1", "pair=1,ksub=2", "native_i8=1", "native_i8=1,group=1"]
 
 
 @pytest.mark.parametrize("plan", I8_PLANS)
@@ -557,6 +573,22 @@ def test_int8_extremes(fill, plan):
     D, p = run_gpu(w, inp, plan=plan)
     want = (A[0, 0].long() * B[0, 0].long() * K) + C.long()
     assert torch.equal(D.long(), want), p
+
+
+@pytest.mark.parametrize("shape", [(1000, 1000, 1000, ROW, ROW, ROW),
+                                   (255, 129, 4097, COL, COL, COL),
+                                   (130, 70, 33, ROW, COL, ROW),
+                                   (64, 520, 160, COL, ROW, COL)])
+def test_native_int8_every_element(shape):
+    """The integer mma.sync kernel: every element bit-exact, for operands read
+    in place (row-major A, column-major B) and copied K-contiguous first, with
+    ragged tiles in M, N and K, and column-major C and D."""
+    M, N, K, la, lb, lcd = shape
+    w = Workload("i8n", 54, M, N, K, I8, I32, I32, "int", la, lb, lcd, lcd)
+    inp = make_inputs(w, seed_offset=M)
+    D, p = run_gpu(w, inp, plan="native_i8=1")
+    assert "native_i8=1" in p and f"repack_a={int(la != ROW or K % 16 != 0)}" in p, p
+    _assert_ok(check_rows(w, inp, D), f"native int8 {shape} [{p}]")
 
 
 # ------------------------------------------------------------------ failure detection

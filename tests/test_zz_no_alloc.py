@@ -32,6 +32,12 @@ CASES = [
     (Workload("noalloc_a", 61, 1000, 384, 4096, BF16, BF16, BF16, "normal", ROW, COL, ROW, ROW), 4),
     # column-major A: its leading dimension M = 336 keeps rows 16-byte aligned (no repack here)
     (Workload("noalloc_b", 62, 336, 200, 2500, F16, F32, F32, "normal", COL, ROW, ROW, COL), 3),
+    # N <= 64: the 128 x 64 tile
+    (Workload("noalloc_c", 63, 520, 48, 1024, BF16, BF16, BF16, "normal", ROW, COL, ROW, ROW), 3),
+    # N <= 128: the 128 x 128 tile; D rows of 100 bf16 are not 16-byte aligned
+    (Workload("noalloc_d", 64, 400, 100, 768, BF16, BF16, BF16, "normal", ROW, COL, ROW, ROW), 2),
+    # no split: the kernel writes D itself and the partial-sum area is unused
+    (Workload("noalloc_e", 65, 300, 264, 640, F16, F16, F16, "normal", ROW, ROW, ROW, ROW), 1),
 ]
 
 
@@ -72,6 +78,8 @@ def test_noalloc_matches_handle_entry_two_calls_in_a_row(case):
                                          None if C is None else C.data_ptr(), Dn.data_ptr(),
                                          stream.cuda_stream)
         assert rc == pkg.GEMM_OK, pkg.gemm_strerror(rc)
+        # its status word, read back without allocating
+        assert pkg.gemm_noalloc_status(stream.cuda_stream) == pkg.GEMM_OK
         # the handle-based entry point, same split of K
         _, _, _, Do = _tensors(w, inp, dev)
         with forced_plan(f"splits={splits},swap=0"):
