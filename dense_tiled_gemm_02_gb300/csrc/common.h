@@ -34,6 +34,13 @@ struct KParams {
   int splits, kb_per_split, num_kb;
   int kb_per_chunk;              // k-blocks accumulated in one TMEM pass (exact-int8 mode)
   int kgroup;                    // single-CTA kernel: K slices loaded as one group (1, 2, 4)
+  // Operands whose rows the TMA unit cannot read (rows off the 16-byte
+  // grid), loaded instead by the kernel's own producer warps (16-bit types):
+  // internal A' (M x K) and B' (K x N) pointers and leading dimensions.
+  int a_lsu, b_lsu;
+  const void* a_src;
+  const void* b_src;
+  long long a_ld, b_ld;
   int a_mn, b_mn;                // operand majors: 0 = K-major, 1 = MN-major
   uint32_t idesc;                // tcgen05 instruction descriptor
   int f8;                        // 8-bit float operands: kind::f8f6f4, 128 K a slice

@@ -46,6 +46,7 @@ struct Operand {
   int64_t ld;          // leading dimension (elements)
   int64_t rows, cols;  // logical extent (A': M' x K, B': K x N')
   bool repack;         // copy into ws before the TMA can read it
+  bool lsu = false;    // read by the kernel's producer warps instead (rows off 16 bytes)
   int64_t ws_ld;       // leading dimension inside the workspace
   size_t ws_off;       // byte offset of its workspace copy
 };
@@ -69,12 +70,12 @@ EncodeFn get_encode() {
   return fn;
 }
 
-const TcVariant* find_variant(int bn, bool i8x) {
+const TcVariant* find_variant(int bn, bool i8x, int pw = 0) {
   const TcVariant* tabs[3] = {kVariantsBN256, kVariantsBN128, kVariantsBN64};
   const int counts[3] = {kNumVariantsBN256, kNumVariantsBN128, kNumVariantsBN64};
   for (int t = 0; t < 3; ++t)
     for (int i = 0; i < counts[t]; ++i)
-      if (tabs[t][i].bn == bn && tabs[t][i].i8x == i8x) return &tabs[t][i];
+      if (tabs[t][i].bn == bn && tabs[t][i].i8x == i8x && tabs[t][i].pw == pw) return &tabs[t][i];
   return nullptr;
 }
 
@@ -215,6 +216,7 @@ void apply_force_plan(PlanChoice& c) {
       else if (k == "native_i8") c.native_i8 = v;
       else if (k == "sk") c.sk = v;
       else if (k == "kgroup") c.kgroup = v;
+      else if (k == "lsu") c.lsu = v;
     }
     pos = end + 1;
   }
@@ -226,7 +228,7 @@ void make_plan_string(gemm_plan* h) {
                 "M=%lld N=%lld K=%lld decode=%d dbulk=%d swap=%d pair=%d bn=%d ksub=%d stages=%d "
                 "group_m=%d splits=%d kb_per_split=%d tail=%d grid=%d i8x=%d a_mn=%d b_mn=%d "
                 "repack_a=%d repack_b=%d stage_c=%d stage_d=%d ws_bytes=%zu native_i8=%d "
-                "sk=%d kgroup=%d",
+                "sk=%d kgroup=%d lsu_a=%d lsu_b=%d",
                 (long long)h->desc.M, (long long)h->desc.N, (long long)h->desc.K, (int)h->decode,
                 (int)h->decode_bulk,
                 h->choice.swap,
@@ -237,7 +239,8 @@ void make_plan_string(gemm_plan* h) {
                 h->kp.sk_len > 0 ? h->kp.tiles_m * h->kp.tiles_n - h->kp.sk_start : 0,
                 h->grid, (int)h->i8x, h->kp.a_mn, h->kp.b_mn,
                 (int)h->a.repack, (int)h->b.repack, (int)h->c_stage, (int)h->d_stage,
-                h->ws_bytes, (int)h->native_i8, h->kp.sk1, h->kp.kgroup);
+                h->ws_bytes, (int)h->native_i8, h->kp.sk1, h->kp.kgroup, (int)h->a.lsu,
+                (int)h->b.lsu);
   h->plan_str = buf;
 }
 
@@ -679,8 +682,13 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     if (!h->pair) c.pair = 0;
   }
   c.ksub = h->pair ? h->pair->ksub : 1;
+  // In-kernel loads of 16-bit operand rows that are off the 16-byte grid
+  // (instead of workspace copies): single-CTA kernel, 128- or 256-wide tiles.
+  const bool lsu_ok = c.lsu && !c.pair && is_f16ish(d.ab_type) && (c.bn == 128 || c.bn == 256);
+  h->a.lsu = lsu_ok && (h->a.ld * 2) % 16 != 0;
+  h->b.lsu = lsu_ok && (h->b.ld * 2) % 16 != 0;
   if (!c.pair) {
-    h->variant = find_variant(c.bn, h->i8x);
+    h->variant = find_variant(c.bn, h->i8x, (h->a.lsu || h->b.lsu) ? 4 : 0);
     if (!h->variant) {
       delete h;
       return GEMM_ERR_UNSUPPORTED;
@@ -771,7 +779,7 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   auto plan_copy = [&](Operand& o, int64_t in_es) {
     const int64_t inner = o.layout == GEMM_ROW_MAJOR ? o.cols : o.rows;
     const int64_t outer = o.layout == GEMM_ROW_MAJOR ? o.rows : o.cols;
-    o.repack = h->i8x || ((o.ld * in_es) % 16 != 0);
+    o.repack = !o.lsu && (h->i8x || ((o.ld * in_es) % 16 != 0));
     if (!o.repack) return;
     const int64_t ws_es = h->f8 ? 1 : 2;  // bf16 (16-bit or widened int8) or 8-bit copies
     // Rows start on 128-byte lines: a TMA row of 128 bytes then reads four
@@ -1024,6 +1032,7 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
   for (int which = 0; which < 2; ++which) {
     Operand& o = which == 0 ? h->a : h->b;
     const void* src = which == 0 ? pa : pb;
+    if (o.lsu) continue;  // read in place by the kernel's producer warps
     const bool need = o.repack || mis(src, 16);
     if (!need) continue;
     if (!o.repack) return GEMM_ERR_MISALIGNED;  // no workspace was planned for this operand
@@ -1047,8 +1056,19 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
 
   const int b_box = h->pair ? h->choice.bn / 2 : h->choice.bn;  // B rows staged per CTA
   const CUtensorMap* tm[2] = {nullptr, nullptr};
+  static const CUtensorMap kNoMap = {};  // an operand the TMA unit does not read
+  kp.a_lsu = h->a.lsu ? 1 : 0;
+  kp.b_lsu = h->b.lsu ? 1 : 0;
+  kp.a_src = pa;
+  kp.b_src = pb;
+  kp.a_ld = h->a.ld;
+  kp.b_ld = h->b.ld;
   for (int which = 0; which < 2; ++which) {
     const void* base = which == 0 ? ta : tb;
+    if ((which == 0 ? h->a : h->b).lsu) {
+      tm[which] = &kNoMap;
+      continue;
+    }
     for (int i = 0; i < gemm_plan::kMapCache; ++i)
       if (h->map_ptr[which][i] == base) tm[which] = &h->map[which][i];
     if (tm[which]) continue;

@@ -103,7 +103,7 @@ const TcVariant* variant_for(int bn) {
   const int counts[3] = {kNumVariantsBN256, kNumVariantsBN128, kNumVariantsBN64};
   for (int t = 0; t < 3; ++t)
     for (int i = 0; i < counts[t]; ++i)
-      if (tabs[t][i].bn == bn && !tabs[t][i].i8x) return &tabs[t][i];
+      if (tabs[t][i].bn == bn && !tabs[t][i].i8x && tabs[t][i].pw == 0) return &tabs[t][i];
   return nullptr;
 }
 

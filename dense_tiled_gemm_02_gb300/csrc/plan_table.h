@@ -33,6 +33,8 @@ struct PlanChoice {
   int sk;        // single-CTA kernel: stream-K over all SMs, shared tiles finished
                  // in the kernel by their last piece (no split-K reduce launch)
   int kgroup;    // single-CTA kernel: consecutive K slices loaded together (0 = 1)
+  int lsu;       // 16-bit operand rows off the 16-byte grid: 1 loads them with the
+                 // single-CTA kernel's producer warps instead of a workspace copy
 };
 
 struct PlanRow {

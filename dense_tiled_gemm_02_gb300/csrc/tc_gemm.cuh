@@ -279,12 +279,99 @@ __device__ __forceinline__ void store_d_i32(const KParams& p, int r, int c0, int
   }
 }
 
+// ------------------------------------------------------------------ in-kernel producer
+// 128-byte segments (64 16-bit elements) of operand rows, copied by groups of
+// 8 lanes (u = lane % 8: one 16-byte unit each) into rows of the
+// 128B-swizzled stage layout that the TMA unit would have written (unit u of
+// stage row srow at position u ^ (srow % 8)).  A row may start on any 2-byte
+// boundary, where the TMA unit cannot read it: each lane loads the aligned
+// 16-byte chunk under its unit, takes the next chunk from its neighbour lane
+// (the 8th lane loads a ninth), and shifts the pair by the row's offset.
+// Elements at or past `ext` and rows at or past `nrows` are zeros (the
+// masked loads of the "Hopper Support in Triton" slides 14-15); a chunk that
+// holds none of the row's elements is not read.
+//
+// The stage tile has `rows_tile` stage rows.  K-major: stage row i is tensor
+// row row0 + i from element k0; MN-major: stage row i is K row k0 + i % 64
+// of the 64-element column block i / 64 from mn0 = row0 (one 8 KB swizzle
+// atom per block).  t is the thread's index among `nthreads` producer
+// threads (a multiple of 32; every lane of their warps calls this, since it
+// shuffles).  Each thread loads NB segments' chunks before it uses any, so
+// that NB memory round trips overlap.
+template <int NB>
+__device__ __forceinline__ void lsu_tile(const uint16_t* base, long long ld, bool kmajor,
+                                         int nrows, int ext, int row0, int k0, int rows_tile,
+                                         uint8_t* dst, int t, int nthreads) {
+  const int u = t & 7;
+  const int groups = nthreads >> 3;
+  for (int i0 = t >> 3; i0 < rows_tile; i0 += NB * groups) {
+    uint4 x[NB], y[NB];
+    uint32_t off[NB];
+    int e0[NB], srow[NB];
+    bool ok[NB];
+    uint8_t* drow[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const int i = i0 + b * groups;
+      const int grow = kmajor ? row0 + i : k0 + (i & 63);
+      const int cstart = kmajor ? k0 : row0 + 64 * (i >> 6);
+      srow[b] = kmajor ? i : (i & 63);
+      drow[b] = kmajor ? dst + i * 128 : dst + (i >> 6) * 8192 + (i & 63) * 128;
+      ok[b] = i < rows_tile && grow < nrows;
+      const uint16_t* rowp = base + static_cast<long long>(ok[b] ? grow : 0) * ld;
+      const uintptr_t seg = reinterpret_cast<uintptr_t>(rowp + cstart);
+      const uintptr_t end = reinterpret_cast<uintptr_t>(rowp + ext);
+      const uintptr_t a0 = seg & ~static_cast<uintptr_t>(15);
+      off[b] = static_cast<uint32_t>(seg - a0);
+      e0[b] = cstart + 8 * u;
+      const uintptr_t c0 = a0 + 16u * static_cast<uint32_t>(u);
+      x[b] = (ok[b] && c0 < end) ? ld_global_v4_pinned(reinterpret_cast<const void*>(c0))
+                                 : make_uint4(0u, 0u, 0u, 0u);
+      y[b] = (ok[b] && u == 7 && c0 + 16 < end)
+                 ? ld_global_v4_pinned(reinterpret_cast<const void*>(c0 + 16))
+                 : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const uint4 nx = make_uint4(__shfl_down_sync(0xffffffffu, x[b].x, 1),
+                                  __shfl_down_sync(0xffffffffu, x[b].y, 1),
+                                  __shfl_down_sync(0xffffffffu, x[b].z, 1),
+                                  __shfl_down_sync(0xffffffffu, x[b].w, 1));
+      if (u != 7) y[b] = nx;
+      if (i0 + b * groups >= rows_tile) continue;
+      const uint32_t w[8] = {x[b].x, x[b].y, x[b].z, x[b].w, y[b].x, y[b].y, y[b].z, y[b].w};
+      const uint32_t q = off[b] >> 2, sh = (off[b] & 3u) * 8u;  // sh: 0 or 16
+      uint32_t r[5];
+#pragma unroll
+      for (int j = 0; j < 5; ++j)
+        r[j] = q == 0 ? w[j] : (q == 1 ? w[j + 1] : (q == 2 ? w[j + 2] : w[j + 3]));
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[j] = __funnelshift_r(r[j], r[j + 1], sh);
+      if (!ok[b] || e0[b] >= ext) {
+        o[0] = o[1] = o[2] = o[3] = 0u;
+      } else if (e0[b] + 8 > ext) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (e0[b] + j >= ext) o[j >> 1] &= (j & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+      }
+      *reinterpret_cast<uint4*>(drow[b] + ((u ^ (srow[b] & 7)) << 4)) =
+          make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ the kernel
 // I8X: exact-int8 mode.  Operands are int8 values held exactly in bf16; the
 // fp32 accumulator is drained to int32 every kb_per_chunk k-blocks, while its
 // magnitude is still below 2^24 and every partial sum is an exact integer.
-template <int BN, int STAGES, bool I8X>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+//
+// PW > 0: PW more warps (6 .. 5 + PW) load the operands marked a_lsu / b_lsu
+// (16-bit rows off the 16-byte grid) into the ring themselves, beside the
+// TMA unit's loads of the others; a stage is full once the TMA bytes have
+// landed and every producer warp has arrived.
+template <int BN, int STAGES, bool I8X, int PW = 0>
+__global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const KParams p) {
   using Cfg = TileCfg<BN>;
@@ -310,7 +397,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full(s), 1);
+      mbar_init(full(s), 1 + PW);
       mbar_init(empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -322,9 +409,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fence_mbar_init();
     fence_proxy_async_smem();
   }
+  const bool a_tma = PW == 0 || !p.a_lsu;
+  const bool b_tma = PW == 0 || !p.b_lsu;
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
+    if (a_tma) tma_prefetch_desc(&tmA);
+    if (b_tma) tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), Cfg::TMEM_COLS);
@@ -385,18 +474,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             continue;
           }
-          mbar_arrive_expect_tx(full(s), Cfg::STAGE_TX);
+          const uint32_t tx = (a_tma ? Cfg::A_BYTES : 0u) + (b_tma ? Cfg::B_BYTES : 0u);
+          if (tx > 0)
+            mbar_arrive_expect_tx(full(s), tx);
+          else
+            mbar_arrive(full(s));
           const uint32_t a_dst = smem_u32(sA + s * Cfg::A_BYTES);
           const uint32_t b_dst = smem_u32(sB + s * Cfg::B_BYTES);
           const int k0 = kb * (p.f8 ? 2 * BK : BK);  // a 128-byte row: 64 or 128 K
-          if (!p.a_mn) {
+          if (!a_tma) {
+          } else if (!p.a_mn) {
             tma_load_2d(a_dst, &tmA, k0, w.m0, full(s));
           } else {
 #pragma unroll
             for (int j = 0; j < BM / 64; ++j)
               tma_load_2d(a_dst + j * 8192u, &tmA, w.m0 + 64 * j, k0, full(s));
           }
-          if (!p.b_mn) {
+          if (!b_tma) {
+          } else if (!p.b_mn) {
             tma_load_2d(b_dst, &tmB, k0, w.n0, full(s));
           } else {
 #pragma unroll
@@ -488,6 +583,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       drain_wait(done_bar, 0, 200000000ull);
     }
     __syncwarp();
+  } else if (PW > 0 && warp >= 6) {
+    // ------------------------------------------------------------ producer warps
+    // The same stages as the TMA producer, in the same order: wait for the
+    // stage to be free, copy the marked operands' tiles, make the writes
+    // visible to the tensor core (async proxy), arrive once per warp.
+    const int t = threadIdx.x - 192;
+    uint32_t s = 0, ph = 0;
+    bool stop = false;
+    for (int i = 0; i < cw.n && !stop; ++i) {
+      const Unit w = cta_unit(p, cw, blockIdx.x, gridDim.x, i, BM, BN, !I8X);
+      for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        int ok = 1;
+        if (lane == 0)
+          ok = bounded_wait(empty(s), ph ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, tmo) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          stop = true;
+          break;
+        }
+        const int k0 = kb * BK;
+        if (p.a_lsu)
+          lsu_tile<8>(static_cast<const uint16_t*>(p.a_src), p.a_ld, !p.a_mn, p.a_mn ? p.K : p.M,
+                   p.a_mn ? p.M : p.K, w.m0, k0, BM, sA + s * Cfg::A_BYTES, t, 32 * PW);
+        if (p.b_lsu)
+          lsu_tile<8>(static_cast<const uint16_t*>(p.b_src), p.b_ld, !p.b_mn, p.b_mn ? p.K : p.N,
+                   p.b_mn ? p.N : p.K, w.n0, k0, BN, sB + s * Cfg::B_BYTES, t, 32 * PW);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full(s));
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // the tensor-memory lane quarter this warp may read

@@ -33,6 +33,7 @@ struct TcVariant {
   int bn;
   int stages;
   bool i8x;
+  int pw;  // producer warps beside the TMA unit (in-kernel loads of unaligned rows)
   uint32_t smem;
   cudaError_t (*launch)(const CUtensorMap&, const CUtensorMap&, const KParams&, int grid,
                         cudaStream_t);

@@ -117,7 +117,8 @@ SHAPES = [
 
 @pytest.mark.parametrize("plan", [None, "pair=1,bn=256", "pair=1,bn=128", "pair=1,bn=256,ksub=2",
                                   "pair=0,bn=128,sk=1", "pair=0,bn=64,sk=1,grid=150",
-                                  "pair=0,bn=64,kgroup=2"])
+                                  "pair=0,bn=64,kgroup=2", "pair=0,bn=128,lsu=1",
+                                  "pair=0,bn=256,lsu=1,swap=0"])
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"{s[0]}x{s[1]}x{s[2]}-{s[3]}{s[4]}{s[5]}{s[6]}"
                                                for s in SHAPES])
 def test_ragged_shapes(shape, plan):
@@ -233,6 +234,40 @@ def test_padding_never_read_or_written(plan, lb):
     mask[1:1 + M, :N] = False
     assert torch.all(host[mask] == 768.0), f"write outside D [{plan_str}]"
     _assert_ok(check_rows(w, inp, D.cpu().contiguous()), f"padded [{plan_str}]")
+
+
+@pytest.mark.parametrize("plan", ["pair=0,bn=128,lsu=1", "pair=0,bn=256,lsu=1"])
+@pytest.mark.parametrize("la,lb", [(ROW, ROW), (ROW, COL), (COL, ROW), (COL, COL)],
+                         ids=["ArowBrow", "ArowBcol", "AcolBrow", "AcolBcol"])
+def test_producer_warps_read_unaligned_rows(plan, la, lb):
+    """Operands whose rows sit off the 16-byte grid (odd leading dimensions,
+    bases one element past an aligned address) read in place by the kernel's
+    producer warps, both majors of A and B; the rows are padded with NaN
+    before and after, which must never reach D."""
+    M, N, K = 300, 260, 203
+    w = Workload("lsu", 15, M, N, K, BF16, BF16, BF16, "normal", la, lb)
+    inp = make_inputs(w, seed_offset=la * 2 + lb)
+    nan = float("nan")
+    As, _ = _placed(inp["A"], 205 if la == ROW else 303, 1, nan)
+    Bs, _ = _placed(inp["B"], 263 if lb == ROW else 205, 1, nan)
+    A = As.t() if la == COL else As
+    B = Bs.t() if lb == COL else Bs
+    C, _ = _placed(inp["C"], 264, 0, nan)
+    D, dbuf = _placed(torch.zeros(M, N, dtype=torch.bfloat16), 264, 0, 768.0)
+    dbuf.fill_(768.0)
+    with forced_plan(plan):
+        g = pkg.Gemm.like(A, B, C, D)
+    plan_str = g.plan()
+    assert "lsu_a=1" in plan_str and "lsu_b=1" in plan_str, plan_str
+    assert "repack_a=0" in plan_str and "repack_b=0" in plan_str, plan_str
+    g.run(A, B, C, D)
+    assert g.status() == pkg.GEMM_OK
+    g.close()
+    host = dbuf.cpu()
+    mask = torch.ones_like(host, dtype=torch.bool)
+    mask[1:1 + M, :N] = False
+    assert torch.all(host[mask] == 768.0), f"write outside D [{plan_str}]"
+    _assert_ok(check_rows(w, inp, D.cpu().contiguous()), f"producer warps [{plan_str}]")
 
 
 def test_k_zero_gives_c():
@@ -383,7 +418,9 @@ FULL = [("sq4096_bf16", None), ("sq4096_bf16", "pair=1,bn=256,tail=0"), ("sq4096
         ("skinny8192x128x4096_bf16", "pair=0,bn=128,sk=1"),
         ("skinny8192x128x4096_bf16", "pair=0,bn=64,sk=1"),
         ("skinny8192x128x4096_bf16", "pair=0,bn=64,kgroup=4"),
-        ("skinny64x8192x8192_bf16", "pair=0,bn=128,splits=2,kgroup=2")]
+        ("skinny64x8192x8192_bf16", "pair=0,bn=128,splits=2,kgroup=2"),
+        ("rag4095x4097x4099_bf16", "pair=0,bn=256,lsu=1"),
+        ("rag4095x4097x4099_bf16", "pair=0,bn=128,lsu=1")]
 
 
 @pytest.mark.parametrize("name,plan", FULL, ids=[f"{n}-{p}" for n, p in FULL])
