@@ -361,7 +361,7 @@ def logical(storage, layout):
 def metric_name(w) -> str:
     from workloads import F8, I8
     if w.ab_type in F8:
-        return "GEMM TFLOPS (fp8)"
+        return "GEMM TFLOPS (fp8, block-scaled)" if w.mx else "GEMM TFLOPS (fp8)"
     return "GEMM TOPS (int8)" if w.ab_type == I8 else "GEMM TFLOPS (bf16/fp16)"
 
 
@@ -446,11 +446,21 @@ def measure(pkg, w, args, dev, stream, world, local, sms, keep_inputs: bool = Fa
         Ds = torch.empty(storage_shape(w.M, w.N, w.layout_d), dtype=TORCH_DTYPE[w.d_type],
                          device=dev)
         sets.append((A, B, C, logical(Ds, w.layout_d)))
-    g = pkg.Gemm.like(*sets[0])
+    g = pkg.Gemm.like(*sets[0], mx=w.mx)
     sptr = stream.cuda_stream
+    if w.mx:  # E8M0 block scales, shared by the input sets
+        from workloads import make_scales
+        sc = {k: v.to(dev) for k, v in make_scales(w).items()}
 
     def step(i):
         A, B, C, D = sets[i % nsets]
+        if w.mx:
+            rc = pkg.gemm_run_mx(g.handle, A.data_ptr(), sc["SA"].data_ptr(), B.data_ptr(),
+                                 sc["SB"].data_ptr(), None if C is None else C.data_ptr(),
+                                 D.data_ptr(), sptr)
+            if rc != pkg.GEMM_OK:
+                raise pkg.GemmError(rc, "gemm_run_mx")
+            return
         g.run_ptrs(A.data_ptr(), B.data_ptr(), None if C is None else C.data_ptr(),
                    D.data_ptr(), sptr)
 
@@ -624,6 +634,8 @@ def launches_per_step(g) -> int:
         n += 1  # the split-K reduce kernel
     flag = {k: int(re.search(k + r"=(\d)", plan).group(1))
             for k in ("repack_a", "repack_b", "stage_c", "stage_d", "i8x")}
+    if re.search(r"\bmx=1\b", plan):
+        n += 2  # the two scale-packing launches
     if flag["i8x"] or re.search(r"\bnative_i8=1\b", plan):
         # int8 operands are widened (or transposed) by one launch each
         n += flag["repack_a"] + flag["repack_b"]

@@ -12,7 +12,7 @@ Low-level names mirror ``include/gemm.h``: ``gemm_create``, ``gemm_run``,
 ``gemm_debug_set``, ``gemm_timing_enable``, ``gemm_timing_read``,
 ``gemm_host_io_enable``, ``gemm_run_host_batch``, ``gemm_pair_schedule``,
 ``gemm_cta_schedule``, ``gemm_decode_ring``, ``gemm_run_splitk_noalloc``,
-``gemm_noalloc_status``.
+``gemm_noalloc_status``, ``gemm_run_mx``.
 ``Gemm`` wraps a handle for torch tensors.
 """
 from __future__ import annotations
@@ -24,6 +24,7 @@ from . import build as _build
 
 GEMM_F16, GEMM_BF16, GEMM_F32, GEMM_I8, GEMM_I32 = 1, 2, 3, 4, 5
 GEMM_E4M3, GEMM_E5M2 = 6, 7  # OCP OFP8 8-bit float operands
+GEMM_MXE4M3, GEMM_MXE5M2 = 8, 9  # the same with E8M0 scales per 32-element K block
 GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
 GEMM_OK = 0
 GEMM_ERR_INVALID_ARG = -1
@@ -39,7 +40,7 @@ EXPORTED = ["gemm_create", "gemm_run", "gemm_get_status", "gemm_destroy", "gemm_
             "gemm_plan_string", "gemm_workspace_bytes", "gemm_raster_tile", "gemm_debug_set",
             "gemm_run_splitk_noalloc", "gemm_noalloc_status", "gemm_timing_enable", "gemm_timing_read",
             "gemm_host_io_enable", "gemm_run_host_batch", "gemm_pair_schedule",
-            "gemm_cta_schedule", "gemm_decode_ring"]
+            "gemm_cta_schedule", "gemm_decode_ring", "gemm_run_mx"]
 GEMM_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
@@ -80,6 +81,8 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
     lib.gemm_create.restype = ci
     lib.gemm_run.argtypes = [vp, vp, vp, vp, vp, vp]
     lib.gemm_run.restype = ci
+    lib.gemm_run_mx.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.gemm_run_mx.restype = ci
     lib.gemm_get_status.argtypes = [vp, vp]
     lib.gemm_get_status.restype = ci
     lib.gemm_destroy.argtypes = [vp]
@@ -126,6 +129,11 @@ def gemm_create(desc: GemmDesc) -> tuple[int, int | None]:
 
 def gemm_run(h: int, A: int, B: int, C: int | None, D: int, stream: int | None) -> int:
     return load().gemm_run(h, A, B, C, D, stream)
+
+
+def gemm_run_mx(h: int, A: int, SA: int, B: int, SB: int, C: int | None, D: int,
+                stream: int | None) -> int:
+    return load().gemm_run_mx(h, A, SA, B, SB, C, D, stream)
 
 
 def gemm_get_status(h: int, stream: int | None) -> int:
@@ -273,8 +281,9 @@ class Gemm:
         self.handle = h
 
     @classmethod
-    def like(cls, A, B, C, D) -> "Gemm":
-        """Plan for the shapes, dtypes and strides of these tensors."""
+    def like(cls, A, B, C, D, mx: bool = False) -> "Gemm":
+        """Plan for the shapes, dtypes and strides of these tensors (mx: 8-bit
+        float operands with block scales, run with run_mx)."""
         M, K = A.shape
         K2, N = B.shape
         assert K == K2 and tuple(D.shape) == (M, N)
@@ -287,7 +296,10 @@ class Gemm:
             ct = _torch_type(C.dtype)
         else:
             lc, ldc, ct = GEMM_ROW_MAJOR, 0, 0
-        desc = GemmDesc(M, N, K, _torch_type(A.dtype), ct, _torch_type(D.dtype), la, lb, lc, ld_,
+        ab = _torch_type(A.dtype)
+        if mx:
+            ab = {GEMM_E4M3: GEMM_MXE4M3, GEMM_E5M2: GEMM_MXE5M2}[ab]
+        desc = GemmDesc(M, N, K, ab, ct, _torch_type(D.dtype), la, lb, lc, ld_,
                         lda, ldb, ldc, ldd)
         return cls(desc)
 
@@ -301,6 +313,18 @@ class Gemm:
                       None if C is None else C.data_ptr(), D.data_ptr(), s)
         if rc != GEMM_OK:
             raise GemmError(rc, "gemm_run")
+
+    def run_mx(self, A, SA, B, SB, C, D, stream=None) -> None:
+        """Enqueue D = (A*SA)(B*SB) + C for a block-scaled handle (SA: M x ceil(K/32)
+        and SB: N x ceil(K/32) uint8 E8M0 exponents on the device)."""
+        if stream is None:
+            import torch
+            stream = torch.cuda.current_stream()
+        s = getattr(stream, "cuda_stream", stream)
+        rc = gemm_run_mx(self.handle, A.data_ptr(), SA.data_ptr(), B.data_ptr(), SB.data_ptr(),
+                         None if C is None else C.data_ptr(), D.data_ptr(), s)
+        if rc != GEMM_OK:
+            raise GemmError(rc, "gemm_run_mx")
 
     def run_ptrs(self, A: int, B: int, C: int | None, D: int, stream: int | None) -> None:
         rc = gemm_run(self.handle, A, B, C, D, stream)

@@ -17,6 +17,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "common.h"
 #include "ptx.cuh"
 #include "tc_launch.h"
@@ -284,7 +286,8 @@ cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint1
     return launch_pdl(widen_i8_x4_kernel, copy_grid(cols / 4, rows, num_sms), dim3(256), 0, st,
                       static_cast<const char4*>(src), ld_src / 4, reinterpret_cast<uint2*>(dst),
                       ld_dst / 4, rows, cols / 4);
-  if (src_type == T_E4M3 || src_type == T_E5M2) {  // bytes into a byte workspace
+  if (src_type == T_E4M3 || src_type == T_E5M2 || src_type == T_MXE4M3 ||
+      src_type == T_MXE5M2) {  // bytes into a byte workspace
     const dim3 g = copy_rows_grid(rows, (cols + 1) / 2, num_sms, 1);
     return launch_pdl(copy_rows8_kernel, g, dim3(256), 0, st, static_cast<const uint8_t*>(src),
                       ld_src, reinterpret_cast<uint8_t*>(dst), ld_dst, rows, cols);
@@ -295,6 +298,39 @@ cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint1
   }
   return launch_pdl(repack_kernel, copy_grid(cols, rows, num_sms), dim3(256), 0, st, src,
                     src_type, ld_src, dst, ld_dst, rows, cols);
+}
+
+// One 32-bit word (four exponents of one row: K blocks 4 g .. 4 g + 3) per
+// thread; consecutive threads write consecutive words of a cell.
+__global__ void pack_scales_kernel(const uint8_t* __restrict__ S, int R, int nsb, int nsb4,
+                                   long long words, uint32_t* __restrict__ dst) {
+  pdl_wait();
+  pdl_trigger();
+  for (long long w = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; w < words;
+       w += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long cell = w >> 7;           // (tile, group): 128 words each
+    const int within = static_cast<int>(w & 127);
+    const long long t = cell / nsb4;
+    const int g = static_cast<int>(cell - t * nsb4);
+    const int j = within >> 2, c = within & 3;
+    const long long row = 128 * t + 32 * c + j;
+    uint32_t v = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int b = 4 * g + k;
+      const uint32_t e = (row < R && b < nsb) ? S[row * nsb + b] : 127u;
+      v |= e << (8 * k);
+    }
+    dst[w] = v;
+  }
+}
+
+cudaError_t launch_pack_scales(const uint8_t* S, int R, int nsb, int nsb4, int tiles,
+                               uint8_t* dst, cudaStream_t st) {
+  const long long words = static_cast<long long>(tiles) * nsb4 * 128;
+  const int grid = static_cast<int>(std::min<long long>((words + 255) / 256, 65535));
+  return launch_pdl(pack_scales_kernel, dim3(grid), dim3(256), 0, st, S, R, nsb, nsb4, words,
+                    reinterpret_cast<uint32_t*>(dst));
 }
 
 cudaError_t launch_copy16(const CopyJob16* jobs, int n, int num_sms, cudaStream_t st) {

@@ -12,7 +12,24 @@
 namespace gb300 {
 
 // Element type codes (the values of gemm_dtype_t).
-enum : int { T_F16 = 1, T_BF16 = 2, T_F32 = 3, T_I8 = 4, T_I32 = 5, T_E4M3 = 6, T_E5M2 = 7 };
+enum : int { T_F16 = 1, T_BF16 = 2, T_F32 = 3, T_I8 = 4, T_I32 = 5, T_E4M3 = 6, T_E5M2 = 7,
+             T_MXE4M3 = 8, T_MXE5M2 = 9 };
+
+// Tensor-memory columns of the block-scaled (mx) mode of the single-CTA
+// kernel: the per-stage scale cells of A and of B (stage s at + 4 s), beside
+// the two 128-column accumulators.
+constexpr uint32_t SFA_COL = 256;
+constexpr uint32_t SFB_COL = 320;
+
+// Instruction descriptor of tcgen05.mma kind::mxf8f6f4: element types
+// (bits 7-9 A, 10-12 B: 0 E4M3, 1 E5M2), majors (bit 15 A, 16 B), N/8 in
+// bits 17-22, scale type E8M0 (bit 23), M/16 in bits 24-28; the scale-data
+// IDs (bits 4-5 B, 29-30 A) are set per instruction.
+GB_HD constexpr uint32_t idesc_mxf8(uint32_t e5m2, uint32_t a_mn, uint32_t b_mn, uint32_t m,
+                                    uint32_t n) {
+  return (e5m2 << 7) | (e5m2 << 10) | (a_mn << 15) | (b_mn << 16) | ((n >> 3) << 17) |
+         (1u << 23) | ((m >> 4) << 24);
+}
 
 // Tile geometry of the tcgen05 kernels: one CTA owns a BM x BN output tile
 // and walks K in BK-wide slices (BK 16-bit elements = one 128-byte row).
@@ -41,6 +58,14 @@ struct KParams {
   const void* a_src;
   const void* b_src;
   long long a_ld, b_ld;
+  // Block-scaled 8-bit floats (mx = 1): the E8M0 exponents of the 32-element
+  // K blocks, packed by pack_scales_kernel into 512-byte cells, one per
+  // (128-row tile, ring stage of four K blocks): cell (t, g) holds at byte
+  // 16 j + 4 c + k the exponent of row 128 t + 32 c + j and K block 4 g + k
+  // (sfa for the rows of A, sfb for the columns of B; nsb4 = cells per tile).
+  int mx, nsb4;
+  const uint8_t* sfa;
+  const uint8_t* sfb;
   int a_mn, b_mn;                // operand majors: 0 = K-major, 1 = MN-major
   uint32_t idesc;                // tcgen05 instruction descriptor
   int f8;                        // 8-bit float operands: kind::f8f6f4, 128 K a slice

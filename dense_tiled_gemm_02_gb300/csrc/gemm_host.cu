@@ -31,13 +31,16 @@ int elem_size(int t) {
     case T_I32: return 4;
     case T_I8:
     case T_E4M3:
-    case T_E5M2: return 1;
+    case T_E5M2:
+    case T_MXE4M3:
+    case T_MXE5M2: return 1;
     default: return 0;
   }
 }
 
 bool is_f16ish(int t) { return t == T_F16 || t == T_BF16; }
-bool is_f8(int t) { return t == T_E4M3 || t == T_E5M2; }
+bool is_mx(int t) { return t == T_MXE4M3 || t == T_MXE5M2; }
+bool is_f8(int t) { return t == T_E4M3 || t == T_E5M2 || is_mx(t); }
 
 // One operand as the kernel sees it: storage pointer (user's or workspace),
 // storage layout and leading dimension, logical rows x cols.
@@ -96,6 +99,8 @@ struct gemm_plan {
   const PairVariant* pair = nullptr;  // set when the CTA-pair kernel runs the plan
   bool i8x = false;
   bool f8 = false;              // 8-bit float operands (kind::f8f6f4, K-major)
+  bool mx = false;              // block-scaled 8-bit floats (kind::mxf8f6f4, gemm_run_mx)
+  size_t ws_sfa_off = 0, ws_sfb_off = 0;  // packed scale cells of A and B
   int mab_type = T_BF16;        // type the tensor cores read (bf16 for int8 input)
   int64_t M = 0, N = 0, K = 0;  // internal problem
   Operand a{}, b{};
@@ -175,7 +180,8 @@ int validate(const gemm_desc_t& d) {
   } else if (ab == T_I8) {
     if (o != T_I32 || !(c == T_I32 || c == 0)) return GEMM_ERR_UNSUPPORTED;
   } else if (is_f8(ab)) {
-    // 8-bit float operands, read K-major only (A row-major, B column-major)
+    // 8-bit float operands (plain or block-scaled), read K-major only (A
+    // row-major, B column-major)
     if (!(is_f16ish(o) || o == T_F32)) return GEMM_ERR_UNSUPPORTED;
     if (!(is_f16ish(c) || c == T_F32 || c == 0)) return GEMM_ERR_UNSUPPORTED;
     if (d.layout_a != GEMM_ROW_MAJOR || d.layout_b != GEMM_COL_MAJOR) return GEMM_ERR_UNSUPPORTED;
@@ -228,7 +234,7 @@ void make_plan_string(gemm_plan* h) {
                 "M=%lld N=%lld K=%lld decode=%d dbulk=%d swap=%d pair=%d bn=%d ksub=%d stages=%d "
                 "group_m=%d splits=%d kb_per_split=%d tail=%d grid=%d i8x=%d a_mn=%d b_mn=%d "
                 "repack_a=%d repack_b=%d stage_c=%d stage_d=%d ws_bytes=%zu native_i8=%d "
-                "sk=%d kgroup=%d lsu_a=%d lsu_b=%d",
+                "sk=%d kgroup=%d lsu_a=%d lsu_b=%d mx=%d",
                 (long long)h->desc.M, (long long)h->desc.N, (long long)h->desc.K, (int)h->decode,
                 (int)h->decode_bulk,
                 h->choice.swap,
@@ -240,7 +246,7 @@ void make_plan_string(gemm_plan* h) {
                 h->grid, (int)h->i8x, h->kp.a_mn, h->kp.b_mn,
                 (int)h->a.repack, (int)h->b.repack, (int)h->c_stage, (int)h->d_stage,
                 h->ws_bytes, (int)h->native_i8, h->kp.sk1, h->kp.kgroup, (int)h->a.lsu,
-                (int)h->b.lsu);
+                (int)h->b.lsu, (int)h->mx);
   h->plan_str = buf;
 }
 
@@ -486,6 +492,11 @@ const CUtensorMap* cached_map(gemm_plan* h, int which, const void* base, Enc enc
 
 }  // namespace
 
+namespace {
+int run_impl(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
+             const uint8_t* SA, const uint8_t* SB, gemm_stream_t stream);
+}  // namespace
+
 extern "C" {
 
 const char* gemm_strerror(int s) {
@@ -600,7 +611,11 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   h->num_sms = sms;
   h->i8x = (static_cast<int>(d.ab_type) == T_I8);
   h->f8 = is_f8(static_cast<int>(d.ab_type));
-  h->mab_type = h->i8x ? static_cast<int>(T_BF16) : static_cast<int>(d.ab_type);
+  h->mx = is_mx(static_cast<int>(d.ab_type));
+  h->mab_type = h->i8x ? static_cast<int>(T_BF16)
+                       : (h->mx ? (static_cast<int>(d.ab_type) == T_MXE5M2 ? static_cast<int>(T_E5M2)
+                                                                          : static_cast<int>(T_E4M3))
+                                : static_cast<int>(d.ab_type));
 
   if (d.M == 0 || d.N == 0) {
     // An empty D: nothing to read, compute or store (gemm_run returns at
@@ -622,6 +637,19 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   }
   h->choice = choose_plan(d.M, d.N, d.K, d.ab_type, d.layout_a, d.layout_b, sms);
   apply_force_plan(h->choice);
+  if (h->mx) {
+    // Block-scaled 8-bit floats: the single-CTA kernel's 128 x 128 tile with
+    // the producer warps that place the scales (no swap, split or stream-K).
+    PlanChoice& m = h->choice;
+    m.pair = 0;
+    m.bn = 128;
+    m.swap = 0;
+    m.splits = 1;
+    m.sk = 0;
+    m.kgroup = 1;
+    m.lsu = 0;
+    m.no_decode = 1;
+  }
   if (!h->choice.no_decode && (d.ab_type == GEMM_F16 || d.ab_type == GEMM_BF16) && d.M >= 1 &&
       d.M <= kDecodeMaxRows && d.layout_b == GEMM_COL_MAJOR && d.K % 8 == 0 && d.K >= 256) {
     const int rc = plan_decode(h, sms);
@@ -688,7 +716,7 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   h->a.lsu = lsu_ok && (h->a.ld * 2) % 16 != 0;
   h->b.lsu = lsu_ok && (h->b.ld * 2) % 16 != 0;
   if (!c.pair) {
-    h->variant = find_variant(c.bn, h->i8x, (h->a.lsu || h->b.lsu) ? 4 : 0);
+    h->variant = find_variant(c.bn, h->i8x, (h->a.lsu || h->b.lsu || h->mx) ? 4 : 0);
     if (!h->variant) {
       delete h;
       return GEMM_ERR_UNSUPPORTED;
@@ -722,6 +750,12 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   // element type code 1: bf16 (kind::f16) or E5M2 (kind::f8f6f4)
   kp.idesc = idesc_f16(h->mab_type == T_BF16 || h->mab_type == T_E5M2 ? 1u : 0u,
                        (uint32_t)kp.a_mn, (uint32_t)kp.b_mn, (uint32_t)tile_m, (uint32_t)c.bn);
+  kp.mx = h->mx ? 1 : 0;
+  if (h->mx) {
+    kp.idesc = idesc_mxf8(h->mab_type == T_E5M2 ? 1u : 0u, (uint32_t)kp.a_mn, (uint32_t)kp.b_mn,
+                          (uint32_t)tile_m, (uint32_t)c.bn);
+    kp.nsb4 = kp.num_kb;  // a ring stage covers 128 K: four 32-element scale blocks
+  }
   kp.c_type = d.c_type;
   kp.d_type = d.d_type;
   kp.c_rs = h->c_layout == GEMM_ROW_MAJOR ? h->ldc : 1;
@@ -800,6 +834,12 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     kp.ws_cs = row ? 1 : h->M;
     kp.ws_split = h->M * h->N;
   }
+  if (h->mx) {
+    h->ws_sfa_off = off;
+    off += (size_t)round_up((int64_t)kp.tiles_m * kp.nsb4 * 512, 256);
+    h->ws_sfb_off = off;
+    off += (size_t)round_up((int64_t)kp.tiles_n * kp.nsb4 * 512, 256);
+  }
   if (kp.sk1) {
     h->ws_fix_off = off;
     off += (size_t)round_up((int64_t)h->grid * BM * c.bn * 4, 256);
@@ -868,7 +908,22 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
 
 int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
              gemm_stream_t stream) {
-  if (!h) return GEMM_ERR_INVALID_ARG;
+  if (!h || h->mx) return GEMM_ERR_INVALID_ARG;  // block-scaled handles run with gemm_run_mx
+  return run_impl(h, A, B, C, D, nullptr, nullptr, stream);
+}
+
+int gemm_run_mx(gemm_handle_t h, const void* A, const uint8_t* SA, const void* B,
+                const uint8_t* SB, const void* C, void* D, gemm_stream_t stream) {
+  if (!h || !h->mx) return GEMM_ERR_INVALID_ARG;
+  if (h->desc.M > 0 && h->desc.N > 0 && h->desc.K > 0 && (!SA || !SB)) return GEMM_ERR_INVALID_ARG;
+  return run_impl(h, A, B, C, D, SA, SB, stream);
+}
+
+}  // extern "C"
+
+namespace {
+int run_impl(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
+             const uint8_t* SA, const uint8_t* SB, gemm_stream_t stream) {
   if (h->desc.M == 0 || h->desc.N == 0) return GEMM_OK;  // an empty D: nothing to do
   if (!D || (h->desc.K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
   const gemm_desc_t& d = h->desc;
@@ -1084,6 +1139,16 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
     h->map_ptr[which][slot] = base;
     tm[which] = &h->map[which][slot];
   }
+  if (h->mx) {
+    uint8_t* ca = reinterpret_cast<uint8_t*>(ws + h->ws_sfa_off);
+    uint8_t* cb = reinterpret_cast<uint8_t*>(ws + h->ws_sfb_off);
+    const int nsb = (int)((d.K + 31) / 32);
+    if (launch_pack_scales(SA, (int)h->M, nsb, kp.nsb4, kp.tiles_m, ca, st) != cudaSuccess ||
+        launch_pack_scales(SB, (int)h->N, nsb, kp.nsb4, kp.tiles_n, cb, st) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    kp.sfa = ca;
+    kp.sfb = cb;
+  }
   if (kp.splits > 1) kp.ws = reinterpret_cast<float*>(ws + h->ws_partial_off);
   if (kp.sk1) {
     kp.fix_ws = reinterpret_cast<float*>(ws + h->ws_fix_off);
@@ -1156,6 +1221,10 @@ int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void*
     return GEMM_ERR_CUDA;
   return GEMM_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 int gemm_get_status(gemm_handle_t h, gemm_stream_t stream) {
   if (!h) return GEMM_ERR_INVALID_ARG;

@@ -232,6 +232,33 @@ __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t adesc, uint6
       : "memory");
 }
 
+// D[tmem] (+)= (A * scale_A)[smem] * (B * scale_B)[smem]: 8-bit float
+// operands with one power-of-two (E8M0) scale per 32 K elements of each row
+// of A and each column of B (kind::mxf8f6f4, scale_vec::1X).  The scales of
+// this instruction's 32 K are read from tensor memory at sfa_tmem (lane =
+// row of A) and sfb_tmem (lane = column of B); the instruction descriptor's
+// scale-data IDs pick the byte of each 32-bit cell.
+__device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Four consecutive 32-bit columns of this warp's 32 tensor-memory lanes:
+// thread t writes lane (taddr.lane + t), columns taddr.col .. + 3 from
+// v.x .. v.w.
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint4 v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
 // Arrive (once) on bar when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {

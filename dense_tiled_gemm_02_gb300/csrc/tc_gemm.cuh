@@ -39,10 +39,12 @@ struct TileCfg {
   static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
 };
 
-template <int BN, int STAGES>
+// Variants with producer warps (PW > 0) also stage the block-scaled mode's
+// scale cells: 1 KB a ring stage (512 bytes of A's, 512 of B's).
+template <int BN, int STAGES, int PW = 0>
 constexpr uint32_t smem_bytes() {
-  // ring + barriers/flags + slack to align the ring to 1024 bytes
-  return STAGES * TileCfg<BN>::STAGE_TX + 256 + 1024;
+  // ring + scale cells + barriers/flags + slack to align the ring to 1024 bytes
+  return STAGES * TileCfg<BN>::STAGE_TX + (PW > 0 ? STAGES * 1024u : 0u) + 256 + 1024;
 }
 
 // ------------------------------------------------------------------ epilogue helpers
@@ -380,8 +382,11 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * Cfg::B_BYTES);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint8_t* sSF = sB + STAGES * Cfg::B_BYTES;  // PW > 0: scale cells, 1 KB a stage
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sSF + (PW > 0 ? STAGES * 1024 : 0));
+  // ring full/empty, accumulator full/empty, done; PW > 0: scale cells landed
+  constexpr int NBARS = 2 * STAGES + 5 + (PW > 0 ? STAGES : 0);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* ep_go = abort_flag + 1;  // the epilogue leader's verdict for its warps
 
@@ -391,6 +396,7 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
   auto acc_full = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + b); };
   auto acc_empty = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto sf_full = [&](uint32_t s) { return bar0 + 8u * (2 * STAGES + 5 + s); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -399,6 +405,7 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full(s), 1 + PW);
       mbar_init(empty(s), 1);
+      if (PW > 0) mbar_init(sf_full(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), 1);
@@ -415,8 +422,11 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
     if (a_tma) tma_prefetch_desc(&tmA);
     if (b_tma) tma_prefetch_desc(&tmB);
   }
+  // Variants with producer warps also hold the block-scaled mode's scale
+  // cells (columns SFA_COL.. and SFB_COL..).
+  constexpr uint32_t TMEM_ALLOC = PW > 0 ? 512u : Cfg::TMEM_COLS;
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), Cfg::TMEM_COLS);
+    tmem_alloc(smem_u32(tmem_holder), TMEM_ALLOC);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -498,6 +508,16 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
             for (int j = 0; j < BN / 64; ++j)
               tma_load_2d(b_dst + j * 8192u, &tmB, w.n0 + 64 * j, k0, full(s));
           }
+          if (PW > 0 && p.mx) {
+            // this stage's scale cells (512 bytes of A's for the tile row,
+            // 512 of B's for the tile column), read by the producer warps
+            const uint32_t sf = smem_u32(sSF + s * 1024);
+            mbar_arrive_expect_tx(sf_full(s), 1024);
+            bulk_load_1d(sf, p.sfa + (static_cast<size_t>(w.m0 / BM) * p.nsb4 + kb) * 512, 512,
+                         sf_full(s));
+            bulk_load_1d(sf + 512, p.sfb + (static_cast<size_t>(w.n0 / 128) * p.nsb4 + kb) * 512,
+                         512, sf_full(s));
+          }
           ++it;
           if (++s == STAGES) {
             s = 0;
@@ -508,6 +528,7 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
       // Let every copy still in flight land before the CTA can exit.
       for (uint32_t j = it > STAGES ? it - STAGES : 0; j < it; ++j) {
         if (static_cast<int64_t>(j) == skipped) continue;
+        if (PW > 0 && p.mx) drain_wait(sf_full(j % STAGES), (j / STAGES) & 1u, 200000000ull);
         drain_wait(full(j % STAGES), (j / STAGES) & 1u, 200000000ull);
       }
     }
@@ -555,7 +576,19 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
             const uint32_t b_lo = b_lo0 + s * (Cfg::B_BYTES >> 4);
             // 8-bit operands: the same four 32-byte steps along the row,
             // 32 K each (both operands K-major)
-            if (f8) {
+            if (PW > 0 && p.mx) {
+              // block-scaled: this stage's scale cells, written by the
+              // producer warps before they arrived on full(s)
+              tc_fence_after();
+              const uint32_t sfa = tmem_base + SFA_COL + 4 * s;
+              const uint32_t sfb = tmem_base + SFB_COL + 4 * s;
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk)
+                mma_mxf8_ss(d_tmem, sdesc(dhi, a_lo + a_off[kk]), sdesc(dhi, b_lo + b_off[kk]),
+                            p.idesc | (static_cast<uint32_t>(kk) << 29) |
+                                (static_cast<uint32_t>(kk) << 4),
+                            sfa, sfb, accumulate | kk);
+            } else if (f8) {
 #pragma unroll
               for (int kk = 0; kk < BK / 16; ++kk)
                 mma_f8_ss(d_tmem, sdesc(dhi, a_lo + a_off[kk]), sdesc(dhi, b_lo + b_off[kk]),
@@ -595,11 +628,35 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
       const Unit w = cta_unit(p, cw, blockIdx.x, gridDim.x, i, BM, BN, !I8X);
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
         int ok = 1;
-        if (lane == 0)
+        if (lane == 0 && !p.mx)
           ok = bounded_wait(empty(s), ph ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, tmo) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
           stop = true;
           break;
+        }
+        if (p.mx) {
+          // The stage's scale cells into tensor memory: columns c = 0..3 of
+          // lane j hold the E8M0 exponents of row (column) 32 c + j of the
+          // tile for the stage's four 32-element K blocks, byte k for block k;
+          // every lane quarter holds the same cells.
+          if (!bounded_wait(sf_full(s), ph, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
+            stop = true;
+            break;
+          }
+          const uint4 ca = *reinterpret_cast<const uint4*>(sSF + s * 1024 + lane * 16);
+          const uint4 cb = *reinterpret_cast<const uint4*>(sSF + s * 1024 + 512 + lane * 16);
+          const uint32_t lane_q = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+          tmem_st_32x32b_x4(tmem_base + lane_q + SFA_COL + 4 * s, ca);
+          tmem_st_32x32b_x4(tmem_base + lane_q + SFB_COL + 4 * s, cb);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full(s));
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+          continue;
         }
         const int k0 = kb * BK;
         if (p.a_lsu)
@@ -869,7 +926,7 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    tmem_dealloc(tmem_base, TMEM_ALLOC);
   }
 }
 

@@ -67,6 +67,11 @@ extern const PairVariant kPairVariants[];
 extern const int kNumPairVariants;
 
 cudaError_t launch_reduce(const KParams& p, int row_order, int num_sms, cudaStream_t st);
+// E8M0 scales S (R rows of nsb 32-element K blocks, row-major) packed into
+// 512-byte cells per (128-row tile, group of four blocks): byte 16 j + 4 c + k
+// of cell (t, g) = S[128 t + 32 c + j][4 g + k], 127 (2^0) outside S.
+cudaError_t launch_pack_scales(const uint8_t* S, int R, int nsb, int nsb4, int tiles,
+                               uint8_t* dst, cudaStream_t st);
 
 // Native int8 GEMM (i8_mma.cu): A and B K-contiguous (element (m, k) of A at
 // A[m * lda + k], element (k, n) of B at B[n * ldb + k]; rows and bases

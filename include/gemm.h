@@ -28,6 +28,13 @@
  *       name a scaled low-precision matrix product (mfma_scaled) as the next
  *       data type; this is its unscaled form.  A must be row-major and B
  *       column-major (both contiguous along K), else GEMM_ERR_UNSUPPORTED.
+ *   (MXE4M3|MXE5M2, F16|BF16|F32 or C absent, F16|BF16|F32): the scaled
+ *       form ("microscaled" data, the mfma_scaled entry point the "Tuning
+ *       Triton" page names in its section 6, read by the OCP Microscaling
+ *       definition): each element of A and B is an E4M3 / E5M2 value times
+ *       the power-of-two scale of its 32-element K block, one scale per block
+ *       of each row of A and of each column of B (tcgen05 kind::mxf8f6f4).
+ *       Same layouts as the unscaled form; the handle runs with gemm_run_mx.
  *
  * Device pointers, caller-owned.  Every call is asynchronous on the given
  * stream.  All sizes are element counts.
@@ -56,7 +63,9 @@ typedef enum {
   GEMM_I8 = 4,
   GEMM_I32 = 5,
   GEMM_E4M3 = 6, /* OCP OFP8 E4M3 (operands only) */
-  GEMM_E5M2 = 7  /* OCP OFP8 E5M2 (operands only) */
+  GEMM_E5M2 = 7, /* OCP OFP8 E5M2 (operands only) */
+  GEMM_MXE4M3 = 8, /* E4M3 operands with E8M0 block scales (operands only; gemm_run_mx) */
+  GEMM_MXE5M2 = 9  /* E5M2 operands with E8M0 block scales (operands only; gemm_run_mx) */
 } gemm_dtype_t;
 
 /* Storage order: row-major X[r,c] = X[r*ld + c]; column-major X[r + c*ld]. */
@@ -137,6 +146,24 @@ GEMM_API int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc);
  */
 GEMM_API int gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
              gemm_stream_t stream);
+
+/*
+ * gemm_run_mx: enqueue D = (A * SA) * (B * SB) + C on stream for a handle
+ * created with ab_type GEMM_MXE4M3 or GEMM_MXE5M2 (gemm_run rejects such a
+ * handle, and this entry rejects any other, with GEMM_ERR_INVALID_ARG).
+ * A, B, C, D as for gemm_run (A row-major, B column-major).  SA and SB are
+ * device arrays of E8M0 exponents, one byte per 32-element block of K
+ * (scale 2^(e - 127); e = 255 is NaN): SA holds M rows of ceil(K / 32)
+ * bytes, row m for row m of A; SB holds N rows of ceil(K / 32) bytes, row n
+ * for column n of B; both packed, any alignment.  A last block shorter than
+ * 32 keeps its own scale.  The scales are first packed into the handle's
+ * workspace by a small kernel, so SA and SB may be reused once the call's
+ * work on the stream has started.  Products are exact and summed in fp32,
+ * C is added and the result rounded once, as for the unscaled types.
+ * Returns what gemm_run returns.
+ */
+GEMM_API int gemm_run_mx(gemm_handle_t h, const void* A, const uint8_t* SA, const void* B,
+                         const uint8_t* SB, const void* C, void* D, gemm_stream_t stream);
 
 /*
  * gemm_get_status: synchronise stream, then return and clear the device

@@ -12,6 +12,15 @@ narrow-output rule is "within one output ulp of the correctly rounded value";
 the other two are the fp32 bound, which only matter where |D| is small next
 to S (cancellation), and the report counts how many elements needed them.
 
+Block-scaled 8-bit floats (the scaled product whose tolerance the pages do
+not state): the same rule with the S coefficient widened to
+max(2e-6, ceil(K / 32) * 2^-23).  The tensor core adds the scaled partial of
+each 32-element K block into an fp32 accumulator, and each of those ceil(K/32)
+additions may be off by up to one fp32 ulp of the running sum, so by at most
+2^-23 * S (the additions measured on the GPU round toward zero: every result
+outside the narrower bound lies on the small-magnitude side of the exact
+value).  ``mx_s_rel(K)`` gives the coefficient.
+
 Integer: D must equal the int64 oracle value exactly.
 """
 from __future__ import annotations
@@ -31,15 +40,22 @@ def spacing(bits: np.ndarray, t: int) -> np.ndarray:
     return np.ldexp(1.0, (e - bias - frac_bits).astype(np.int64))
 
 
-def check_float(oracle, D, D_ref, S, C_abs, out_type: int, max_report: int = 8) -> dict:
+def mx_s_rel(K: int) -> float:
+    """S coefficient of the block-scaled rule: max(2e-6, ceil(K/32) * 2^-23)."""
+    return max(2e-6, -(-K // 32) * 2.0 ** -23)
+
+
+def check_float(oracle, D, D_ref, S, C_abs, out_type: int, max_report: int = 8,
+                s_rel: float = 2e-6) -> dict:
     """Compare computed values D (fp64 view of the output) with the oracle.
 
     D, D_ref, S, C_abs are same-shape fp64 arrays (C_abs = |C| or zeros).
-    Returns a report dict; ``report["ok"]`` is the verdict.
+    s_rel is the coefficient of S (2e-6, or mx_s_rel(K) for the block-scaled
+    product).  Returns a report dict; ``report["ok"]`` is the verdict.
     """
     D = np.asarray(D, dtype=np.float64)
     D_ref = np.asarray(D_ref, dtype=np.float64)
-    slack = 2e-6 * np.asarray(S, dtype=np.float64) + np.ldexp(np.asarray(C_abs, np.float64), -24)
+    slack = s_rel * np.asarray(S, dtype=np.float64) + np.ldexp(np.asarray(C_abs, np.float64), -24)
     if out_type == F32:
         err = np.abs(D - D_ref)
         bound = slack

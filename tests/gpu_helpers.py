@@ -115,3 +115,40 @@ def check_points(w: Workload, inp: dict, D_storage: torch.Tensor, pi, pj) -> dic
                                    c_type=w.c_type or 0, **kw)
     Cabs = c_abs(w, inp)[pi, pj] if inp["C"] is not None else np.zeros(pi.size)
     return compare.check_float(orc, Dv, D_ref, S, Cabs, w.d_type)
+
+
+def run_gpu_mx(w: Workload, inp: dict, sc: dict, plan: str | None = None):
+    """D (host, D's storage order) and the plan of a block-scaled run: A and B
+    hold E4M3 / E5M2 values, sc["SA"] / sc["SB"] their E8M0 block scales."""
+    import dense_tiled_gemm_02_gb300 as pkg
+    dev = torch.device("cuda")
+    A = logical(inp["A"].to(dev), w.layout_a)
+    B = logical(inp["B"].to(dev), w.layout_b)
+    C = None if inp["C"] is None else logical(inp["C"].to(dev), w.layout_c)
+    D_storage = torch.zeros(storage_shape(w.M, w.N, w.layout_d), dtype=TYPE_TORCH[w.d_type],
+                            device=dev)
+    D = logical(D_storage, w.layout_d)
+    SA, SB = sc["SA"].to(dev), sc["SB"].to(dev)
+    with forced_plan(plan):
+        g = pkg.Gemm.like(A, B, C, D, mx=True)
+    try:
+        g.run_mx(A, SA, B, SB, C, D)
+        st = g.status()
+        assert st == pkg.GEMM_OK, pkg.gemm_strerror(st)
+        return D_storage.cpu(), g.plan()
+    finally:
+        g.close()
+
+
+def check_rows_mx(w: Workload, inp: dict, sc: dict, D_storage: torch.Tensor, rows=None) -> dict:
+    """Compare whole rows of a block-scaled D with the oracle's block-scaled product."""
+    orc = oracle.get()
+    A, B, C = _oracle_args(w, inp)
+    Dv = d_values(w, D_storage)
+    if rows is not None:
+        Dv = Dv[np.asarray(rows)]
+    D_ref, S = orc.gemm_mx_rows(w.M, w.N, w.K, A, B, C, sc["SA"].numpy(), sc["SB"].numpy(),
+                                ab_type=w.ab_type, c_type=w.c_type or 0, a_col=w.layout_a,
+                                b_col=w.layout_b, c_col=w.layout_c, rows=rows)
+    return compare.check_float(orc, Dv, D_ref, S, c_abs(w, inp, rows), w.d_type,
+                               s_rel=compare.mx_s_rel(w.K))

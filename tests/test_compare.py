@@ -120,3 +120,18 @@ def test_int_rule():
     D[0, 2] += 1
     rep = compare.check_int(D, D_ref)
     assert not rep["ok"] and rep["n_fail"] == 1 and rep["first_failures"][0][0] == (0, 2)
+
+
+def test_block_scaled_coefficient():
+    """max(2e-6, ceil(K/32) * 2^-23): the default below K = 544, one fp32 ulp
+    of the running sum per 32-element block above it."""
+    assert compare.mx_s_rel(32) == 2e-6
+    assert compare.mx_s_rel(512) == 2e-6
+    assert compare.mx_s_rel(8192) == 256 * 2.0 ** -23
+    assert compare.mx_s_rel(8193) == 257 * 2.0 ** -23
+    D_ref = np.array([1000.0])
+    S = np.array([1000.0])
+    over = 1000.0 - 1.5 * 256 * 2.0 ** -23 * 1000.0  # outside 2e-6 S, inside the wider bound
+    assert not compare.check_float(None, np.array([over]), D_ref, S, np.zeros(1), F32)["ok"]
+    assert compare.check_float(None, np.array([over]), D_ref, S, np.zeros(1), F32,
+                               s_rel=compare.mx_s_rel(8192 * 2))["ok"]

@@ -15,10 +15,11 @@ import pytest
 import torch
 
 import dense_tiled_gemm_02_gb300 as pkg
-from gpu_helpers import check_points, check_rows, forced_plan, logical, run_gpu
+from gpu_helpers import (check_points, check_rows, check_rows_mx, forced_plan, logical, run_gpu,
+                         run_gpu_mx)
 from workloads import (BF16, COL, E4M3, E5M2, F16, F32, I8, I32, ROW, TORCH_DTYPE, WORKLOADS,
-                       Workload, draw,
-                       make_inputs, sample_points, sample_rows, storage_shape)
+                       Workload, draw, draw_scales,
+                       make_inputs, make_scales, sample_points, sample_rows, storage_shape)
 
 pytestmark = pytest.mark.gpu
 
@@ -567,6 +568,63 @@ def test_decode_bulk_form_engages_at_4096_columns():
         assert "decode=1 dbulk=1" in g.plan(), g.plan()
     finally:
         g.close()
+
+
+# ------------------------------------------------------------------ block-scaled 8-bit floats
+# (M, N, K, C type or None, D type); A row-major, B column-major.  K not a
+# multiple of 32 (a short last block with its own scale), of 128 (a ring
+# stage of four blocks), ragged tiles, rows that are copied to workspace.
+MX_CASES = [
+    (128, 128, 128, BF16, BF16),
+    (300, 520, 200, BF16, BF16),
+    (129, 257, 72, None, F32),
+    (1000, 1000, 1000, F16, BF16),  # scales up to 2^14: |D| beyond fp16's range
+    (513, 770, 4096, F32, BF16),
+    (256, 384, 8192, BF16, F32),
+    (64, 136, 4000, BF16, BF16),
+]
+
+
+@pytest.mark.parametrize("t", [E4M3, E5M2], ids=["e4m3", "e5m2"])
+@pytest.mark.parametrize("case", MX_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}" for c in MX_CASES])
+def test_mx_every_element(case, t):
+    """kind::mxf8f6f4: every element against the oracle's block-scaled
+    product (each element times 2^(e - 127) of its 32-element K block)."""
+    M, N, K, ct, dt = case
+    w = Workload("mx", 16, M, N, K, t, ct, dt, "normal", ROW, COL)
+    inp = make_inputs(w, seed_offset=M + K)
+    sc = make_scales(w, seed_offset=M + K)
+    D, p = run_gpu_mx(w, inp, sc)
+    assert " mx=1" in p, p
+    _assert_ok(check_rows_mx(w, inp, sc, D), f"mx {case} [{p}]")
+
+
+def test_mx_8192_sampled_rows():
+    """The block-scaled 8192^3 workload: 64 sampled rows (the sampling rule's
+    rows) against the oracle."""
+    w = WORKLOADS["sq8192_mxe4m3"]
+    inp = make_inputs(w)
+    sc = make_scales(w)
+    D, p = run_gpu_mx(w, inp, sc)
+    rows = sample_rows(w.M).numpy()
+    _assert_ok(check_rows_mx(w, inp, sc, D, rows=rows), f"sq8192_mxe4m3 rows [{p}]")
+
+
+def test_mx_scales_reach_the_right_rows_and_blocks():
+    """All-ones operands: D[m, n] = sum over K blocks of 32 (or the short last
+    block's length) x 2^(ea(m, b) + eb(n, b) - 254), exact in fp32, so a scale
+    read from the wrong row, column or block shows up exactly."""
+    M, N, K = 256, 128, 300
+    w = Workload("mx1", 17, M, N, K, E4M3, None, F32, "normal", ROW, COL)
+    inp = {"A": torch.ones(M, K).to(torch.float8_e4m3fn),
+           "B": torch.ones(N, K).to(torch.float8_e4m3fn), "C": None}
+    sc = {"SA": draw_scales(M, K, 71, 124, 130), "SB": draw_scales(N, K, 72, 124, 130)}
+    D, p = run_gpu_mx(w, inp, sc)
+    ea = sc["SA"].double() - 127
+    eb = sc["SB"].double() - 127
+    width = torch.tensor([min(32, K - 32 * b) for b in range((K + 31) // 32)], dtype=torch.float64)
+    want = torch.einsum("mb,nb,b->mn", torch.exp2(ea), torch.exp2(eb), width)
+    assert torch.equal(D.double(), want), p
 
 
 # ------------------------------------------------------------------ exact int8

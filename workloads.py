@@ -50,6 +50,7 @@ class Workload:
     layout_b: int = ROW
     layout_c: int = ROW
     layout_d: int = ROW
+    mx: bool = False        # 8-bit float operands with E8M0 scales per 32-element K block
     note: str = field(default="", compare=False)
 
     @property
@@ -82,6 +83,11 @@ WORKLOADS = {
                             layout_b=COL),
     "sq8192_e4m3": Workload("sq8192_e4m3", 52, 8192, 8192, 8192, E4M3, BF16, BF16, "normal",
                             layout_b=COL),
+    # the same with E8M0 block scales (make_scales: 2^-7 .. 2^7 per block)
+    "sq4096_mxe4m3": Workload("sq4096_mxe4m3", 53, 4096, 4096, 4096, E4M3, BF16, BF16, "normal",
+                              layout_b=COL, mx=True),
+    "sq8192_mxe4m3": Workload("sq8192_mxe4m3", 54, 8192, 8192, 8192, E4M3, BF16, BF16, "normal",
+                              layout_b=COL, mx=True),
     # decode regime (M <= 16, N = K = 4096), with B K-contiguous (a weight
     # stored N x K) and N-contiguous
     "decode1x4096x4096_bf16": Workload("decode1x4096x4096_bf16", 61, 1, 4096, 4096, BF16, BF16,
@@ -124,6 +130,22 @@ def make_inputs(w: Workload, seed_offset: int = 0) -> dict:
     if w.c_type is not None:
         C = draw(storage_shape(w.M, w.N, w.layout_c), w.c_type, w.dist, base + 2, c_operand=True)
     return {"A": A, "B": B, "C": C}
+
+
+def draw_scales(rows: int, K: int, seed: int, lo: int = 120, hi: int = 134) -> torch.Tensor:
+    """E8M0 exponents (uint8) of the 32-element K blocks of `rows` rows (rows
+    of A, or columns of B): rows x ceil(K / 32), i.i.d. uniform integers in
+    [lo, hi] (scales 2^-7 .. 2^7 by default)."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(lo, hi + 1, (rows, (K + 31) // 32), generator=g,
+                         dtype=torch.int32).to(torch.uint8)
+
+
+def make_scales(w: Workload, seed_offset: int = 0) -> dict:
+    """Seeded E8M0 block scales of a block-scaled workload: SA for the rows of
+    A, SB for the columns of B (seeds 1000 idx + 3 and + 4)."""
+    base = 1000 * w.idx + seed_offset
+    return {"SA": draw_scales(w.M, w.K, base + 3), "SB": draw_scales(w.N, w.K, base + 4)}
 
 
 def sample_points(M: int, N: int, n: int = 65536, seed: int = 0x5EED):
