@@ -71,9 +71,12 @@ def family_of(plan: str) -> str:
 
 
 def kernel_stem(plan: str) -> str:
-    """File-name stem of the kernel a plan launches."""
-    return {"decode": "decode", "i8mma": "i8_mma", "pair": "tc_gemm_pair",
-            "cta1": "tc_gemm"}[family_of(plan)]
+    """File-name stem of the kernel a plan launches (the decode family's two
+    forms are two kernels)."""
+    fam = family_of(plan)
+    if fam == "decode":
+        return "decode_bulk" if re.search(r"\bdbulk=1\b", plan) else "decode_kn"
+    return {"i8mma": "i8_mma", "pair": "tc_gemm_pair", "cta1": "tc_gemm"}[fam]
 
 
 def source_hash(family: str) -> str:

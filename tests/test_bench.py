@@ -79,7 +79,8 @@ def test_algorithmic_bytes_and_job_value():
 def test_family_stems_and_native_int8_plan():
     assert ncu_record.kernel_stem(plan(pair=1)) == "tc_gemm_pair"
     assert ncu_record.kernel_stem(plan(bn=64)) == "tc_gemm"
-    assert ncu_record.kernel_stem(plan(decode=1)) == "decode"
+    assert ncu_record.kernel_stem(plan(decode=1, dbulk=1)) == "decode_bulk"
+    assert ncu_record.kernel_stem(plan(decode=1, dbulk=0)) == "decode_kn"
     p = plan(bn=128) + " native_i8=1"
     assert ncu_record.family_of(p) == "i8mma"
     assert bench.kernel_name(p) == "i8_mma_kernel"
