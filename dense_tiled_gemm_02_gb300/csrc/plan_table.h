@@ -35,6 +35,8 @@ struct PlanChoice {
   int kgroup;    // single-CTA kernel: consecutive K slices loaded together (0 = 1)
   int lsu;       // 16-bit operand rows off the 16-byte grid: 1 loads them with the
                  // single-CTA kernel's producer warps instead of a workspace copy
+  int i8chunk;   // exact int8: K of one exact fp32 accumulation pass, a multiple of
+                 // 64 up to 960 (0 = the default)
 };
 
 struct PlanRow {
@@ -57,7 +59,8 @@ static const PlanRow kTable[] = {
     // 128x256 1486.
     {8192, 8192, 8192, T_BF16, 0, 1, {256, 8, 1, 0, 0, 1, 1, 1}},
     // 8192^3 int8: pair 256x256 1209; with 2 K slices per stage 1184;
-    // single-CTA 128x128 858.
+    // single-CTA 128x128 858 (512-K exact passes).  With 960-K passes (the
+    // default since): 1591, GROUP_M 16 1567, 768-K passes 1568.
     {8192, 8192, 8192, T_I8, 0, 0, {256, 8, 1, 0, 0, 1, 1, 0}},
     // (64, 8192, 8192) bf16, all row-major: 128x128 tiles, split 2: 246;
     // 128x256 split 4: 241; swapped 128x64 split 4: 230, split 2: 211.

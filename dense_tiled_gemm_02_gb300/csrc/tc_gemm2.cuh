@@ -58,6 +58,11 @@ struct PairCfg {
 // two 4 KB buffers (32 rows x 32 int32) per epilogue warp for C and D.
 constexpr uint32_t D_STAGE_BYTES = BM * 64 * 2;
 
+// Exact int8: accumulator columns each epilogue thread reads from tensor
+// memory per wait while draining a finished pass (two 16-column loads; 64
+// columns no longer fit the registers beside the 128 int32 sums).
+constexpr int I8_DRAIN = 32;
+
 template <bool I8X>
 __host__ __device__ constexpr uint32_t pair_stage_bytes() {
   return (I8X ? 4 : 2) * D_STAGE_BYTES;
@@ -104,11 +109,11 @@ __device__ __forceinline__ void st_d_chunk_rows(const uint8_t* chunk, uint16_t* 
 //
 // I8X: exact int8 GEMM on the bf16 tensor pipe (operands widened to bf16
 // beforehand, which is exact for |v| <= 128).  Each run of kb_per_chunk K
-// slices (512 K) is accumulated afresh in fp32, where every partial sum is an
-// integer of magnitude at most 512 * 2^14 = 2^23 and therefore exact; the
-// epilogue converts each finished chunk to int32 and adds it to running sums
-// held in registers (eight epilogue warps, 128 columns each), while the MMA
-// fills the other accumulator with the next chunk.  After the last chunk C is
+// slices (960 K by default) is accumulated afresh in fp32, where every partial
+// sum is an integer of magnitude at most 960 * 2^14 < 2^24 and therefore
+// exact; the epilogue converts each finished chunk to int32 and adds it to
+// running sums held in registers (eight epilogue warps, 128 columns each),
+// while the MMA fills the other accumulator with the next chunk.  After the last chunk C is
 // added and the sums are stored as int32.
 template <int BN, int STAGES, int KSUB, bool I8X>
 __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
@@ -393,20 +398,27 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
           named_barrier_sync(1, 32 * Cfg::EPI_WARPS);
           if (!ok) break;
           tc_fence_after();
-          // 16 columns at a time: the 128 sums already hold most of the
-          // registers a thread of this 320-thread block may have.
+          // I8_DRAIN columns per tensor-memory round trip: the loads of a
+          // batch are all issued before the one wait, so the latency of a
+          // load is paid once per batch, not once per 16 columns (the 128
+          // sums already hold most of the registers a thread of this
+          // 320-thread block may have, which bounds the batch).
+          constexpr int DC = I8_DRAIN;
 #pragma unroll
-          for (int c = 0; c < HC / 16; ++c) {
-            uint32_t v[16];
-            tmem_ld_32x32b_x16(tmem_base + lane_base + buf * BN + col0 + c * 16, v);
+          for (int c = 0; c < HC / DC; ++c) {
+            uint32_t v[DC];
+#pragma unroll
+            for (int x = 0; x < DC / 16; ++x)
+              tmem_ld_32x32b_x16(tmem_base + lane_base + buf * BN + col0 + c * DC + 16 * x,
+                                 *reinterpret_cast<uint32_t(*)[16]>(v + 16 * x));
             tmem_ld_wait();
-            if (c == HC / 16 - 1) {
+            if (c == HC / DC - 1) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive_cluster(map_shared_rank(acc_empty(buf), 0));
             }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) isum[c * 16 + j] += __float2int_rn(__uint_as_float(v[j]));
+            for (int j = 0; j < DC; ++j) isum[c * DC + j] += __float2int_rn(__uint_as_float(v[j]));
           }
           ++acc_it;
         }

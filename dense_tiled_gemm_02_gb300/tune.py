@@ -29,7 +29,8 @@ L2_BYTES = 129 * 10 ** 6
 class LibraryReference:
     """The candidate "cublas": PyTorch's own GEMM on the same operands, timed
     beside the plans as context (torch.addmm / torch.mm for 16-bit types,
-    torch._int_mm plus C for int8).  Not part of the library."""
+    torch._int_mm plus C for int8, torch._scaled_mm with unit scales plus C
+    for 8-bit floats).  Not part of the library."""
 
     def __init__(self, w):
         self.w = w
@@ -38,6 +39,12 @@ class LibraryReference:
         import torch
         if A.dtype == torch.int8:
             r = torch._int_mm(A, B)
+            torch.add(r, C, out=D) if C is not None else D.copy_(r)
+        elif A.element_size() == 1:
+            one = getattr(self, "_one", None)
+            if one is None:
+                one = self._one = torch.ones((), dtype=torch.float32, device=A.device)
+            r = torch._scaled_mm(A, B, scale_a=one, scale_b=one, out_dtype=D.dtype)
             torch.add(r, C, out=D) if C is not None else D.copy_(r)
         elif D.dtype == A.dtype:
             if C is not None and C.dtype == D.dtype:

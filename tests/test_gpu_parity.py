@@ -436,6 +436,7 @@ def test_full_config_every_element(name, plan):
 
 @pytest.mark.parametrize("name,plan", [("sq8192_bf16", None), ("sq8192_i8", None),
                                        ("sq8192_i8", "pair=0"), ("sq8192_i8", "native_i8=1"),
+                                       ("sq8192_i8", "i8chunk=960"),
                                        ("sq8192_e4m3", None)])
 def test_8192_sampled(name, plan):
     w = WORKLOADS[name]
@@ -628,7 +629,10 @@ def test_mx_scales_reach_the_right_rows_and_blocks():
 
 
 # ------------------------------------------------------------------ exact int8
-I8_PLANS = [None, "pair=1,ksub=1", "pair=1,ksub=2", "native_i8=1", "native_i8=1,group=1"]
+# i8chunk: K of one exact fp32 pass; 960 is the longest whose partial sums
+# stay below 2^24 (the all -128 case below reaches 960 * 2^14 per pass)
+I8_PLANS = [None, "pair=1,ksub=1", "pair=1,ksub=2", "native_i8=1", "native_i8=1,group=1",
+            "pair=1,i8chunk=960", "pair=1,ksub=2,i8chunk=768", "pair=0,i8chunk=960"]
 
 
 @pytest.mark.parametrize("plan", I8_PLANS)
@@ -641,6 +645,8 @@ def test_int8_exact_small(shape, plan):
     w = Workload("i8", 51, M, N, K, I8, I32, I32, "int", la, lb)
     inp = make_inputs(w)
     D, p = run_gpu(w, inp, plan=plan)
+    if plan and "i8chunk" in plan:
+        assert plan.split("i8chunk=")[1].split(",")[0] in p.split("i8chunk=")[1], p
     _assert_ok(check_rows(w, inp, D), f"int8 {shape} [{p}]")
 
 
