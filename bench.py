@@ -630,8 +630,9 @@ def launches_per_step(g) -> int:
         return 1  # the decode kernel finishes D itself
     n = 1
     m = re.search(r"splits=(\d+)", plan)
-    if m and int(m.group(1)) > 1 and not re.search(r"\bfixup=1\b", plan):
-        n += 1  # the split-K reduce kernel
+    csk = re.search(r"\bcsk=(\d+)", plan)
+    if m and int(m.group(1)) > 1 and not (csk and int(csk.group(1)) > 1):
+        n += 1  # the split-K reduce kernel (none when the splits meet in a cluster)
     flag = {k: int(re.search(k + r"=(\d)", plan).group(1))
             for k in ("repack_a", "repack_b", "stage_c", "stage_d", "i8x")}
     if re.search(r"\bmx=1\b", plan):

@@ -12,7 +12,7 @@ Low-level names mirror ``include/gemm.h``: ``gemm_create``, ``gemm_run``,
 ``gemm_debug_set``, ``gemm_timing_enable``, ``gemm_timing_read``,
 ``gemm_host_io_enable``, ``gemm_run_host_batch``, ``gemm_pair_schedule``,
 ``gemm_cta_schedule``, ``gemm_decode_ring``, ``gemm_run_splitk_noalloc``,
-``gemm_noalloc_status``, ``gemm_run_mx``.
+``gemm_noalloc_status``, ``gemm_run_mx``, ``gemm_trace_set``.
 ``Gemm`` wraps a handle for torch tensors.
 """
 from __future__ import annotations
@@ -40,7 +40,8 @@ EXPORTED = ["gemm_create", "gemm_run", "gemm_get_status", "gemm_destroy", "gemm_
             "gemm_plan_string", "gemm_workspace_bytes", "gemm_raster_tile", "gemm_debug_set",
             "gemm_run_splitk_noalloc", "gemm_noalloc_status", "gemm_timing_enable", "gemm_timing_read",
             "gemm_host_io_enable", "gemm_run_host_batch", "gemm_pair_schedule",
-            "gemm_cta_schedule", "gemm_decode_ring", "gemm_run_mx"]
+            "gemm_cta_schedule", "gemm_decode_ring", "gemm_run_mx", "gemm_trace_set"]
+GEMM_TRACE_EVENTS = 10
 GEMM_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
@@ -97,6 +98,8 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
     lib.gemm_raster_tile.restype = ci
     lib.gemm_debug_set.argtypes = [vp, ci, ctypes.c_uint64]
     lib.gemm_debug_set.restype = ci
+    lib.gemm_trace_set.argtypes = [vp, vp]
+    lib.gemm_trace_set.restype = ci
     lib.gemm_run_splitk_noalloc.argtypes = [ctypes.POINTER(GemmDesc), ci, vp, vp, vp, vp, vp]
     lib.gemm_run_splitk_noalloc.restype = ci
     lib.gemm_noalloc_status.argtypes = [vp]
@@ -167,6 +170,10 @@ def gemm_raster_tile(t: int, num_pid_m: int, num_pid_n: int, group_m: int):
 
 def gemm_debug_set(h: int, flags: int, timeout_ns: int = 0) -> int:
     return load().gemm_debug_set(h, flags, timeout_ns)
+
+
+def gemm_trace_set(h: int, dev_buf: int | None) -> int:
+    return load().gemm_trace_set(h, dev_buf)
 
 
 def gemm_pair_schedule(tiles_m: int, tiles_n: int, group_m: int, num_kb: int, ksub: int,

@@ -35,6 +35,7 @@ UNITS = [
     ("tc_launch.cu", ["-DTC_BN=64"], "tc_bn64.o"),
     ("tc_pair_launch.cu", [], "tc_pair.o"),
     ("decode.cu", [], "decode.o"),
+    ("decode_mma.cu", [], "decode_mma.o"),
     ("i8_mma.cu", [], "i8_mma.o"),
 ]
 

@@ -106,9 +106,21 @@ struct KParams {
   // nothing), adds them up into its idle accumulator buffer while its own
   // MMAs run, then adds its accumulator and C and stores D.
   int sk1;
+  // Split-K over a cluster (csk = splits > 1, single-CTA kernel, one unit
+  // per CTA, cluster of csk consecutive CTAs = the splits of one tile): the
+  // CTAs of splits 1.. store their fp32 sums into the shared memory of the
+  // split-0 CTA (distributed shared memory), which adds them in split order,
+  // adds C and stores D: no partials in global memory, no reduce launch.
+  int csk;
   float* fix_ws;                 // [G][BM * BN] fp32, interleaved (see tc_gemm.cuh)
   uint32_t* fix_flag;            // [G], the epoch of the run that wrote fix_ws[c]
+  // Timeline hook (tests and profiling; null in normal runs): the tensor-core
+  // kernels write global-timer stamps of kTraceEvents events per CTA at
+  // trace[cta * kTraceEvents + event] (see trace_at in tc_gemm.cuh).
+  unsigned long long* trace;
 };
+
+constexpr int kTraceEvents = 10;
 
 // Instruction descriptor of tcgen05.mma kind::f16 and kind::f8f6f4: fp32
 // accumulator (bits 4-5 = 1), A/B element type (bits 7-9, 10-12: 0 fp16,

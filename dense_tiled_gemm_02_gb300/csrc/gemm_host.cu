@@ -73,13 +73,22 @@ EncodeFn get_encode() {
   return fn;
 }
 
-const TcVariant* find_variant(int bn, bool i8x, int pw = 0) {
+// cluster = 0: a variant without cluster split-K; cluster >= 2: the one
+// with the smallest cluster capacity that holds `cluster` splits.
+const TcVariant* find_variant(int bn, bool i8x, int pw = 0, int cluster = 0) {
   const TcVariant* tabs[3] = {kVariantsBN256, kVariantsBN128, kVariantsBN64};
   const int counts[3] = {kNumVariantsBN256, kNumVariantsBN128, kNumVariantsBN64};
+  const TcVariant* best = nullptr;
   for (int t = 0; t < 3; ++t)
-    for (int i = 0; i < counts[t]; ++i)
-      if (tabs[t][i].bn == bn && tabs[t][i].i8x == i8x && tabs[t][i].pw == pw) return &tabs[t][i];
-  return nullptr;
+    for (int i = 0; i < counts[t]; ++i) {
+      const TcVariant& v = tabs[t][i];
+      if (v.bn != bn || v.i8x != i8x || v.pw != pw) continue;
+      if (cluster == 0 ? v.cs == 1 : (v.cs >= cluster && (!best || v.cs < best->cs))) {
+        if (cluster == 0) return &v;
+        best = &v;
+      }
+    }
+  return best;
 }
 
 const PairVariant* find_pair(int bn, int ksub, bool i8x) {
@@ -123,6 +132,9 @@ struct gemm_plan {
   // 16-byte aligned; otherwise the split-K form planned beside it runs).
   bool decode_bulk = false;
   int decode_cpb = 0, decode_stages = 0, decode_cps = 0;
+  // Tensor-core form of the decode regime (decode_mma.cu): M <= 16 rows, B
+  // K-contiguous (decode_bk) or N-contiguous.
+  bool decode_mma = false, decode_bk = true;
   // 16-bit C / D whose rows are not 16-byte aligned: aligned workspace copies
   // (leading dimension stage_ld) that the kernel reads / writes instead.
   bool c_stage = false, d_stage = false;
@@ -131,6 +143,7 @@ struct gemm_plan {
   uint32_t epoch = 0;                         // flag value of the latest run
   uint32_t* status = nullptr;
   int debug_flags = 0;
+  unsigned long long* trace = nullptr;  // timeline hook (gemm_trace_set)
   uint64_t timeout_ns = kDefaultTimeoutNs;
   // Tensor maps of recently seen operand addresses (a few entries per
   // operand, replaced round-robin): encoding one costs microseconds of host
@@ -224,6 +237,8 @@ void apply_force_plan(PlanChoice& c) {
       else if (k == "kgroup") c.kgroup = v;
       else if (k == "lsu") c.lsu = v;
       else if (k == "i8chunk") c.i8chunk = v;
+      else if (k == "dmma") c.dmma = v ? 1 : -1;
+      else if (k == "csk") c.csk = v;
     }
     pos = end + 1;
   }
@@ -235,7 +250,7 @@ void make_plan_string(gemm_plan* h) {
                 "M=%lld N=%lld K=%lld decode=%d dbulk=%d swap=%d pair=%d bn=%d ksub=%d stages=%d "
                 "group_m=%d splits=%d kb_per_split=%d tail=%d grid=%d i8x=%d a_mn=%d b_mn=%d "
                 "repack_a=%d repack_b=%d stage_c=%d stage_d=%d ws_bytes=%zu native_i8=%d "
-                "sk=%d kgroup=%d lsu_a=%d lsu_b=%d mx=%d i8chunk=%d",
+                "sk=%d kgroup=%d lsu_a=%d lsu_b=%d mx=%d i8chunk=%d dmma=%d csk=%d",
                 (long long)h->desc.M, (long long)h->desc.N, (long long)h->desc.K, (int)h->decode,
                 (int)h->decode_bulk,
                 h->choice.swap,
@@ -247,15 +262,17 @@ void make_plan_string(gemm_plan* h) {
                 h->grid, (int)h->i8x, h->kp.a_mn, h->kp.b_mn,
                 (int)h->a.repack, (int)h->b.repack, (int)h->c_stage, (int)h->d_stage,
                 h->ws_bytes, (int)h->native_i8, h->kp.sk1, h->kp.kgroup, (int)h->a.lsu,
-                (int)h->b.lsu, (int)h->mx, h->choice.i8chunk);
+                (int)h->b.lsu, (int)h->mx, h->choice.i8chunk, (int)h->decode_mma, h->kp.csk);
   h->plan_str = buf;
 }
 
 // Plan of the decode kernel (no operand swap, no tensor maps): K split into
 // slices so that about four blocks per SM stream B, the slices' fp32
-// partials in the workspace, finished by the split-K reduce.  Leaves h's
-// workspace and status word allocated, or frees them and returns an error.
-int plan_decode(gemm_plan* h, int sms) {
+// partials in the workspace, finished by the last block of each column
+// block.  mma: the tensor-core form (decode_mma.cu) for up to 16 rows and
+// either B layout.  Leaves h's workspace and status word allocated, or frees
+// them and returns an error.
+int plan_decode(gemm_plan* h, int sms, bool mma) {
   const gemm_desc_t& d = h->desc;
   h->decode = true;
   h->M = d.M;
@@ -275,17 +292,36 @@ int plan_decode(gemm_plan* h, int sms) {
   kp.c_cs = d.layout_c == GEMM_ROW_MAJOR ? 1 : d.ldc;
   kp.d_rs = d.layout_d == GEMM_ROW_MAJOR ? d.ldd : 1;
   kp.d_cs = d.layout_d == GEMM_ROW_MAJOR ? 1 : d.ldd;
-  // Slices of kc K elements (a multiple of 256, the width of one warp step;
-  // at most 2048: a slice of A is at most 4 rows x 2048 x 2 bytes of shared
-  // memory), as many as fill one wave of resident blocks: a second, partial
-  // wave would double the time of the ones in it.
-  const int64_t col_blocks = (d.N + decode_columns_per_block() - 1) / decode_columns_per_block();
-  const int64_t slots = (int64_t)sms * decode_blocks_per_sm((int)d.M, 1024);
-  int64_t s = std::max<int64_t>(1, slots / col_blocks);
-  s = std::min<int64_t>(s, std::max<int64_t>(1, d.K / 256));
-  int64_t kc = round_up((d.K + s - 1) / s, 256);
-  kc = std::min<int64_t>(kc, 2048);
-  s = (d.K + kc - 1) / kc;
+  int64_t col_blocks = 0, s = 1, kc = 0;
+  if (mma) {
+    // Tensor-core form: blocks of decode_mma_cols() columns, K slices of a
+    // whole number of warp steps, about three blocks per SM (two for the
+    // N-contiguous form, whose partials hold all 128 columns of a block);
+    // a slice of A (16 rows at most) stays below 64 KB of shared memory.
+    h->decode_mma = true;
+    h->decode_bk = d.layout_b == GEMM_COL_MAJOR;
+    const int64_t cols = decode_mma_cols(h->decode_bk);
+    const int64_t step = decode_mma_kstep(h->decode_bk);
+    col_blocks = (d.N + cols - 1) / cols;
+    const int64_t target = (int64_t)sms * (h->decode_bk ? 3 : 2);
+    s = std::max<int64_t>(1, (target + col_blocks / 2) / col_blocks);
+    s = std::min<int64_t>(s, std::max<int64_t>(1, (d.K + step - 1) / step));
+    kc = round_up((d.K + s - 1) / s, step);
+    kc = std::min<int64_t>(kc, 1920);
+    s = (d.K + kc - 1) / kc;
+  } else {
+    // Slices of kc K elements (a multiple of 256, the width of one warp step;
+    // at most 2048: a slice of A is at most 4 rows x 2048 x 2 bytes of shared
+    // memory), as many as fill one wave of resident blocks: a second, partial
+    // wave would double the time of the ones in it.
+    col_blocks = (d.N + decode_columns_per_block() - 1) / decode_columns_per_block();
+    const int64_t slots = (int64_t)sms * decode_blocks_per_sm((int)d.M, 1024);
+    s = std::max<int64_t>(1, slots / col_blocks);
+    s = std::min<int64_t>(s, std::max<int64_t>(1, d.K / 256));
+    kc = round_up((d.K + s - 1) / s, 256);
+    kc = std::min<int64_t>(kc, 2048);
+    s = (d.K + kc - 1) / kc;
+  }
   h->decode_kc = (int)kc;
   kp.splits = (int)s;
   // Bulk-copy form: when A's and B's rows are K-contiguous with strides of
@@ -299,7 +335,7 @@ int plan_decode(gemm_plan* h, int sms) {
   const int64_t cpb = std::min<int64_t>(cmax, (d.N + sms * waves - 1) / (sms * waves));
   int cps = 0;
   const int stages = decode_bulk_ring((int)d.M, d.K, (int)cpb, &cps);
-  if (h->choice.no_dbulk != 1 && a_k_rows && d.ldb % 8 == 0 &&
+  if (!mma && h->choice.no_dbulk != 1 && a_k_rows && d.ldb % 8 == 0 &&
       (stages * cps >= cpb || stages >= 2) &&
       (h->choice.no_dbulk == -1 || d.N >= 4 * (int64_t)sms)) {
     h->decode_bulk = true;
@@ -651,9 +687,23 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     m.lsu = 0;
     m.no_decode = 1;
   }
-  if (!h->choice.no_decode && (d.ab_type == GEMM_F16 || d.ab_type == GEMM_BF16) && d.M >= 1 &&
-      d.M <= kDecodeMaxRows && d.layout_b == GEMM_COL_MAJOR && d.K % 8 == 0 && d.K >= 256) {
-    const int rc = plan_decode(h, sms);
+  // Decode regime: a handful of rows, 16-bit operands.  Up to four rows
+  // against a K-contiguous B take the CUDA-core forms (decode.cu).  The
+  // warp-level tensor-core form (decode_mma.cu: up to 16 rows, B of either
+  // layout) runs only when asked for (dmma=1): it measured slower than the
+  // tcgen05 path at 1 and 16 rows with either B layout at N = K = 4096
+  // (16 x 4096 x 4096: 23.1 against 16.3 us with K-contiguous B, 46.7
+  // against 16.8 with N-contiguous B; 1 x 4096 x 4096 N-contiguous: 20.7
+  // against 16.0) and slower than the bulk-copy form at one row (14.7
+  // against 9.7).
+  const bool f16ab = d.ab_type == GEMM_F16 || d.ab_type == GEMM_BF16;
+  const bool dec_cuda = f16ab && d.M >= 1 && d.M <= kDecodeMaxRows &&
+                        d.layout_b == GEMM_COL_MAJOR && d.K % 8 == 0 && d.K >= 256;
+  const bool dec_mma = f16ab && d.M >= 1 && d.M <= kDecodeMmaMaxRows && d.K >= 1 &&
+                       (d.layout_b == GEMM_ROW_MAJOR || d.K % 8 == 0);
+  const bool use_mma = dec_mma && h->choice.dmma == 1;
+  if (!h->choice.no_decode && (use_mma || dec_cuda)) {
+    const int rc = plan_decode(h, sms, use_mma);
     if (rc != GEMM_OK) {
       delete h;
       return rc;
@@ -796,6 +846,18 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   const int64_t units = (int64_t)kp.tiles_m * kp.tiles_n *
                         (kp.sk1 ? std::max(1, kp.num_kb) : kp.splits);
   if (!c.pair) h->grid = (int)std::max<int64_t>(1, std::min<int64_t>(units, max_ctas));
+  // Split-K over clusters: every unit its own CTA (no persistent loop), the
+  // splits of a tile one cluster, their sums added through shared memory.
+  kp.csk = 0;
+  if (c.csk && !c.pair && !h->i8x && !kp.sk1 && !h->mx && !h->a.lsu && !h->b.lsu &&
+      kp.splits >= 2 && units <= max_ctas) {
+    const TcVariant* v = find_variant(c.bn, false, 0, kp.splits);
+    if (v) {
+      h->variant = v;
+      kp.csk = kp.splits;
+      h->grid = (int)units;
+    }
+  }
 
   // Kernel attributes and, for the pair kernel, how many 2-CTA clusters
   // can be resident at once (the persistent grid).
@@ -842,7 +904,7 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   const int64_t in_es = elem_size(d.ab_type);
   plan_copy(h->a, in_es);
   plan_copy(h->b, in_es);
-  if (kp.splits > 1) {
+  if (kp.splits > 1 && !kp.csk) {
     h->ws_partial_off = off;
     off += (size_t)round_up((int64_t)kp.splits * h->M * h->N * 4, 256);
     const bool row = h->d_layout == GEMM_ROW_MAJOR;
@@ -961,6 +1023,7 @@ int run_impl(gemm_handle_t h, const void* A, const void* B, const void* C, void*
   kp.timeout_ns = h->timeout_ns;
   kp.debug_flags = h->debug_flags;
   h->debug_flags = 0;  // test hooks apply to one run
+  kp.trace = h->trace;
   const bool row_order = h->d_layout == GEMM_ROW_MAJOR;
   auto set_vec = [&]() {
     kp.c_vec = (kp.C && kp.c_cs == 1 && (reinterpret_cast<uintptr_t>(kp.C) % 16) == 0 &&
@@ -1063,10 +1126,13 @@ int run_impl(gemm_handle_t h, const void* A, const void* B, const void* C, void*
     a.status = h->status;
     a.timeout_ns = h->timeout_ns;
     a.debug_flags = kp.debug_flags;
+    a.mma = h->decode_mma;
+    a.b_kcontig = h->decode_bk;
     const bool timed = h->timing_used < h->timing_n;
     if (timed && cudaEventRecord(h->timing_ev[2 * h->timing_used], st) != cudaSuccess)
       return GEMM_ERR_CUDA;
-    if (launch_decode(a, st) != cudaSuccess) return GEMM_ERR_CUDA;
+    if ((a.mma ? launch_decode_mma(a, st) : launch_decode(a, st)) != cudaSuccess)
+      return GEMM_ERR_CUDA;
     if (timed) {
       if (cudaEventRecord(h->timing_ev[2 * h->timing_used + 1], st) != cudaSuccess)
         return GEMM_ERR_CUDA;
@@ -1165,7 +1231,7 @@ int run_impl(gemm_handle_t h, const void* A, const void* B, const void* C, void*
     kp.sfa = ca;
     kp.sfb = cb;
   }
-  if (kp.splits > 1) kp.ws = reinterpret_cast<float*>(ws + h->ws_partial_off);
+  if (kp.splits > 1 && !kp.csk) kp.ws = reinterpret_cast<float*>(ws + h->ws_partial_off);
   if (kp.sk1) {
     kp.fix_ws = reinterpret_cast<float*>(ws + h->ws_fix_off);
     kp.fix_flag = reinterpret_cast<uint32_t*>(ws + h->ws_fixflag_off);
@@ -1230,7 +1296,7 @@ int run_impl(gemm_handle_t h, const void* A, const void* B, const void* C, void*
       return GEMM_ERR_CUDA;
     ++h->timing_used;
   }
-  if (kp.splits > 1 && launch_reduce(kp, row_order, h->num_sms, st) != cudaSuccess)
+  if (kp.splits > 1 && !kp.csk && launch_reduce(kp, row_order, h->num_sms, st) != cudaSuccess)
     return GEMM_ERR_CUDA;
   if (d_staged && launch_copy_out16(d_staged, h->stage_ld, static_cast<uint16_t*>(D), h->ldd,
                                     h->M, h->N, h->num_sms, st) != cudaSuccess)
@@ -1377,6 +1443,12 @@ int gemm_debug_set(gemm_handle_t h, int flags, uint64_t timeout_ns) {
   if (!h) return GEMM_ERR_INVALID_ARG;
   h->debug_flags = flags;
   h->timeout_ns = timeout_ns ? timeout_ns : kDefaultTimeoutNs;
+  return GEMM_OK;
+}
+
+int gemm_trace_set(gemm_handle_t h, uint64_t* dev_buf) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  h->trace = reinterpret_cast<unsigned long long*>(dev_buf);
   return GEMM_OK;
 }
 

@@ -37,6 +37,10 @@ struct PlanChoice {
                  // single-CTA kernel's producer warps instead of a workspace copy
   int i8chunk;   // exact int8: K of one exact fp32 accumulation pass, a multiple of
                  // 64 up to 960 (0 = the default)
+  int dmma;      // decode regime: 1 takes the tensor-core (mma.sync) form whenever
+                 // the shape allows, -1 never, 0 the planner decides
+  int csk;       // single-CTA kernel with split-K: 1 adds the splits' sums through the
+                 // shared memory of a cluster of split CTAs instead of a reduce launch
 };
 
 struct PlanRow {

@@ -74,6 +74,40 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, vola
   }
 }
 
+// Non-blocking test of the same phase (the thread is never suspended).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// bounded_wait polling with the non-blocking test: for barriers completed by
+// another CTA of the cluster, where a suspended try_wait was seen to resume
+// microseconds after the phase completed.
+__device__ __forceinline__ bool bounded_spin_wait(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort, uint32_t* status,
+                                                  uint32_t code, uint64_t timeout_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((n & 255u) == 0u) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > timeout_ns) {
+        *abort = 1;
+        atomicOr(status, code);
+        return false;
+      }
+    }
+  }
+}
+
 // The same wait without the abort flag, for draining work already in flight.
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
   const uint64_t t0 = global_timer_ns();
@@ -353,6 +387,19 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
                    "memory");
+}
+
+// Bulk copy of `bytes` bytes (a multiple of 16, both addresses 16-byte
+// aligned) from this CTA's shared memory into the shared memory of a CTA of
+// this cluster; completion is counted as transaction bytes on a barrier of
+// that CTA (dst and bar from map_shared_rank).
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src,
+                                                     uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst_cluster),
+      "r"(src), "r"(bytes), "r"(bar_cluster)
+      : "memory");
 }
 
 // Arrive on a barrier that may live in the other CTA of the cluster.

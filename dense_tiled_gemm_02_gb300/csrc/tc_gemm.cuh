@@ -40,11 +40,15 @@ struct TileCfg {
 };
 
 // Variants with producer warps (PW > 0) also stage the block-scaled mode's
-// scale cells: 1 KB a ring stage (512 bytes of A's, 512 of B's).
-template <int BN, int STAGES, int PW = 0>
+// scale cells: 1 KB a ring stage (512 bytes of A's, 512 of B's).  Variants
+// for split-K over clusters of up to CS CTAs hold CS - 1 landing slots of
+// 128 x BN fp32 sums for the other splits' CTAs to store into.
+template <int BN, int STAGES, int PW = 0, int CS = 1>
 constexpr uint32_t smem_bytes() {
-  // ring + scale cells + barriers/flags + slack to align the ring to 1024 bytes
-  return STAGES * TileCfg<BN>::STAGE_TX + (PW > 0 ? STAGES * 1024u : 0u) + 256 + 1024;
+  // ring + scale cells + landing slots + barriers/flags + slack to align the
+  // ring to 1024 bytes
+  return STAGES * TileCfg<BN>::STAGE_TX + (PW > 0 ? STAGES * 1024u : 0u) +
+         static_cast<uint32_t>(CS - 1) * BM * BN * 4u + 256 + 1024;
 }
 
 // ------------------------------------------------------------------ epilogue helpers
@@ -281,6 +285,17 @@ __device__ __forceinline__ void store_d_i32(const KParams& p, int r, int c0, int
   }
 }
 
+// ------------------------------------------------------------------ timeline hook
+// Events of one CTA: 0 entry, 1 past the wait for the previous kernel,
+// 2 first loads issued (thread 0), 3 first stage landed, 4 last accumulator
+// committed (the MMA thread), 5 last accumulator seen by the epilogue, 6
+// last tile stored, 7 past the final block barrier (thread 64); cluster
+// split-K: 8 the other splits' sums landed (split 0), 9 this split's sums
+// copied out (splits > 0).  Events 4-6 keep the stamp of the CTA's last unit.
+__device__ __forceinline__ void trace_at(const KParams& p, int e) {
+  if (p.trace) p.trace[blockIdx.x * kTraceEvents + e] = global_timer_ns();
+}
+
 // ------------------------------------------------------------------ in-kernel producer
 // 128-byte segments (64 16-bit elements) of operand rows, copied by groups of
 // 8 lanes (u = lane % 8: one 16-byte unit each) into rows of the
@@ -372,7 +387,15 @@ __device__ __forceinline__ void lsu_tile(const uint16_t* base, long long ld, boo
 // (16-bit rows off the 16-byte grid) into the ring themselves, beside the
 // TMA unit's loads of the others; a stage is full once the TMA bytes have
 // landed and every producer warp has arrived.
-template <int BN, int STAGES, bool I8X, int PW = 0>
+//
+// CS > 1: launched in clusters of p.csk <= CS CTAs for split-K (KParams::csk):
+// the epilogue of split s > 0 writes its sums into its own first landing
+// slot, and one thread bulk-copies the slot into slot s - 1 of the split-0
+// CTA (the copy engine moves it between the SMs; its bytes complete that
+// CTA's reduction barrier); the split-0 epilogue waits for the bytes of all
+// of them, adds the slots in split order to its own sums, then adds C and
+// stores D.
+template <int BN, int STAGES, bool I8X, int PW = 0, int CS = 1>
 __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const KParams p) {
@@ -383,9 +406,13 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
   uint8_t* sSF = sB + STAGES * Cfg::B_BYTES;  // PW > 0: scale cells, 1 KB a stage
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sSF + (PW > 0 ? STAGES * 1024 : 0));
-  // ring full/empty, accumulator full/empty, done; PW > 0: scale cells landed
-  constexpr int NBARS = 2 * STAGES + 5 + (PW > 0 ? STAGES : 0);
+  // CS > 1: landing slots, slot s holding float4 (chunk q, row i) at
+  // ((s * BN / 4 + q) * 128 + i) * 16 bytes (a warp's 32 rows adjacent)
+  uint8_t* sLand = sSF + (PW > 0 ? STAGES * 1024 : 0);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sLand + (CS - 1) * BM * BN * 4);
+  // ring full/empty, accumulator full/empty, done; PW > 0: scale cells
+  // landed; CS > 1: the other splits' sums landed
+  constexpr int NBARS = 2 * STAGES + 5 + (PW > 0 ? STAGES : 0) + (CS > 1 ? 1 : 0);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* ep_go = abort_flag + 1;  // the epilogue leader's verdict for its warps
@@ -397,11 +424,14 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
   auto acc_empty = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
   auto sf_full = [&](uint32_t s) { return bar0 + 8u * (2 * STAGES + 5 + s); };
+  const uint32_t red_bar = bar0 + 8u * (2 * STAGES + 5 + (PW > 0 ? STAGES : 0));
+  const bool csk = CS > 1 && p.csk > 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    trace_at(p, 0);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full(s), 1 + PW);
       mbar_init(empty(s), 1);
@@ -412,6 +442,12 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
       mbar_init(acc_empty(b), 128);
     }
     mbar_init(done_bar, 1);
+    if (CS > 1) {
+      mbar_init(red_bar, 1);
+      // split 0 of a cluster split-K: the other splits' slots, as bytes
+      if (p.csk > 1 && cluster_ctarank() == 0)
+        mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>(p.csk - 1) * BM * BN * 4u);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -432,11 +468,15 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Cluster split-K: every CTA's reduction barrier exists before any CTA of
+  // the cluster can arrive on another's.
+  if (csk) cluster_sync_all();
   const uint32_t tmem_base = *tmem_holder;
   // Everything above touches only on-chip state: it overlaps the previous
   // kernel in the stream; global memory is read and written only after it.
   pdl_wait();
   pdl_trigger();
+  if (threadIdx.x == 0) trace_at(p, 1);
 
   const CtaWork cw = cta_work(p, blockIdx.x, gridDim.x, !I8X);
   const uint64_t tmo = p.timeout_ns;
@@ -508,6 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
             for (int j = 0; j < BN / 64; ++j)
               tma_load_2d(b_dst + j * 8192u, &tmB, w.n0 + 64 * j, k0, full(s));
           }
+          if (it == 0) trace_at(p, 2);
           if (PW > 0 && p.mx) {
             // this stage's scale cells (512 bytes of A's for the tile row,
             // 512 of B's for the tile column), read by the producer warps
@@ -572,6 +613,7 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
               stop = true;
               break;
             }
+            if (i == 0 && kb == c0 && c0 == w.kb0) trace_at(p, 3);
             const uint32_t a_lo = a_lo0 + s * (Cfg::A_BYTES >> 4);
             const uint32_t b_lo = b_lo0 + s * (Cfg::B_BYTES >> 4);
             // 8-bit operands: the same four 32-byte steps along the row,
@@ -609,6 +651,7 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
           if (stop) break;
           mma_commit(acc_full(buf));
           ++acc_it;
+          trace_at(p, 4);
         }
       }
       // Every MMA issued so far must finish before tensor memory is freed.
@@ -681,6 +724,8 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
     uint32_t acc_it = 0;
     bool stop = false;
     const int row_local = q * 32 + lane;
+    // cluster split-K: the landing slots of the split-0 CTA (cluster rank 0)
+    const uint32_t land0 = csk ? map_shared_rank(smem_u32(sLand), 0) : 0u;
     for (int i = 0; i < cw.n && !stop; ++i) {
       const Unit w = cta_unit(p, cw, blockIdx.x, gridDim.x, i, BM, BN, !I8X);
       const int r = w.m0 + row_local;
@@ -689,7 +734,9 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
         // slices in flight (slice c in cb[c & 1]); the loop over slices is
         // kept rolled so that its code stays in the instruction cache.
         // In a tile that crosses N the groups past N are masked (ld_c8).
-        const bool c_rows = p.splits == 1 && !(w.tail && w.part == 1) && p.C != nullptr &&
+        // The CTA that stores D: no K split, or split 0 of a cluster split.
+        const bool owner = p.splits == 1 || (csk && w.split == 0);
+        const bool c_rows = owner && !(w.tail && w.part == 1) && p.C != nullptr &&
                             p.c_vec && p.c_type != T_F32 && r < p.M;
         const int c_ncols = min(BN, p.N - w.n0);
         const uint16_t* crow =
@@ -754,9 +801,11 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
         }
         // One thread waits and tells the other 127, so that all of them take
         // the same path through the named barriers below.
-        if (threadIdx.x == 64)
+        if (threadIdx.x == 64) {
           *ep_go = bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status,
                                 STATUS_TIMEOUT, tmo) ? 1 : 0;
+          trace_at(p, 5);
+        }
         named_barrier_sync(1, 128);
         const bool go = *ep_go != 0;
         named_barrier_sync(1, 128);
@@ -764,14 +813,28 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
           stop = true;
           break;
         }
+        if (csk && w.split == 0) {
+          // the other splits' sums have landed in this CTA's slots
+          if (threadIdx.x == 64) {
+            *ep_go = bounded_spin_wait(red_bar, 0u, abort_flag, p.status, STATUS_TIMEOUT, tmo)
+                         ? 1 : 0;
+            trace_at(p, 8);
+          }
+          named_barrier_sync(1, 128);
+          const bool rok = *ep_go != 0;
+          named_barrier_sync(1, 128);
+          if (!rok) {
+            stop = true;
+            break;
+          }
+        }
         tc_fence_after();
         // Typed fast path: 16-bit D rows contiguous and 16-byte aligned, C
         // absent or of D's type read by rows.  Every slice starts with a
         // warp-wide tcgen05.ld, so the path must be the same for all
         // threads: it depends on the call only.  Ragged tiles take it too: a
         // row past M adds no C and stores nothing, columns past N are masked.
-        const bool typed = p.splits == 1 && p.d_vec &&
-                           (p.d_type == T_BF16 || p.d_type == T_F16) &&
+        const bool typed = owner && p.d_vec && (p.d_type == T_BF16 || p.d_type == T_F16) &&
                            (p.C == nullptr || (p.c_vec && p.c_type == p.d_type));
         const int kind = !typed ? 0 : (p.C ? 1 : 2) + (p.d_type == T_F16 ? 2 : 0);
         auto slice = [&](const int c, uint4 (&cbuf)[4], auto ct_tag, auto dt_tag) {
@@ -807,7 +870,29 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) f[j] += __uint_as_float(o[j]);
           }
-          if (p.splits > 1) {
+          if (csk) {
+            const uint32_t q0 = static_cast<uint32_t>(c * 8);
+            if (w.split > 0) {
+              // into this CTA's own first slot, bulk-copied to the split-0 CTA below
+              float4* dst = reinterpret_cast<float4*>(sLand) + q0 * BM + row_local;
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                dst[k * BM] = make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+              return;
+            }
+            for (int sl = 0; sl < p.csk - 1; ++sl) {
+              const float4* src = reinterpret_cast<const float4*>(sLand) +
+                                  (static_cast<uint32_t>(sl) * (BN / 4) + q0) * BM + row_local;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const float4 v = src[k * BM];
+                f[4 * k] += v.x;
+                f[4 * k + 1] += v.y;
+                f[4 * k + 2] += v.z;
+                f[4 * k + 3] += v.w;
+              }
+            }
+          } else if (p.splits > 1) {
             store_partial(p, r, c0, w.split, f);
             return;
           }
@@ -876,6 +961,17 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
           }
         }
         ++acc_it;
+        if (csk && w.split > 0) {
+          // the slot is complete (and visible to the copy engine): one bulk
+          // copy into slot split - 1 of the split-0 CTA
+          fence_proxy_async_smem();
+          named_barrier_sync(1, 128);
+          if (threadIdx.x == 64) {
+            bulk_copy_to_cluster(land0 + static_cast<uint32_t>(w.split - 1) * BM * BN * 4u,
+                                 smem_u32(sLand), BM * BN * 4u, map_shared_rank(red_bar, 0));
+            trace_at(p, 9);
+          }
+        }
         if (w.tail && w.part == 1) {
           // Publish: every epilogue thread of this CTA has written its rows.
           __threadfence();
@@ -922,8 +1018,13 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
     }
   }
 
+  if (threadIdx.x == 64) trace_at(p, 6);
+  // Cluster split-K: no CTA leaves while another may still store into its
+  // shared memory.
+  if (csk) cluster_sync_all();
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 64) trace_at(p, 7);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_ALLOC);

@@ -34,6 +34,7 @@ struct TcVariant {
   int stages;
   bool i8x;
   int pw;  // producer warps beside the TMA unit (in-kernel loads of unaligned rows)
+  int cs;  // largest cluster for split-K through shared memory (1: none)
   uint32_t smem;
   cudaError_t (*launch)(const CUtensorMap&, const CUtensorMap&, const KParams&, int grid,
                         cudaStream_t);
@@ -133,8 +134,20 @@ struct DecodeArgs {
   uint32_t* status = nullptr;
   unsigned long long timeout_ns = 0;
   int debug_flags = 0;
+  // Tensor-core form (decode_mma.cu, mma = true): M <= kDecodeMmaMaxRows,
+  // B K-contiguous (b_kcontig, K a multiple of 8) or N-contiguous (element
+  // (k, n) at B[k * ldb + n]); blocks of decode_mma_cols(b_kcontig) columns
+  // and K slices of kc (a multiple of decode_mma_kstep(b_kcontig)); the
+  // same partials, counters and finish as the split-K form.
+  bool mma = false;
+  bool b_kcontig = true;
 };
 cudaError_t launch_decode(const DecodeArgs& d, cudaStream_t st);
+constexpr int kDecodeMmaMaxRows = 16;
+cudaError_t launch_decode_mma(const DecodeArgs& d, cudaStream_t st);
+int decode_mma_cols(bool b_kcontig);
+int decode_mma_kstep(bool b_kcontig);
+size_t decode_mma_smem(int M, int kc, bool b_kcontig);
 // Ring of the bulk-copy form for M rows of K elements and cpb columns per
 // block, in the shared memory it may use beside A: when all cpb columns fit,
 // a slot for each (stages * *cps >= cpb, one round trip, no stage reused);

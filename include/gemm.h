@@ -357,6 +357,27 @@ GEMM_API int gemm_decode_ring(int M, int64_t K, int cpb, int* cps, int64_t* smem
 #define GEMM_DEBUG_SKIP_FIRST_FILL 1
 GEMM_API int gemm_debug_set(gemm_handle_t h, int flags, uint64_t timeout_ns);
 
+/*
+ * Timeline hook (profiling and tests; not for production use): with a
+ * non-null dev_buf (device memory of at least grid x GEMM_TRACE_EVENTS
+ * uint64 values, owned by the caller), every later gemm_run whose plan runs
+ * the single-CTA tensor-core kernel writes, per CTA c, global-timer stamps
+ * (ns) at dev_buf[c * GEMM_TRACE_EVENTS + e] for the events e: 0 kernel
+ * entry, 1 past the wait for the previous kernel in the stream, 2 first
+ * operand loads issued, 3 first ring stage landed, 4 last accumulator
+ * committed by the MMA thread, 5 last accumulator seen by the epilogue, 6
+ * last tile stored, 7 past the final block barrier (0-2 stamped by thread
+ * 0, 3-4 by the MMA thread, 5-7 by the first epilogue thread); with the
+ * splits of a tile reduced within a cluster, 8 the other splits' sums
+ * landed (split-0 CTA) and 9 the CTA's own sums sent (other splits).
+ * Stamps of CTAs without work, and events that do not apply, are not
+ * defined.
+ * A null dev_buf turns the hook off.  The grid is the "grid=" field of the
+ * plan string.
+ */
+#define GEMM_TRACE_EVENTS 10
+GEMM_API int gemm_trace_set(gemm_handle_t h, uint64_t* dev_buf);
+
 #ifdef __cplusplus
 }
 #endif

@@ -84,9 +84,10 @@ def test_family_stems_and_native_int8_plan():
     p = plan(bn=128) + " native_i8=1"
     assert ncu_record.family_of(p) == "i8mma"
     assert bench.kernel_name(p) == "i8_mma_kernel"
-    # the split-K reduce kernel is not launched when the GEMM kernel finishes
-    # its split tiles itself
-    assert bench.launches_per_step(_G(plan(splits=2) + " fixup=1")) == 1
+    # the split-K reduce kernel is not launched when the splits of a tile add
+    # their sums within a cluster
+    assert bench.launches_per_step(_G(plan(splits=2) + " csk=2")) == 1
+    assert bench.launches_per_step(_G(plan(splits=2) + " csk=0")) == 2
 
 
 RAW = """"ID","Process ID","Kernel Name","gpu__time_duration.sum","dram__bytes_read.sum","dram__bytes_write.sum","launch__grid_size"

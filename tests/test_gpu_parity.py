@@ -421,7 +421,11 @@ FULL = [("sq4096_bf16", None), ("sq4096_bf16", "pair=1,bn=256,tail=0"), ("sq4096
         ("skinny8192x128x4096_bf16", "pair=0,bn=64,kgroup=4"),
         ("skinny64x8192x8192_bf16", "pair=0,bn=128,splits=2,kgroup=2"),
         ("rag4095x4097x4099_bf16", "pair=0,bn=256,lsu=1"),
-        ("rag4095x4097x4099_bf16", "pair=0,bn=128,lsu=1")]
+        ("rag4095x4097x4099_bf16", "pair=0,bn=128,lsu=1"),
+        ("skinny8192x128x4096_bf16", "pair=0,bn=128,splits=2,csk=1"),
+        ("skinny64x8192x8192_bf16", "pair=0,bn=128,splits=2,csk=1"),
+        ("decode16x4096x4096_bf16", "decode=0,pair=0,bn=64,splits=4,csk=1"),
+        ("decode1x4096x4096_bf16_brow", "decode=0,pair=0,bn=64,splits=4,csk=1")]
 
 
 @pytest.mark.parametrize("name,plan", FULL, ids=[f"{n}-{p}" for n, p in FULL])
@@ -515,7 +519,7 @@ DECODE_CASES = [
 ]
 
 
-@pytest.mark.parametrize("plan", [None, "decode=0", "dbulk=1", "dbulk=0"])
+@pytest.mark.parametrize("plan", [None, "decode=0", "dbulk=1", "dbulk=0", "dmma=1"])
 @pytest.mark.parametrize("case", DECODE_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}-off{c[8]}"
                                                    for c in DECODE_CASES])
 def test_decode_kernel(case, plan):
@@ -551,6 +555,56 @@ def test_decode_kernel(case, plan):
         assert e.value.code == pkg.GEMM_ERR_MISALIGNED
         g.close()
         return
+    g.run(A, B, C, D)
+    assert g.status() == pkg.GEMM_OK
+    g.close()
+    _assert_ok(check_rows(w, inp, D_storage.cpu()), f"{case} [{p}]")
+
+
+# The tensor-core decode form (mma.sync, up to 16 rows, B in either layout):
+# (M, N, K, layout_a, ab, c, d, layout_d, B element offset, layout_b).
+DMMA_CASES = [
+    (1, 4096, 4096, ROW, BF16, BF16, BF16, ROW, 0, ROW),
+    (16, 4096, 4096, ROW, BF16, BF16, BF16, ROW, 0, ROW),
+    (5, 1000, 1000, COL, F16, F32, F16, ROW, 0, ROW),    # K ends inside a 16-row step
+    (9, 777, 333, ROW, BF16, None, F32, COL, 0, ROW),    # N off the 8-column grid: 2-byte loads
+    (16, 264, 2050, ROW, BF16, BF16, BF16, ROW, 1, ROW),  # B off the 16-byte grid
+    (8, 136, 24, ROW, F16, F16, F16, ROW, 0, ROW),       # one short K slice
+    (7, 4096, 512, ROW, F16, F16, F16, ROW, 0, COL),
+    (16, 1000, 4104, COL, BF16, F32, BF16, COL, 0, COL),  # K not a multiple of 128
+    (12, 130, 8192, ROW, BF16, BF16, BF16, ROW, 1, COL),  # B off the 16-byte grid, few columns
+    (3, 4096, 4096, ROW, BF16, BF16, BF16, ROW, 0, COL),  # forced below 5 rows
+    (16, 8, 64, ROW, BF16, BF16, BF16, ROW, 0, COL),
+]
+
+
+# every case with the form forced, the aligned ones also with the default plan
+DMMA_RUNS = [(c, "dmma=1") for c in DMMA_CASES] + [(c, None) for c in DMMA_CASES if c[8] == 0]
+
+
+@pytest.mark.parametrize("case,plan", DMMA_RUNS,
+                         ids=[f"{c[0]}x{c[1]}x{c[2]}-{'kc' if c[9] == COL else 'nc'}-off{c[8]}-{p}"
+                              for c, p in DMMA_RUNS])
+def test_decode_mma_form(case, plan):
+    """The warp-level tensor-core decode form (up to 16 rows, B of either
+    layout; taken when asked for with dmma=1, else these shapes run on the
+    tcgen05 path or, at most 4 rows against a K-contiguous B, the CUDA-core
+    decode forms); every element against the oracle."""
+    M, N, K, la, ab, ct, dt, ld, off, lb = case
+    w = Workload("dmma", 66, M, N, K, ab, ct, dt, "normal", la, lb, ROW, ld)
+    inp = make_inputs(w)
+    dev = torch.device("cuda")
+    A = logical(inp["A"].to(dev), la)
+    flat = torch.zeros(N * K + 8, dtype=inp["B"].dtype, device=dev)
+    flat[off:off + N * K] = inp["B"].to(dev).reshape(-1)
+    B = logical(flat[off:off + N * K].view(storage_shape(K, N, lb)), lb)
+    C = None if inp["C"] is None else inp["C"].to(dev)
+    D_storage = torch.zeros(storage_shape(M, N, ld), dtype=TORCH_DTYPE[dt], device=dev)
+    D = logical(D_storage, ld)
+    with forced_plan(plan):
+        g = pkg.Gemm.like(A, B, C, D)
+    p = g.plan()
+    assert ("dmma=1" in p) == (plan == "dmma=1"), p
     g.run(A, B, C, D)
     assert g.status() == pkg.GEMM_OK
     g.close()
@@ -738,3 +792,57 @@ def test_decode_bulk_wait_reports_timeout_and_context_survives():
     assert g.status() == pkg.GEMM_OK
     g.close()
     _assert_ok(check_rows(w, inp, D.cpu()), "after timeout")
+
+
+# Split-K over clusters (csk): (M, N, K, layouts A/B/C/D, types C/D, bn, splits)
+CSK_CASES = [
+    (1000, 520, 2000, ROW, ROW, ROW, ROW, BF16, BF16, 128, 2),
+    (300, 200, 4100, ROW, COL, ROW, ROW, None, F32, 64, 3),      # 3 CTAs in a cluster of up to 4
+    (129, 64, 8192, COL, ROW, COL, COL, F16, F16, 64, 4),       # column-major C and D
+    (64, 1000, 4096, ROW, COL, ROW, ROW, BF16, BF16, 64, 4),    # swapped (long N on the M side)
+    (256, 256, 128, ROW, ROW, ROW, ROW, BF16, BF16, 128, 2),    # one K slice per split
+]
+
+
+@pytest.mark.parametrize("case", CSK_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}-s{c[10]}" for c in CSK_CASES])
+def test_cluster_split_k(case):
+    """The splits of a tile add their sums through the shared memory of
+    their cluster; every element against the oracle, no reduce launch."""
+    M, N, K, la, lb, lc, ld, ct, dt, bn, s = case
+    ab = F16 if ct == F16 else BF16
+    w = Workload("csk", 68, M, N, K, ab, ct, dt, "normal", la, lb, lc, ld)
+    inp = make_inputs(w)
+    D, p = run_gpu(w, inp, plan=f"pair=0,bn={bn},splits={s},csk=1,decode=0")
+    assert f"csk={s}" in p and f"splits={s}" in p, p
+    _assert_ok(check_rows(w, inp, D), f"csk {case} [{p}]")
+
+
+def test_timeline_hook_stamps_in_order():
+    """gemm_trace_set: every CTA of the single-CTA kernel stamps its events in
+    causal order; with the hook off the buffer is left alone."""
+    import re
+    w = Workload("tl", 67, 1000, 520, 700, BF16, BF16, BF16, "normal")
+    inp = make_inputs(w)
+    dev = torch.device("cuda")
+    A, B, C = inp["A"].to(dev), inp["B"].to(dev), inp["C"].to(dev)
+    D = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
+    with forced_plan("pair=0,bn=64"):
+        g = pkg.Gemm.like(A, B, C, D)
+    grid = int(re.search(r"grid=(\d+)", g.plan()).group(1))
+    buf = torch.zeros(grid * pkg.GEMM_TRACE_EVENTS, dtype=torch.int64, device=dev)
+    assert pkg.gemm_trace_set(g.handle, buf.data_ptr()) == pkg.GEMM_OK
+    g.run(A, B, C, D)
+    assert g.status() == pkg.GEMM_OK
+    t = buf.view(grid, pkg.GEMM_TRACE_EVENTS).cpu()[:, :8]  # 8, 9: cluster split-K only
+    assert (t > 0).all()
+    # each thread's own stamps are in order (0-2 thread 0, 3-4 the MMA
+    # thread, 5-7 the first epilogue thread)
+    for a, b in ((0, 1), (1, 2), (3, 4), (5, 6), (6, 7)):
+        assert (t[:, b] >= t[:, a]).all(), (a, b, t)
+    assert pkg.gemm_trace_set(g.handle, None) == pkg.GEMM_OK
+    buf.zero_()
+    g.run(A, B, C, D)
+    assert g.status() == pkg.GEMM_OK
+    assert int(buf.abs().sum()) == 0
+    g.close()
+    _assert_ok(check_rows(w, inp, D.cpu()), "timeline run")
