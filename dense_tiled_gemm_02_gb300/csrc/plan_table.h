@@ -68,10 +68,15 @@ static const PlanRow kTable[] = {
     {8192, 8192, 8192, T_I8, 0, 0, {256, 8, 1, 0, 0, 1, 1, 0}},
     // (64, 8192, 8192) bf16, all row-major: 128x128 tiles, split 2: 246;
     // 128x256 split 4: 241; swapped 128x64 split 4: 230, split 2: 211.
-    {64, 8192, 8192, T_BF16, 0, 0, {128, 8, 2, 0, 0, 0, 1, 0}},
+    // The two splits of a tile reduced within their cluster (csk): 232
+    // against 226 with the reduce launch (128x128 unsplit: 149).
+    {64, 8192, 8192, T_BF16, 0, 0, {128, 8, 2, 0, 0, 0, 1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 1}},
     // (8192, 128, 4096) bf16: 128x64 tiles, no split: 370; 128x128 no
-    // split: 319, split 2: 286; pair 256x128 split 4: 260.
-    {8192, 128, 4096, T_BF16, 0, 0, {64, 8, 1, 0, 0, 0, 1, 0}},
+    // split: 319, split 2: 286; pair 256x128 split 4: 260.  128x128 with
+    // two splits reduced within their cluster: 347 against 291 for 128x64
+    // unsplit on the same box (the K loops of the 128 CTAs stream A at
+    // 5.3 TB/s; 128x64 tiles read each A row twice).
+    {8192, 128, 4096, T_BF16, 0, 0, {128, 8, 2, 0, 0, 0, 1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 1}},
     // (1000, 1000, 1000) bf16: 128x64: 130; 128x128: 104; pair: 105 / 84.
     {1000, 1000, 1000, T_BF16, 0, 0, {64, 8, 1, 0, 0, 0, 1, 0}},
     // 1024^3 fp16: 128x64: 202; 128x128: 174; pair 256x128: 168.

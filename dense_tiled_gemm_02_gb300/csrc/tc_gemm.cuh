@@ -152,10 +152,28 @@ __device__ __forceinline__ void add_c_f(const KParams& p, int r, int c0, float (
     }
     return;
   }
+  // Element loads (a strided or unaligned C): all 32 issued before the
+  // first is used, so that the row pays one memory latency, not 32.
+  if (p.c_type == T_F32) {
+    const float* C = static_cast<const float*>(p.C) + r * p.c_rs;
+    float v[32];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const int c = c0 + j;
-    if (c < p.N) f[j] += load_elem_f(p.C, p.c_type, r * p.c_rs + c * p.c_cs);
+    for (int j = 0; j < 32; ++j) v[j] = c0 + j < p.N ? C[(c0 + j) * p.c_cs] : 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) f[j] += v[j];
+    return;
+  }
+  const uint16_t* C = static_cast<const uint16_t*>(p.C) + r * p.c_rs;
+  uint32_t v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = c0 + j < p.N ? C[(c0 + j) * p.c_cs] : 0u;
+  if (p.c_type == T_BF16) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) f[j] += __uint_as_float(v[j] << 16);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      f[j] += __half2float(__ushort_as_half(static_cast<unsigned short>(v[j])));
   }
 }
 
@@ -472,13 +490,18 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
   // the cluster can arrive on another's.
   if (csk) cluster_sync_all();
   const uint32_t tmem_base = *tmem_holder;
+  // The work split and the load thread's first unit depend on the kernel
+  // parameters only: computed before the wait (their 64-bit index
+  // arithmetic otherwise delays the first loads by a microsecond or two).
+  const CtaWork cw = cta_work(p, blockIdx.x, gridDim.x, !I8X);
+  Unit w_first{};
+  if (threadIdx.x == 0 && cw.n > 0) w_first = cta_unit(p, cw, blockIdx.x, gridDim.x, 0, BM, BN, !I8X);
   // Everything above touches only on-chip state: it overlaps the previous
   // kernel in the stream; global memory is read and written only after it.
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x == 0) trace_at(p, 1);
 
-  const CtaWork cw = cta_work(p, blockIdx.x, gridDim.x, !I8X);
   const uint64_t tmo = p.timeout_ns;
 
   if (warp == 0) {
@@ -488,7 +511,7 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
       int64_t skipped = -1;
       bool stop = false;
       for (int i = 0; i < cw.n && !stop; ++i) {
-        const Unit w = cta_unit(p, cw, blockIdx.x, gridDim.x, i, BM, BN, !I8X);
+        const Unit w = i == 0 ? w_first : cta_unit(p, cw, blockIdx.x, gridDim.x, i, BM, BN, !I8X);
         for (int kb = w.kb0; kb < w.kb1 && !stop; ++kb) {
           // Slices are issued in groups of kgroup consecutive K slices once
           // that many stages are free, so that each row of a K-major operand

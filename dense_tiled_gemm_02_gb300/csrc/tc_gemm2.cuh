@@ -182,14 +182,19 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
   cluster_sync_all();  // both CTAs' barriers exist before either signals the other
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // The work split and the load thread's first unit depend on the kernel
+  // parameters only: computed before the wait, so that the first loads go
+  // out as soon as it returns.
+  const int cid = blockIdx.x >> 1;
+  const int ncl = gridDim.x >> 1;
+  const PairWork pw = pair_work(p, KSUB, cid, ncl);
+  Unit w_first{};
+  if (threadIdx.x == 0 && pw.n > 0) w_first = pair_unit(p, pw, KSUB, cid, ncl, 0, BN);
   // Everything above touches only on-chip state: it overlaps the previous
   // kernel in the stream; global memory is read and written only after it.
   pdl_wait();
   pdl_trigger();
 
-  const int cid = blockIdx.x >> 1;
-  const int ncl = gridDim.x >> 1;
-  const PairWork pw = pair_work(p, KSUB, cid, ncl);
   const uint64_t tmo = p.timeout_ns;
 
   if (warp == 0) {
@@ -199,7 +204,7 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
       int64_t skipped = -1;
       bool stop = false;
       for (int i = 0; i < pw.n && !stop; ++i) {
-        const Unit w = pair_unit(p, pw, KSUB, cid, ncl, i, BN);
+        const Unit w = i == 0 ? w_first : pair_unit(p, pw, KSUB, cid, ncl, i, BN);
         const int am = w.m0 + BM * static_cast<int>(rank);
         const int bn0 = w.n0 + Cfg::BNH * static_cast<int>(rank);
         for (int kb = w.kb0; kb < w.kb1; kb += KSUB) {

@@ -383,8 +383,8 @@ TABLE_ROWS = {
     "sq4096_bf16": "pair=1 bn=256 ksub=1",
     "sq8192_bf16": "pair=1 bn=256 ksub=1",
     "sq8192_i8": "pair=1 bn=256 ksub=1",
-    "skinny64x8192x8192_bf16": "swap=0 pair=0 bn=128 ksub=1 stages=7",
-    "skinny8192x128x4096_bf16": "swap=0 pair=0 bn=64 ksub=1 stages=9",
+    "skinny64x8192x8192_bf16": "swap=0 pair=0 bn=128 ksub=1 stages=5",
+    "skinny8192x128x4096_bf16": "swap=0 pair=0 bn=128 ksub=1 stages=5",
     "rag1000_bf16": "swap=0 pair=0 bn=64",
     "sq1024_f16": "swap=0 pair=0 bn=64",
 }
@@ -404,8 +404,10 @@ def test_plan_table_rows_engage(name):
     plan = g.plan()
     g.close()
     assert TABLE_ROWS[name] in plan, plan
-    want_splits = {"skinny64x8192x8192_bf16": 2}.get(name, 1)
+    want_splits = {"skinny64x8192x8192_bf16": 2, "skinny8192x128x4096_bf16": 2}.get(name, 1)
     assert f" splits={want_splits} " in plan, plan
+    if want_splits > 1:
+        assert f"csk={want_splits}" in plan, plan
 
 
 # ------------------------------------------------------------------ full-size configs
@@ -419,6 +421,8 @@ FULL = [("sq4096_bf16", None), ("sq4096_bf16", "pair=1,bn=256,tail=0"), ("sq4096
         ("skinny8192x128x4096_bf16", "pair=0,bn=128,sk=1"),
         ("skinny8192x128x4096_bf16", "pair=0,bn=64,sk=1"),
         ("skinny8192x128x4096_bf16", "pair=0,bn=64,kgroup=4"),
+        ("skinny8192x128x4096_bf16", "pair=0,bn=64,splits=1"),
+        ("skinny64x8192x8192_bf16", "pair=0,bn=128,splits=2,csk=0"),
         ("skinny64x8192x8192_bf16", "pair=0,bn=128,splits=2,kgroup=2"),
         ("rag4095x4097x4099_bf16", "pair=0,bn=256,lsu=1"),
         ("rag4095x4097x4099_bf16", "pair=0,bn=128,lsu=1"),
