@@ -41,7 +41,7 @@ EXPORTED = ["gemm_create", "gemm_run", "gemm_get_status", "gemm_destroy", "gemm_
             "gemm_run_splitk_noalloc", "gemm_noalloc_status", "gemm_timing_enable", "gemm_timing_read",
             "gemm_host_io_enable", "gemm_run_host_batch", "gemm_pair_schedule",
             "gemm_cta_schedule", "gemm_decode_ring", "gemm_run_mx", "gemm_trace_set"]
-GEMM_TRACE_EVENTS = 10
+GEMM_TRACE_EVENTS = 32
 GEMM_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 

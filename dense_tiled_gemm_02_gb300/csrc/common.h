@@ -78,6 +78,8 @@ struct KParams {
   long long d_rs, d_cs;
   int d_vec;                     // D rows contiguous and 16-byte aligned
   int d_tma;                     // 16-bit D stored through shared memory by TMA (pair kernel)
+  int c_tma;                     // with d_tma: C of D's type loaded by TMA into the same
+                                 // staging buffers (pair kernel, 16-bit types)
   int c_vec;                     // C rows contiguous and 16-byte aligned
   float* ws;                     // split-K partial sums (fp32), or null
   long long ws_rs, ws_cs, ws_split;
@@ -120,7 +122,7 @@ struct KParams {
   unsigned long long* trace;
 };
 
-constexpr int kTraceEvents = 10;
+constexpr int kTraceEvents = 32;
 
 // Instruction descriptor of tcgen05.mma kind::f16 and kind::f8f6f4: fp32
 // accumulator (bits 4-5 = 1), A/B element type (bits 7-9, 10-12: 0 fp16,

@@ -1276,6 +1276,7 @@ int run_impl(gemm_handle_t h, const void* A, const void* B, const void* C, void*
   } else {
     kp.d_tma = (h->pair && kp.splits == 1 && kp.d_vec &&
                 (d.d_type == GEMM_BF16 || d.d_type == GEMM_F16)) ? 1 : 0;
+    kp.c_tma = 0;
     if (kp.d_tma) {
       void* dp = kp.D;
       const int64_t drs = kp.d_rs;
@@ -1283,6 +1284,17 @@ int run_impl(gemm_handle_t h, const void* A, const void* B, const void* C, void*
         return encode_store_d(m, dp, drs, h->M, h->N);
       });
       if (!tmd) return GEMM_ERR_CUDA;
+      // A C of D's type with 16-byte rows comes in by TMA into the staging
+      // buffers (the same 32 x 64 boxes, 128-byte swizzle).
+      if (kp.C && kp.c_vec && d.c_type == d.d_type) {
+        void* cp = const_cast<void*>(kp.C);
+        const int64_t crs = kp.c_rs;
+        tmc = cached_map(h, 3, cp, [&](CUtensorMap* m) {
+          return encode_store_d(m, cp, crs, h->M, h->N);
+        });
+        if (!tmc) return GEMM_ERR_CUDA;
+        kp.c_tma = 1;
+      }
     }
   }
   const bool timed = h->timing_used < h->timing_n;

@@ -310,6 +310,9 @@ __device__ __forceinline__ void store_d_i32(const KParams& p, int r, int c0, int
 // last tile stored, 7 past the final block barrier (thread 64); cluster
 // split-K: 8 the other splits' sums landed (split 0), 9 this split's sums
 // copied out (splits > 0).  Events 4-6 keep the stamp of the CTA's last unit.
+// The pair kernel (tc_gemm2.cuh) stamps 0-7 the same way and, in the
+// cluster's even CTA, 10 + 2i / 11 + 2i when the MMA thread starts / commits
+// its unit i (i < 11).
 __device__ __forceinline__ void trace_at(const KParams& p, int e) {
   if (p.trace) p.trace[blockIdx.x * kTraceEvents + e] = global_timer_ns();
 }

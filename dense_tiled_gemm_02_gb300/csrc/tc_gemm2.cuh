@@ -129,13 +129,14 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
   uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
   uint8_t* sD = sB + STAGES * Cfg::B_BYTES;  // staging buffers, 1024-aligned
   uint64_t* bars = reinterpret_cast<uint64_t*>(sD + pair_stage_bytes<I8X>());
-  // ring full/empty, accumulator full/empty, done; int8: C-load barriers of
-  // the 8 epilogue warps' two staging buffers
-  constexpr int NBARS = 2 * STAGES + 5 + (I8X ? 2 * Cfg::EPI_WARPS : 0);
+  // ring full/empty, accumulator full/empty, done; C-load barriers of the
+  // epilogue warps' two staging buffers
+  constexpr int NBARS = 2 * STAGES + 5 + 2 * Cfg::EPI_WARPS;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* ep_go = abort_flag + 1;  // the epilogue leader's verdict for its warps
 
+  if (threadIdx.x == 0) trace_at(p, 0);
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](uint32_t s) { return bar0 + 8u * s; };
   auto empty = [&](uint32_t s) { return bar0 + 8u * (STAGES + s); };
@@ -159,11 +160,10 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
       mbar_init(acc_empty(b), 2 * Cfg::EPI_WARPS);  // one arrival per epilogue warp of both CTAs
     }
     mbar_init(done_bar, 1);
-    if constexpr (I8X)
-      for (int e = 0; e < Cfg::EPI_WARPS; ++e) {
-        mbar_init(cbar(e, 0), 1);
-        mbar_init(cbar(e, 1), 1);
-      }
+    for (int e = 0; e < Cfg::EPI_WARPS; ++e) {
+      mbar_init(cbar(e, 0), 1);
+      mbar_init(cbar(e, 1), 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (p.d_tma) tma_prefetch_desc(&tmD);
-    if (I8X && p.d_tma && p.C) tma_prefetch_desc(&tmC);
+    if ((I8X && p.d_tma && p.C) || (!I8X && p.c_tma)) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_holder), Cfg::TMEM_COLS);
@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
   // kernel in the stream; global memory is read and written only after it.
   pdl_wait();
   pdl_trigger();
+  if (threadIdx.x == 0) trace_at(p, 1);
 
   const uint64_t tmo = p.timeout_ns;
 
@@ -239,6 +240,7 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
               }
             }
           }
+          if (it == 0) trace_at(p, 2);
           ++it;
           if (++s == STAGES) {
             s = 0;
@@ -279,6 +281,7 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
       bool stop = false;
       const bool f8 = !I8X && p.f8 != 0;
       // One pass of the K loop into accumulator buffer `buf`.
+      bool first_stage = true;
       auto k_loop = [&](const int kc, const int ke, const uint32_t buf) {
         const uint32_t d_tmem = tmem_base + buf * BN;
         uint32_t accumulate = 0;
@@ -286,6 +289,10 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
           if (!bounded_wait(full(s), ph, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
             stop = true;
             return;
+          }
+          if (first_stage) {
+            trace_at(p, 3);
+            first_stage = false;
           }
           const uint32_t a_lo = a_lo0 + s * (Cfg::A_BYTES >> 4);
           const uint32_t b_lo = b_lo0 + s * (Cfg::B_BYTES >> 4);
@@ -331,12 +338,15 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
                             STATUS_TIMEOUT, tmo))
             break;
           tc_fence_after();
+          if (i < 11) trace_at(p, 10 + 2 * i);
           k_loop(w.kb0, w.kb1, buf);
           if (stop) break;
           mma_commit_pair_both(acc_full(buf));
+          if (i < 11) trace_at(p, 11 + 2 * i);
           ++acc_it;
         }
       }
+      trace_at(p, 4);
       mma_commit_pair_both(done_bar);
       drain_wait(done_bar, 0, 200000000ull);
     }
@@ -483,18 +493,33 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
         bulk_wait_all();
       }
     } else {
+    // C by TMA (p.c_tma): each warp loads its 32 rows x 64 columns of C per
+    // chunk into the staging buffer that the chunk's D then leaves from, D
+    // written over C in place.  Chunks 0 and 1 of a tile are requested
+    // before the accumulator wait (under the tile's MMAs), chunk j + 2 once
+    // chunk j's store has read the buffer.  Register-held C waited on DRAM
+    // once every two 32-column slices: about 7 of a 256-wide tile's 7.5 us.
+    const int ew = warp - 2;  // this epilogue warp's C barriers
+    // bit b of ctw: parity of the next wait on buffer b; byte b of ctn: loads
+    // into buffer b not waited for yet
+    uint32_t ctw = 0u, ctn = 0u;
+    auto load_ct = [&](int b, int x, int y) {  // lane 0: one 32 x 64 box into buffer b
+      mbar_arrive_expect_tx(cbar(ew, b), 32 * 128);
+      tma_load_2d(smem_u32(sD + b * D_STAGE_BYTES + q * 32 * 128), &tmC, x, y, cbar(ew, b));
+    };
     for (int i = 0; i < pw.n; ++i) {
       const Unit w = pair_unit(p, pw, KSUB, cid, ncl, i, BN);
       const int r = w.m0 + BM * static_cast<int>(rank) + row_local;
       const bool leaves_partial = w.tail && w.part == 1;
       const bool staged_store = p.d_tma && !leaves_partial && p.splits == 1;
+      const bool use_ctma = p.c_tma && staged_store;
       const int y0w = w.m0 + BM * static_cast<int>(rank) + 32 * q;  // the warp's first row
       // C of a slice comes as four 16-byte loads of this thread's row, issued
       // one slice ahead (the first one before the accumulator wait); in a
       // tile that crosses N the groups past N are masked (ld_c8), and a row
       // past M reads nothing and adds zeros.
-      const bool c_rows = !leaves_partial && p.C != nullptr && p.c_vec && p.c_type != T_F32 &&
-                          r < p.M;
+      const bool c_rows = !use_ctma && !leaves_partial && p.C != nullptr && p.c_vec &&
+                          p.c_type != T_F32 && r < p.M;
       const int c_ncols = min(BN, p.N - w.n0);
       const uint16_t* crow =
           c_rows ? static_cast<const uint16_t*>(p.C) + r * p.c_rs + w.n0 : nullptr;
@@ -548,6 +573,14 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
           tmem_st_wait();
         }
       }
+      if (use_ctma) {
+        const uint32_t s0 = staged;  // chunk j of this tile uses buffer (s0 + j) & 1
+        if (lane == 0) {
+          bulk_wait_read_all();  // the previous tile's stores have read the buffers
+          for (int j = 0; j < 2 && j < BN / 64; ++j) load_ct((s0 + j) & 1u, w.n0 + 64 * j, y0w);
+        }
+        for (int j = 0; j < 2 && j < BN / 64; ++j) ctn += 1u << (8u * ((s0 + j) & 1u));
+      }
       uint4 cb0[4], cb1[4];
       if (c_rows) {
 #pragma unroll
@@ -568,9 +601,11 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 8; ++j) pb1[j] = pbase[(8 + j) * BM];
       }
-      if (ep_leader)
+      if (ep_leader) {
         *ep_go = bounded_wait(acc_full(buf), (acc_it >> 1) & 1u, abort_flag, p.status,
                               STATUS_TIMEOUT, tmo) ? 1 : 0;
+        trace_at(p, 5);
+      }
       named_barrier_sync(1, 128);
       const bool go = *ep_go != 0;
       named_barrier_sync(1, 128);
@@ -593,7 +628,13 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
         // Each warp stages its own 32 rows and stores them itself, so the
         // chunk loop needs no barrier across warps.
         uint8_t* stage = sD + (staged & 1u) * D_STAGE_BYTES;
-        if (staged_store && h == 0 && staged >= 2) {
+        if (use_ctma && h == 0) {
+          // this chunk's C has landed in its buffer
+          const uint32_t b = staged & 1u;
+          bounded_wait(cbar(ew, b), (ctw >> b) & 1u, abort_flag, p.status, STATUS_TIMEOUT, tmo);
+          ctw ^= 1u << b;
+          ctn -= 1u << (8u * b);
+        } else if (staged_store && h == 0 && staged >= 2) {
           // the store this warp issued from this buffer two chunks ago must have read it
           if (lane == 0) bulk_wait_read_le1();
           __syncwarp();
@@ -654,7 +695,12 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
         } else if (CT != 0) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint32_t cw[4] = {cbuf[k].x, cbuf[k].y, cbuf[k].z, cbuf[k].w};
+            // C from the staging buffer (the unit D takes below), else from registers
+            const uint4 cv = use_ctma ? *reinterpret_cast<const uint4*>(
+                                            stage + row_local * 128 +
+                                            (((h * 4 + k) ^ (row_local & 7)) * 16))
+                                      : cbuf[k];
+            const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               float lo, hi;
@@ -663,7 +709,7 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
               f[8 * k + 2 * e + 1] += hi;
             }
           }
-          reload_c(c, cbuf);
+          if (!use_ctma) reload_c(c, cbuf);
         }
         // 16 bytes = 8 outputs per swizzle unit; the unit's position in the
         // 128-byte row is XORed with row % 8 (the TMA's 128B swizzle), which
@@ -698,6 +744,15 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
             st_d_chunk_rows(stage + q * 32 * 128, static_cast<uint16_t*>(p.D), p.d_rs, y0w, x0,
                             p.M, p.N, lane);
             __syncwarp();  // read out before the buffer takes a later chunk
+          }
+          const int j = (c - 1) >> 1;  // this chunk
+          if (use_ctma && j + 2 < BN / 64) {
+            // chunk j + 2's C into this buffer once the store has read it
+            if (lane == 0) {
+              bulk_wait_read_all();
+              load_ct(staged & 1u, w.n0 + 64 * (j + 2), y0w);
+            }
+            ctn += 1u << (8u * (staged & 1u));
           }
           ++staged;
         }
@@ -747,13 +802,20 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
       }
       ++acc_it;
     }
-    // Shared memory must outlive the stores that read it.
-    if (lane == 0) bulk_wait_all();
+    // Shared memory must outlive the stores that read it and the C loads
+    // still in flight (after a timeout) must land.
+    if (lane == 0) {
+      for (uint32_t b = 0; b < 2; ++b)
+        if ((ctn >> (8u * b)) & 0xFFu) drain_wait(cbar(ew, b), (ctw >> b) & 1u, 200000000ull);
+      bulk_wait_all();
+    }
     }
   }
 
+  if (threadIdx.x == 64) trace_at(p, 6);
   tc_fence_before();
   cluster_sync_all();
+  if (threadIdx.x == 64) trace_at(p, 7);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);

@@ -79,11 +79,28 @@ def main(argv=None) -> int:
     t = buf.view(grid, pkg.GEMM_TRACE_EVENTS).cpu().double()
     t0 = t[:, 0].min()
     rel = ((t - t0) / 1e3).tolist()  # us
+    units = []  # pair kernel: MMA busy spans per unit of each cluster (even CTAs)
+    if "pair=1" in plan:
+        for c in range(0, grid, 2):
+            row = rel[c]
+            spans = [(row[10 + 2 * i], row[11 + 2 * i]) for i in range(11)
+                     if t[c, 10 + 2 * i] > 0 and t[c, 11 + 2 * i] > 0]
+            units.append(spans)
     out = {"workload": w.name, "plan": plan, "ctas": grid,
            "span_us": round((t[:, 7].max() - t0).item() / 1e3, 3),
            "events_us": {name: stats([r[e] for r in rel]) for e, name in enumerate(EVENTS)},
            "intervals_us": {name: stats([r[j] - r[i] for r in rel])
                             for name, i, j in INTERVALS}}
+    if units:
+        first = [u[0][0] for u in units if u]
+        last = [u[-1][1] for u in units if u]
+        gaps = [u[i + 1][0] - u[i][1] for u in units for i in range(len(u) - 1)]
+        busy = [sum(b - a for a, b in u) for u in units if u]
+        out["mma_units"] = {"per_cluster": stats([len(u) for u in units]),
+                            "first_start": stats(first), "last_commit": stats(last),
+                            "gap_between_units": stats(gaps) if gaps else None,
+                            "issue_span": stats([b - a for a, b in zip(first, last)]),
+                            "unit_time": stats([b - a for u in units for a, b in u])}
     if a.raw:
         out["ctas_us"] = [[round(x, 3) for x in r] for r in rel]
     g.close()

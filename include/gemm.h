@@ -361,7 +361,7 @@ GEMM_API int gemm_debug_set(gemm_handle_t h, int flags, uint64_t timeout_ns);
  * Timeline hook (profiling and tests; not for production use): with a
  * non-null dev_buf (device memory of at least grid x GEMM_TRACE_EVENTS
  * uint64 values, owned by the caller), every later gemm_run whose plan runs
- * the single-CTA tensor-core kernel writes, per CTA c, global-timer stamps
+ * a tcgen05 kernel (single CTA or CTA pair) writes, per CTA c, global-timer stamps
  * (ns) at dev_buf[c * GEMM_TRACE_EVENTS + e] for the events e: 0 kernel
  * entry, 1 past the wait for the previous kernel in the stream, 2 first
  * operand loads issued, 3 first ring stage landed, 4 last accumulator
@@ -369,13 +369,15 @@ GEMM_API int gemm_debug_set(gemm_handle_t h, int flags, uint64_t timeout_ns);
  * last tile stored, 7 past the final block barrier (0-2 stamped by thread
  * 0, 3-4 by the MMA thread, 5-7 by the first epilogue thread); with the
  * splits of a tile reduced within a cluster, 8 the other splits' sums
- * landed (split-0 CTA) and 9 the CTA's own sums sent (other splits).
+ * landed (split-0 CTA) and 9 the CTA's own sums sent (other splits).  In
+ * the CTA-pair kernel the even CTA of each cluster also stamps 10 + 2i and
+ * 11 + 2i when its MMA thread starts and commits its unit i (i < 11).
  * Stamps of CTAs without work, and events that do not apply, are not
  * defined.
  * A null dev_buf turns the hook off.  The grid is the "grid=" field of the
  * plan string.
  */
-#define GEMM_TRACE_EVENTS 10
+#define GEMM_TRACE_EVENTS 32
 GEMM_API int gemm_trace_set(gemm_handle_t h, uint64_t* dev_buf);
 
 #ifdef __cplusplus

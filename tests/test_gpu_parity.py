@@ -837,7 +837,7 @@ def test_timeline_hook_stamps_in_order():
     assert pkg.gemm_trace_set(g.handle, buf.data_ptr()) == pkg.GEMM_OK
     g.run(A, B, C, D)
     assert g.status() == pkg.GEMM_OK
-    t = buf.view(grid, pkg.GEMM_TRACE_EVENTS).cpu()[:, :8]  # 8, 9: cluster split-K only
+    t = buf.view(grid, pkg.GEMM_TRACE_EVENTS).cpu()[:, :8]  # 8 on: split-K and pair kernel only
     assert (t > 0).all()
     # each thread's own stamps are in order (0-2 thread 0, 3-4 the MMA
     # thread, 5-7 the first epilogue thread)
