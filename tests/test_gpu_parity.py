@@ -821,6 +821,32 @@ def test_cluster_split_k(case):
     _assert_ok(check_rows(w, inp, D), f"csk {case} [{p}]")
 
 
+# Pair kernel epilogue with C by TMA into the staging buffers: several units
+# per cluster (few clusters forced by grid=), stream-K pieces, N off the
+# 16-byte grid, no C, and a C of another type (the register path).
+PAIR_EPI_CASES = [
+    (1000, 1000, 1000, BF16, BF16, "pair=1,bn=256,grid=4"),
+    (1000, 1003, 1000, BF16, BF16, "pair=1,bn=256,grid=6,tail=1"),
+    (777, 1030, 520, F16, F16, "pair=1,bn=256,grid=6,tail=1"),
+    (1000, 1000, 1000, None, BF16, "pair=1,bn=256,grid=4"),
+    (1000, 1000, 1000, F32, BF16, "pair=1,bn=256,grid=4"),
+    (1024, 768, 2048, BF16, BF16, "pair=1,bn=128,grid=4,tail=1"),
+    (1024, 768, 2048, BF16, BF16, "pair=1,bn=256,grid=4,ksub=2"),
+]
+
+
+@pytest.mark.parametrize("case", PAIR_EPI_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}-{c[5]}"
+                                                      for c in PAIR_EPI_CASES])
+def test_pair_epilogue_c_by_tma(case):
+    M, N, K, ct, dt, plan = case
+    ab = F16 if dt == F16 else BF16
+    w = Workload("pepi", 69, M, N, K, ab, ct, dt, "normal")
+    inp = make_inputs(w)
+    D, p = run_gpu(w, inp, plan=plan)
+    assert "pair=1" in p, p
+    _assert_ok(check_rows(w, inp, D), f"{case} [{p}]")
+
+
 def test_timeline_hook_stamps_in_order():
     """gemm_trace_set: every CTA of the single-CTA kernel stamps its events in
     causal order; with the hook off the buffer is left alone."""
