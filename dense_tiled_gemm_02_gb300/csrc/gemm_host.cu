@@ -761,6 +761,7 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     if (!h->pair) c.pair = 0;
   }
   c.ksub = h->pair ? h->pair->ksub : 1;
+  if (!c.pair && c.bn == 224) c.bn = 256;  // 224-wide tiles exist for the pair kernel only
   // In-kernel loads of 16-bit operand rows that are off the 16-byte grid
   // (instead of workspace copies): single-CTA kernel, 128- or 256-wide tiles.
   const bool lsu_ok = c.lsu && !c.pair && is_f16ish(d.ab_type) && (c.bn == 128 || c.bn == 256);

@@ -58,6 +58,12 @@ static const PlanRow kTable[] = {
     // 1605, without 1579; 2 K slices per stage 1495; GROUP_M 4 / 16 within
     // 1 % of 8.
     {4096, 4096, 4096, T_BF16, 0, 1, {256, 8, 1, 0, 0, 1, 1, 1}},
+    // 4096^3 E4M3 (A row, B column-major): pair 256x224, whose 16 x 19 tiles
+    // are exactly four waves of the 76 pairs (no stream-K pieces): 2507
+    // TFLOPS against 2432 for 256x256 with the stream-K hybrid (cuBLAS
+    // 2442).  At bf16 the 224-wide tile measured slower (1514 against 1593):
+    // a 224-column MMA took as long as a 256-column one there.
+    {4096, 4096, 4096, T_E4M3, 0, 1, {224, 8, 1, 0, 0, 1, 1, 1}},
     // 8192^3 bf16, B column-major: pair 256x256 with stream-K 1940, without
     // 1913; pair 256x128 1099 (1453 with 2 K slices per stage); single-CTA
     // 128x256 1486.

@@ -48,7 +48,8 @@ struct PairCfg {
   // int32 sums of half the tile's columns in registers.
   static constexpr int EPI_WARPS = I8X ? 8 : 4;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static_assert(BN == 128 || BN == 256, "pair tile width");
+  // 224: 16 x 19 tiles at 4096^2 are exactly four waves of 76 pairs
+  static_assert(BN == 128 || BN == 224 || BN == 256, "pair tile width");
   static_assert(!I8X || BN == 256, "the int8 pair variant uses 256-wide tiles");
   static_assert(B_ATOM % 1024 == 0, "stage alignment");
 };
@@ -500,6 +501,8 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
     // chunk j's store has read the buffer.  Register-held C waited on DRAM
     // once every two 32-column slices: about 7 of a 256-wide tile's 7.5 us.
     const int ew = warp - 2;  // this epilogue warp's C barriers
+    // 64-column chunks of a tile (a 224-wide tile ends in a 32-column one)
+    constexpr int NCHUNK = (BN + 63) / 64;
     // bit b of ctw: parity of the next wait on buffer b; byte b of ctn: loads
     // into buffer b not waited for yet
     uint32_t ctw = 0u, ctn = 0u;
@@ -554,21 +557,24 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
         if (!fok) break;
         if (preloaded) {
           // two 32-column slices per batch: 16 loads in flight per thread
+          // (a 224-wide tile ends in one single slice)
 #pragma unroll 1
           for (int c = 0; c < BN / 32; c += 2) {
+            const int nh = c + 1 < BN / 32 ? 2 : 1;
             uint32_t x[2][32];
 #pragma unroll
             for (int h = 0; h < 2; ++h)
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                const float4 q = pbase[((c + h) * 8 + j) * BM];
+                const float4 q = h < nh ? pbase[((c + h) * 8 + j) * BM]
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
                 x[h][4 * j] = __float_as_uint(q.x);
                 x[h][4 * j + 1] = __float_as_uint(q.y);
                 x[h][4 * j + 2] = __float_as_uint(q.z);
                 x[h][4 * j + 3] = __float_as_uint(q.w);
               }
             tmem_st_32x32b_x32(pcol + c * 32, x[0]);
-            tmem_st_32x32b_x32(pcol + (c + 1) * 32, x[1]);
+            if (nh == 2) tmem_st_32x32b_x32(pcol + (c + 1) * 32, x[1]);
           }
           tmem_st_wait();
         }
@@ -577,9 +583,9 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
         const uint32_t s0 = staged;  // chunk j of this tile uses buffer (s0 + j) & 1
         if (lane == 0) {
           bulk_wait_read_all();  // the previous tile's stores have read the buffers
-          for (int j = 0; j < 2 && j < BN / 64; ++j) load_ct((s0 + j) & 1u, w.n0 + 64 * j, y0w);
+          for (int j = 0; j < 2 && j < NCHUNK; ++j) load_ct((s0 + j) & 1u, w.n0 + 64 * j, y0w);
         }
-        for (int j = 0; j < 2 && j < BN / 64; ++j) ctn += 1u << (8u * ((s0 + j) & 1u));
+        for (int j = 0; j < 2 && j < NCHUNK; ++j) ctn += 1u << (8u * ((s0 + j) & 1u));
       }
       uint4 cb0[4], cb1[4];
       if (c_rows) {
@@ -731,22 +737,27 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
           const int unit = (h * 4 + k) ^ (row_local & 7);
           *reinterpret_cast<uint4*>(stage + row_local * 128 + unit * 16) = x;
         }
-        if (h == 1) {
-          const int x0 = w.n0 + 32 * (c - 1);
-          if (x0 + 64 <= p.N || (p.N & 7) == 0) {
+        // a chunk is stored after its second slice, or after its only one
+        // (the 32-column chunk that ends a 224-wide tile)
+        const bool half = (BN % 64) != 0 && c == BN / 32 - 1;
+        if (h == 1 || half) {
+          const int x0 = w.n0 + 32 * (c - h);
+          if (!half && (x0 + 64 <= p.N || (p.N & 7) == 0)) {
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0 && x0 < p.N && y0w < p.M)  // boxes entirely outside D are skipped
               tma_store_2d(&tmD, smem_u32(stage + q * 32 * 128), x0, y0w);
             if (lane == 0) bulk_commit();
           } else {
+            // by rows: the chunk that crosses an N off the 16-byte grid, or
+            // the half chunk (a 64-column box would reach into the next tile)
             __syncwarp();
             st_d_chunk_rows(stage + q * 32 * 128, static_cast<uint16_t*>(p.D), p.d_rs, y0w, x0,
-                            p.M, p.N, lane);
+                            p.M, half ? min(p.N, x0 + 32) : p.N, lane);
             __syncwarp();  // read out before the buffer takes a later chunk
           }
-          const int j = (c - 1) >> 1;  // this chunk
-          if (use_ctma && j + 2 < BN / 64) {
+          const int j = c >> 1;  // this chunk
+          if (use_ctma && j + 2 < NCHUNK) {
             // chunk j + 2's C into this buffer once the store has read it
             if (lane == 0) {
               bulk_wait_read_all();
@@ -771,23 +782,23 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
         switch (kind) {
           case 1:
             slice(c, cb0, pb0, IntTag<T_BF16>{}, IntTag<T_BF16>{});
-            slice(c + 1, cb1, pb1, IntTag<T_BF16>{}, IntTag<T_BF16>{});
+            if (c + 1 < BN / 32) slice(c + 1, cb1, pb1, IntTag<T_BF16>{}, IntTag<T_BF16>{});
             break;
           case 2:
             slice(c, cb0, pb0, IntTag<0>{}, IntTag<T_BF16>{});
-            slice(c + 1, cb1, pb1, IntTag<0>{}, IntTag<T_BF16>{});
+            if (c + 1 < BN / 32) slice(c + 1, cb1, pb1, IntTag<0>{}, IntTag<T_BF16>{});
             break;
           case 3:
             slice(c, cb0, pb0, IntTag<T_F16>{}, IntTag<T_F16>{});
-            slice(c + 1, cb1, pb1, IntTag<T_F16>{}, IntTag<T_F16>{});
+            if (c + 1 < BN / 32) slice(c + 1, cb1, pb1, IntTag<T_F16>{}, IntTag<T_F16>{});
             break;
           case 4:
             slice(c, cb0, pb0, IntTag<0>{}, IntTag<T_F16>{});
-            slice(c + 1, cb1, pb1, IntTag<0>{}, IntTag<T_F16>{});
+            if (c + 1 < BN / 32) slice(c + 1, cb1, pb1, IntTag<0>{}, IntTag<T_F16>{});
             break;
           default:
             slice(c, cb0, pb0, IntTag<-1>{}, IntTag<-1>{});
-            slice(c + 1, cb1, pb1, IntTag<-1>{}, IntTag<-1>{});
+            if (c + 1 < BN / 32) slice(c + 1, cb1, pb1, IntTag<-1>{}, IntTag<-1>{});
             break;
         }
       }

@@ -62,8 +62,8 @@ int max_clusters_pair() {
               &max_clusters_pair<BN_, ST_, KS_, I8_>}
 
 const PairVariant kPairVariants[] = {GB_PAIR(256, 6, 1, false), GB_PAIR(256, 3, 2, false),
-                                     GB_PAIR(128, 8, 1, false), GB_PAIR(128, 4, 2, false),
-                                     GB_PAIR(256, 5, 1, true)};
-const int kNumPairVariants = 5;
+                                     GB_PAIR(224, 6, 1, false), GB_PAIR(128, 8, 1, false),
+                                     GB_PAIR(128, 4, 2, false), GB_PAIR(256, 5, 1, true)};
+const int kNumPairVariants = 6;
 
 }  // namespace gb300

@@ -383,6 +383,7 @@ TABLE_ROWS = {
     "sq4096_bf16": "pair=1 bn=256 ksub=1",
     "sq8192_bf16": "pair=1 bn=256 ksub=1",
     "sq8192_i8": "pair=1 bn=256 ksub=1",
+    "sq4096_e4m3": "pair=1 bn=224 ksub=1",
     "skinny64x8192x8192_bf16": "swap=0 pair=0 bn=128 ksub=1 stages=5",
     "skinny8192x128x4096_bf16": "swap=0 pair=0 bn=128 ksub=1 stages=5",
     "rag1000_bf16": "swap=0 pair=0 bn=64",
@@ -422,6 +423,8 @@ FULL = [("sq4096_bf16", None), ("sq4096_bf16", "pair=1,bn=256,tail=0"), ("sq4096
         ("skinny8192x128x4096_bf16", "pair=0,bn=64,sk=1"),
         ("skinny8192x128x4096_bf16", "pair=0,bn=64,kgroup=4"),
         ("skinny8192x128x4096_bf16", "pair=0,bn=64,splits=1"),
+        ("sq4096_bf16", "pair=1,bn=224"), ("sq4096_bf16", "pair=1,bn=224,tail=1"),
+        ("rag4095x4097x4099_bf16", "pair=1,bn=224"), ("sq4096_e4m3", "pair=1,bn=224"),
         ("skinny64x8192x8192_bf16", "pair=0,bn=128,splits=2,csk=0"),
         ("skinny64x8192x8192_bf16", "pair=0,bn=128,splits=2,kgroup=2"),
         ("rag4095x4097x4099_bf16", "pair=0,bn=256,lsu=1"),
@@ -832,6 +835,14 @@ PAIR_EPI_CASES = [
     (1000, 1000, 1000, F32, BF16, "pair=1,bn=256,grid=4"),
     (1024, 768, 2048, BF16, BF16, "pair=1,bn=128,grid=4,tail=1"),
     (1024, 768, 2048, BF16, BF16, "pair=1,bn=256,grid=4,ksub=2"),
+    # 224-wide tiles (B K-major: 112 rows per CTA): seven 32-column slices,
+    # the last 64-column chunk half
+    (1000, 1000, 1000, BF16, BF16, "pair=1,bn=224,grid=4,lb=col"),
+    (1000, 1003, 1000, BF16, BF16, "pair=1,bn=224,grid=6,tail=1,lb=col"),
+    (777, 1030, 520, F16, F16, "pair=1,bn=224,grid=6,tail=1,lb=col"),
+    (1000, 1000, 1000, None, BF16, "pair=1,bn=224,grid=4,lb=col"),
+    (1000, 1000, 1000, F32, F32, "pair=1,bn=224,grid=4,lb=col"),
+    (512, 448, 512, BF16, BF16, "pair=1,bn=224,lb=col"),
 ]
 
 
@@ -840,10 +851,12 @@ PAIR_EPI_CASES = [
 def test_pair_epilogue_c_by_tma(case):
     M, N, K, ct, dt, plan = case
     ab = F16 if dt == F16 else BF16
-    w = Workload("pepi", 69, M, N, K, ab, ct, dt, "normal")
+    lb = COL if plan.endswith(",lb=col") else ROW  # (lb= is the test's, not a plan key)
+    plan = plan.replace(",lb=col", "")
+    w = Workload("pepi", 69, M, N, K, ab, ct, dt, "normal", ROW, lb)
     inp = make_inputs(w)
     D, p = run_gpu(w, inp, plan=plan)
-    assert "pair=1" in p, p
+    assert "pair=1" in p and ("bn=224" in p) == ("bn=224" in plan), p
     _assert_ok(check_rows(w, inp, D), f"{case} [{p}]")
 
 
