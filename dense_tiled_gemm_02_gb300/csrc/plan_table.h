@@ -83,6 +83,19 @@ static const PlanRow kTable[] = {
     // unsplit on the same box (the K loops of the 128 CTAs stream A at
     // 5.3 TB/s; 128x64 tiles read each A row twice).
     {8192, 128, 4096, T_BF16, 0, 0, {128, 8, 2, 0, 0, 0, 1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 1}},
+    // Decode shapes the CUDA-core decode kernel does not take (16 rows, or
+    // an N-contiguous B): the long N on the tensor-core M side (swap),
+    // 128x64 tiles, K split 4 ways and reduced by the reduce kernel.
+    // 16x4096x4096, B K-contiguous: 16.3-16.9 us; the same splits reduced
+    // within a cluster 24.9 (the split-0 CTA's strided epilogue), 2 splits
+    // 21.9, unswapped 20.0-30.1, the mma.sync decode form 23.1, cuBLAS 29-31.
+    {16, 4096, 4096, T_BF16, 0, 1, {64, 8, 4, 1, 0, 0, 1, 0}},
+    // 16x4096x4096, B N-contiguous: 16.3-16.8 us; cluster split 25.2, 2
+    // splits 22.9, unswapped 20.0-31.9, the mma.sync form 46.7, cuBLAS 28.
+    {16, 4096, 4096, T_BF16, 0, 0, {64, 8, 4, 1, 0, 0, 1, 0}},
+    // 1x4096x4096, B N-contiguous: 15.6-16.2 us; cluster split 24.8, the
+    // mma.sync form 20.7, cuBLAS 31.9.
+    {1, 4096, 4096, T_BF16, 0, 0, {64, 8, 4, 1, 0, 0, 1, 0}},
     // (1000, 1000, 1000) bf16: 128x64: 130; 128x128: 104; pair: 105 / 84.
     {1000, 1000, 1000, T_BF16, 0, 0, {64, 8, 1, 0, 0, 0, 1, 0}},
     // 1024^3 fp16: 128x64: 202; 128x128: 174; pair 256x128: 168.

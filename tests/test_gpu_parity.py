@@ -387,6 +387,9 @@ TABLE_ROWS = {
     "skinny64x8192x8192_bf16": "swap=0 pair=0 bn=128 ksub=1 stages=5",
     "skinny8192x128x4096_bf16": "swap=0 pair=0 bn=128 ksub=1 stages=5",
     "rag1000_bf16": "swap=0 pair=0 bn=64",
+    "decode16x4096x4096_bf16": "swap=1 pair=0 bn=64",
+    "decode16x4096x4096_bf16_brow": "swap=1 pair=0 bn=64",
+    "decode1x4096x4096_bf16_brow": "swap=1 pair=0 bn=64",
     "sq1024_f16": "swap=0 pair=0 bn=64",
 }
 
@@ -405,9 +408,11 @@ def test_plan_table_rows_engage(name):
     plan = g.plan()
     g.close()
     assert TABLE_ROWS[name] in plan, plan
-    want_splits = {"skinny64x8192x8192_bf16": 2, "skinny8192x128x4096_bf16": 2}.get(name, 1)
+    want_splits = {"skinny64x8192x8192_bf16": 2, "skinny8192x128x4096_bf16": 2,
+                   "decode16x4096x4096_bf16": 4, "decode16x4096x4096_bf16_brow": 4,
+                   "decode1x4096x4096_bf16_brow": 4}.get(name, 1)
     assert f" splits={want_splits} " in plan, plan
-    if want_splits > 1:
+    if name.startswith("skinny"):
         assert f"csk={want_splits}" in plan, plan
 
 
