@@ -499,23 +499,62 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
   const CtaWork cw = cta_work(p, blockIdx.x, gridDim.x, !I8X);
   Unit w_first{};
   if (threadIdx.x == 0 && cw.n > 0) w_first = cta_unit(p, cw, blockIdx.x, gridDim.x, 0, BM, BN, !I8X);
+  // The TMA loads of one ring stage: K slice kb of unit w into slot s.
+  auto issue_stage = [&](const Unit& w, const int kb, const uint32_t s) {
+    const uint32_t tx = (a_tma ? Cfg::A_BYTES : 0u) + (b_tma ? Cfg::B_BYTES : 0u);
+    if (tx > 0)
+      mbar_arrive_expect_tx(full(s), tx);
+    else
+      mbar_arrive(full(s));
+    const uint32_t a_dst = smem_u32(sA + s * Cfg::A_BYTES);
+    const uint32_t b_dst = smem_u32(sB + s * Cfg::B_BYTES);
+    const int k0 = kb * (p.f8 ? 2 * BK : BK);  // a 128-byte row: 64 or 128 K
+    if (!a_tma) {
+    } else if (!p.a_mn) {
+      tma_load_2d(a_dst, &tmA, k0, w.m0, full(s));
+    } else {
+#pragma unroll
+      for (int j = 0; j < BM / 64; ++j)
+        tma_load_2d(a_dst + j * 8192u, &tmA, w.m0 + 64 * j, k0, full(s));
+    }
+    if (!b_tma) {
+    } else if (!p.b_mn) {
+      tma_load_2d(b_dst, &tmB, k0, w.n0, full(s));
+    } else {
+#pragma unroll
+      for (int j = 0; j < BN / 64; ++j)
+        tma_load_2d(b_dst + j * 8192u, &tmB, w.n0 + 64 * j, k0, full(s));
+    }
+  };
+  // The first stage goes out right after the wait below, before the load
+  // loop's code is first fetched (plain plans: no producer warps, K slices
+  // issued one by one, no test hook); the loop then starts at the second.
+  const bool early = PW == 0 && p.kgroup <= 1 && !(p.debug_flags & DBG_SKIP_FIRST_FILL) &&
+                     cw.n > 0 && w_first.kb0 < w_first.kb1;
   // Everything above touches only on-chip state: it overlaps the previous
   // kernel in the stream; global memory is read and written only after it.
   pdl_wait();
   pdl_trigger();
-  if (threadIdx.x == 0) trace_at(p, 1);
+  if (threadIdx.x == 0) {
+    trace_at(p, 1);
+    if (early) {
+      issue_stage(w_first, w_first.kb0, 0u);
+      trace_at(p, 2);
+    }
+  }
 
   const uint64_t tmo = p.timeout_ns;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      uint32_t it = 0, s = 0, ph = 0;  // it: slices issued; (s, ph): ring slot and phase
+      // it: slices issued; (s, ph): ring slot and phase (STAGES >= 2)
+      uint32_t it = early ? 1u : 0u, s = early ? 1u : 0u, ph = 0;
       int64_t skipped = -1;
       bool stop = false;
       for (int i = 0; i < cw.n && !stop; ++i) {
         const Unit w = i == 0 ? w_first : cta_unit(p, cw, blockIdx.x, gridDim.x, i, BM, BN, !I8X);
-        for (int kb = w.kb0; kb < w.kb1 && !stop; ++kb) {
+        for (int kb = (i == 0 && early) ? w.kb0 + 1 : w.kb0; kb < w.kb1 && !stop; ++kb) {
           // Slices are issued in groups of kgroup consecutive K slices once
           // that many stages are free, so that each row of a K-major operand
           // is requested as one run of kgroup * 128 bytes rather than as
@@ -550,30 +589,7 @@ __global__ void __launch_bounds__(NUM_THREADS + 32 * PW, 1)
             }
             continue;
           }
-          const uint32_t tx = (a_tma ? Cfg::A_BYTES : 0u) + (b_tma ? Cfg::B_BYTES : 0u);
-          if (tx > 0)
-            mbar_arrive_expect_tx(full(s), tx);
-          else
-            mbar_arrive(full(s));
-          const uint32_t a_dst = smem_u32(sA + s * Cfg::A_BYTES);
-          const uint32_t b_dst = smem_u32(sB + s * Cfg::B_BYTES);
-          const int k0 = kb * (p.f8 ? 2 * BK : BK);  // a 128-byte row: 64 or 128 K
-          if (!a_tma) {
-          } else if (!p.a_mn) {
-            tma_load_2d(a_dst, &tmA, k0, w.m0, full(s));
-          } else {
-#pragma unroll
-            for (int j = 0; j < BM / 64; ++j)
-              tma_load_2d(a_dst + j * 8192u, &tmA, w.m0 + 64 * j, k0, full(s));
-          }
-          if (!b_tma) {
-          } else if (!p.b_mn) {
-            tma_load_2d(b_dst, &tmB, k0, w.n0, full(s));
-          } else {
-#pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(b_dst + j * 8192u, &tmB, w.n0 + 64 * j, k0, full(s));
-          }
+          issue_stage(w, kb, s);
           if (it == 0) trace_at(p, 2);
           if (PW > 0 && p.mx) {
             // this stage's scale cells (512 bytes of A's for the tile row,

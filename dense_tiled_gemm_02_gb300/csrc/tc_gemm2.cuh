@@ -191,25 +191,64 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
   const PairWork pw = pair_work(p, KSUB, cid, ncl);
   Unit w_first{};
   if (threadIdx.x == 0 && pw.n > 0) w_first = pair_unit(p, pw, KSUB, cid, ncl, 0, BN);
+  // This CTA's TMA loads of one ring stage: K slices kb .. kb+KSUB-1 of unit
+  // w into slot s, counted on the even CTA's barrier (armed by the even CTA
+  // with both CTAs' bytes).
+  auto issue_stage = [&](const Unit& w, const int kb, const uint32_t s) {
+    const int am = w.m0 + BM * static_cast<int>(rank);
+    const int bn0 = w.n0 + Cfg::BNH * static_cast<int>(rank);
+    const uint32_t fb = map_shared_rank(full(s), 0);
+    if (leader) mbar_arrive_expect_tx(full(s), Cfg::PAIR_TX);
+#pragma unroll
+    for (int j = 0; j < KSUB; ++j) {
+      // a K slice past the end still lands (as zeros) and is counted
+      const int k0 = (kb + j) * (p.f8 ? 2 * BK : BK);  // a 128-byte row: 64 or 128 K
+      const uint32_t a_dst = smem_u32(sA + s * Cfg::A_BYTES + j * Cfg::A_ATOM);
+      const uint32_t b_dst = smem_u32(sB + s * Cfg::B_BYTES + j * Cfg::B_ATOM);
+      if (!p.a_mn) {
+        tma_load_2d_pair(a_dst, &tmA, k0, am, fb);
+      } else {
+#pragma unroll
+        for (int i = 0; i < BM / 64; ++i)
+          tma_load_2d_pair(a_dst + i * 8192u, &tmA, am + 64 * i, k0, fb);
+      }
+      if (!p.b_mn) {
+        tma_load_2d_pair(b_dst, &tmB, k0, bn0, fb);
+      } else {
+#pragma unroll
+        for (int i = 0; i < Cfg::BNH / 64; ++i)
+          tma_load_2d_pair(b_dst + i * 8192u, &tmB, bn0 + 64 * i, k0, fb);
+      }
+    }
+  };
+  // The first stage goes out right after the wait below, before the load
+  // loop's code is first fetched; the loop then starts at the second.
+  const bool early = !(p.debug_flags & DBG_SKIP_FIRST_FILL) && pw.n > 0 &&
+                     w_first.kb0 < w_first.kb1;
   // Everything above touches only on-chip state: it overlaps the previous
   // kernel in the stream; global memory is read and written only after it.
   pdl_wait();
   pdl_trigger();
-  if (threadIdx.x == 0) trace_at(p, 1);
+  if (threadIdx.x == 0) {
+    trace_at(p, 1);
+    if (early) {
+      issue_stage(w_first, w_first.kb0, 0u);
+      trace_at(p, 2);
+    }
+  }
 
   const uint64_t tmo = p.timeout_ns;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
-      uint32_t it = 0, s = 0, ph = 0;  // it: stages issued; (s, ph): ring slot and phase
+      // it: stages issued; (s, ph): ring slot and phase (STAGES >= 2)
+      uint32_t it = early ? 1u : 0u, s = early ? 1u : 0u, ph = 0;
       int64_t skipped = -1;
       bool stop = false;
       for (int i = 0; i < pw.n && !stop; ++i) {
         const Unit w = i == 0 ? w_first : pair_unit(p, pw, KSUB, cid, ncl, i, BN);
-        const int am = w.m0 + BM * static_cast<int>(rank);
-        const int bn0 = w.n0 + Cfg::BNH * static_cast<int>(rank);
-        for (int kb = w.kb0; kb < w.kb1; kb += KSUB) {
+        for (int kb = (i == 0 && early) ? w.kb0 + KSUB : w.kb0; kb < w.kb1; kb += KSUB) {
           if (!bounded_wait(empty(s), ph ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, tmo)) {
             stop = true;
             break;
@@ -217,29 +256,7 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
           if (leader && (p.debug_flags & DBG_SKIP_FIRST_FILL) && it == 0) {
             skipped = 0;  // test hook: never arm stage 0, so the MMA wait on it expires
           } else {
-            const uint32_t fb = map_shared_rank(full(s), 0);
-            if (leader) mbar_arrive_expect_tx(full(s), Cfg::PAIR_TX);
-#pragma unroll
-            for (int j = 0; j < KSUB; ++j) {
-              // a K slice past the end still lands (as zeros) and is counted
-              const int k0 = (kb + j) * (p.f8 ? 2 * BK : BK);  // a 128-byte row: 64 or 128 K
-              const uint32_t a_dst = smem_u32(sA + s * Cfg::A_BYTES + j * Cfg::A_ATOM);
-              const uint32_t b_dst = smem_u32(sB + s * Cfg::B_BYTES + j * Cfg::B_ATOM);
-              if (!p.a_mn) {
-                tma_load_2d_pair(a_dst, &tmA, k0, am, fb);
-              } else {
-#pragma unroll
-                for (int i = 0; i < BM / 64; ++i)
-                  tma_load_2d_pair(a_dst + i * 8192u, &tmA, am + 64 * i, k0, fb);
-              }
-              if (!p.b_mn) {
-                tma_load_2d_pair(b_dst, &tmB, k0, bn0, fb);
-              } else {
-#pragma unroll
-                for (int i = 0; i < Cfg::BNH / 64; ++i)
-                  tma_load_2d_pair(b_dst + i * 8192u, &tmB, bn0 + 64 * i, k0, fb);
-              }
-            }
+            issue_stage(w, kb, s);
           }
           if (it == 0) trace_at(p, 2);
           ++it;
