@@ -110,9 +110,11 @@ struct KParams {
   int sk1;
   // Split-K over a cluster (csk = splits > 1, single-CTA kernel, one unit
   // per CTA, cluster of csk consecutive CTAs = the splits of one tile): the
-  // CTAs of splits 1.. store their fp32 sums into the shared memory of the
-  // split-0 CTA (distributed shared memory), which adds them in split order,
-  // adds C and stores D: no partials in global memory, no reduce launch.
+  // tile's 32-column slices are owned round-robin by the cluster's CTAs;
+  // each copies its fp32 sums of the others' slices into their shared
+  // memory (distributed shared memory) and adds the sums it receives for
+  // its own, in split order, then C, and stores them: no partials in global
+  // memory, no reduce launch.
   int csk;
   float* fix_ws;                 // [G][BM * BN] fp32, interleaved (see tc_gemm.cuh)
   uint32_t* fix_flag;            // [G], the epoch of the run that wrote fix_ws[c]

@@ -389,6 +389,17 @@ __device__ __forceinline__ void cluster_sync_all() {
                    "memory");
 }
 
+// The two halves of a cluster barrier, for threads that finish their part
+// early: arrive without ordering (no memory is handed over through this
+// barrier), wait with acquire at the end.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Bulk copy of `bytes` bytes (a multiple of 16, both addresses 16-byte
 // aligned) from this CTA's shared memory into the shared memory of a CTA of
 // this cluster; completion is counted as transaction bytes on a barrier of

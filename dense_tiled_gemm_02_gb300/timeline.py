@@ -20,7 +20,8 @@ import sys
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 EVENTS = ("entry", "past_pdl_wait", "first_loads", "first_stage_landed", "last_acc_committed",
           "last_acc_seen", "last_tile_stored", "past_final_barrier", "splits_landed",
-          "split_sent")
+          "split_sent", "epilogue_all_in", "epilogue_pos0", "epilogue_pos1", "epilogue_pos2",
+          "epilogue_pos3")
 INTERVALS = (("load_latency", 2, 3), ("k_loop", 3, 4), ("handover", 4, 5), ("epilogue", 5, 6),
              ("cta", 0, 7))
 
@@ -88,7 +89,9 @@ def main(argv=None) -> int:
             units.append(spans)
     out = {"workload": w.name, "plan": plan, "ctas": grid,
            "span_us": round((t[:, 7].max() - t0).item() / 1e3, 3),
-           "events_us": {name: stats([r[e] for r in rel]) for e, name in enumerate(EVENTS)},
+           "events_us": {name: stats([r[e] for c, r in enumerate(rel) if t[c, e] > 0])
+                         for e, name in enumerate(EVENTS[:10] if "pair=1" in plan else EVENTS)
+                         if (t[:, e] > 0).any()},
            "intervals_us": {name: stats([r[j] - r[i] for r in rel])
                             for name, i, j in INTERVALS}}
     if units:

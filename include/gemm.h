@@ -368,8 +368,12 @@ GEMM_API int gemm_debug_set(gemm_handle_t h, int flags, uint64_t timeout_ns);
  * committed by the MMA thread, 5 last accumulator seen by the epilogue, 6
  * last tile stored, 7 past the final block barrier (0-2 stamped by thread
  * 0, 3-4 by the MMA thread, 5-7 by the first epilogue thread); with the
- * splits of a tile reduced within a cluster, 8 the other splits' sums
- * landed (split-0 CTA) and 9 the CTA's own sums sent (other splits).  In
+ * splits of a tile reduced within a cluster, 8 the other splits' sums of
+ * the CTA's own column slices landed and 9 its sums of the other CTAs'
+ * slices sent.  The single-CTA kernel also stamps, in its first unit's
+ * epilogue, 10 when every epilogue warp is past the accumulator wait and
+ * 11 + i when the slice at position i < 4 is done (without a K split the
+ * slices go in pairs, both stamped when the pair is done).  In
  * the CTA-pair kernel the even CTA of each cluster also stamps 10 + 2i and
  * 11 + 2i when its MMA thread starts and commits its unit i (i < 11).
  * Stamps of CTAs without work, and events that do not apply, are not

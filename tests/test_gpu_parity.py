@@ -813,6 +813,10 @@ CSK_CASES = [
     (129, 64, 8192, COL, ROW, COL, COL, F16, F16, 64, 4),       # column-major C and D
     (64, 1000, 4096, ROW, COL, ROW, ROW, BF16, BF16, 64, 4),    # swapped (long N on the M side)
     (256, 256, 128, ROW, ROW, ROW, ROW, BF16, BF16, 128, 2),    # one K slice per split
+    # rows below M in one 64-row half of the tile only (one half moves)
+    (64, 512, 2048, ROW, ROW, ROW, ROW, BF16, BF16, 128, 2),
+    (40, 200, 1500, ROW, ROW, ROW, ROW, F16, F16, 64, 3),       # ranks owning 1, 1, 0 slices
+    (170, 320, 2500, ROW, ROW, COL, ROW, BF16, BF16, 64, 4),     # C column-major, 4 ranks
 ]
 
 
@@ -827,6 +831,21 @@ def test_cluster_split_k(case):
     D, p = run_gpu(w, inp, plan=f"pair=0,bn={bn},splits={s},csk=1,decode=0")
     assert f"csk={s}" in p and f"splits={s}" in p, p
     _assert_ok(check_rows(w, inp, D), f"csk {case} [{p}]")
+
+
+@pytest.mark.parametrize("case", CSK_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}-s{c[10]}" for c in CSK_CASES])
+def test_cluster_split_k_matches_reduce_launch(case):
+    """Both split-K forms add the splits' fp32 sums in split order and then
+    C: the cluster exchange gives the same bits as the partials-and-reduce
+    form with the same splits."""
+    M, N, K, la, lb, lc, ld, ct, dt, bn, s = case
+    ab = F16 if ct == F16 else BF16
+    w = Workload("csk", 69, M, N, K, ab, ct, dt, "normal", la, lb, lc, ld)
+    inp = make_inputs(w)
+    D1, p1 = run_gpu(w, inp, plan=f"pair=0,bn={bn},splits={s},csk=1,decode=0")
+    D0, p0 = run_gpu(w, inp, plan=f"pair=0,bn={bn},splits={s},csk=0,decode=0")
+    assert f"csk={s}" in p1 and "csk=0" in p0, (p1, p0)
+    assert torch.equal(D1.view(torch.uint8), D0.view(torch.uint8)), (case, p1)
 
 
 # Pair kernel epilogue with C by TMA into the staging buffers: several units
