@@ -177,8 +177,10 @@ def gemm_trace_set(h: int, dev_buf: int | None) -> int:
 
 
 def gemm_pair_schedule(tiles_m: int, tiles_n: int, group_m: int, num_kb: int, ksub: int,
-                       clusters: int, stream_k: bool, cid: int) -> list[tuple]:
-    """All units of cluster cid: (tile_row, tile_col, kb0, kb1, shared, part, slot)."""
+                       clusters: int, stream_k: int, cid: int) -> list[tuple]:
+    """All units of cluster cid: (tile_row, tile_col, kb0, kb1, shared, part, slot).
+    stream_k: 0 round-robin, 1 equal stream-K runs, 2 the kernel's default
+    (chained runs where they apply)."""
     lib = load()
     n = lib.gemm_pair_schedule(tiles_m, tiles_n, group_m, num_kb, ksub, clusters, int(stream_k),
                                cid, 0, None)

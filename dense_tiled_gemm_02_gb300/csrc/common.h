@@ -94,7 +94,10 @@ struct KParams {
   // it last (the end of its run); the other (at the start of its run)
   // leaves its fp32 partial in tail_ws[c] and raises tail_flags[c] to epoch.
   // sk_len = 0: units are dealt round-robin.
-  int sk_dp, sk_start, sk_len, sk_rem;
+  // sk_n3 >= 0: the runs are laid out in chains instead (plan_stream_k):
+  // sk_n3 chains of three runs over four tiles, then chains of two runs
+  // over three tiles, so that no run holds more than two pieces.
+  int sk_dp, sk_start, sk_len, sk_rem, sk_n3;
   float* tail_ws;                // [leaving cluster][CTA half][128 rows][BN] fp32
   uint32_t* tail_flags;          // [leaving cluster][CTA half]
   uint32_t epoch;                // value the flags take during this run
@@ -171,8 +174,22 @@ struct Unit {
 // least `clusters`), so a tile is shared by at most two clusters.  Leaves
 // the fields zero (round-robin units) when the waves are already full or a
 // run would be shorter than a tile.
-GB_HD void plan_stream_k(int64_t tiles, int clusters, int num_kb, int ksub, KParams& p) {
+//
+// Chains (chains = true): equal runs put both ends of many runs inside
+// tiles with a whole tile between them (three pieces), and such a run's
+// finishing piece waits for a partner's long leaving piece while the whole
+// tile's accumulator waits behind it; those clusters end last.  When the
+// S stream-K tiles over C clusters satisfy 4C/3 <= S <= 3C/2, the runs are
+// laid out instead as n3 = 3C - 2S chains of three runs over four tiles
+// (run ends at 4/3 and 8/3 tiles: [W, F], [L, F], [L, W]) followed by
+// n2 = 3S - 4C chains of two runs over three tiles (ends at 1.5 tiles:
+// [W, F], [L, W]): every run holds at most two pieces, at the price of runs
+// of 4/3 and 3/2 tiles instead of S/C.  At 4096^3 (S = 104, C = 76): 20
+// triples and 8 pairs, runs of 85 - 96 stages instead of 87 - 88.
+GB_HD void plan_stream_k(int64_t tiles, int clusters, int num_kb, int ksub, KParams& p,
+                         bool chains = true) {
   p.sk_dp = p.sk_start = p.sk_len = p.sk_rem = 0;
+  p.sk_n3 = -1;
   if (clusters <= 0 || tiles < clusters || tiles % clusters == 0 || ksub <= 0 ||
       num_kb % ksub != 0 || num_kb / ksub < 2)
     return;
@@ -183,6 +200,9 @@ GB_HD void plan_stream_k(int64_t tiles, int clusters, int num_kb, int ksub, KPar
   p.sk_start = static_cast<int>((waves - 1) * clusters);
   p.sk_len = static_cast<int>(work / clusters);
   p.sk_rem = static_cast<int>(work % clusters);
+  if (chains && num_kb / ksub >= 8 && 3 * sk_tiles >= 4 * static_cast<int64_t>(clusters) &&
+      2 * sk_tiles <= 3 * static_cast<int64_t>(clusters))
+    p.sk_n3 = static_cast<int>(3 * static_cast<int64_t>(clusters) - 2 * sk_tiles);
 }
 
 // Work of one cluster.  Round-robin: units u = cid, cid + ncl, ... of the
@@ -197,8 +217,18 @@ GB_HD PairWork pair_work(const KParams& p, int ksub, int cid, int ncl) {
   PairWork pw;
   if (p.sk_len > 0) {
     const int nks = p.num_kb / ksub;
-    pw.g0 = cid * p.sk_len + (cid < p.sk_rem ? cid : p.sk_rem);
-    pw.g1 = pw.g0 + p.sk_len + (cid < p.sk_rem ? 1 : 0);
+    if (p.sk_n3 >= 0) {
+      // chain of `parts` runs over `span` tiles from tile `base`; this is run r
+      const int t3 = 3 * p.sk_n3;
+      const int base = cid < t3 ? 4 * (cid / 3) : 4 * p.sk_n3 + 3 * ((cid - t3) / 2);
+      const int r = cid < t3 ? cid % 3 : (cid - t3) % 2;
+      const int span = cid < t3 ? 4 : 3, parts = cid < t3 ? 3 : 2;
+      pw.g0 = base * nks + (r * span * nks) / parts;
+      pw.g1 = base * nks + ((r + 1) * span * nks) / parts;
+    } else {
+      pw.g0 = cid * p.sk_len + (cid < p.sk_rem ? cid : p.sk_rem);
+      pw.g1 = pw.g0 + p.sk_len + (cid < p.sk_rem ? 1 : 0);
+    }
     pw.n = p.sk_dp + ((pw.g1 - 1) / nks - pw.g0 / nks + 1);
   } else {
     const int total = p.tiles_m * p.tiles_n * p.splits;

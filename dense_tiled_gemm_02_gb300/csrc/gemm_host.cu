@@ -239,6 +239,7 @@ void apply_force_plan(PlanChoice& c) {
       else if (k == "i8chunk") c.i8chunk = v;
       else if (k == "dmma") c.dmma = v ? 1 : -1;
       else if (k == "csk") c.csk = v;
+      else if (k == "skpat") c.skpat = v ? 0 : -1;
     }
     pos = end + 1;
   }
@@ -250,7 +251,7 @@ void make_plan_string(gemm_plan* h) {
                 "M=%lld N=%lld K=%lld decode=%d dbulk=%d swap=%d pair=%d bn=%d ksub=%d stages=%d "
                 "group_m=%d splits=%d kb_per_split=%d tail=%d grid=%d i8x=%d a_mn=%d b_mn=%d "
                 "repack_a=%d repack_b=%d stage_c=%d stage_d=%d ws_bytes=%zu native_i8=%d "
-                "sk=%d kgroup=%d lsu_a=%d lsu_b=%d mx=%d i8chunk=%d dmma=%d csk=%d",
+                "sk=%d kgroup=%d lsu_a=%d lsu_b=%d mx=%d i8chunk=%d dmma=%d csk=%d skchain=%d",
                 (long long)h->desc.M, (long long)h->desc.N, (long long)h->desc.K, (int)h->decode,
                 (int)h->decode_bulk,
                 h->choice.swap,
@@ -262,7 +263,8 @@ void make_plan_string(gemm_plan* h) {
                 h->grid, (int)h->i8x, h->kp.a_mn, h->kp.b_mn,
                 (int)h->a.repack, (int)h->b.repack, (int)h->c_stage, (int)h->d_stage,
                 h->ws_bytes, (int)h->native_i8, h->kp.sk1, h->kp.kgroup, (int)h->a.lsu,
-                (int)h->b.lsu, (int)h->mx, h->choice.i8chunk, (int)h->decode_mma, h->kp.csk);
+                (int)h->b.lsu, (int)h->mx, h->choice.i8chunk, (int)h->decode_mma, h->kp.csk,
+                h->kp.sk_n3);
   h->plan_str = buf;
 }
 
@@ -578,7 +580,7 @@ int gemm_pair_schedule(int64_t tiles_m, int64_t tiles_n, int64_t group_m, int nu
   p.num_kb = num_kb;
   p.splits = 1;
   p.kb_per_split = num_kb;
-  if (stream_k) plan_stream_k(tiles_m * tiles_n, clusters, num_kb, ksub, p);
+  if (stream_k) plan_stream_k(tiles_m * tiles_n, clusters, num_kb, ksub, p, stream_k == 2);
   const PairWork pw = pair_work(p, ksub, cid, clusters);
   if (!out) return pw.n;
   if (i >= pw.n) return GEMM_ERR_INVALID_ARG;
@@ -880,8 +882,9 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   // tile is shared by at most two clusters.
   const int64_t tiles = (int64_t)kp.tiles_m * kp.tiles_n;
   kp.sk_dp = kp.sk_start = kp.sk_len = kp.sk_rem = 0;
+  kp.sk_n3 = -1;
   if (h->pair && c.tail && !h->i8x && kp.splits == 1)
-    plan_stream_k(tiles, clusters, kp.num_kb, c.ksub, kp);
+    plan_stream_k(tiles, clusters, kp.num_kb, c.ksub, kp, c.skpat >= 0);
   const int64_t sk_slots = kp.sk_len > 0 ? clusters : 0;
   if (h->pair) h->grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(
                                  kp.sk_len > 0 ? clusters : units, clusters));

@@ -41,6 +41,8 @@ struct PlanChoice {
                  // the shape allows, -1 never, 0 the planner decides
   int csk;       // single-CTA kernel with split-K: 1 adds the splits' sums through the
                  // shared memory of a cluster of split CTAs instead of a reduce launch
+  int skpat;     // pair kernel stream-K: -1 keeps equal runs where the chained layout
+                 // would apply (0: chains where they apply)
 };
 
 struct PlanRow {

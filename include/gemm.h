@@ -304,7 +304,9 @@ GEMM_API int gemm_run_host_batch(gemm_handle_t h, int n, const void* const* A,
  * grid of tiles in the grouped order (group_m), num_kb 64-wide K slices,
  * ring stages of ksub slices and `clusters` clusters, with the stream-K
  * hybrid when stream_k != 0 and it applies (a partial last wave, at least
- * one full wave), it returns the number of units of cluster cid; when out
+ * one full wave) -- its runs equal (stream_k = 1), or laid out in chains of
+ * at most two pieces a run where the shape allows (stream_k = 2, what the
+ * kernel runs by default) -- it returns the number of units of cluster cid; when out
  * is non-NULL it also writes unit i of that cluster as out[0..6] = tile
  * row, tile column, first K slice, end K slice, shared-tile flag, part
  * (1 leaves its fp32 partial, 0 adds the partial and finishes the tile) and

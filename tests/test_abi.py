@@ -221,6 +221,56 @@ def test_pair_schedule_covers_every_tile_stage_once(tm, tn, group, nkb, ksub, cl
         assert all(u[4] == 0 for units in sched for u in units)
 
 
+@pytest.mark.parametrize("tm,tn,group,nkb,ksub,clusters", SCHEDULES)
+def test_pair_schedule_chained_runs(tm, tn, group, nkb, ksub, clusters):
+    """The kernel's default stream-K layout: every (tile, K slice) once, a
+    shared tile split between the end of one run (it finishes) and the start
+    of the next (it leaves its partial), every run of at most two pieces
+    where the chained layout applies (4C/3 <= S <= 3C/2 stream-K tiles),
+    with run lengths of 4/3 or 3/2 tiles; otherwise the equal runs."""
+    sched = _schedule(tm, tn, group, nkb, ksub, clusters, 2)
+    seen = set()
+    pieces = {}
+    for cid, units in enumerate(sched):
+        for (r, c, kb0, kb1, shared, part, slot) in units:
+            for k in range(kb0, kb1):
+                assert (r, c, k) not in seen
+                seen.add((r, c, k))
+            pieces.setdefault((r, c), []).append((cid, kb0, kb1, shared, part, slot))
+    assert len(seen) == tm * tn * nkb
+    for tile, ps in pieces.items():
+        if len(ps) == 2:
+            first, second = sorted(ps, key=lambda x: x[1])
+            assert first[1] == 0 and first[3:5] == (1, 0) and second[2] == nkb
+            assert second[3:5] == (1, 1) and first[5] == second[5] == second[0] == first[0] + 1
+        else:
+            assert len(ps) == 1 and ps[0][1:4] == (0, nkb, 0)
+    tiles, nks = tm * tn, nkb // ksub
+    waves = tiles // clusters if tiles >= clusters else 0
+    S = tiles - (waves - 1) * clusters
+    chained = (tiles >= clusters and tiles % clusters and nkb % ksub == 0 and nks >= 8
+               and 3 * S >= 4 * clusters and 2 * S <= 3 * clusters)
+    equal = _schedule(tm, tn, group, nkb, ksub, clusters, 1)
+    if not chained:
+        assert sched == equal
+        return
+    n3 = 3 * clusters - 2 * S
+    for cid, units in enumerate(sched):
+        sk_units = units[waves - 1:]
+        assert all(u[2] == 0 and u[3] == nkb and u[4] == 0 for u in units[:waves - 1])
+        shared = [u for u in sk_units if u[4]]
+        assert len(sk_units) <= 2 and len(shared) <= 2
+        work = sum(u[3] - u[2] for u in sk_units) // ksub
+        want = (4 * nks) / 3 if cid < 3 * n3 else (3 * nks) / 2
+        assert abs(work - want) < 1, (cid, work, want)
+        # the wait (if any) comes first or after the leaving piece, and at most
+        # one unit follows it, as in the equal layout
+        waits = [i for i, u in enumerate(units) if u[4] and u[5] == 0]
+        leaves = [i for i, u in enumerate(units) if u[4] and u[5] == 1]
+        assert all(i == waves - 1 for i in leaves)
+        assert all(i == waves - 1 + len(leaves) for i in waits)
+
+
 # ------------------------------------------------------------------ decode ring
 def test_decode_ring_fits_and_never_lets_a_warp_run_a_phase_ahead():
     """The bulk-copy decode form's ring, over every row count, K (multiples

@@ -884,6 +884,34 @@ def test_pair_epilogue_c_by_tma(case):
     _assert_ok(check_rows(w, inp, D), f"{case} [{p}]")
 
 
+# Pair kernel stream-K with the chained run layout (4C/3 <= S <= 3C/2 of the
+# partial last wave's tiles over C clusters, forced by grid=): pairs of runs
+# only, triples only, both; ragged K; row-major B; C of another type.
+CHAIN_CASES = [
+    (512, 1280, 1024, ROW, BF16, BF16, 8, 0),      # C = 4, S = 6: two pairs
+    (512, 1792, 1000, COL, BF16, BF16, 12, 2),     # C = 6, S = 8: two triples
+    (1024, 1536, 1024, COL, F16, F16, 20, 2),      # C = 10, S = 14: two of each
+    (1024, 1536, 2048, ROW, F32, BF16, 20, 2),
+]
+
+
+@pytest.mark.parametrize("case", CHAIN_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}-g{c[6]}"
+                                                   for c in CHAIN_CASES])
+def test_pair_stream_k_chained_runs(case):
+    """Every element against the oracle with the chained stream-K runs and,
+    forced back (skpat=0), with the equal runs."""
+    M, N, K, lb, ct, dt, grid, n3 = case
+    ab = F16 if dt == F16 or ct == F16 else BF16
+    w = Workload("chain", 70, M, N, K, ab, ct, dt, "normal", ROW, lb)
+    inp = make_inputs(w)
+    D, p = run_gpu(w, inp, plan=f"pair=1,bn=256,tail=1,grid={grid}")
+    assert f"skchain={n3}" in p, p
+    _assert_ok(check_rows(w, inp, D), f"{case} [{p}]")
+    D0, p0 = run_gpu(w, inp, plan=f"pair=1,bn=256,tail=1,grid={grid},skpat=0")
+    assert "skchain=-1" in p0 and "tail=0" not in p0, p0
+    _assert_ok(check_rows(w, inp, D0), f"{case} [{p0}]")
+
+
 def test_timeline_hook_stamps_in_order():
     """gemm_trace_set: every CTA of the single-CTA kernel stamps its events in
     causal order; with the hook off the buffer is left alone."""
