@@ -727,10 +727,11 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   if (h->i8x) {
     // The exact-int8 kernels: the pair kernel's 256 x 256 tile or the
     // single-CTA 128 x 128 tile (each epilogue thread keeps 128 int32 sums in
-    // registers), with no K split.
+    // registers), with no K split; the pair kernel's stream-K pieces pass
+    // int32 partials.
     h->choice.bn = h->choice.pair ? 256 : 128;
     h->choice.splits = 1;
-    h->choice.tail = 0;
+    if (!h->choice.pair) h->choice.tail = 0;
   }
   PlanChoice& c = h->choice;
   const bool swap = c.swap != 0;
@@ -883,7 +884,7 @@ int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
   const int64_t tiles = (int64_t)kp.tiles_m * kp.tiles_n;
   kp.sk_dp = kp.sk_start = kp.sk_len = kp.sk_rem = 0;
   kp.sk_n3 = -1;
-  if (h->pair && c.tail && !h->i8x && kp.splits == 1)
+  if (h->pair && c.tail && kp.splits == 1)
     plan_stream_k(tiles, clusters, kp.num_kb, c.ksub, kp, c.skpat >= 0);
   const int64_t sk_slots = kp.sk_len > 0 ? clusters : 0;
   if (h->pair) h->grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(

@@ -72,8 +72,11 @@ static const PlanRow kTable[] = {
     {8192, 8192, 8192, T_BF16, 0, 1, {256, 8, 1, 0, 0, 1, 1, 1}},
     // 8192^3 int8: pair 256x256 1209; with 2 K slices per stage 1184;
     // single-CTA 128x128 858 (512-K exact passes).  With 960-K passes (the
-    // default since): 1591, GROUP_M 16 1567, 768-K passes 1568.
-    {8192, 8192, 8192, T_I8, 0, 0, {256, 8, 1, 0, 0, 1, 1, 0}},
+    // default since): 1591, GROUP_M 16 1567, 768-K passes 1568.  Stream-K
+    // pieces for the partial last wave (13.47 waves; int32 partials, chained
+    // runs): 742-748 us against 749-753 without and 761 with equal runs
+    // (one box, two interleaved sweeps; the spreads were 4 %).
+    {8192, 8192, 8192, T_I8, 0, 0, {256, 8, 1, 0, 0, 1, 1, 1}},
     // (64, 8192, 8192) bf16, all row-major: 128x128 tiles, split 2: 246;
     // 128x256 split 4: 241; swapped 128x64 split 4: 230, split 2: 211.
     // The two splits of a tile reduced within their cluster (csk): 232

@@ -411,11 +411,17 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
         const int nch = (w.kb1 - w.kb0 + p.kb_per_chunk - 1) / p.kb_per_chunk;
         const int gy = w.m0 + BM * static_cast<int>(rank) + 32 * q;  // this warp's rows
         const int gx0 = w.n0 + static_cast<int>(col0);
+        // Stream-K pieces of a shared tile: the leaving piece stores its
+        // int32 sums (as the 16-bit path stores its fp32 ones: int4 of
+        // column group g of row i at [g][i]) and raises its flag; the
+        // finishing piece adds them, then C, and stores D.  Integer sums:
+        // the result is the same bits as without stream-K.
+        const bool leaves = w.tail && w.part == 1;
 #pragma unroll
         for (int j = 0; j < HC; ++j) isum[j] = 0;
         for (int ch = 0; ch < nch; ++ch) {
           const uint32_t buf = acc_it & 1u;
-          if (p.d_tma && p.C && ch == nch - 1) {
+          if (p.d_tma && p.C && !leaves && ch == nch - 1) {
             // C of the tile's first two slices, while the last chunk runs
             if (lane == 0) {
               load_c(0, gx0, gy);
@@ -456,6 +462,52 @@ __global__ void __launch_bounds__(PairCfg<BN, KSUB, I8X>::THREADS, 1)
           ++acc_it;
         }
         if (!ok) break;
+        // (the piece's slot and flag, computed here so that they are not
+        // held across the chunk loop)
+        int4* const pbase = w.tail ? reinterpret_cast<int4*>(
+                                         p.tail_ws + static_cast<size_t>(w.ti * 2 + rank) * BM * BN) +
+                                         row_local
+                                   : nullptr;
+        uint32_t* const flag = w.tail ? p.tail_flags + w.ti * 2 + rank : nullptr;
+        if (leaves) {
+#pragma unroll
+          for (int g = 0; g < HC / 4; ++g)
+            pbase[(static_cast<int>(col0) / 4 + g) * BM] =
+                make_int4(isum[4 * g], isum[4 * g + 1], isum[4 * g + 2], isum[4 * g + 3]);
+          // Publish: every epilogue thread of this CTA has written its row.
+          __threadfence();
+          named_barrier_sync(1, 32 * Cfg::EPI_WARPS);
+          if (ep_leader) {
+            __threadfence();
+            st_release_gpu(flag, p.epoch);
+          }
+          continue;
+        }
+        if (w.tail && w.part == 0) {
+          if (ep_leader)
+            *ep_go = bounded_flag_wait(flag, p.epoch, abort_flag, p.status, STATUS_TIMEOUT, tmo)
+                         ? 1 : 0;
+          named_barrier_sync(1, 32 * Cfg::EPI_WARPS);
+          ok = *ep_go != 0;
+          named_barrier_sync(1, 32 * Cfg::EPI_WARPS);
+          if (!ok) break;
+          // four 16-byte loads in flight per batch (the 128 sums hold most
+          // of the registers)
+#pragma unroll
+          for (int g0 = 0; g0 < HC / 4; g0 += 4) {
+            int4 v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              v[k] = __ldcg(pbase + (static_cast<int>(col0) / 4 + g0 + k) * BM);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              isum[4 * (g0 + k)] += v[k].x;
+              isum[4 * (g0 + k) + 1] += v[k].y;
+              isum[4 * (g0 + k) + 2] += v[k].z;
+              isum[4 * (g0 + k) + 3] += v[k].w;
+            }
+          }
+        }
         if (p.d_tma) {
 #pragma unroll
           for (int c = 0; c < HC / 32; ++c) {

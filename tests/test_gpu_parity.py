@@ -716,6 +716,30 @@ def test_int8_exact_small(shape, plan):
     _assert_ok(check_rows(w, inp, D), f"int8 {shape} [{p}]")
 
 
+I8_SK_CASES = [
+    (520, 640, 4160, "pair=1,tail=1,grid=8", -1),     # 9 tiles, 4 clusters: equal runs
+    (520, 640, 4160, "pair=1,tail=1,grid=12", 0),     # 9 tiles, 6 clusters: pair chains
+    (1024, 1536, 2048, "pair=1,tail=1,grid=20", 2),   # 24 tiles, 10 clusters: both chains
+    (1024, 1536, 2048, "pair=1,tail=1,grid=20,ksub=2,i8chunk=512", 2),
+]
+
+
+@pytest.mark.parametrize("case", I8_SK_CASES, ids=[c[3] for c in I8_SK_CASES])
+def test_int8_stream_k(case):
+    """Exact int8 with stream-K pieces (int32 partials between clusters):
+    every element of the sampled rows exact, and the same bits as round-robin
+    whole tiles."""
+    M, N, K, plan, n3 = case
+    w = Workload("i8sk", 54, M, N, K, I8, I32, I32, "int")
+    inp = make_inputs(w)
+    D, p = run_gpu(w, inp, plan=plan)
+    assert "i8x=1" in p and f"skchain={n3}" in p and "tail=0" not in p, p
+    _assert_ok(check_rows(w, inp, D), f"int8 stream-K [{p}]")
+    D0, p0 = run_gpu(w, inp, plan=plan.replace("tail=1", "tail=0"))
+    assert "tail=0" in p0, p0
+    assert torch.equal(D, D0), (p, p0)
+
+
 @pytest.mark.parametrize("plan", I8_PLANS)
 def test_int8_without_c(plan):
     """C absent: D = A*B exactly (the pair kernel stages D alone)."""
