@@ -7,9 +7,9 @@
 //    alignment: operands whose rows the TMA unit cannot read in place into a
 //    padded workspace, and C / D rows that are not 16-byte aligned into and
 //    out of aligned workspace rows.
-//  * widen_i8_x4_kernel / repack_kernel: int8 operands widened to bf16 in
-//    the workspace (exact: |v| <= 128 needs 8 bits), four elements a thread
-//    when rows allow it, else one.
+//  * widen_i8_x16_kernel / widen_i8_x4_kernel / repack_kernel: int8
+//    operands widened to bf16 in the workspace (exact: |v| <= 128 needs 8
+//    bits), sixteen or four elements a thread when rows allow it, else one.
 //
 // All of them put consecutive threads on consecutive addresses and are
 // launched with programmatic stream serialisation (pdl_wait first).
@@ -240,6 +240,48 @@ __global__ void widen_i8_x4_kernel(const char4* __restrict__ src, long long ld_s
   }
 }
 
+// int8 -> bf16 widening, 16 elements per thread (rows whose starts and
+// lengths are multiples of 16 elements): one 16-byte load and two 16-byte
+// stores per row, so a warp moves 512 contiguous bytes in and 1 KB out per
+// access; two rows per step.
+__global__ void widen_i8_x16_kernel(const uint4* __restrict__ src, long long ld_src16,
+                                    uint4* __restrict__ dst, long long ld_dst8, long long rows,
+                                    long long cols16) {
+  pdl_wait();
+  pdl_trigger();
+  const long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c >= cols16) return;
+  constexpr int R = 2;
+  const long long step = static_cast<long long>(gridDim.y) * R;
+  for (long long r0 = static_cast<long long>(blockIdx.y) * R; r0 < rows; r0 += step) {
+    uint4 x[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      if (r0 + i < rows) x[i] = src[(r0 + i) * ld_src16 + c];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      if (r0 + i >= rows) break;
+      const uint32_t w[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+      uint32_t o[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        // bytes of w[k], low to high: elements 4k .. 4k + 3 (signed)
+        const float e0 = static_cast<float>(static_cast<int8_t>(w[k] & 0xFFu));
+        const float e1 = static_cast<float>(static_cast<int8_t>((w[k] >> 8) & 0xFFu));
+        const float e2 = static_cast<float>(static_cast<int8_t>((w[k] >> 16) & 0xFFu));
+        const float e3 = static_cast<float>(static_cast<int8_t>(w[k] >> 24));
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(e0, e1);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(e2, e3);
+        o[2 * k] = *reinterpret_cast<const uint32_t*>(&lo);
+        o[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+      }
+      uint4* const d = dst + (r0 + i) * ld_dst8 + 2 * c;
+      d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+  }
+}
+
 namespace {
 // copy_rows16_kernel: 2048 columns per block, rows strided over block y.
 dim3 copy_rows_grid(long long rows, long long cols, int num_sms, int njobs) {
@@ -280,6 +322,13 @@ cudaError_t launch_repack(const void* src, int src_type, long long ld_src, uint1
                           long long ld_dst, long long rows, long long cols, int num_sms,
                           cudaStream_t st) {
   if (rows == 0 || cols == 0) return cudaSuccess;
+  const bool x16 = src_type == T_I8 && cols % 16 == 0 && ld_src % 16 == 0 && ld_dst % 8 == 0 &&
+                   reinterpret_cast<uintptr_t>(src) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(dst) % 16 == 0;
+  if (x16)
+    return launch_pdl(widen_i8_x16_kernel, copy_grid(cols / 16, rows, num_sms), dim3(256), 0, st,
+                      static_cast<const uint4*>(src), ld_src / 16, reinterpret_cast<uint4*>(dst),
+                      ld_dst / 8, rows, cols / 16);
   const bool x4 = src_type == T_I8 && cols % 4 == 0 && ld_src % 4 == 0 && ld_dst % 4 == 0 &&
                   reinterpret_cast<uintptr_t>(src) % 4 == 0;
   if (x4)

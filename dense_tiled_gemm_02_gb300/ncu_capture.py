@@ -113,7 +113,11 @@ def main(argv=None) -> int:
                                  ncu_record.bench_line(plain_log), a.kernel_regex)
     if a.plan:
         rec["forced_plan"] = a.plan
-    stem = ncu_record.kernel_stem(rec["plan"])
+    stem = ncu_record.aux_stem(a.kernel_regex) or ncu_record.kernel_stem(rec["plan"])
+    if not ncu_record.aux_stem(a.kernel_regex) and stem + "_kernel" not in rec["kernel"]:
+        # a GEMM record must hold the plan's GEMM kernel, whatever the regex matched
+        print(f"captured {rec['kernel']}, not the plan's {stem}_kernel: no record", flush=True)
+        return 4
     out = os.path.join(a.out_dir, f"{stem}_{rec['workload']}")
     import json
     with open(out + ".json", "w") as f:

@@ -41,6 +41,16 @@ FAMILY_SOURCES = {
     "cta1": ("common.h", "ptx.cuh", "tc_gemm.cuh", "tc_launch.cu"),
     "decode": ("common.h", "ptx.cuh", "decode.cu"),
     "i8mma": ("common.h", "ptx.cuh", "i8_mma.cu"),
+    # the auxiliary kernels around a GEMM (split-K reduce, row copies, int8
+    # widening); their records are informational, the benchmark reads none
+    "aux": ("common.h", "ptx.cuh", "aux_kernels.cu"),
+}
+
+# Records of auxiliary kernels: kernel-name pattern -> file-name stem.
+AUX_STEMS = {
+    "splitk_reduce_kernel": "splitk_reduce",
+    "copy_rows16_kernel": "copy_rows16",
+    "widen_i8": "widen_i8",
 }
 
 # Metrics copied into the record (base units): name -> key in the record.
@@ -77,6 +87,14 @@ def kernel_stem(plan: str) -> str:
     if fam == "decode":
         return "decode_bulk" if re.search(r"\bdbulk=1\b", plan) else "decode_kn"
     return {"i8mma": "i8_mma", "pair": "tc_gemm_pair", "cta1": "tc_gemm"}[fam]
+
+
+def aux_stem(kernel_regex):
+    """File-name stem when the captured kernel is an auxiliary one, else None."""
+    for pat, stem in AUX_STEMS.items():
+        if kernel_regex and pat in kernel_regex:
+            return stem
+    return None
 
 
 def source_hash(family: str) -> str:
@@ -179,8 +197,10 @@ def make_record(raw_rows: list[dict], launches: list[dict], line: dict,
         rows = [r for r in rows if re.search(kernel_regex, str(r.get("Kernel Name", "")))]
     if not rows:
         raise ValueError("no captured launch matches")
-    rec = {"workload": workload, "plan": plan, "family": family_of(plan),
-           "source_hash": source_hash(family_of(plan)),
+    aux = aux_stem(kernel_regex)
+    family = "aux" if aux else family_of(plan)
+    rec = {"workload": workload, "plan": plan, "family": family,
+           "source_hash": source_hash(family),
            "kernel": str(rows[0].get("Kernel Name", "")).split("(")[0].replace("void ", ""),
            "launches_captured": len(rows)}
     for name, key in RECORD_METRICS.items():
@@ -189,7 +209,11 @@ def make_record(raw_rows: list[dict], launches: list[dict], line: dict,
             rec[key] = statistics.mean(vals)
     if "dram_read_bytes" in rec and "dram_write_bytes" in rec:
         rec["dram_bytes_per_launch"] = rec["dram_read_bytes"] + rec["dram_write_bytes"]
-        algo = line.get("roofline", {}).get("algorithmic_bytes")
+        if rec.get("duration_ns"):
+            rec["dram_gbs"] = round(rec["dram_bytes_per_launch"] / rec["duration_ns"], 1)
+        # (the bench line's algorithmic bytes are the GEMM's, not an
+        # auxiliary kernel's)
+        algo = None if aux else line.get("roofline", {}).get("algorithmic_bytes")
         if algo:
             rec["algorithmic_bytes"] = algo
             rec["traffic_over_algorithmic"] = round(rec["dram_bytes_per_launch"] / algo, 4)
@@ -204,7 +228,7 @@ def markdown(rec: dict) -> str:
     """A short table of the record, for the human-written summary beside it."""
     out = [f"| metric | value |", "|---|---|"]
     for key in ("duration_ns", "sm_clock_hz", "dram_read_bytes", "dram_write_bytes",
-                "dram_bytes_per_launch", "algorithmic_bytes", "traffic_over_algorithmic",
+                "dram_bytes_per_launch", "dram_gbs", "algorithmic_bytes", "traffic_over_algorithmic",
                 "dram_busy_pct", "tensor_pipe_pct_elapsed", "tensor_pipe_pct_active",
                 "sm_throughput_pct", "l2_hit_pct", "registers_per_thread", "grid_size",
                 "block_size", "dynamic_smem_bytes"):
