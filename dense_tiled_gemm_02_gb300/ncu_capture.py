@@ -53,11 +53,14 @@ def run(cmd: list[str], log: str, env: dict) -> int:
 
 def summary(rec: dict, cmds: dict) -> str:
     algo = rec.get("algorithmic_bytes")
+    use = (["capture; the JSON beside this file holds the same figures (an auxiliary",
+            "kernel of the call: informational, `bench.py` reads no such record)."]
+           if rec.get("family") == "aux" else
+           ["capture; the JSON beside this file holds the same figures and is what",
+            "`bench.py` reads for `roofline.traffic` (only while the kernel family's",
+            "device sources hash to `source_hash` and the plan string is the same)."])
     lines = [f"# {rec['kernel']} -- {rec['workload']}", "",
-             "Machine-written by `dense_tiled_gemm_02_gb300/ncu_capture.py` from one ncu",
-             "capture; the JSON beside this file holds the same figures and is what",
-             "`bench.py` reads for `roofline.traffic` (only while the kernel family's",
-             "device sources hash to `source_hash` and the plan string is the same).", "",
+             "Machine-written by `dense_tiled_gemm_02_gb300/ncu_capture.py` from one ncu"] + use + ["",
              f"- plan: `{rec['plan']}`", f"- source_hash ({rec['family']}): `{rec['source_hash']}`"]
     if algo and rec.get("dram_bytes_per_launch"):
         lines.append(f"- DRAM bytes per launch {rec['dram_bytes_per_launch'] / 1e6:.1f} MB against "
