@@ -116,12 +116,18 @@ typedef void* gemm_stream_t;
  * Environment: GEMM_LOG=1 prints the chosen plan to stderr;
  * GEMM_FORCE_PLAN="bn=128,splits=2,group=8,swap=1" overrides fields of the
  * plan (for tuning sweeps; keys bn, splits, group, swap, grid, pair, ksub,
- * tail, sk (1: the single-CTA kernel's stream-K schedule, shared tiles
- * finished in the kernel), decode, dbulk: 1 takes the decode kernel's bulk-copy form whenever
- * A's and B's rows allow it, 0 never; native_i8: 1 runs an int8 problem on
- * the integer mma.sync kernel, which reads A and B contiguous along K and
- * copies them so first when they are stored otherwise, instead of the exact
- * emulation on the bf16 tensor cores).
+ * tail (the pair kernel's stream-K hybrid), skpat (0: its runs equal
+ * instead of chained), sk (1: the single-CTA kernel's stream-K schedule,
+ * shared tiles finished in the kernel), csk (1: a K split's CTAs reduce
+ * their sums in a cluster instead of a reduce launch), kgroup (K slices
+ * issued together), lsu (1: unaligned 16-bit rows loaded by producer warps
+ * instead of a workspace copy), i8chunk (K of an exact int8 pass), decode,
+ * dbulk: 1 takes the decode kernel's bulk-copy form whenever A's and B's
+ * rows allow it, 0 never; dmma (1: the decode shapes' mma.sync form);
+ * native_i8: 1 runs an int8 problem on the integer mma.sync kernel, which
+ * reads A and B contiguous along K and copies them so first when they are
+ * stored otherwise, instead of the exact emulation on the bf16 tensor
+ * cores).
  */
 GEMM_API int gemm_create(gemm_handle_t* out, const gemm_desc_t* desc);
 
