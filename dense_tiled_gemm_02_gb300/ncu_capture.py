@@ -2,7 +2,7 @@
 to the committed record.
 
     python -m dense_tiled_gemm_02_gb300.ncu_capture --workload sq4096_bf16 \
-        --kernel-regex tc_gemm_pair_kernel --out-dir gpurun_out/profiles \
+        --kernel-regex tc_gemm_pair_kernel --out-dir out/profiles \
         [--plan native_i8=1] [--skip 3]
 
 For one workload this
