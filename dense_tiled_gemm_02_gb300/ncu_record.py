@@ -49,7 +49,7 @@ FAMILY_SOURCES = {
 # Records of auxiliary kernels: kernel-name pattern -> file-name stem.
 AUX_STEMS = {
     "splitk_reduce_kernel": "splitk_reduce",
-    "copy_rows16_kernel": "copy_rows16",
+    "copy_rows16": "copy_rows16",
     "widen_i8": "widen_i8",
 }
 

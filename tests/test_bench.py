@@ -159,6 +159,7 @@ def test_aux_kernel_records_are_named_and_hashed_apart():
     over the auxiliary sources, so they never stand in for a GEMM record."""
     assert ncu_record.aux_stem("splitk_reduce_kernel") == "splitk_reduce"
     assert ncu_record.aux_stem("regex:copy_rows16_kernel") == "copy_rows16"
+    assert ncu_record.aux_stem("copy_rows16_v_kernel") == "copy_rows16"
     assert ncu_record.aux_stem("widen_i8_x16_kernel") == "widen_i8"
     assert ncu_record.aux_stem("tc_gemm_kernel") is None
     assert ncu_record.source_hash("aux") != ncu_record.source_hash("cta1")
